@@ -1,0 +1,47 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the smoke check.
+
+This module holds no attention arithmetic: it only draws numbers.  Each
+tensor has its own sub-seed (q=seed, k=seed+1, v=seed+2, dout=seed+3,
+lens=seed+4), values are float32 N(0, 1) draws rounded to bfloat16
+(round-to-nearest-even), so the CUDA path and the float64 oracle read the
+very same bf16 values.
+"""
+
+import torch
+
+__all__ = ["attention_inputs", "decode_inputs", "to_f64"]
+
+
+def _normal(shape, seed, scale=1.0):
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if scale != 1.0:
+        x = x * scale
+    return x.to(torch.bfloat16)
+
+
+def attention_inputs(B, S, Hq, Hkv, Dqk, Dv, seed=0, q_scale=1.0):
+    """q [B,S,Hq,Dqk], k [B,S,Hkv,Dqk], v [B,S,Hkv,Dv], dout [B,S,Hq,Dv];
+    bf16 CPU tensors.  ``q_scale`` multiplies the fp32 draw of q before the
+    bf16 rounding (the Llama2-shaped workload draws q with 1/sqrt(128))."""
+    q = _normal((B, S, Hq, Dqk), seed, q_scale)
+    k = _normal((B, S, Hkv, Dqk), seed + 1)
+    v = _normal((B, S, Hkv, Dv), seed + 2)
+    dout = _normal((B, S, Hq, Dv), seed + 3)
+    return q, k, v, dout
+
+
+def decode_inputs(B, Hq, Hkv, D, Smax, len_lo, len_hi, seed=0):
+    """q [B,Hq,D], kcache/vcache [B,Hkv,Smax,D] (bf16) and lens [B] (int32)
+    drawn uniformly from the closed range [len_lo, len_hi]."""
+    q = _normal((B, Hq, D), seed)
+    kc = _normal((B, Hkv, Smax, D), seed + 1)
+    vc = _normal((B, Hkv, Smax, D), seed + 2)
+    g = torch.Generator(device="cpu").manual_seed(int(seed) + 4)
+    lens = torch.randint(int(len_lo), int(len_hi) + 1, (B,), generator=g, dtype=torch.int32)
+    return q, kc, vc, lens
+
+
+def to_f64(t):
+    """bf16/float torch tensor -> float64 NumPy array (exact upcast)."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
