@@ -1,0 +1,205 @@
+"""ctypes binding of libcpattn.so (argument marshalling only).
+
+Every function here takes torch tensors that already live on the GPU, checks
+dtype/shape/contiguity, passes raw device pointers and the current CUDA
+stream to the C ABI declared in ``include/cpattn.h``, and raises
+``CpAttnError`` on a non-zero status.  No computation happens in Python and
+there is no fallback: if the library is missing the import of the first
+call fails loudly.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "CpAttnError", "load", "lb_permute", "lb_unpermute", "attn_fwd", "attn_fwd_shard",
+    "attn_bwd", "gqa_decode", "lb_positions", "tile_counts", "check_device", "release",
+    "EXPORTED_SYMBOLS",
+]
+
+EXPORTED_SYMBOLS = (
+    "cp_lb_permute", "cp_lb_unpermute", "cp_attn_fwd", "cp_attn_fwd_shard", "cp_attn_bwd",
+    "gqa_decode", "cp_lb_positions", "cp_attn_tile_counts", "cp_attn_check_device",
+    "cp_attn_last_error", "cp_attn_release",
+)
+
+_lib = None
+
+
+class CpAttnError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("cpattn error %d: %s" % (code, msg))
+        self.code = code
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_longlong
+
+
+def load(path=None):
+    """Load libcpattn.so (built in-tree by ``build.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError("libcpattn.so is not built (%s); run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    sig = {
+        "cp_lb_permute": [_P, _P, _I, _I, _L, _I, _P],
+        "cp_lb_unpermute": [_P, _P, _I, _I, _L, _I, _P],
+        "cp_attn_fwd": [_P, _P, _P, _P, _P] + [_I] * 8 + [_P],
+        "cp_attn_fwd_shard": [_P, _P, _P, _P, _P] + [_I] * 9 + [_P],
+        "cp_attn_bwd": [_P] * 9 + [_I] * 8 + [_P],
+        "gqa_decode": [_P] * 5 + [_I] * 5 + [_P],
+        "cp_lb_positions": [_I, _I, _I, ctypes.POINTER(ctypes.c_int)],
+        "cp_attn_tile_counts": [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)],
+        "cp_attn_check_device": [_P],
+        "cp_attn_release": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.cp_attn_last_error.argtypes = []
+    lib.cp_attn_last_error.restype = ctypes.c_char_p
+    if path == _build.lib_path():
+        _lib = lib
+    return lib
+
+
+def _check(rc):
+    if rc != 0:
+        msg = load().cp_attn_last_error().decode(errors="replace")
+        raise CpAttnError(rc, msg)
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+
+
+def lb_permute(x, cp, out=None):
+    """Load-balance reorder of axis 1 of a [B, S, ...] CUDA tensor."""
+    return _perm(x, cp, out, False)
+
+
+def lb_unpermute(x, cp, out=None):
+    return _perm(x, cp, out, True)
+
+
+def _perm(x, cp, out, inverse):
+    if not x.is_cuda or not x.is_contiguous() or x.dim() < 2:
+        raise ValueError("x must be a contiguous CUDA tensor [B, S, ...]")
+    out = torch.empty_like(x) if out is None else out
+    B, S = x.shape[:2]
+    row = x[0, 0].numel() * x.element_size()
+    f = load().cp_lb_unpermute if inverse else load().cp_lb_permute
+    _check(f(_ptr(x), _ptr(out), B, S, row, cp, _stream(x)))
+    return out
+
+
+def _shape(q, k, v):
+    _need(q, torch.bfloat16, "q", 4)
+    _need(k, torch.bfloat16, "k", 4)
+    _need(v, torch.bfloat16, "v", 4)
+    B, S, Hq, Dqk = q.shape
+    if k.shape[:2] != (B, S) or v.shape[:3] != k.shape[:3] or k.shape[3] != Dqk:
+        raise ValueError("q/k/v shapes do not match")
+    return B, S, Hq, k.shape[2], Dqk, v.shape[3]
+
+
+def attn_fwd(q, k, v, cp, load_balance=True, out=None, lse=None, shard=None):
+    """out [B,S,Hq,Dv] bf16 and lse [B,Hq,S] fp32 of causal CP attention;
+    q/k/v in load-balanced slot order when load_balance is true."""
+    B, S, Hq, Hkv, Dqk, Dv = _shape(q, k, v)
+    if out is None:
+        out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out", 4)
+    _need(lse, torch.float32, "lse", 3)
+    lib = load()
+    if shard is None:
+        rc = lib.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, Dqk, Dv,
+                             cp, int(bool(load_balance)), _stream(q))
+    else:
+        rc = lib.cp_attn_fwd_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, Dqk,
+                                   Dv, cp, int(bool(load_balance)), int(shard), _stream(q))
+    _check(rc)
+    return out, lse
+
+
+def attn_fwd_shard(q, k, v, cp, shard, load_balance=True, out=None, lse=None):
+    return attn_fwd(q, k, v, cp, load_balance, out, lse, shard)
+
+
+def attn_bwd(q, k, v, out, lse, dout, cp, load_balance=True, dq=None, dk=None, dv=None):
+    """dq, dk, dv (bf16, shapes of q/k/v) of sum(out * dout)."""
+    B, S, Hq, Hkv, Dqk, Dv = _shape(q, k, v)
+    _need(out, torch.bfloat16, "out", 4)
+    _need(dout, torch.bfloat16, "dout", 4)
+    _need(lse, torch.float32, "lse", 3)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    rc = load().cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                            _ptr(dk), _ptr(dv), B, Hq, Hkv, S, Dqk, Dv, cp, int(bool(load_balance)),
+                            _stream(q))
+    _check(rc)
+    return dq, dk, dv
+
+
+def gqa_decode(q, kcache, vcache, lens, out=None):
+    """q [B,Hq,D], kcache/vcache [B,Hkv,Smax,D] bf16, lens [B] int32 -> out [B,Hq,D]."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kcache, torch.bfloat16, "kcache", 4)
+    _need(vcache, torch.bfloat16, "vcache", 4)
+    _need(lens, torch.int32, "lens", 1)
+    B, Hq, D = q.shape
+    Hkv, Smax = kcache.shape[1], kcache.shape[2]
+    out = torch.empty_like(q) if out is None else out
+    rc = load().gqa_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(lens), _ptr(out), B, Hq, Hkv,
+                           Smax, D, _stream(q))
+    _check(rc)
+    return out
+
+
+def lb_positions(S, cp, load_balance=True):
+    arr = (ctypes.c_int * S)()
+    _check(load().cp_lb_positions(S, cp, int(bool(load_balance)), arr))
+    return list(arr)
+
+
+def tile_counts(S, cp, load_balance=True):
+    arr = (ctypes.c_longlong * cp)()
+    _check(load().cp_attn_tile_counts(S, cp, int(bool(load_balance)), arr))
+    return list(arr)
+
+
+def check_device(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _check(load().cp_attn_check_device(ctypes.c_void_p(s)))
+
+
+def release():
+    _check(load().cp_attn_release())

@@ -1,0 +1,514 @@
+// C ABI of libcpattn.so: argument checks, TMA descriptors, work lists,
+// cached scratch, launches.  See include/cpattn.h for the contract.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/cpattn.h"
+#include "common.cuh"
+#include "internal.h"
+
+using namespace cpattn;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(CPATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ---- tensor maps -----------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [B, S, H, D] bf16 tensor seen as 4-D {D, H, S, B}; box = 64 columns x rows
+// (128-byte rows, 128-byte swizzle, zero fill past S)
+int make_tmap(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return CPATTN_OK;
+}
+
+// ---- per-device state ---------------------------------------------------------
+template <typename T>
+struct DevBuf {
+  T* ptr = nullptr;
+  size_t n = 0;
+};
+
+struct DevState {
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* err = nullptr;  // device error word
+  std::map<std::vector<int>, DevBuf<FwdUnit>> fwd_units;
+  std::map<std::vector<int>, DevBuf<BwdUnit>> bwd_units;
+  DevBuf<float> bwd_stats;  // lse_l2 then delta
+  DevBuf<float> dec_o, dec_ml;
+  DevBuf<int> dec_cnt;
+};
+
+std::mutex g_mu;
+std::map<int, DevState> g_dev;
+
+int get_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DevState& s = g_dev[dev];
+  if (!s.err) {
+    cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    e = cudaMalloc(&s.err, sizeof(int));
+    if (e != cudaSuccess) { s.err = nullptr; return fail(CPATTN_ERR_NO_MEMORY, "cudaMalloc(error word) failed"); }
+    e = cudaMemset(s.err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  }
+  *out = &s;
+  return CPATTN_OK;
+}
+
+int need_sm103(const DevState& s) {
+  if (s.cc_major != 10 || s.cc_minor != 3)
+    return fail(CPATTN_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device is sm_%d%d",
+                s.cc_major, s.cc_minor);
+  return CPATTN_OK;
+}
+
+template <typename T>
+int ensure(DevBuf<T>& b, size_t n, cudaStream_t st, bool zero) {
+  if (b.n >= n && b.ptr) return CPATTN_OK;
+  if (b.ptr) {
+    cudaStreamSynchronize(st);
+    cudaFree(b.ptr);
+    b.ptr = nullptr;
+    b.n = 0;
+  }
+  cudaError_t e = cudaMalloc(&b.ptr, n * sizeof(T));
+  if (e != cudaSuccess) {
+    b.ptr = nullptr;
+    return fail(CPATTN_ERR_NO_MEMORY, "cudaMalloc(%zu bytes) failed", n * sizeof(T));
+  }
+  if (zero) {
+    e = cudaMemsetAsync(b.ptr, 0, n * sizeof(T), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  }
+  b.n = n;
+  return CPATTN_OK;
+}
+
+template <typename T>
+int upload(DevBuf<T>& b, const std::vector<T>& v) {
+  cudaError_t e = cudaMalloc(&b.ptr, std::max<size_t>(1, v.size()) * sizeof(T));
+  if (e != cudaSuccess) { b.ptr = nullptr; return fail(CPATTN_ERR_NO_MEMORY, "cudaMalloc(work list) failed"); }
+  if (!v.empty()) {
+    e = cudaMemcpy(b.ptr, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(work list)");
+  }
+  b.n = v.size();
+  return CPATTN_OK;
+}
+
+// ---- argument checks ------------------------------------------------------
+int check_attn(const AttnShape& sh) {
+  if (sh.B < 1 || sh.S < 1 || sh.Hq < 1 || sh.Hkv < 1 || sh.cp < 1)
+    return fail(CPATTN_ERR_INVALID_ARG, "B, S, Hq, Hkv and cp must be >= 1");
+  if (sh.Hq % sh.Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", sh.Hq, sh.Hkv);
+  if (sh.S % sh.cp) return fail(CPATTN_ERR_INVALID_ARG, "S (%d) must be a multiple of cp (%d)", sh.S, sh.cp);
+  if (sh.lb && sh.S % (2 * sh.cp))
+    return fail(CPATTN_ERR_INVALID_ARG, "load balance needs S (%d) to be a multiple of 2*cp (%d)", sh.S, 2 * sh.cp);
+  const bool dims_ok = (sh.Dqk == 64 && sh.Dv == 64) || (sh.Dqk == 128 && sh.Dv == 128) ||
+                       (sh.Dqk == 192 && sh.Dv == 128);
+  if (!dims_ok)
+    return fail(CPATTN_ERR_UNSUPPORTED, "head dims (Dqk=%d, Dv=%d) not in {(64,64),(128,128),(192,128)}", sh.Dqk,
+                sh.Dv);
+  if ((long long)sh.B * sh.S * sh.Hq > (1LL << 31) - 1)
+    return fail(CPATTN_ERR_UNSUPPORTED, "B*S*Hq exceeds 2^31");
+  return CPATTN_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps) {
+    if (!p) return fail(CPATTN_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(p)) return fail(CPATTN_ERR_INVALID_ARG, "tensor pointer %p is not 16-byte aligned", p);
+  }
+  return CPATTN_OK;
+}
+
+// ---- work lists ------------------------------------------------------------
+constexpr int kTile = 128;
+
+int count_kv_tiles(const PosMap& pm, int bound) {
+  int n = 0;
+  for (int kt = next_kv_tile(pm, kTile, -1, bound); kt >= 0; kt = next_kv_tile(pm, kTile, kt, bound)) ++n;
+  return n;
+}
+int tile_max_pos(const PosMap& pm, int t, int T) {
+  int mn, mx;
+  pm.range(t * T, t * T + T, mn, mx);
+  return mx;
+}
+int tile_min_pos(const PosMap& pm, int t, int T) {
+  int mn, mx;
+  pm.range(t * T, t * T + T, mn, mx);
+  return mn;
+}
+
+// forward units: pairs of 128-row query tiles sharing a KV head, heaviest first
+std::vector<FwdUnit> build_fwd_units(const AttnShape& sh, int shard) {
+  const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
+  const int nqt = (sh.S + kTile - 1) / kTile;
+  const int G = sh.Hq / sh.Hkv;
+  const int per = sh.S / sh.cp;
+  auto in_shard = [&](int qt) { return shard < 0 || (qt * kTile >= shard * per && qt * kTile < (shard + 1) * per); };
+  std::vector<int> qmax(nqt);
+  for (int qt = 0; qt < nqt; ++qt) qmax[qt] = tile_max_pos(pm, qt, kTile);
+  std::vector<std::pair<long long, FwdUnit>> w;
+  auto add = [&](int b, int hkv, int h0, int t0, int h1, int t1) {
+    FwdUnit u{b, h0, h1, t0, t1, hkv, 0, 0};
+    int bound = qmax[t0];
+    if (h1 >= 0) bound = std::max(bound, qmax[t1]);
+    long long cost = (long long)count_kv_tiles(pm, bound) * (h1 >= 0 ? 2 : 1);
+    w.push_back({cost, u});
+  };
+  // tiles of one head paired with their neighbour in the same memory chunk
+  auto pair_rows = [&](int b, int hkv, int h) {
+    int qt = 0;
+    while (qt < nqt) {
+      if (!in_shard(qt)) { ++qt; continue; }
+      const bool same_chunk = !pm.lb || (pm.c % kTile != 0) || ((qt * kTile) / pm.c == ((qt + 1) * kTile) / pm.c);
+      if (qt + 1 < nqt && in_shard(qt + 1) && same_chunk) {
+        add(b, hkv, h, qt, h, qt + 1);
+        qt += 2;
+      } else {
+        add(b, hkv, h, qt, -1, 0);
+        qt += 1;
+      }
+    }
+  };
+  for (int b = 0; b < sh.B; ++b)
+    for (int hkv = 0; hkv < sh.Hkv; ++hkv) {
+      const int h_first = hkv * G;
+      int i = 0;
+      for (; i + 1 < G; i += 2)  // two heads of the group on the same rows
+        for (int qt = 0; qt < nqt; ++qt)
+          if (in_shard(qt)) add(b, hkv, h_first + i, qt, h_first + i + 1, qt);
+      if (i < G) pair_rows(b, hkv, h_first + i);
+    }
+  std::stable_sort(w.begin(), w.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+  std::vector<FwdUnit> out(w.size());
+  for (size_t i = 0; i < w.size(); ++i) out[i] = w[i].second;
+  return out;
+}
+
+int fwd_units_cached(DevState& ds, const AttnShape& sh, int shard, DevBuf<FwdUnit>** out) {
+  std::vector<int> key{sh.B, sh.Hq, sh.Hkv, sh.S, sh.cp, sh.lb, shard};
+  auto it = ds.fwd_units.find(key);
+  if (it == ds.fwd_units.end()) {
+    DevBuf<FwdUnit> buf;
+    int rc = upload(buf, build_fwd_units(sh, shard));
+    if (rc) return rc;
+    it = ds.fwd_units.emplace(key, buf).first;
+  }
+  *out = &it->second;
+  return CPATTN_OK;
+}
+
+// backward units.  kind 0: dk/dv, one 128-row key tile of a KV head, cost =
+// query tiles (of BQ rows, all heads of the group) that see it.  kind 1: dq,
+// one 128-row query tile of a query head, cost = key tiles it sees.
+int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, DevBuf<BwdUnit>** out) {
+  std::vector<int> key{kind, sh.B, sh.Hq, sh.Hkv, sh.S, sh.cp, sh.lb, sh.Dqk};
+  auto it = ds.bwd_units.find(key);
+  if (it == ds.bwd_units.end()) {
+    const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
+    const int nt = (sh.S + kTile - 1) / kTile;
+    std::vector<std::pair<long long, BwdUnit>> w;
+    if (kind == 0) {
+      const int BQ = bwd_dkdv_q_tile(sh.Dqk);
+      for (int kt = 0; kt < nt; ++kt) {
+        const int bound = tile_min_pos(pm, kt, kTile);
+        long long n = 0;
+        for (int qt = next_q_tile(pm, BQ, -1, bound); qt >= 0; qt = next_q_tile(pm, BQ, qt, bound)) ++n;
+        for (int b = 0; b < sh.B; ++b)
+          for (int g = 0; g < sh.Hkv; ++g) w.push_back({n, BwdUnit{b, g, kt, 0}});
+      }
+    } else {
+      const int BK = bwd_dq_kv_tile(sh.Dqk);
+      for (int qt = 0; qt < nt; ++qt) {
+        const int bound = tile_max_pos(pm, qt, kTile);
+        long long n = 0;
+        for (int kt = next_kv_tile(pm, BK, -1, bound); kt >= 0; kt = next_kv_tile(pm, BK, kt, bound)) ++n;
+        for (int b = 0; b < sh.B; ++b)
+          for (int h = 0; h < sh.Hq; ++h) w.push_back({n, BwdUnit{b, h, qt, 0}});
+      }
+    }
+    std::stable_sort(w.begin(), w.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+    std::vector<BwdUnit> v(w.size());
+    for (size_t i = 0; i < w.size(); ++i) v[i] = w[i].second;
+    DevBuf<BwdUnit> buf;
+    int rc = upload(buf, v);
+    if (rc) return rc;
+    it = ds.bwd_units.emplace(key, buf).first;
+  }
+  *out = &it->second;
+  return CPATTN_OK;
+}
+
+int permute_impl(const void* src, void* dst, int B, int S, long long row_bytes, int cp, int inverse,
+                 cudaStream_t st) {
+  if (!src || !dst) return fail(CPATTN_ERR_INVALID_ARG, "null pointer");
+  if (src == dst) return fail(CPATTN_ERR_INVALID_ARG, "src and dst must differ (the reorder is not in place)");
+  if (B < 1 || S < 1 || cp < 1 || row_bytes < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, S, cp, row_bytes must be >= 1");
+  if (S % (2 * cp)) return fail(CPATTN_ERR_INVALID_ARG, "S (%d) must be a multiple of 2*cp (%d)", S, 2 * cp);
+  const long long total = (long long)B * S * row_bytes;
+  const char* s8 = static_cast<const char*>(src);
+  const char* d8 = static_cast<const char*>(dst);
+  if (s8 < d8 + total && d8 < s8 + total) return fail(CPATTN_ERR_INVALID_ARG, "src and dst overlap");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds;
+  int rc = get_state(&ds);
+  if (rc) return rc;
+  cudaError_t e = launch_lb_permute(src, dst, B, S, row_bytes, cp, inverse, ds->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "lb_permute launch");
+  return CPATTN_OK;
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, const AttnShape& sh, int shard,
+             cudaStream_t st) {
+  int rc = check_attn(sh);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k, v, out, lse}))) return rc;
+  if (shard >= sh.cp) return fail(CPATTN_ERR_INVALID_ARG, "shard %d out of range [0, %d)", shard, sh.cp);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds;
+  if ((rc = get_state(&ds))) return rc;
+  if ((rc = need_sm103(*ds))) return rc;
+  DevBuf<FwdUnit>* units;
+  if ((rc = fwd_units_cached(*ds, sh, shard, &units))) return rc;
+  if (units->n == 0) return CPATTN_OK;
+  FwdArgs a;
+  if ((rc = make_tmap(&a.tq, q, sh.B, sh.S, sh.Hq, sh.Dqk, 128))) return rc;
+  if ((rc = make_tmap(&a.tk, k, sh.B, sh.S, sh.Hkv, sh.Dqk, 128))) return rc;
+  if ((rc = make_tmap(&a.tv, v, sh.B, sh.S, sh.Hkv, sh.Dv, 128))) return rc;
+  a.out = out;
+  a.lse = lse;
+  a.units = units->ptr;
+  a.n_units = (int)units->n;
+  a.sh = sh;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.Dqk));
+  a.err = ds->err;
+  const int grid = (int)std::min<size_t>(units->n, (size_t)ds->num_sms);
+  cudaError_t e = launch_attn_fwd(a, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
+  return CPATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cp_lb_permute(const void* src, void* dst, int B, int S, long long row_bytes, int cp, cudaStream_t stream) {
+  return permute_impl(src, dst, B, S, row_bytes, cp, 0, stream);
+}
+
+int cp_lb_unpermute(const void* src, void* dst, int B, int S, long long row_bytes, int cp, cudaStream_t stream) {
+  return permute_impl(src, dst, B, S, row_bytes, cp, 1, stream);
+}
+
+int cp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int S,
+                int Dqk, int Dv, int cp, int load_balance, cudaStream_t stream) {
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  return fwd_impl(q, k, v, out, lse, sh, -1, stream);
+}
+
+int cp_attn_fwd_shard(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                      int S, int Dqk, int Dv, int cp, int load_balance, int shard, cudaStream_t stream) {
+  if (shard < 0) return fail(CPATTN_ERR_INVALID_ARG, "shard must be >= 0");
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  return fwd_impl(q, k, v, out, lse, sh, shard, stream);
+}
+
+int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+                void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int cp,
+                int load_balance, cudaStream_t stream) {
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  int rc = check_attn(sh);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv}))) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds;
+  if ((rc = get_state(&ds))) return rc;
+  if ((rc = need_sm103(*ds))) return rc;
+  const int Spad = (S + kTile - 1) / kTile * kTile;
+  const size_t nstat = (size_t)B * Hq * Spad;
+  if ((rc = ensure(ds->bwd_stats, 2 * nstat, stream, false))) return rc;
+  DevBuf<BwdUnit>* u_kv;
+  DevBuf<BwdUnit>* u_q;
+  if ((rc = bwd_units_cached(*ds, sh, 0, &u_kv))) return rc;
+  if ((rc = bwd_units_cached(*ds, sh, 1, &u_q))) return rc;
+  BwdArgs a;
+  a.lse_l2 = ds->bwd_stats.ptr;
+  a.delta = ds->bwd_stats.ptr + nstat;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.Spad = Spad;
+  a.sh = sh;
+  a.scale = (float)(1.0 / std::sqrt((double)Dqk));
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)Dqk));
+  a.err = ds->err;
+  cudaError_t e = launch_bwd_preprocess(out, dout, lse, const_cast<float*>(a.lse_l2), const_cast<float*>(a.delta),
+                                        sh, Spad, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
+  // dk/dv: key tiles of 128 rows, query/dout boxes of BQ rows
+  const int BQ = bwd_dkdv_q_tile(Dqk);
+  if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, BQ))) return rc;
+  if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, BQ))) return rc;
+  if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, 128))) return rc;
+  if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
+  a.units = u_kv->ptr;
+  a.n_units = (int)u_kv->n;
+  e = launch_attn_bwd_dkdv(a, (int)std::min<size_t>(u_kv->n, (size_t)ds->num_sms), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dk/dv launch");
+  // dq: query tiles of 128 rows, key/value boxes of BK rows
+  const int BK = bwd_dq_kv_tile(Dqk);
+  if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, 128))) return rc;
+  if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, 128))) return rc;
+  if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, BK))) return rc;
+  if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, BK))) return rc;
+  a.units = u_q->ptr;
+  a.n_units = (int)u_q->n;
+  e = launch_attn_bwd_dq(a, (int)std::min<size_t>(u_q->n, (size_t)ds->num_sms), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
+  return CPATTN_OK;
+}
+
+int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out, int B, int Hq,
+               int Hkv, int Smax, int D, cudaStream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Smax < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, Hq, Hkv, Smax must be >= 1");
+  if (Hq % Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Hq / Hkv > 16) return fail(CPATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16", Hq / Hkv);
+  if (D != 64 && D != 128) return fail(CPATTN_ERR_UNSUPPORTED, "decode head dim %d not in {64, 128}", D);
+  if (!lens) return fail(CPATTN_ERR_INVALID_ARG, "null lens");
+  int rc = check_ptrs({q, kcache, vcache, out});
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds;
+  if ((rc = get_state(&ds))) return rc;
+  if ((rc = need_sm103(*ds))) return rc;
+  if ((rc = ensure(ds->dec_o, decode_part_o_floats(B, Hq, Hkv, Smax, D), stream, false))) return rc;
+  if ((rc = ensure(ds->dec_ml, decode_part_ml_floats(B, Hq, Hkv, Smax), stream, false))) return rc;
+  if ((rc = ensure(ds->dec_cnt, (size_t)B * Hkv, stream, true))) return rc;
+  DecodeArgs a{q, kcache, vcache, lens, out, B, Hq, Hkv, Smax, D, ds->dec_o.ptr, ds->dec_ml.ptr, ds->dec_cnt.ptr,
+               ds->err};
+  cudaError_t e = launch_gqa_decode(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gqa_decode launch");
+  return CPATTN_OK;
+}
+
+int cp_lb_positions(int S, int cp, int load_balance, int* pos_host) {
+  if (!pos_host) return fail(CPATTN_ERR_INVALID_ARG, "null pos_host");
+  if (S < 1 || cp < 1) return fail(CPATTN_ERR_INVALID_ARG, "S and cp must be >= 1");
+  if (load_balance && S % (2 * cp)) return fail(CPATTN_ERR_INVALID_ARG, "S must be a multiple of 2*cp");
+  const PosMap pm = PosMap::make(S, cp, load_balance);
+  for (int j = 0; j < S; ++j) pos_host[j] = pm.pos(j);
+  return CPATTN_OK;
+}
+
+int cp_attn_tile_counts(int S, int cp, int load_balance, long long* per_shard_host) {
+  if (!per_shard_host) return fail(CPATTN_ERR_INVALID_ARG, "null per_shard_host");
+  if (S < 1 || cp < 1 || S % cp) return fail(CPATTN_ERR_INVALID_ARG, "need S >= 1, cp >= 1, S %% cp == 0");
+  if (load_balance && S % (2 * cp)) return fail(CPATTN_ERR_INVALID_ARG, "S must be a multiple of 2*cp");
+  const PosMap pm = PosMap::make(S, cp, load_balance);
+  const int nqt = (S + kTile - 1) / kTile;
+  const int per = S / cp;
+  for (int s = 0; s < cp; ++s) per_shard_host[s] = 0;
+  for (int qt = 0; qt < nqt; ++qt) {
+    const int s = std::min(cp - 1, (qt * kTile) / per);
+    per_shard_host[s] += count_kv_tiles(pm, tile_max_pos(pm, qt, kTile));
+  }
+  return CPATTN_OK;
+}
+
+int cp_attn_check_device(cudaStream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds;
+  int rc = get_state(&ds);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+  if (word == DEV_OK) return CPATTN_OK;
+  cudaMemset(ds->err, 0, sizeof(int));
+  if (word == DEV_TIMEOUT) return fail(CPATTN_ERR_DEVICE_TIMEOUT, "a kernel pipeline wait timed out");
+  if (word == DEV_LENS_CLAMPED) return fail(CPATTN_ERR_DEVICE_BOUNDS, "decode lens outside [0, Smax] were clamped");
+  return fail(CPATTN_ERR_CUDA, "unknown device error %d", word);
+}
+
+const char* cp_attn_last_error(void) { return g_last_error.c_str(); }
+
+int cp_attn_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(CPATTN_ERR_CUDA, "cudaGetDevice failed");
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) return CPATTN_OK;
+  cudaDeviceSynchronize();
+  DevState& s = it->second;
+  for (auto& kv : s.fwd_units) cudaFree(kv.second.ptr);
+  for (auto& kv : s.bwd_units) cudaFree(kv.second.ptr);
+  cudaFree(s.bwd_stats.ptr);
+  cudaFree(s.dec_o.ptr);
+  cudaFree(s.dec_ml.ptr);
+  cudaFree(s.dec_cnt.ptr);
+  cudaFree(s.err);
+  g_dev.erase(it);
+  return CPATTN_OK;
+}
+
+}  // extern "C"

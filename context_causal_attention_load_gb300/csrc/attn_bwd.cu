@@ -1,0 +1,737 @@
+// Flash backward of load-balanced context-parallel causal attention on
+// tcgen05 tensor cores.
+//
+// The pages train with context parallelism ("Add context parallelism",
+// MaxText pull request 1445, Tests: training runs; "rename context to
+// context_autoregressive", Tests: separate flash block sizes for the dq and
+// dkv passes) but give no formula; this is the textbook gradient of
+// out = softmax(scale q k^T + mask) v under the reordered causal mask
+// (query slot i sees key slot j iff pos(j) <= pos(i)):
+//   D = rowsum(dO * O),  P = exp(scale q k^T - lse),  dV = P^T dO,
+//   dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+// dK/dV of a KV head sum over the query heads of its group and over every
+// shard (the transpose of the K/V all-gather).
+//
+// Three launches, none of them with atomics (results are deterministic):
+//  * preprocess: D and lse*log2(e) per query row, padded to 128 rows;
+//  * dK/dV kernel, key-stationary: a CTA owns a 128-row key tile of one KV
+//    head and walks every (query head of the group, 64-row query tile) that
+//    can see it.  S^T = K Q^T and dP^T = V dO^T land in TMEM (128 key lanes
+//    x 64 query columns, double buffered so the tensor core computes step
+//    i+1 while the element-wise warps turn step i into P^T and dS^T, which
+//    are written back to TMEM as bf16 and feed dV += P^T dO and
+//    dK += dS^T Q straight from TMEM;
+//  * dQ kernel, query-stationary: a CTA owns a 128-row query tile of one
+//    head and walks the 64-row key tiles it sees; S = Q K^T and dP = dO V^T
+//    in TMEM, dS back to TMEM as bf16, dQ += dS K.
+// Warp roles as in the forward: warps 0-7 element-wise (two groups, each
+// half of the columns), warp 8 TMA producer, warp 9 MMA issuer.
+#include "common.cuh"
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int TK = 128;  // key rows per dk/dv unit; query rows per dq unit
+
+__device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
+  return r * ncta + ((r & 1) ? (ncta - 1 - cta) : cta);
+}
+
+// ============================================================================
+// preprocess: lse_l2 = lse*log2(e) (+inf past S), delta = rowsum(dO*O) (0 past S)
+// layout [B, Hq, Spad]; one warp per (b, s, h) row
+// ============================================================================
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
+                                                             const __nv_bfloat16* __restrict__ dout,
+                                                             const float* __restrict__ lse, float* lse_l2,
+                                                             float* delta, AttnShape sh, int Spad) {
+  const long long nrows = (long long)sh.B * Spad * sh.Hq;
+  const int lane = threadIdx.x & 31;
+  for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nrows;
+       w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int h = int(w % sh.Hq);
+    const long long bs = w / sh.Hq;
+    const int s = int(bs % Spad);
+    const int b = int(bs / Spad);
+    const size_t o_idx = ((size_t)b * sh.Hq + h) * Spad + s;
+    if (s >= sh.S) {
+      if (lane == 0) {
+        lse_l2[o_idx] = INFINITY;
+        delta[o_idx] = 0.f;
+      }
+      continue;
+    }
+    const size_t base = (((size_t)b * sh.S + s) * sh.Hq + h) * sh.Dv;
+    float acc = 0.f;
+    for (int d = lane * 2; d < sh.Dv; d += 64) {
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(out + base + d);
+      const uint32_t g = *reinterpret_cast<const uint32_t*>(dout + base + d);
+      acc = fmaf(bf16lo(a), bf16lo(g), acc);
+      acc = fmaf(bf16hi(a), bf16hi(g), acc);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      delta[o_idx] = acc;
+      lse_l2[o_idx] = lse[((size_t)b * sh.Hq + h) * sh.S + s] * 1.4426950408889634f;
+    }
+  }
+}
+
+// ============================================================================
+// dK / dV
+// ============================================================================
+template <int DQK, int DV, int NBUF>
+struct KvCfg {
+  static constexpr int BQ = 64;
+  static constexpr int NQ = DQK == 192 ? 3 : 4;  // query stages
+  static constexpr int K_BYTES = TK * DQK * 2;
+  static constexpr int V_BYTES = TK * DV * 2;
+  static constexpr int QT_BYTES = BQ * DQK * 2;
+  static constexpr int DO_BYTES = BQ * DV * 2;
+  static constexpr int VEC_BYTES = BQ * 4;
+  static constexpr int ST_Q = 0;
+  static constexpr int ST_DO = QT_BYTES;
+  static constexpr int ST_LSE = ST_DO + DO_BYTES;
+  static constexpr int ST_DEL = ST_LSE + VEC_BYTES;
+  static constexpr int ST_POS = ST_DEL + VEC_BYTES;
+  static constexpr int STAGE = (ST_POS + VEC_BYTES + 1023) / 1024 * 1024;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = K_BYTES;
+  static constexpr int OFF_ST = OFF_V + V_BYTES;
+  static constexpr int OFF_BAR = OFF_ST + NQ * STAGE;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  // TMEM columns
+  static constexpr int T_S = 0;                  // S^T / P^T, buffer b at b*BQ
+  static constexpr int T_DP = NBUF * BQ;         // dP^T / dS^T
+  static constexpr int T_DV = 2 * NBUF * BQ;
+  static constexpr int T_DK = T_DV + DV;
+  static_assert(T_DK + DQK <= 512, "TMEM budget");
+};
+
+struct KvBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[4], q_empty[4];
+  uint64_t sd_full[2], ew_full[2];
+  uint64_t acc_full;
+  uint64_t done;
+};
+
+template <int DQK, int DV, int NBUF>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+  using C = KvCfg<DQK, DV, NBUF>;
+  constexpr int BQ = C::BQ;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  KvBars& bar = *reinterpret_cast<KvBars*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PosMap pm = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb);
+  const Abort ab{abort_flag, a.err};
+  const int G = a.sh.Hq / a.sh.Hkv;
+
+  if (tid == 0) {
+    mbar_init(&bar.kv_full, 1);
+    mbar_init(&bar.kv_empty, 1);
+    for (int i = 0; i < C::NQ; ++i) { mbar_init(&bar.q_full[i], 1); mbar_init(&bar.q_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.sd_full[i], 1); mbar_init(&bar.ew_full[i], 256); }
+    mbar_init(&bar.acc_full, 1);
+    mbar_init(&bar.done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (warp == 8 && lane == 0) { prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tdo); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ncta = gridDim.x, cta = blockIdx.x;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer (whole warp)
+    int qs = 0, qph = 0, kvph = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int ui = unit_index(r, cta, ncta);
+      if (ui >= a.n_units) break;
+      const BwdUnit u = a.units[ui];
+      if (lane == 0) {
+        ok = mbar_wait(&bar.kv_empty, kvph ^ 1, ab);
+        if (ok) {
+          mbar_expect_tx(&bar.kv_full, C::K_BYTES + C::V_BYTES);
+          for (int bx = 0; bx < DQK / 64; ++bx)
+            tma_load_4d(smem + C::OFF_K + bx * TK * 128, &a.tk, &bar.kv_full, bx * 64, u.h, u.t * TK, u.b);
+          for (int bx = 0; bx < DV / 64; ++bx)
+            tma_load_4d(smem + C::OFF_V + bx * TK * 128, &a.tv, &bar.kv_full, bx * 64, u.h, u.t * TK, u.b);
+        }
+      }
+      kvph ^= 1;
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      int kmin, kmax;
+      pm.range(u.t * TK, u.t * TK + TK, kmin, kmax);
+      for (int hq = u.h * G; hq < u.h * G + G && ok; ++hq) {
+        for (int qt = next_q_tile(pm, BQ, -1, kmin); qt >= 0; qt = next_q_tile(pm, BQ, qt, kmin)) {
+          if (lane == 0) ok = mbar_wait(&bar.q_empty[qs], qph ^ 1, ab);
+          if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+          unsigned char* st = smem + C::OFF_ST + qs * C::STAGE;
+          int* qp = reinterpret_cast<int*>(st + C::ST_POS);
+          for (int i = lane; i < BQ; i += 32) {
+            const int s = qt * BQ + i;
+            qp[i] = s < pm.S ? pm.pos(s) : -1;
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_expect_tx(&bar.q_full[qs], C::QT_BYTES + C::DO_BYTES + 2 * C::VEC_BYTES);
+            for (int bx = 0; bx < DQK / 64; ++bx)
+              tma_load_4d(st + C::ST_Q + bx * BQ * 128, &a.tq, &bar.q_full[qs], bx * 64, hq, qt * BQ, u.b);
+            for (int bx = 0; bx < DV / 64; ++bx)
+              tma_load_4d(st + C::ST_DO + bx * BQ * 128, &a.tdo, &bar.q_full[qs], bx * 64, hq, qt * BQ, u.b);
+            const size_t vo = ((size_t)u.b * a.sh.Hq + hq) * a.Spad + (size_t)qt * BQ;
+            bulk_load(st + C::ST_LSE, a.lse_l2 + vo, C::VEC_BYTES, &bar.q_full[qs]);
+            bulk_load(st + C::ST_DEL, a.delta + vo, C::VEC_BYTES, &bar.q_full[qs]);
+          }
+          if (++qs == C::NQ) { qs = 0; qph ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(TK, BQ, 0, 0);   // S^T, dP^T: K-major x K-major
+      constexpr uint32_t IDESC_DV = idesc_bf16(TK, DV, 0, 1);  // P^T(tmem) x dO (MN-major)
+      constexpr uint32_t IDESC_DK = idesc_bf16(TK, DQK, 0, 1); // dS^T(tmem) x Q (MN-major)
+      const uint32_t sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      const uint32_t sSt = smem_u32(smem + C::OFF_ST);
+      int qs = 0, qph = 0, kvph = 0;
+      int ewph[2] = {0, 0};
+      bool ok = true;
+
+      auto issue_sdp = [&](int buf, int stage) {
+        const uint32_t st = sSt + stage * C::STAGE;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sK + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(st + C::ST_Q + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + C::T_S + buf * BQ, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sV + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(st + C::ST_DO + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + C::T_DP + buf * BQ, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_acc = [&](int buf, int stage, bool acc) {
+        const uint32_t st = sSt + stage * C::STAGE;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint64_t bdo = sdesc_sw128(st + C::ST_DO + kk * 16 * 128, BQ * 128, 1024);
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + buf * BQ + kk * 8, bdo, IDESC_DV, (acc || kk > 0) ? 1u : 0u);
+          const uint64_t bq = sdesc_sw128(st + C::ST_Q + kk * 16 * 128, BQ * 128, 1024);
+          mma_ts(tmem + C::T_DK, tmem + C::T_DP + buf * BQ + kk * 8, bq, IDESC_DK, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int r = 0; ok; ++r) {
+        const int ui = unit_index(r, cta, ncta);
+        if (ui >= a.n_units) break;
+        const BwdUnit u = a.units[ui];
+        if (!(ok = mbar_wait(&bar.kv_full, kvph, ab))) break;
+        kvph ^= 1;
+        tc_fence_after();
+        int kmin, kmax;
+        pm.range(u.t * TK, u.t * TK + TK, kmin, kmax);
+        // flatten (head, query tile) steps; step i uses buffer i % NBUF and ring stage
+        int hq = u.h * G, qt = next_q_tile(pm, BQ, -1, kmin);
+        auto advance = [&](int& h_, int& t_) {
+          t_ = next_q_tile(pm, BQ, t_, kmin);
+          if (t_ < 0 && ++h_ < u.h * G + G) t_ = next_q_tile(pm, BQ, -1, kmin);
+        };
+        int cur_stage = qs;
+        if (!(ok = mbar_wait(&bar.q_full[qs], qph, ab))) break;
+        tc_fence_after();
+        issue_sdp(0, qs);
+        mma_commit(&bar.sd_full[0]);
+        if (++qs == C::NQ) { qs = 0; qph ^= 1; }
+        for (int i = 0; ok; ++i) {
+          int nh = hq, nt = qt;
+          advance(nh, nt);
+          const bool has_next = nh < u.h * G + G && nt >= 0;
+          int next_stage = qs;
+          if (NBUF == 2 && has_next) {
+            if (!(ok = mbar_wait(&bar.q_full[qs], qph, ab))) break;
+            tc_fence_after();
+            issue_sdp((i + 1) & 1, qs);
+            mma_commit(&bar.sd_full[(i + 1) & 1]);
+            if (++qs == C::NQ) { qs = 0; qph ^= 1; }
+          }
+          const int buf = NBUF == 2 ? (i & 1) : 0;
+          if (!(ok = mbar_wait(&bar.ew_full[buf], ewph[buf], ab))) break;
+          ewph[buf] ^= 1;
+          tc_fence_after();
+          issue_acc(buf, cur_stage, i > 0);
+          mma_commit(&bar.q_empty[cur_stage]);
+          if (!has_next) break;
+          if (NBUF == 1) {
+            if (!(ok = mbar_wait(&bar.q_full[qs], qph, ab))) break;
+            tc_fence_after();
+            issue_sdp(0, qs);
+            mma_commit(&bar.sd_full[0]);
+            if (++qs == C::NQ) { qs = 0; qph ^= 1; }
+          }
+          cur_stage = next_stage;
+          hq = nh;
+          qt = nt;
+        }
+        if (!ok) break;
+        mma_commit(&bar.acc_full);
+        mma_commit(&bar.kv_empty);
+      }
+      mma_commit(&bar.done);
+      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise groups
+    const int g = warp >> 2;              // column half
+    const int row = tid & 127;            // key row == TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    constexpr int HC = BQ / 2;            // query columns per group (32)
+    const float sl2 = a.scale_log2;
+    int qs = 0, qph = 0, acc_ph = 0;
+    int sdph[2] = {0, 0};
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int ui = unit_index(r, cta, ncta);
+      if (ui >= a.n_units) break;
+      const BwdUnit u = a.units[ui];
+      const int kslot = u.t * TK + row;
+      const bool kvalid = kslot < pm.S;
+      const int kpos = kvalid ? pm.pos(kslot) : 0x7fffffff;
+      int kmin, kmax;
+      pm.range(u.t * TK, u.t * TK + TK, kmin, kmax);
+      const bool k_inside = u.t * TK + TK <= pm.S;
+      int i = 0;
+      for (int hq = u.h * G; hq < u.h * G + G && ok; ++hq) {
+        for (int qt = next_q_tile(pm, BQ, -1, kmin); qt >= 0; qt = next_q_tile(pm, BQ, qt, kmin), ++i) {
+          const int buf = NBUF == 2 ? (i & 1) : 0;
+          ok = mbar_wait(&bar.q_full[qs], qph, ab);
+          if (ok) ok = mbar_wait(&bar.sd_full[buf], sdph[buf], ab);
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          sdph[buf] ^= 1;
+          tc_fence_after();
+          const unsigned char* st = smem + C::OFF_ST + qs * C::STAGE;
+          const float* lse_s = reinterpret_cast<const float*>(st + C::ST_LSE) + g * HC;
+          const float* del_s = reinterpret_cast<const float*>(st + C::ST_DEL) + g * HC;
+          const int* qp_s = reinterpret_cast<const int*>(st + C::ST_POS) + g * HC;
+          int qmin, qmax;
+          pm.range(qt * BQ, qt * BQ + BQ, qmin, qmax);
+          const bool full = (kmax <= qmin) && k_inside;
+          uint32_t sv[32], dp[32];
+          tmem_ld32(tmem + lane_base + C::T_S + buf * BQ + g * HC, sv);
+          tmem_ld32(tmem + lane_base + C::T_DP + buf * BQ + g * HC, dp);
+          tmem_ld_wait();
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int c = 0; c < HC; c += 2) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse_s[c]));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse_s[c + 1]));
+            if (!full) {
+              p0 = (kpos <= qp_s[c]) ? p0 : 0.f;
+              p1 = (kpos <= qp_s[c + 1]) ? p1 : 0.f;
+            }
+            const float d0 = p0 * (__uint_as_float(dp[c]) - del_s[c]);
+            const float d1 = p1 * (__uint_as_float(dp[c + 1]) - del_s[c + 1]);
+            pk[c >> 1] = pack_bf16(p0, p1);
+            dk[c >> 1] = pack_bf16(d0, d1);
+          }
+          tmem_st16(tmem + lane_base + C::T_S + buf * BQ + g * (HC / 2), pk);
+          tmem_st16(tmem + lane_base + C::T_DP + buf * BQ + g * (HC / 2), dk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bar.ew_full[buf]);
+          if (++qs == C::NQ) { qs = 0; qph ^= 1; }
+        }
+      }
+      if (!ok) break;
+      // epilogue: dV and scale*dK for this key tile, this group's column half
+      ok = mbar_wait(&bar.acc_full, acc_ph, ab);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      acc_ph ^= 1;
+      tc_fence_after();
+      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) + (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * DV;
+      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) + (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * DQK;
+#pragma unroll 1
+      for (int c0 = g * (DV / 2); c0 < (g + 1) * (DV / 2); c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + C::T_DV + c0, o);
+        tmem_ld_wait();
+        if (kvalid) {
+          uint4* dst = reinterpret_cast<uint4*>(dvp + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pack_bf16(__uint_as_float(o[8 * v4 + 0]), __uint_as_float(o[8 * v4 + 1])),
+                                 pack_bf16(__uint_as_float(o[8 * v4 + 2]), __uint_as_float(o[8 * v4 + 3])),
+                                 pack_bf16(__uint_as_float(o[8 * v4 + 4]), __uint_as_float(o[8 * v4 + 5])),
+                                 pack_bf16(__uint_as_float(o[8 * v4 + 6]), __uint_as_float(o[8 * v4 + 7])));
+        }
+      }
+      const float sc = a.scale;
+#pragma unroll 1
+      for (int c0 = g * (DQK / 2); c0 < (g + 1) * (DQK / 2); c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + C::T_DK + c0, o);
+        tmem_ld_wait();
+        if (kvalid) {
+          uint4* dst = reinterpret_cast<uint4*>(dkp + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pack_bf16(sc * __uint_as_float(o[8 * v4 + 0]), sc * __uint_as_float(o[8 * v4 + 1])),
+                                 pack_bf16(sc * __uint_as_float(o[8 * v4 + 2]), sc * __uint_as_float(o[8 * v4 + 3])),
+                                 pack_bf16(sc * __uint_as_float(o[8 * v4 + 4]), sc * __uint_as_float(o[8 * v4 + 5])),
+                                 pack_bf16(sc * __uint_as_float(o[8 * v4 + 6]), sc * __uint_as_float(o[8 * v4 + 7])));
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================
+// dQ
+// ============================================================================
+template <int DQK, int DV>
+struct QCfg {
+  static constexpr int BK = 64;
+  static constexpr int NS = DQK == 192 ? 3 : 4;  // key/value stages
+  static constexpr int Q_BYTES = TK * DQK * 2;
+  static constexpr int DO_BYTES = TK * DV * 2;
+  static constexpr int K_BYTES = BK * DQK * 2;
+  static constexpr int V_BYTES = BK * DV * 2;
+  static constexpr int ST_K = 0;
+  static constexpr int ST_V = K_BYTES;
+  static constexpr int ST_POS = ST_V + V_BYTES;
+  static constexpr int STAGE = (ST_POS + BK * 4 + 1023) / 1024 * 1024;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = Q_BYTES;
+  static constexpr int OFF_ST = OFF_DO + DO_BYTES;
+  static constexpr int OFF_BAR = OFF_ST + NS * STAGE;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static constexpr int T_S = 0;        // S / dS (bf16), buffer b at b*BK
+  static constexpr int T_DP = 2 * BK;  // dP
+  static constexpr int T_DQ = 4 * BK;
+  static_assert(T_DQ + DQK <= 512, "TMEM budget");
+};
+
+struct QBars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[4], kv_empty[4];
+  uint64_t sd_full[2], ew_full[2];
+  uint64_t acc_full;
+  uint64_t done;
+};
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+  using C = QCfg<DQK, DV>;
+  constexpr int BK = C::BK;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  QBars& bar = *reinterpret_cast<QBars*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PosMap pm = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb);
+  const Abort ab{abort_flag, a.err};
+  const int G = a.sh.Hq / a.sh.Hkv;
+
+  if (tid == 0) {
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_empty, 1);
+    for (int i = 0; i < C::NS; ++i) { mbar_init(&bar.kv_full[i], 1); mbar_init(&bar.kv_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.sd_full[i], 1); mbar_init(&bar.ew_full[i], 256); }
+    mbar_init(&bar.acc_full, 1);
+    mbar_init(&bar.done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (warp == 8 && lane == 0) { prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tdo); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ncta = gridDim.x, cta = blockIdx.x;
+
+  auto q_bound = [&](const BwdUnit& u) {
+    int mn, mx;
+    pm.range(u.t * TK, u.t * TK + TK, mn, mx);
+    return mx;
+  };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer (whole warp)
+    int ks = 0, kph = 0, qph = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int ui = unit_index(r, cta, ncta);
+      if (ui >= a.n_units) break;
+      const BwdUnit u = a.units[ui];
+      const int hkv = u.h / G;
+      if (lane == 0) {
+        ok = mbar_wait(&bar.q_empty, qph ^ 1, ab);
+        if (ok) {
+          mbar_expect_tx(&bar.q_full, C::Q_BYTES + C::DO_BYTES);
+          for (int bx = 0; bx < DQK / 64; ++bx)
+            tma_load_4d(smem + C::OFF_Q + bx * TK * 128, &a.tq, &bar.q_full, bx * 64, u.h, u.t * TK, u.b);
+          for (int bx = 0; bx < DV / 64; ++bx)
+            tma_load_4d(smem + C::OFF_DO + bx * TK * 128, &a.tdo, &bar.q_full, bx * 64, u.h, u.t * TK, u.b);
+        }
+      }
+      qph ^= 1;
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      const int bound = q_bound(u);
+      for (int kt = next_kv_tile(pm, BK, -1, bound); kt >= 0; kt = next_kv_tile(pm, BK, kt, bound)) {
+        if (lane == 0) ok = mbar_wait(&bar.kv_empty[ks], kph ^ 1, ab);
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        unsigned char* st = smem + C::OFF_ST + ks * C::STAGE;
+        int* kp = reinterpret_cast<int*>(st + C::ST_POS);
+        for (int i = lane; i < BK; i += 32) {
+          const int s = kt * BK + i;
+          kp[i] = s < pm.S ? pm.pos(s) : 0x7fffffff;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(&bar.kv_full[ks], C::K_BYTES + C::V_BYTES);
+          for (int bx = 0; bx < DQK / 64; ++bx)
+            tma_load_4d(st + C::ST_K + bx * BK * 128, &a.tk, &bar.kv_full[ks], bx * 64, hkv, kt * BK, u.b);
+          for (int bx = 0; bx < DV / 64; ++bx)
+            tma_load_4d(st + C::ST_V + bx * BK * 128, &a.tv, &bar.kv_full[ks], bx * 64, hkv, kt * BK, u.b);
+        }
+        if (++ks == C::NS) { ks = 0; kph ^= 1; }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(TK, BK, 0, 0);
+      constexpr uint32_t IDESC_DQ = idesc_bf16(TK, DQK, 0, 1);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+      const uint32_t sDO = smem_u32(smem + C::OFF_DO);
+      const uint32_t sSt = smem_u32(smem + C::OFF_ST);
+      int ks = 0, kph = 0, qph = 0;
+      int ewph[2] = {0, 0};
+      bool ok = true;
+      auto issue_sdp = [&](int buf, int stage) {
+        const uint32_t st = sSt + stage * C::STAGE;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(st + C::ST_K + (kk >> 2) * (BK * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + C::T_S + buf * BK, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sDO + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(st + C::ST_V + (kk >> 2) * (BK * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + C::T_DP + buf * BK, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_dq = [&](int buf, int stage, bool acc) {
+        const uint32_t st = sSt + stage * C::STAGE;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(st + C::ST_K + kk * 16 * 128, BK * 128, 1024);
+          mma_ts(tmem + C::T_DQ, tmem + C::T_S + buf * BK + kk * 8, bd, IDESC_DQ, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int r = 0; ok; ++r) {
+        const int ui = unit_index(r, cta, ncta);
+        if (ui >= a.n_units) break;
+        const BwdUnit u = a.units[ui];
+        const int bound = q_bound(u);
+        if (!(ok = mbar_wait(&bar.q_full, qph, ab))) break;
+        qph ^= 1;
+        tc_fence_after();
+        int kt = next_kv_tile(pm, BK, -1, bound);
+        int cur_stage = ks;
+        if (!(ok = mbar_wait(&bar.kv_full[ks], kph, ab))) break;
+        tc_fence_after();
+        issue_sdp(0, ks);
+        mma_commit(&bar.sd_full[0]);
+        if (++ks == C::NS) { ks = 0; kph ^= 1; }
+        for (int i = 0; ok; ++i) {
+          const int nkt = next_kv_tile(pm, BK, kt, bound);
+          const int next_stage = ks;
+          if (nkt >= 0) {
+            if (!(ok = mbar_wait(&bar.kv_full[ks], kph, ab))) break;
+            tc_fence_after();
+            issue_sdp((i + 1) & 1, ks);
+            mma_commit(&bar.sd_full[(i + 1) & 1]);
+            if (++ks == C::NS) { ks = 0; kph ^= 1; }
+          } else {
+            mma_commit(&bar.q_empty);  // every S/dP MMA (the readers of Q and dO) is already issued
+          }
+          const int buf = i & 1;
+          if (!(ok = mbar_wait(&bar.ew_full[buf], ewph[buf], ab))) break;
+          ewph[buf] ^= 1;
+          tc_fence_after();
+          issue_dq(buf, cur_stage, i > 0);
+          mma_commit(&bar.kv_empty[cur_stage]);
+          if (nkt < 0) break;
+          cur_stage = next_stage;
+          kt = nkt;
+        }
+        if (!ok) break;
+        mma_commit(&bar.acc_full);
+      }
+      mma_commit(&bar.done);
+      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise groups
+    const int g = warp >> 2;
+    const int row = tid & 127;  // query row == TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    constexpr int HC = BK / 2;  // key columns per group
+    const float sl2 = a.scale_log2;
+    int ks = 0, kph = 0, acc_ph = 0;
+    int sdph[2] = {0, 0};
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int ui = unit_index(r, cta, ncta);
+      if (ui >= a.n_units) break;
+      const BwdUnit u = a.units[ui];
+      const int bound = q_bound(u);
+      const int qslot = u.t * TK + row;
+      const bool qvalid = qslot < pm.S;
+      const int qpos = qvalid ? pm.pos(qslot) : -1;
+      const size_t vo = ((size_t)u.b * a.sh.Hq + u.h) * a.Spad + qslot;
+      const float lse2 = a.lse_l2[vo];
+      const float del = a.delta[vo];
+      int qmin, qmax;
+      pm.range(u.t * TK, u.t * TK + TK, qmin, qmax);
+      int i = 0;
+      for (int kt = next_kv_tile(pm, BK, -1, bound); kt >= 0; kt = next_kv_tile(pm, BK, kt, bound), ++i) {
+        const int buf = i & 1;
+        ok = mbar_wait(&bar.kv_full[ks], kph, ab);
+        if (ok) ok = mbar_wait(&bar.sd_full[buf], sdph[buf], ab);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        sdph[buf] ^= 1;
+        tc_fence_after();
+        const int* kp_s = reinterpret_cast<const int*>(smem + C::OFF_ST + ks * C::STAGE + C::ST_POS) + g * HC;
+        int kmin, kmax;
+        pm.range(kt * BK, kt * BK + BK, kmin, kmax);
+        const bool full = (kmax <= qmin) && (kt * BK + BK <= pm.S);
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tmem + lane_base + C::T_S + buf * BK + g * HC, sv);
+        tmem_ld32(tmem + lane_base + C::T_DP + buf * BK + g * HC, dp);
+        tmem_ld_wait();
+        uint32_t dk[16];
+#pragma unroll
+        for (int c = 0; c < HC; c += 2) {
+          float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse2));
+          float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2));
+          if (!full) {
+            p0 = (kp_s[c] <= qpos) ? p0 : 0.f;
+            p1 = (kp_s[c + 1] <= qpos) ? p1 : 0.f;
+          }
+          dk[c >> 1] = pack_bf16(p0 * (__uint_as_float(dp[c]) - del), p1 * (__uint_as_float(dp[c + 1]) - del));
+        }
+        tmem_st16(tmem + lane_base + C::T_S + buf * BK + g * (HC / 2), dk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar.ew_full[buf]);
+        if (++ks == C::NS) { ks = 0; kph ^= 1; }
+      }
+      if (!ok) break;
+      ok = mbar_wait(&bar.acc_full, acc_ph, ab);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      acc_ph ^= 1;
+      tc_fence_after();
+      __nv_bfloat16* dqp = static_cast<__nv_bfloat16*>(a.dq) + (((size_t)u.b * pm.S + (qvalid ? qslot : 0)) * a.sh.Hq + u.h) * DQK;
+      const float sc = a.scale;
+#pragma unroll 1
+      for (int c0 = g * (DQK / 2); c0 < (g + 1) * (DQK / 2); c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + C::T_DQ + c0, o);
+        tmem_ld_wait();
+        if (qvalid) {
+          uint4* dst = reinterpret_cast<uint4*>(dqp + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pack_bf16(sc * __uint_as_float(o[8 * v4 + 0]), sc * __uint_as_float(o[8 * v4 + 1])),
+                                 pack_bf16(sc * __uint_as_float(o[8 * v4 + 2]), sc * __uint_as_float(o[8 * v4 + 3])),
+                                 pack_bf16(sc * __uint_as_float(o[8 * v4 + 4]), sc * __uint_as_float(o[8 * v4 + 5])),
+                                 pack_bf16(sc * __uint_as_float(o[8 * v4 + 6]), sc * __uint_as_float(o[8 * v4 + 7])));
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename K>
+cudaError_t launch_k(K kern, int smem, int grid, const BwdArgs& a, cudaStream_t st) {
+  // more than half of an SM's shared memory: one CTA per SM, so the CTA's
+  // 512-column TMEM allocation never waits for a neighbour
+  if (smem < 120 * 1024) smem = 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int bwd_dkdv_q_tile(int) { return 64; }
+int bwd_dq_kv_tile(int) { return 64; }
+
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, float* lse_l2, float* delta,
+                                  const AttnShape& sh, int Spad, cudaStream_t st) {
+  const long long rows = (long long)sh.B * Spad * sh.Hq;
+  long long blocks = (rows * 32 + 255) / 256;
+  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  bwd_preprocess_kernel<<<(int)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
+                                                     static_cast<const __nv_bfloat16*>(dout), lse, lse_l2, delta, sh,
+                                                     Spad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, int grid, cudaStream_t st) {
+  if (a.sh.Dqk == 64) return launch_k(attn_bwd_dkdv_kernel<64, 64, 2>, KvCfg<64, 64, 2>::SMEM, grid, a, st);
+  if (a.sh.Dqk == 128) return launch_k(attn_bwd_dkdv_kernel<128, 128, 2>, KvCfg<128, 128, 2>::SMEM, grid, a, st);
+  return launch_k(attn_bwd_dkdv_kernel<192, 128, 1>, KvCfg<192, 128, 1>::SMEM, grid, a, st);
+}
+
+cudaError_t launch_attn_bwd_dq(const BwdArgs& a, int grid, cudaStream_t st) {
+  if (a.sh.Dqk == 64) return launch_k(attn_bwd_dq_kernel<64, 64>, QCfg<64, 64>::SMEM, grid, a, st);
+  if (a.sh.Dqk == 128) return launch_k(attn_bwd_dq_kernel<128, 128>, QCfg<128, 128>::SMEM, grid, a, st);
+  return launch_k(attn_bwd_dq_kernel<192, 128>, QCfg<192, 128>::SMEM, grid, a, st);
+}
+
+}  // namespace cpattn

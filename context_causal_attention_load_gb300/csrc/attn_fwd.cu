@@ -1,0 +1,453 @@
+// Flash forward of load-balanced context-parallel causal attention on
+// tcgen05 tensor cores.
+//
+// What it computes ("Add context parallelism", MaxText pull request 1445,
+// Description): every cp shard's queries attend to the whole gathered K/V;
+// tokens and the causal mask are reordered so that slot i sees slot j iff
+// pos(j) <= pos(i).  All shards run in one persistent launch as independent
+// work units.  MHA and MLA head layouts ("Add support for EP to context
+// parallelism in self-attention", Main code changes) and grouped KV heads.
+//
+// Work unit = two 128-row query tiles that read the same KV head (two heads
+// of a GQA group on the same rows, or two neighbouring row tiles of one
+// head).  Their KV tiles are the union of the tiles either one can see;
+// tiles every row of a query tile can see need no mask, tiles no row can see
+// are skipped (load balancing follows from the reorder: every shard visits
+// the same number of tiles).  Units are sorted heaviest first on the host
+// and dealt to the CTAs in snake order.
+//
+// CTA = 10 warps, one CTA per SM (all 512 TMEM columns):
+//   warps 0-3  softmax group 0 (query tile 0, one thread per row)
+//   warps 4-7  softmax group 1 (query tile 1)
+//   warp  8    TMA producer: Q tiles, then K and V tiles into two rings
+//   warp  9    MMA issuer (one thread): S_t = Q_t K^T into TMEM, and
+//              O_t += P_t V with P_t read straight from TMEM
+// TMEM columns: [t*256, t*256+128) = S_t, overwritten in place by P_t as
+// packed bf16 (64 columns); [t*256+128, t*256+128+Dv) = O_t.
+// The MMA thread interleaves the groups (PV_0, QK_0', PV_1, QK_1'), so one
+// group's softmax runs while the tensor core serves the other.  Online
+// softmax in the log2 domain with a lazy rescale: O_t is rescaled in TMEM
+// only when a row maximum grows by more than 8 (a factor 256).
+#include "common.cuh"
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // key rows per tile
+constexpr int kThreads = 320;
+
+template <int DQK, int DV>
+struct FwdCfg {
+  static constexpr int NK = DQK == 192 ? 2 : (DQK == 64 ? 4 : 2);
+  static constexpr int NV = DQK == 192 ? 1 : (DQK == 64 ? 4 : 2);
+  static constexpr int Q_BYTES = BM * DQK * 2;
+  static constexpr int K_BYTES = BN * DQK * 2;
+  static constexpr int V_BYTES = BN * DV * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NV * V_BYTES;
+  static constexpr int OFF_POS = OFF_BAR + 256;      // int kpos[2 groups][128]
+  static constexpr int OFF_MISC = OFF_POS + 2 * BN * 4;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t kpos[2];  // per softmax group: key-position table written
+  uint64_t done;
+};
+static_assert(sizeof(Bars) <= 256, "barrier area");
+
+__device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
+  // snake order over the heaviest-first list
+  return r * ncta + ((r & 1) ? (ncta - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ int kv_bound(const PosMap& pm, const FwdUnit& u) {
+  int mn, mx, mx2 = -1;
+  pm.range(u.t0 * BM, u.t0 * BM + BM, mn, mx);
+  if (u.h1 >= 0) pm.range(u.t1 * BM, u.t1 * BM + BM, mn, mx2);
+  return mx > mx2 ? mx : mx2;
+}
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdArgs a) {
+  using C = FwdCfg<DQK, DV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars& bar = *reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  int* kpos_s = reinterpret_cast<int*>(smem + C::OFF_POS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const PosMap pm = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb);
+  const Abort ab{abort_flag, a.err};
+
+  if (tid == 0) {
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_empty, 1);
+    for (int i = 0; i < C::NK; ++i) { mbar_init(&bar.k_full[i], 1); mbar_init(&bar.k_empty[i], 1); }
+    for (int i = 0; i < C::NV; ++i) { mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_empty[i], 1); }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar.s_full[t], 1);
+      mbar_init(&bar.p_full[t], 128);
+      mbar_init(&bar.o_full[t], 1);
+      mbar_init(&bar.kpos[t], 128);
+    }
+    mbar_init(&bar.done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && (tid & 31) == 0) {
+    prefetch_tmap(&a.tq);
+    prefetch_tmap(&a.tk);
+    prefetch_tmap(&a.tv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ncta = gridDim.x, cta = blockIdx.x;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if ((tid & 31) == 0) {
+      int ks = 0, kph = 0, vs = 0, vph = 0, qph = 0;
+      int kiss[4] = {-1, -1, -1, -1}, viss[4] = {-1, -1, -1, -1}, qiss = -1;  // parity of last issue
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int ui = unit_index(r, cta, ncta);
+        if (ui >= a.n_units) break;
+        const FwdUnit u = a.units[ui];
+        const bool has1 = u.h1 >= 0;
+        if (r > 0) {
+          if (!(ok = mbar_wait(&bar.q_empty, qph, ab))) break;
+          qph ^= 1;
+        }
+        mbar_expect_tx(&bar.q_full, (has1 ? 2 : 1) * C::Q_BYTES);
+        qiss = r & 1;
+        for (int bx = 0; bx < DQK / 64; ++bx)
+          tma_load_4d(smem + C::OFF_Q + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h0, u.t0 * BM, u.b);
+        if (has1)
+          for (int bx = 0; bx < DQK / 64; ++bx)
+            tma_load_4d(smem + C::OFF_Q + C::Q_BYTES + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h1,
+                        u.t1 * BM, u.b);
+        const int bound = kv_bound(pm, u);
+        for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0; kt = next_kv_tile(pm, BN, kt, bound)) {
+          if (!(ok = mbar_wait(&bar.k_empty[ks], kph ^ 1, ab))) break;
+          mbar_expect_tx(&bar.k_full[ks], C::K_BYTES);
+          kiss[ks] = kph;
+          for (int bx = 0; bx < DQK / 64; ++bx)
+            tma_load_4d(smem + C::OFF_K + ks * C::K_BYTES + bx * BN * 128, &a.tk, &bar.k_full[ks], bx * 64,
+                        u.hkv, kt * BN, u.b);
+          if (++ks == C::NK) { ks = 0; kph ^= 1; }
+          if (!(ok = mbar_wait(&bar.v_empty[vs], vph ^ 1, ab))) break;
+          mbar_expect_tx(&bar.v_full[vs], C::V_BYTES);
+          viss[vs] = vph;
+          for (int bx = 0; bx < DV / 64; ++bx)
+            tma_load_4d(smem + C::OFF_V + vs * C::V_BYTES + bx * BN * 128, &a.tv, &bar.v_full[vs], bx * 64,
+                        u.hkv, kt * BN, u.b);
+          if (++vs == C::NV) { vs = 0; vph ^= 1; }
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land (bounded) before the CTA exits
+        volatile int own = 0;
+        const Abort quiet{&own, a.err};
+        for (int i = 0; i < C::NK; ++i)
+          if (kiss[i] >= 0) mbar_wait(&bar.k_full[i], kiss[i], quiet);
+        for (int i = 0; i < C::NV; ++i)
+          if (viss[i] >= 0) mbar_wait(&bar.v_full[i], viss[i], quiet);
+        if (qiss >= 0) mbar_wait(&bar.q_full, qiss, quiet);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if ((tid & 31) == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, 0, 1);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+      const uint32_t sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      int ks = 0, kph = 0, vs = 0, vph = 0, qph = 0;
+      int pph[2] = {0, 0};
+      bool ok = true;
+
+      auto issue_qk = [&](int t, int kslot) {
+        const uint32_t d = tmem + t * 256;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sQ + t * C::Q_BYTES + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + kslot * C::K_BYTES + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int vslot, bool acc) {
+        const uint32_t d = tmem + t * 256 + 128;
+        const uint32_t p = tmem + t * 256;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(sV + vslot * C::V_BYTES + kk * 16 * 128, BN * 128, 1024);
+          mma_ts(d, p + kk * 8, bd, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int r = 0; ok; ++r) {
+        const int ui = unit_index(r, cta, ncta);
+        if (ui >= a.n_units) break;
+        const FwdUnit u = a.units[ui];
+        const bool has1 = u.h1 >= 0;
+        const int bound = kv_bound(pm, u);
+        if (!(ok = mbar_wait(&bar.q_full, qph, ab))) break;
+        qph ^= 1;
+        tc_fence_after();
+        int kt = next_kv_tile(pm, BN, -1, bound);
+        // prologue: S_0 and S_1 of the first key tile
+        if (!(ok = mbar_wait(&bar.k_full[ks], kph, ab))) break;
+        tc_fence_after();
+        issue_qk(0, ks);
+        mma_commit(&bar.s_full[0]);
+        if (has1) {
+          issue_qk(1, ks);
+          mma_commit(&bar.s_full[1]);
+        }
+        mma_commit(&bar.k_empty[ks]);
+        if (++ks == C::NK) { ks = 0; kph ^= 1; }
+        for (int j = 0; ok; ++j) {
+          const int nkt = next_kv_tile(pm, BN, kt, bound);
+          if (nkt < 0) mma_commit(&bar.q_empty);  // every QK of this unit is issued
+          if (!(ok = mbar_wait(&bar.v_full[vs], vph, ab))) break;
+          bool knext = false;
+          for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+            if (!(ok = mbar_wait(&bar.p_full[t], pph[t], ab))) break;
+            pph[t] ^= 1;
+            tc_fence_after();
+            issue_pv(t, vs, j > 0);
+            if (nkt < 0) mma_commit(&bar.o_full[t]);
+            if (nkt >= 0) {
+              if (!knext) {
+                if (!(ok = mbar_wait(&bar.k_full[ks], kph, ab))) break;
+                tc_fence_after();
+                knext = true;
+              }
+              issue_qk(t, ks);
+              mma_commit(&bar.s_full[t]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bar.v_empty[vs]);
+          if (++vs == C::NV) { vs = 0; vph ^= 1; }
+          if (nkt < 0) break;
+          mma_commit(&bar.k_empty[ks]);
+          if (++ks == C::NK) { ks = 0; kph ^= 1; }
+          kt = nkt;
+        }
+      }
+      // wait for every issued MMA before TMEM is released
+      mma_commit(&bar.done);
+      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+    }
+  } else {
+    // ------------------------------------------------------------ softmax groups
+    const int t = warp >> 2;          // group
+    const int row = tid & 127;        // query row in tile == TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + t * 256 + lane_base;
+    const uint32_t tO = tS + 128;
+    const float sl2 = a.scale_log2;
+    int sph = 0, oph = 0, kbph = 0;
+    bool ok = true;
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
+
+    for (int r = 0; ok; ++r) {
+      const int ui = unit_index(r, cta, ncta);
+      if (ui >= a.n_units) break;
+      const FwdUnit u = a.units[ui];
+      if (t == 1 && u.h1 < 0) continue;
+      const int h = t ? u.h1 : u.h0;
+      const int qt = t ? u.t1 : u.t0;
+      const int bound = kv_bound(pm, u);
+      const int qslot = qt * BM + row;
+      const bool qvalid = qslot < pm.S;
+      const int qpos = qvalid ? pm.pos(qslot) : -1;
+      int qmin, qmax;
+      pm.range(qt * BM, qt * BM + BM, qmin, qmax);
+
+      float m = -INFINITY, l = 0.f;
+      int j = 0;
+      for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0; kt = next_kv_tile(pm, BN, kt, bound), ++j) {
+        int kmin, kmax;
+        pm.range(kt * BN, kt * BN + BN, kmin, kmax);
+        const bool inside = kt * BN + BN <= pm.S;
+        const int cls = (kmin > qmax) ? 0 : ((kmax <= qmin && inside) ? 2 : 1);  // 0 none, 1 partial, 2 all
+        const int* kp = kpos_s + t * BN;
+        if (cls == 1) {
+          // table of the key tile's original positions, shared by the group
+          // (the group syncs again once every thread has read it)
+          const int ks = kt * BN + row;
+          kpos_s[t * BN + row] = ks < pm.S ? pm.pos(ks) : 0x7fffffff;
+          mbar_arrive(&bar.kpos[t]);
+          ok = mbar_wait(&bar.kpos[t], kbph, ab);
+          kbph ^= 1;
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        }
+        ok = mbar_wait(&bar.s_full[t], sph, ab);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        sph ^= 1;
+        tc_fence_after();
+        float rowsum = 0.f;
+        if (cls == 0) {
+          uint32_t z[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0u;
+          tmem_st32(tS + 0, z);
+          tmem_st32(tS + 32, z);
+        } else {
+          // pass 1: row maximum (masked), 32 columns at a time
+          float mx = -INFINITY;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t sr[32];
+            tmem_ld32(tS + q4 * 32, sr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float v = (cls == 1 && kp[q4 * 32 + i] > qpos) ? -INFINITY : __uint_as_float(sr[i]);
+              mx = fmaxf(mx, v);
+            }
+          }
+          mx *= sl2;
+          const float m_new = fmaxf(m, mx);
+          const bool need = (m == -INFINITY) ? (m_new != -INFINITY) : (m_new > m + 8.0f);
+          if (__any_sync(0xffffffffu, need && j > 0)) {
+            const float alpha = (need && m != -INFINITY) ? fast_exp2(m - m_new) : (need ? 0.f : 1.0f);
+#pragma unroll 1
+            for (int c0 = 0; c0 < DV; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tO + c0, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + c0, o);
+            }
+            tmem_st_wait();
+          }
+          if (need) {
+            l = (m == -INFINITY) ? 0.f : l * fast_exp2(m - m_new);
+            m = m_new;
+          }
+          const float mref = (m == -INFINITY) ? 0.f : m;
+          // pass 2: P = exp2(s*scale*log2e - m) as packed bf16; packed
+          // columns [16q, 16q+16) overwrite S columns already read
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t sr[32];
+            tmem_ld32(tS + q4 * 32, sr);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), sl2, -mref));
+              float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -mref));
+              if (cls == 1) {
+                p0 = kp[q4 * 32 + 2 * i] > qpos ? 0.f : p0;
+                p1 = kp[q4 * 32 + 2 * i + 1] > qpos ? 0.f : p1;
+              }
+              rowsum += p0 + p1;
+              pk[i] = pack_bf16(p0, p1);
+            }
+            tmem_st16(tS + q4 * 16, pk);
+          }
+          if (cls == 1) {
+            mbar_arrive(&bar.kpos[t]);  // table read; it may be rewritten
+            ok = mbar_wait(&bar.kpos[t], kbph, ab);
+            kbph ^= 1;
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar.p_full[t]);
+        l += rowsum;
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, lse
+      ok = mbar_wait(&bar.o_full[t], oph, ab);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      oph ^= 1;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      __nv_bfloat16* orow = outp + (((size_t)u.b * pm.S + (qvalid ? qslot : 0)) * a.sh.Hq + h) * DV;
+#pragma unroll 1
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c0, o);
+        tmem_ld_wait();
+        uint32_t pkd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pkd[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (qvalid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+        }
+      }
+      if (qvalid) {
+        const float lse = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        a.lse[((size_t)u.b * a.sh.Hq + h) * pm.S + qslot] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV>
+cudaError_t launch_t(const FwdArgs& a, int grid, cudaStream_t st) {
+  auto kern = attn_fwd_kernel<DQK, DV>;
+  // more than half of an SM's shared memory: one CTA per SM, so the CTA's
+  // 512-column TMEM allocation never waits for a neighbour
+  const int smem = FwdCfg<DQK, DV>::SMEM > 120 * 1024 ? FwdCfg<DQK, DV>::SMEM : 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_fwd_smem_bytes(int Dqk, int Dv) {
+  if (Dqk == 64) return FwdCfg<64, 64>::SMEM;
+  if (Dqk == 128) return FwdCfg<128, 128>::SMEM;
+  return FwdCfg<192, 128>::SMEM;
+}
+
+cudaError_t launch_attn_fwd(const FwdArgs& a, int grid, cudaStream_t st) {
+  if (a.sh.Dqk == 64 && a.sh.Dv == 64) return launch_t<64, 64>(a, grid, st);
+  if (a.sh.Dqk == 128 && a.sh.Dv == 128) return launch_t<128, 128>(a, grid, st);
+  if (a.sh.Dqk == 192 && a.sh.Dv == 128) return launch_t<192, 128>(a, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cpattn

@@ -1,0 +1,85 @@
+// Launchers shared between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace cpattn {
+
+cudaError_t launch_lb_permute(const void* src, void* dst, int B, int S, long long row_bytes, int cp,
+                              int inverse, int num_sms, cudaStream_t st);
+
+// split-K decode: scratch = partial (o, m, l) per split and one counter per
+// (batch, kv head); counters must be zero before the first launch and are
+// left zero by every launch.
+struct DecodeArgs {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  const int* lens;
+  void* out;
+  int B, Hq, Hkv, Smax, D;
+  float* part_o;    // [B*Hkv][max_split][G][D]
+  float* part_ml;   // [B*Hkv][max_split][G][2]
+  int* counters;    // [B*Hkv]
+  int* err;
+};
+constexpr int kDecodeSplit = 256;  // tokens per CTA
+int decode_max_split(int Smax);
+size_t decode_part_o_floats(int B, int Hq, int Hkv, int Smax, int D);
+size_t decode_part_ml_floats(int B, int Hq, int Hkv, int Smax);
+cudaError_t launch_gqa_decode(const DecodeArgs& a, cudaStream_t st);
+
+// ---- attention ------------------------------------------------------------
+struct AttnShape {
+  int B, Hq, Hkv, S, Dqk, Dv, cp, lb;
+};
+
+// one forward work unit: two query tiles (qt, head) that share a KV head
+struct FwdUnit {
+  int b;
+  int h0, h1;   // query heads of the two tiles; h1 < 0: single tile
+  int t0, t1;   // query tile indices (128-slot tiles)
+  int hkv;
+  int pad0, pad1;
+};
+
+struct FwdArgs {
+  CUtensorMap tq, tk, tv;
+  void* out;
+  float* lse;
+  const FwdUnit* units;
+  int n_units;
+  AttnShape sh;
+  float scale_log2;
+  int* err;
+};
+cudaError_t launch_attn_fwd(const FwdArgs& a, int grid, cudaStream_t st);
+int attn_fwd_smem_bytes(int Dqk, int Dv);
+
+struct BwdUnit {  // dk/dv unit: one key tile of one KV head; dq unit: one query tile of one head
+  int b, h, t, pad;
+};
+struct BwdArgs {
+  CUtensorMap tq, tk, tv, tdo;  // dq kernel uses 128-row boxes; dkdv uses BQ-row boxes for q/do
+  const float* lse_l2;          // [B, Hq, Spad] lse * log2(e), +inf in padding
+  const float* delta;           // [B, Hq, Spad] rowsum(dout*out), 0 in padding
+  void* dq;
+  void* dk;
+  void* dv;
+  const BwdUnit* units;
+  int n_units;
+  int Spad;
+  AttnShape sh;
+  float scale_log2;
+  float scale;
+  int* err;
+};
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, float* lse_l2,
+                                  float* delta, const AttnShape& sh, int Spad, cudaStream_t st);
+cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_attn_bwd_dq(const BwdArgs& a, int grid, cudaStream_t st);
+int bwd_dkdv_q_tile(int Dqk);  // query rows per step of the dk/dv kernel
+int bwd_dq_kv_tile(int Dqk);   // key rows per step of the dq kernel
+
+}  // namespace cpattn

@@ -1,0 +1,156 @@
+/*
+ * cpattn -- load-balanced context-parallel causal attention and GQA decode
+ * on GB300 (sm_103a).  C ABI of libcpattn.so.
+ *
+ * The method (MaxText pull request 1445 "Add context parallelism",
+ * Description): keys and values are all-gathered, queries are sharded on
+ * the sequence, and tokens are reordered so that every shard does about
+ * the same attention work.  The sequence is cut into 2*cp chunks of
+ * c = S/(2cp) tokens; shard s holds chunk s followed by chunk 2cp-1-s (for
+ * cp = 2 and eight tokens: 0,1,6,7 | 2,3,4,5).  In memory the reordered
+ * ("load-balanced", LB) sequence is the concatenation of the shards, so
+ * memory slot j holds original position
+ *     pos(j) = chunk(k)*c + (j mod c),   k = j / c,
+ *     chunk(k) = k/2 for even k, 2cp-1-k/2 for odd k.
+ * The attention mask is reordered with the tokens: the query in slot i
+ * sees the key in slot j iff pos(j) <= pos(i).  All cp shards run on one
+ * GPU as independent work units over the single gathered K/V; no
+ * collective is involved.
+ *
+ * Tensor layouts (row-major, contiguous, every pointer 16-byte aligned):
+ *   q    [B, S, Hq,  Dqk]  bf16      k  [B, S, Hkv, Dqk]  bf16
+ *   v    [B, S, Hkv, Dv ]  bf16      out[B, S, Hq,  Dv ]  bf16
+ *   lse  [B, Hq, S]        fp32 (natural-log logsumexp of the scaled scores)
+ *   dq/dk/dv: bf16 with the shapes of q/k/v.
+ * When load_balance = 1 every sequence-indexed tensor (q, k, v, out, lse,
+ * dout, dq, dk, dv) is in LB slot order; cp_lb_permute produces it.
+ * Query head h reads KV head h / (Hq/Hkv) (grouped-query attention; MLA is
+ * the case Dqk = 192, Dv = 128 with Hq = Hkv).  scale = 1/sqrt(Dqk).
+ *
+ * Ownership: the caller owns every tensor.  All tensor pointers are DEVICE
+ * pointers except where a parameter says "host".  Work lists and scratch
+ * (backward row statistics, decode split partials) are allocated by the
+ * library on first use per device and shape, cached, and freed by
+ * cp_attn_release().
+ *
+ * Execution: every call is asynchronous on `stream` and never
+ * synchronises.  Calls on one stream are ordered; the library keeps
+ * per-device scratch, so concurrent calls on different streams of the same
+ * device must not overlap (serialise them or use one stream).
+ *
+ * Errors: every call returns a cpattn_status.  A negative value means
+ * nothing was launched; cp_attn_last_error() gives a message (thread
+ * local).  Faults found on the device (a pipeline wait that timed out,
+ * decode lengths outside [0, Smax]) are latched in a device error word and
+ * returned by cp_attn_check_device().
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CPATTN_OK = 0,
+  CPATTN_ERR_INVALID_ARG = -1,    /* bad pointer, size or alignment */
+  CPATTN_ERR_UNSUPPORTED = -2,    /* valid but not implemented (head dims, GPU arch) */
+  CPATTN_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed */
+  CPATTN_ERR_NO_MEMORY = -4,      /* scratch allocation failed */
+  CPATTN_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded pipeline wait ran out */
+  CPATTN_ERR_DEVICE_BOUNDS = -6   /* decode lens[b] outside [0, Smax] (clamped) */
+} cpattn_status;
+
+/*
+ * Load-balance reorder and its inverse ("Add context parallelism",
+ * Description: the token reorder done with jnp.take).
+ *   cp_lb_permute:   dst[b, j, :] = src[b, pos(j), :]
+ *   cp_lb_unpermute: dst[b, pos(j), :] = src[b, j, :]
+ * src, dst: device, [B, S, row_bytes] bytes, src != dst (not in place).
+ * Requires S % (2*cp) == 0, cp >= 1, row_bytes >= 1.  The copy is
+ * bit-exact for any element type.
+ */
+int cp_lb_permute(const void* src, void* dst, int B, int S, long long row_bytes, int cp,
+                  cudaStream_t stream);
+int cp_lb_unpermute(const void* src, void* dst, int B, int S, long long row_bytes, int cp,
+                    cudaStream_t stream);
+
+/*
+ * Forward attention of all cp shards ("Add context parallelism",
+ * Description: each shard's queries against the gathered K/V under the
+ * reordered causal mask; "Add support for EP to context parallelism":
+ * MHA and MLA head layouts).
+ *   out = softmax(scale * q k^T + mask) v,  lse = ln sum exp(scale q k^T).
+ * q, k, v: device inputs; out, lse: device outputs (overwritten).
+ * Requires B >= 1, S >= 1, Hkv >= 1, Hq % Hkv == 0, S % cp == 0 and, with
+ * load_balance = 1, S % (2*cp) == 0.  (Dqk, Dv) in {(64,64), (128,128),
+ * (192,128)}.  Runs on tcgen05 tensor cores; needs an sm_103 GPU.
+ */
+int cp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                int Hkv, int S, int Dqk, int Dv, int cp, int load_balance, cudaStream_t stream);
+
+/*
+ * Forward work of ONE shard only: writes the out/lse rows of the query
+ * tiles that start inside slots [shard*S/cp, (shard+1)*S/cp).  Used to time
+ * and check per-shard work.  Arguments as cp_attn_fwd plus 0 <= shard < cp.
+ */
+int cp_attn_fwd_shard(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                      int Hq, int Hkv, int S, int Dqk, int Dv, int cp, int load_balance,
+                      int shard, cudaStream_t stream);
+
+/*
+ * Backward of cp_attn_fwd (gradient of sum(out * dout)).
+ *   D = rowsum(dout * out); P = exp(scale q k^T - lse); dv = P^T dout;
+ *   dP = dout v^T; dS = P * (dP - D); dq = scale dS k; dk = scale dS^T q.
+ * dk/dv sum over the query heads of a group and over all shards (the
+ * transpose of the K/V all-gather).  q, k, v, out, lse, dout: device
+ * inputs (out and lse as written by cp_attn_fwd); dq, dk, dv: device
+ * outputs (overwritten).  Constraints as cp_attn_fwd.
+ */
+int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
+                int Dqk, int Dv, int cp, int load_balance, cudaStream_t stream);
+
+/*
+ * Grouped-query decode attention ("Add Pallas GPU decode attention in
+ * Maxtext inference", Description: decode attention through a GQA kernel):
+ * one query token per sequence against a KV cache.
+ *   out[b, h] = softmax_{t < lens[b]}(scale q[b,h] . kcache[b,g,t]) vcache[b,g,t],
+ *   g = h / (Hq/Hkv), scale = 1/sqrt(D).
+ * q [B, Hq, D] bf16, kcache/vcache [B, Hkv, Smax, D] bf16, lens [B] int32,
+ * out [B, Hq, D] bf16; all device.  lens[b] == 0 gives out = 0; lens[b]
+ * outside [0, Smax] is clamped and latched as CPATTN_ERR_DEVICE_BOUNDS.
+ * Requires D in {64, 128}, Hq % Hkv == 0, Hq/Hkv <= 16.
+ */
+int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out,
+               int B, int Hq, int Hkv, int Smax, int D, cudaStream_t stream);
+
+/* ---- helpers ---------------------------------------------------------- */
+
+/* pos(j) for j in [0, S) into pos_host (host array of S ints). */
+int cp_lb_positions(int S, int cp, int load_balance, int* pos_host);
+
+/*
+ * Work of each shard in (query tile, key tile) pairs of 128 x 128 slots
+ * that the forward kernel visits per (batch, query head): per_shard_host
+ * is a host array of cp long longs.  With load balance and c a multiple of
+ * 128 every shard gets (2cp-1)m^2 + m(m+1) pairs, m = c/128.
+ */
+int cp_attn_tile_counts(int S, int cp, int load_balance, long long* per_shard_host);
+
+/* Synchronise `stream`, then read and clear the device error word. */
+int cp_attn_check_device(cudaStream_t stream);
+
+/* Thread-local message of the last failed call ("" if none). */
+const char* cp_attn_last_error(void);
+
+/* Free cached work lists and scratch of the current device. */
+int cp_attn_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CPATTN_H_ */

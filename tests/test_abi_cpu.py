@@ -1,0 +1,83 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function the header declares, and its host-side helpers and argument
+checks behave (no CUDA compute call is made)."""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from oracle import cp_attention as O
+from tests._lib import built_lib, header_functions
+
+lib = None
+
+
+def setup_module(_):
+    global lib
+    lib = built_lib()
+
+
+def test_every_declared_symbol_is_exported():
+    names = header_functions()
+    assert {"cp_lb_permute", "cp_lb_unpermute", "cp_attn_fwd", "cp_attn_bwd", "gqa_decode"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), "libcpattn.so does not export %s" % n
+
+
+@pytest.mark.parametrize("S,cp,lb", [(8, 2, 1), (256, 2, 1), (8192, 4, 1), (96, 3, 1), (64, 4, 0), (12, 1, 1)])
+def test_positions_match_oracle(S, cp, lb):
+    arr = (ctypes.c_int * S)()
+    assert lib.cp_lb_positions(S, cp, lb, arr) == 0
+    assert np.array_equal(np.array(arr), O.lb_positions(S, cp, bool(lb)))
+
+
+def _tile_counts(S, cp, lb):
+    arr = (ctypes.c_longlong * cp)()
+    assert lib.cp_attn_tile_counts(S, cp, lb, arr) == 0
+    return list(arr)
+
+
+@pytest.mark.parametrize("cp,m", [(2, 1), (4, 8), (8, 4), (3, 2)])
+def test_tile_counts_closed_form(cp, m):
+    """With c = 128m every shard visits (2cp-1)m^2 + m(m+1) (query, key)
+    tile pairs; without the reorder shard i visits 4m^2 i + m(2m+1)."""
+    S = 2 * cp * 128 * m
+    assert _tile_counts(S, cp, 1) == [(2 * cp - 1) * m * m + m * (m + 1)] * cp
+    assert _tile_counts(S, cp, 0) == [4 * m * m * i + m * (2 * m + 1) for i in range(cp)]
+
+
+def test_tile_counts_llama2_workload():
+    # 8192 tokens, cp=4: 520 tile pairs per shard balanced; 136..904 unbalanced
+    assert _tile_counts(8192, 4, 1) == [520] * 4
+    assert _tile_counts(8192, 4, 0) == [136, 392, 648, 904]
+
+
+def _err():
+    return lib.cp_attn_last_error().decode()
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: argument checks fail first
+
+
+def test_bad_arguments_are_rejected_on_host():
+    P = FAKE
+    # permute: S not a multiple of 2cp, in place, null
+    assert lib.cp_lb_permute(P, ctypes.c_void_p(0x2000000), 1, 10, 16, 2, None) == -1
+    assert "2*cp" in _err()
+    assert lib.cp_lb_permute(P, P, 1, 16, 16, 2, None) == -1
+    assert lib.cp_lb_permute(None, P, 1, 16, 16, 2, None) == -1
+    # attention: Hq % Hkv, S % 2cp, head dims, misaligned pointer
+    args = [P] * 5
+    assert lib.cp_attn_fwd(*args, 1, 6, 4, 256, 128, 128, 2, 1, None) == -1
+    assert "multiple of Hkv" in _err()
+    assert lib.cp_attn_fwd(*args, 1, 4, 4, 250, 128, 128, 2, 1, None) == -1
+    assert lib.cp_attn_fwd(*args, 1, 4, 4, 256, 96, 96, 2, 1, None) == -2
+    assert lib.cp_attn_fwd(ctypes.c_void_p(0x1008), *args[1:], 1, 4, 4, 256, 128, 128, 2, 1, None) == -1
+    assert "aligned" in _err()
+    assert lib.cp_attn_fwd_shard(*args, 1, 4, 4, 256, 128, 128, 2, 1, 2, None) == -1
+    assert lib.cp_attn_bwd(*([P] * 9), 1, 4, 4, 256, 64, 128, 2, 1, None) == -2
+    # decode: group too large, bad head dim, null lens
+    assert lib.gqa_decode(P, P, P, P, P, 1, 64, 2, 128, 128, None) == -2
+    assert lib.gqa_decode(P, P, P, P, P, 1, 8, 2, 128, 96, None) == -2
+    assert lib.gqa_decode(P, P, P, None, P, 1, 8, 2, 128, 128, None) == -1

@@ -1,0 +1,219 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle on the
+same seeded bf16 inputs.  Needs a GB300."""
+
+import numpy as np
+import pytest
+import torch
+
+from context_causal_attention_load_gb300 import synth
+from oracle import cp_attention as O
+from tests._lib import assert_close_grad, assert_close_out, built_lib
+
+pytestmark = pytest.mark.gpu
+
+cp_ = None
+
+
+def setup_module(_):
+    global cp_
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    built_lib()
+    from context_causal_attention_load_gb300 import cpattn
+    cp_ = cpattn
+
+
+def _f64(t):
+    return synth.to_f64(t)
+
+
+def _run_fwd(B, S, Hq, Hkv, Dqk, Dv, cp, lb, seed=0, q_scale=1.0, v_override=None):
+    q, k, v, dout = synth.attention_inputs(B, S, Hq, Hkv, Dqk, Dv, seed=seed, q_scale=q_scale)
+    if v_override is not None:
+        v = v_override
+    pos = O.lb_positions(S, cp, lb)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    if lb:
+        qd, kd, vd = cp_.lb_permute(qd, cp), cp_.lb_permute(kd, cp), cp_.lb_permute(vd, cp)
+    out, lse = cp_.attn_fwd(qd, kd, vd, cp, lb)
+    torch.cuda.synchronize()
+    cp_.check_device()
+    # oracle in slot order on the same bf16 values
+    qs, ks, vs = (O.permute(_f64(x), pos) for x in (q, k, v))
+    o_ref, l_ref = O.cp_attention_fwd(qs, ks, vs, cp, lb)
+    return dict(q=q, k=k, v=v, dout=dout, qd=qd, kd=kd, vd=vd, out=out, lse=lse, o_ref=o_ref,
+                l_ref=l_ref, pos=pos)
+
+
+def _check_fwd(r, name):
+    assert_close_out(_f64(r["out"]), r["o_ref"], name + " out")
+    lse = r["lse"].cpu().numpy().astype(np.float64)
+    err = float(np.max(np.abs(lse - r["l_ref"])))
+    assert err <= 1e-2, "%s lse max-abs %.3e" % (name, err)
+
+
+# ---------------------------------------------------------------------------
+# permutation: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,S,cp,row", [(2, 256, 2, 128), (1, 96, 3, 6), (3, 64, 4, 3), (1, 8192, 4, 8192)])
+def test_permute_bit_exact(B, S, cp, row):
+    g = torch.Generator().manual_seed(B * 1000 + S)
+    x = torch.randint(0, 256, (B, S, row), generator=g, dtype=torch.uint8)
+    pos = O.lb_positions(S, cp, True)
+    y = cp_.lb_permute(x.cuda(), cp)
+    assert torch.equal(y.cpu(), torch.from_numpy(O.permute(x.numpy(), pos)))
+    z = cp_.lb_unpermute(y, cp)
+    assert torch.equal(z.cpu(), x)
+
+
+def test_permute_bf16_page_example():
+    # 8 tokens, cp=2: slots hold tokens 0,1,6,7,2,3,4,5
+    x = torch.arange(8, dtype=torch.float32).to(torch.bfloat16).reshape(1, 8, 1).repeat(1, 1, 8).cuda()
+    y = cp_.lb_permute(x, 2)
+    assert y[0, :, 0].float().cpu().tolist() == [0, 1, 6, 7, 2, 3, 4, 5]
+
+
+# ---------------------------------------------------------------------------
+# forward
+# ---------------------------------------------------------------------------
+
+def test_fwd_identity_v_exposes_probabilities():
+    """V = identity (128 keys, Dv = 128): out row i is row i of the causal
+    attention probability matrix."""
+    S = 128
+    v = torch.eye(S, dtype=torch.float32).reshape(1, S, 1, S).to(torch.bfloat16)
+    r = _run_fwd(1, S, 1, 1, 128, 128, 1, False, seed=3, v_override=v)
+    got = _f64(r["out"])[0, :, 0, :]
+    want = r["o_ref"][0, :, 0, :]
+    err = np.abs(got - want)
+    assert float(err.max()) <= 2e-2, "max err %.3e at %s" % (err.max(), np.unravel_index(err.argmax(), err.shape))
+    _check_fwd(r, "identity-v")
+
+
+@pytest.mark.parametrize("cfg", [
+    # B, S, Hq, Hkv, Dqk, Dv, cp, lb
+    (1, 256, 2, 2, 64, 64, 2, True),      # the tiny workload (chunks of 64)
+    (1, 256, 2, 2, 64, 64, 2, False),
+    (2, 512, 4, 4, 128, 128, 2, True),
+    (1, 1024, 8, 2, 128, 128, 4, True),   # GQA
+    (1, 320, 4, 2, 128, 128, 2, True),    # ragged: chunks of 80, last tile partial
+    (2, 200, 2, 1, 128, 128, 1, True),    # cp=1, S not a multiple of 128
+    (1, 384, 2, 2, 192, 128, 2, True),    # MLA head dims
+    (1, 768, 6, 3, 128, 128, 3, True),    # odd cp, group of 2
+    (1, 512, 3, 1, 64, 64, 4, True),      # odd group size (3 heads per KV head)
+])
+def test_fwd_parity(cfg):
+    r = _run_fwd(*cfg)
+    _check_fwd(r, "fwd%s" % (cfg,))
+
+
+def test_fwd_cp_invariant():
+    """The pages' criterion: permute -> sharded attention -> unpermute equals
+    unsharded causal attention computed in natural order."""
+    B, S, H, D, cp = 1, 1024, 4, 128, 4
+    r = _run_fwd(B, S, H, H, D, D, cp, True, seed=5)
+    nat = cp_.lb_unpermute(r["out"], cp)
+    o_nat, _ = O.causal_attention_fwd(_f64(r["q"]), _f64(r["k"]), _f64(r["v"]))
+    assert_close_out(_f64(nat), o_nat, "unpermuted out")
+
+
+def test_fwd_shards_partition_the_rows():
+    B, S, H, D, cp = 1, 1024, 2, 128, 4
+    r = _run_fwd(B, S, H, H, D, D, cp, True, seed=6)
+    full = r["out"].clone()
+    acc = torch.zeros_like(full)
+    for s in range(cp):
+        out = torch.full_like(full, float("nan"))
+        lse = torch.empty_like(r["lse"])
+        cp_.attn_fwd_shard(r["qd"], r["kd"], r["vd"], cp, s, True, out, lse)
+        torch.cuda.synchronize()
+        rows = slice(s * S // cp, (s + 1) * S // cp)
+        assert torch.equal(out[:, rows], full[:, rows])
+        acc[:, rows] = out[:, rows]
+    assert torch.equal(acc, full)
+
+
+def test_fwd_deterministic():
+    r = _run_fwd(1, 512, 4, 2, 128, 128, 2, True, seed=7)
+    out2, lse2 = cp_.attn_fwd(r["qd"], r["kd"], r["vd"], 2, True)
+    assert torch.equal(out2, r["out"]) and torch.equal(lse2, r["lse"])
+
+
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [
+    (1, 256, 2, 2, 64, 64, 2, True),
+    (1, 512, 4, 4, 128, 128, 2, True),
+    (1, 1024, 8, 2, 128, 128, 4, True),
+    (1, 320, 4, 2, 128, 128, 2, True),
+    (2, 200, 2, 1, 128, 128, 1, True),
+    (1, 384, 2, 2, 192, 128, 2, True),
+    (1, 512, 4, 4, 128, 128, 4, False),
+])
+def test_bwd_parity(cfg):
+    B, S, Hq, Hkv, Dqk, Dv, cp, lb = cfg
+    r = _run_fwd(*cfg, seed=11)
+    doutd = r["dout"].cuda()
+    if lb:
+        doutd = cp_.lb_permute(doutd, cp)
+    dq, dk, dv = cp_.attn_bwd(r["qd"], r["kd"], r["vd"], r["out"], r["lse"], doutd, cp, lb)
+    torch.cuda.synchronize()
+    cp_.check_device()
+    pos = r["pos"]
+    qs, ks, vs, ds = (O.permute(_f64(x), pos) for x in (r["q"], r["k"], r["v"], r["dout"]))
+    # the oracle's backward runs on its own forward output (no GPU value enters it)
+    g_ref = O.cp_attention_bwd(qs, ks, vs, r["o_ref"], r["l_ref"], ds, cp, lb)
+    for got, want, name in zip((dq, dk, dv), g_ref, ("dq", "dk", "dv")):
+        assert_close_grad(_f64(got), want, "%s %s" % (name, cfg))
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [
+    # B, Hq, Hkv, D, Smax, lo, hi
+    (24, 32, 8, 128, 2048, 1024, 2048),   # the decode workload
+    (3, 8, 8, 128, 300, 1, 300),          # G = 1, ragged splits
+    (4, 16, 1, 64, 700, 200, 700),        # G = 16, D = 64
+    (2, 6, 2, 128, 512, 255, 257),        # G = 3, around a split boundary
+])
+def test_decode_parity(cfg):
+    B, Hq, Hkv, D, Smax, lo, hi = cfg
+    q, kc, vc, lens = synth.decode_inputs(B, Hq, Hkv, D, Smax, lo, hi, seed=21)
+    out = cp_.gqa_decode(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref = O.gqa_decode(_f64(q), _f64(kc), _f64(vc), lens.numpy())
+    assert_close_out(_f64(out), ref, "decode %s" % (cfg,))
+    # a second call reuses the split counters
+    out2 = cp_.gqa_decode(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda())
+    assert torch.equal(out2, out)
+
+
+def test_decode_edge_lengths():
+    B, Hq, Hkv, D, Smax = 5, 8, 2, 128, 1024
+    q, kc, vc, _ = synth.decode_inputs(B, Hq, Hkv, D, Smax, 1, 1, seed=22)
+    lens = torch.tensor([0, 1, 256, 257, 1024], dtype=torch.int32)
+    out = cp_.gqa_decode(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref = O.gqa_decode(_f64(q), _f64(kc), _f64(vc), lens.numpy())
+    assert torch.all(out[0] == 0)
+    assert_close_out(_f64(out), ref, "decode edge lengths")
+
+
+def test_decode_bad_lengths_are_flagged():
+    B, Hq, Hkv, D, Smax = 2, 4, 1, 128, 256
+    q, kc, vc, _ = synth.decode_inputs(B, Hq, Hkv, D, Smax, 1, 1, seed=23)
+    lens = torch.tensor([300, 10], dtype=torch.int32)  # 300 > Smax: clamped to 256
+    out = cp_.gqa_decode(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda())
+    with pytest.raises(cp_.CpAttnError) as e:
+        cp_.check_device()
+    assert e.value.code == -6
+    ref = O.gqa_decode(_f64(q), _f64(kc), _f64(vc), np.array([256, 10]))
+    assert_close_out(_f64(out), ref, "clamped decode")
+    cp_.check_device()  # the flag was cleared
