@@ -1,0 +1,553 @@
+#!/usr/bin/env python
+"""Benchmark of load-balanced context-parallel causal attention on GB300.
+
+One step = the whole hot path over one batch of seeded synthetic input:
+  load-balance permute of q, k, v, dout -> forward (all cp shards) ->
+  backward -> unpermute of out, dq, dk, dv -> one GQA decode batch.
+Default workload: the Llama2-7B-shaped attention layer (B=1, Hq=Hkv=32,
+S=8192, head dim 128, cp=4 load-balanced) plus the decode batch (B=24,
+Hq=32, Hkv=8, D=128, cache 2048, lengths U[1024, 2048]).
+
+Prints ONE JSON line (rank 0).  `value` is fwd+bwd TFLOP/s (unmasked pairs
+only, S(S+1)/2 per head; fwd 2(Dqk+Dv), bwd 2(3Dqk+2Dv) FLOPs per pair)
+summed over all ranks; each rank runs its own replica (the cp shards are
+emulated on one GPU, there is no collective on the data path).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: B, S, Hq, Hkv, Dqk, Dv, cp, lb, q_scale
+    "llama2_7b_s8192_cp4": dict(B=1, S=8192, Hq=32, Hkv=32, Dqk=128, Dv=128, cp=4, lb=True,
+                                q_scale=1.0 / math.sqrt(128)),
+    "llama3_70b_s131072_cp8": dict(B=1, S=131072, Hq=64, Hkv=8, Dqk=128, Dv=128, cp=8, lb=True,
+                                   q_scale=1.0),
+    "deepseek_v3_mla_s32768_cp4": dict(B=1, S=32768, Hq=128, Hkv=128, Dqk=192, Dv=128, cp=4, lb=True,
+                                       q_scale=1.0),
+    "tiny_s256_cp2": dict(B=1, S=256, Hq=2, Hkv=2, Dqk=64, Dv=64, cp=2, lb=True, q_scale=1.0),
+}
+DECODE = dict(B=24, Hq=32, Hkv=8, D=128, Smax=2048, lo=1024, hi=2048)
+METRIC = "causal CP-attention fwd+bwd TFLOP/s and % of BF16 peak; decode KV-read GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "attn_fwd": "attn_fwd.cu", "attn_fwd_shard": "attn_fwd.cu", "attn_bwd_dkdv": "attn_bwd.cu",
+    "attn_bwd_dq": "attn_bwd.cu", "bwd_preprocess": "attn_bwd.cu", "gqa_decode": "decode.cu",
+    "lb_permute": "permute.cu", "lb_unpermute": "permute.cu",
+}
+
+
+# ---------------------------------------------------------------------------
+# work accounting
+# ---------------------------------------------------------------------------
+
+def pairs(w):
+    return w["B"] * w["Hq"] * w["S"] * (w["S"] + 1) / 2
+
+
+def flops_fwd(w):
+    return 2.0 * pairs(w) * (w["Dqk"] + w["Dv"])
+
+
+def flops_bwd(w):
+    return 2.0 * pairs(w) * (3 * w["Dqk"] + 2 * w["Dv"])
+
+
+def kernel_flops(name, w):
+    """Algorithmic FLOPs of one launch of each attention kernel.  The dk/dv
+    kernel owns the S and dP recomputes plus dV and dK; the dq kernel is
+    credited only with dQ (its own S/dP recompute is extra work)."""
+    p = pairs(w)
+    return {
+        "attn_fwd": 2.0 * p * (w["Dqk"] + w["Dv"]),
+        "attn_bwd_dkdv": 2.0 * p * (2 * w["Dqk"] + 2 * w["Dv"]),
+        "attn_bwd_dq": 2.0 * p * w["Dqk"],
+    }.get(name)
+
+
+def decode_bytes(lens, D=DECODE["D"], Hkv=DECODE["Hkv"]):
+    return int(sum(int(x) for x in lens)) * Hkv * D * 2 * 2
+
+
+def kernel_bytes(name, w, lens):
+    """Algorithmic HBM bytes of one launch of the streaming kernels."""
+    if name == "gqa_decode":
+        return decode_bytes(lens) + 2 * DECODE["B"] * DECODE["Hq"] * DECODE["D"] * 2
+    if name in ("lb_permute", "lb_unpermute"):
+        return None  # four different tensors per step: reported per launch below
+    return None
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one replica per rank)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(x, device=None):
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(work_per_rank, seconds_max, world):
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return work_per_rank * world / seconds_max
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, stored ncu traffic
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(kernel):
+    src = KERNEL_SOURCES.get(kernel)
+    if not src:
+        return None
+    h = hashlib.sha256()
+    for f in (src, "common.cuh"):
+        with open(os.path.join(ROOT, "context_causal_attention_load_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel, workload):
+    """dram read+write bytes per launch from a committed ncu summary, or None
+    if none exists or the kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get("%s/%s" % (kernel, workload))
+    if not e or e.get("source_sha") != source_hash(kernel):
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, rows=256, heads=1, seed=0):
+    """Run the float64 oracle forward+backward for `heads` query heads and a
+    spread sample of `rows` query rows (each against every key it sees) of
+    the workload.  Returns (seconds, flops of the sample, description)."""
+    import numpy as np
+    from oracle import cp_attention as O
+    rng = np.random.default_rng(seed)
+    S, Dqk, Dv = w["S"], w["Dqk"], w["Dv"]
+    q = rng.standard_normal((1, rows, heads, Dqk)) * w["q_scale"]
+    k = rng.standard_normal((1, S, 1, Dqk))
+    v = rng.standard_normal((1, S, 1, Dv))
+    dout = rng.standard_normal((1, rows, heads, Dv))
+    qpos = np.linspace(0, S - 1, rows).astype(np.int64)
+    kpos = np.arange(S)
+    t0 = time.perf_counter()
+    out, lse = O.masked_attention_fwd(q, k, v, qpos, kpos)
+    O.masked_attention_bwd(q, k, v, out, lse, dout, qpos, kpos)
+    dt = time.perf_counter() - t0
+    npairs = float(np.sum(qpos + 1)) * heads
+    fl = 2.0 * npairs * (Dqk + Dv) + 2.0 * npairs * (3 * Dqk + 2 * Dv)
+    desc = "%d query heads x %d query rows spread over S=%d (every visible key), fwd+bwd" % (heads, rows, S)
+    return dt, fl, desc
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def cpu_baseline(w, budget_s=12.0):
+    dt, fl, desc = oracle_sample(w, rows=64)
+    rows = 64
+    if dt < budget_s / 4:  # grow the sample toward the budget
+        rows = int(min(w["S"], 64 * max(1.0, budget_s / max(dt, 1e-3) / 2)))
+        dt, fl, desc = oracle_sample(w, rows=rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": desc + "; float64 NumPy on the host cores, %.1f s" % dt}
+
+
+def run_reference(args, w, wname):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    rows = 128
+    for _ in range(max(0, args.warmup)):
+        oracle_sample(w, rows=rows)
+    total_t, total_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl, desc = oracle_sample(w, rows=rows)
+        total_t += dt
+        total_f += fl
+    val = total_f / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wname, **{k: w[k] for k in ("B", "S", "Hq", "Hkv", "Dqk", "Dv", "cp")},
+                                        "load_balance": w["lb"]},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": desc + " per step (float64 NumPy, host cores)"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU path
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w, wname):
+    import torch
+    import torch.distributed as dist
+
+    from context_causal_attention_load_gb300 import build as cbuild
+    from context_causal_attention_load_gb300 import synth
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        cbuild.build()
+    barrier()
+    from context_causal_attention_load_gb300 import cpattn
+    cpattn.load()
+
+    B, S, Hq, Hkv, Dqk, Dv, cp, lb = (w[k] for k in ("B", "S", "Hq", "Hkv", "Dqk", "Dv", "cp", "lb"))
+    g = torch.Generator(device=dev).manual_seed(args.seed + 1000 * rank)
+
+    def randn(*shape, scale=1.0):
+        x = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
+        return (x * scale).to(torch.bfloat16) if scale != 1.0 else x.to(torch.bfloat16)
+
+    q = randn(B, S, Hq, Dqk, scale=w["q_scale"])
+    k = randn(B, S, Hkv, Dqk)
+    v = randn(B, S, Hkv, Dv)
+    dout = randn(B, S, Hq, Dv)
+    D = DECODE
+    dq_, dkc, dvc, dlens = synth.decode_inputs(D["B"], D["Hq"], D["Hkv"], D["D"], D["Smax"], D["lo"], D["hi"],
+                                               seed=args.seed + 4)
+    dq_, dkc, dvc, dlens = dq_.to(dev), dkc.to(dev), dvc.to(dev), dlens.to(dev)
+    lens_host = dlens.cpu().tolist()
+
+    # persistent buffers: permuted inputs, outputs, gradients (natural order)
+    qp, kp, vp, dop = (torch.empty_like(x) for x in (q, k, v, dout))
+    out_p = torch.empty(B, S, Hq, Dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+    dq_p, dk_p, dv_p = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    out_n, dq_n, dk_n, dv_n = (torch.empty_like(x) for x in (out_p, q, k, v))
+    dec_out = torch.empty_like(dq_)
+
+    def step(qi=q, ki=k, vi=v, di=dout, dqi=dq_, dkci=dkc, dvci=dvc, dli=dlens):
+        if lb:
+            cpattn.lb_permute(qi, cp, qp)
+            cpattn.lb_permute(ki, cp, kp)
+            cpattn.lb_permute(vi, cp, vp)
+            cpattn.lb_permute(di, cp, dop)
+            a, bk, c, d = qp, kp, vp, dop
+        else:
+            a, bk, c, d = qi, ki, vi, di
+        cpattn.attn_fwd(a, bk, c, cp, lb, out_p, lse)
+        cpattn.attn_bwd(a, bk, c, out_p, lse, d, cp, lb, dq_p, dk_p, dv_p)
+        if lb:
+            cpattn.lb_unpermute(out_p, cp, out_n)
+            cpattn.lb_unpermute(dq_p, cp, dq_n)
+            cpattn.lb_unpermute(dk_p, cp, dk_n)
+            cpattn.lb_unpermute(dv_p, cp, dv_n)
+        cpattn.gqa_decode(dqi, dkci, dvci, dli, dec_out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cpattn.check_device()
+
+    # ---- timed region ---------------------------------------------------
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    cpattn.profile_start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        step()
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier()
+    prof = cpattn.profile_stop()
+    clocks = sampler.stop()
+    cpattn.check_device()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(ms, dev)
+    f_step = flops_fwd(w) + flops_bwd(w)
+    value = aggregate_throughput(f_step, ms_max / 1e3, world) / 1e12
+    launches = sum(n for n, _ in prof.values())
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel of the step
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    dname, (dn, dms) = dom
+    davg = dms / dn
+    fl = kernel_flops(dname, w)
+    if fl is not None:
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        achieved = fl / (davg / 1e3) / 1e12
+        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": "%s bf16_tflops_sustained" % peak_src,
+                "traffic": stored_traffic(dname, wname), "ms_per_launch": davg,
+                "algorithmic_flops_per_launch": fl}
+    else:
+        by = kernel_bytes(dname, w, lens_host)
+        peak = peaks["hbm_gbs"]
+        achieved = (by / (davg / 1e3) / 1e9) if by else None
+        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak if achieved else None, "peak_source": "%s hbm_gbs" % peak_src,
+                "traffic": stored_traffic(dname, wname), "ms_per_launch": davg}
+
+    kernels = {}
+    for name, (n, tot) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        e = {"launches": n, "ms_per_launch": tot / n, "share": tot / sum(t for _, t in prof.values())}
+        kf = kernel_flops(name, w)
+        if kf is not None:
+            e["tflops"] = kf / (tot / n / 1e3) / 1e12
+            e["frac_of_bf16_sustained"] = e["tflops"] / peaks.get("bf16_tflops_sustained", 1700.0)
+        if name == "gqa_decode":
+            e["gbs"] = kernel_bytes(name, w, lens_host) / (tot / n / 1e3) / 1e9
+            e["frac_of_hbm"] = e["gbs"] / peaks["hbm_gbs"]
+        if name in ("lb_permute", "lb_unpermute"):
+            per_launch = (2 * (q.numel() + k.numel() + v.numel() + dout.numel()) * 2) / 4
+            e["gbs_avg_tensor"] = per_launch / (tot / n / 1e3) / 1e9
+        kernels[name] = e
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wname, "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "Dqk": Dqk, "Dv": Dv, "cp": cp,
+                   "load_balance": lb, "decode": "B=24 Hq=32 Hkv=8 D=128 Smax=2048 lens~U[1024,2048]",
+                   "parallelism": "replicas%d" % world,
+                   "l2": "inputs larger than L2 (q,k,v,dout %.0f MB + decode KV %.0f MB per step)" % (
+                       4 * q.numel() * 2 / 1e6, 2 * dkc.numel() * 2 / 1e6)},
+        "roofline": roof,
+        "gpu_launches": launches,
+        "kernels": kernels,
+        "clocks": clocks,
+    }
+
+    if not args.no_extras:
+        line["e2e"] = measure_e2e(args, w, step, (q, k, v, dout, dq_, dkc, dvc, dlens),
+                                  (out_n if lb else out_p, dq_n if lb else dq_p, dk_n if lb else dk_p,
+                                   dv_n if lb else dv_p, dec_out), f_step, world, dev)
+        line["decode"] = measure_decode(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
+        line["shards"] = measure_shards(w, qp if lb else q, kp if lb else k, vp if lb else v, cpattn)
+        if rank == 0 and world == 1:
+            line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(args, w, step, inputs, outputs, f_step, world, dev):
+    """Same metric through the public API with the step's inputs copied from
+    pinned host memory and its results copied back, inside the timed region."""
+    import torch
+    host_in = [x.cpu().pin_memory() for x in inputs]
+    dev_in = [torch.empty_like(x) for x in inputs]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outputs]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    n = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        step(*dev_in)
+        for h, d in zip(host_out, outputs):
+            h.copy_(d, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(n):
+        e2e_step()
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / n, dev)
+    return {"value": aggregate_throughput(f_step, ms / 1e3, world) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n}
+
+
+def measure_decode(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
+    """Decode alone, L2 flushed (a 512 MB write) before every timed launch."""
+    import torch
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q)
+    for _ in range(3):
+        cpattn.gqa_decode(q, kc, vc, lens, out)
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        cpattn.gqa_decode(q, kc, vc, lens, out)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    med = ts[len(ts) // 2]
+    by = decode_bytes(lens_host)
+    gbs = by / (med / 1e3) / 1e9
+    return {"us": med * 1e3, "kv_bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "l2": "flushed before each launch"}
+
+
+def measure_shards(w, q, k, v, cpattn, iters=5):
+    """Per-shard forward time (each shard alone on the whole GPU) and tile
+    counts, load balance on vs off."""
+    import torch
+    res = {}
+    cp = w["cp"]
+    out = torch.empty(w["B"], w["S"], w["Hq"], w["Dv"], dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty(w["B"], w["Hq"], w["S"], dtype=torch.float32, device=q.device)
+    for lb in (True, False):
+        times = []
+        for s in range(cp):
+            cpattn.attn_fwd_shard(q, k, v, cp, s, lb, out, lse)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(iters):
+                cpattn.attn_fwd_shard(q, k, v, cp, s, lb, out, lse)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / iters)
+        res["lb_on" if lb else "lb_off"] = {
+            "tile_pairs_per_head": cpattn.tile_counts(w["S"], cp, lb), "fwd_ms": times,
+            "max_over_min": max(times) / min(times)}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama2_7b_s8192_cp4")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true", help="skip e2e/decode/shard/cpu measurements")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, args.workload)
+    else:
+        run_ours(args, w, args.workload)
+
+
+if __name__ == "__main__":
+    main()

@@ -18,14 +18,18 @@ from . import build as _build
 __all__ = [
     "CpAttnError", "load", "lb_permute", "lb_unpermute", "attn_fwd", "attn_fwd_shard",
     "attn_bwd", "gqa_decode", "lb_positions", "tile_counts", "check_device", "release",
-    "EXPORTED_SYMBOLS",
+    "profile_start", "profile_stop", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "cp_lb_permute", "cp_lb_unpermute", "cp_attn_fwd", "cp_attn_fwd_shard", "cp_attn_bwd",
     "gqa_decode", "cp_lb_positions", "cp_attn_tile_counts", "cp_attn_check_device",
-    "cp_attn_last_error", "cp_attn_release",
+    "cp_attn_last_error", "cp_attn_release", "cp_attn_profile_start", "cp_attn_profile_stop",
 )
+
+
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
 
 _lib = None
 
@@ -61,6 +65,8 @@ def load(path=None):
         "cp_attn_tile_counts": [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)],
         "cp_attn_check_device": [_P],
         "cp_attn_release": [],
+        "cp_attn_profile_start": [],
+        "cp_attn_profile_stop": [ctypes.POINTER(KernelStat), ctypes.c_int, ctypes.POINTER(ctypes.c_int)],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -203,3 +209,16 @@ def check_device(stream=None):
 
 def release():
     _check(load().cp_attn_release())
+
+
+def profile_start():
+    """Start bracketing every library kernel launch with CUDA events."""
+    _check(load().cp_attn_profile_start())
+
+
+def profile_stop():
+    """Stop profiling; returns {kernel name: (launches, total device ms)}."""
+    arr = (KernelStat * 64)()
+    n = ctypes.c_int(0)
+    _check(load().cp_attn_profile_stop(arr, 64, ctypes.byref(n)))
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(min(n.value, 64))}

@@ -92,6 +92,42 @@ struct DevState {
 std::mutex g_mu;
 std::map<int, DevState> g_dev;
 
+// ---- optional per-launch timing (CUDA events on the launching stream) ------
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_ev_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_ev_pool.empty()) {
+    cudaEvent_t e = g_ev_pool.back();
+    g_ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct ProfScope {  // brackets one kernel launch when profiling is on
+  cudaEvent_t b = nullptr;
+  ProfScope(const char* name, cudaStream_t st) {
+    if (!g_prof_on) return;
+    ProfRec r{name, prof_event(), prof_event()};
+    cudaEventRecord(r.a, st);
+    b = r.b;
+    g_prof.push_back(r);
+    stream = st;
+  }
+  ~ProfScope() {
+    if (b) cudaEventRecord(b, stream);
+  }
+  cudaStream_t stream = nullptr;
+};
+
 int get_state(DevState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -311,7 +347,11 @@ int permute_impl(const void* src, void* dst, int B, int S, long long row_bytes, 
   DevState* ds;
   int rc = get_state(&ds);
   if (rc) return rc;
-  cudaError_t e = launch_lb_permute(src, dst, B, S, row_bytes, cp, inverse, ds->num_sms, st);
+  cudaError_t e;
+  {
+    ProfScope ps(inverse ? "lb_unpermute" : "lb_permute", st);
+    e = launch_lb_permute(src, dst, B, S, row_bytes, cp, inverse, ds->num_sms, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "lb_permute launch");
   return CPATTN_OK;
 }
@@ -341,7 +381,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.Dqk));
   a.err = ds->err;
   const int grid = (int)std::min<size_t>(units->n, (size_t)ds->num_sms);
-  cudaError_t e = launch_attn_fwd(a, grid, st);
+  cudaError_t e;
+  {
+    ProfScope ps(shard < 0 ? "attn_fwd" : "attn_fwd_shard", st);
+    e = launch_attn_fwd(a, grid, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
   return CPATTN_OK;
 }
@@ -400,8 +444,12 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   a.scale = (float)(1.0 / std::sqrt((double)Dqk));
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)Dqk));
   a.err = ds->err;
-  cudaError_t e = launch_bwd_preprocess(out, dout, lse, const_cast<float*>(a.lse_l2), const_cast<float*>(a.delta),
-                                        sh, Spad, stream);
+  cudaError_t e;
+  {
+    ProfScope ps("bwd_preprocess", stream);
+    e = launch_bwd_preprocess(out, dout, lse, const_cast<float*>(a.lse_l2), const_cast<float*>(a.delta), sh, Spad,
+                              stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
   // dk/dv: key tiles of 128 rows, query/dout boxes of BQ rows
   const int BQ = bwd_dkdv_q_tile(Dqk);
@@ -411,7 +459,10 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
   a.units = u_kv->ptr;
   a.n_units = (int)u_kv->n;
-  e = launch_attn_bwd_dkdv(a, (int)std::min<size_t>(u_kv->n, (size_t)ds->num_sms), stream);
+  {
+    ProfScope ps("attn_bwd_dkdv", stream);
+    e = launch_attn_bwd_dkdv(a, (int)std::min<size_t>(u_kv->n, (size_t)ds->num_sms), stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dk/dv launch");
   // dq: query tiles of 128 rows, key/value boxes of BK rows
   const int BK = bwd_dq_kv_tile(Dqk);
@@ -421,7 +472,10 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, BK))) return rc;
   a.units = u_q->ptr;
   a.n_units = (int)u_q->n;
-  e = launch_attn_bwd_dq(a, (int)std::min<size_t>(u_q->n, (size_t)ds->num_sms), stream);
+  {
+    ProfScope ps("attn_bwd_dq", stream);
+    e = launch_attn_bwd_dq(a, (int)std::min<size_t>(u_q->n, (size_t)ds->num_sms), stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
   return CPATTN_OK;
 }
@@ -444,7 +498,11 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
   if ((rc = ensure(ds->dec_cnt, (size_t)B * Hkv, stream, true))) return rc;
   DecodeArgs a{q, kcache, vcache, lens, out, B, Hq, Hkv, Smax, D, ds->dec_o.ptr, ds->dec_ml.ptr, ds->dec_cnt.ptr,
                ds->err};
-  cudaError_t e = launch_gqa_decode(a, stream);
+  cudaError_t e;
+  {
+    ProfScope ps("gqa_decode", stream);
+    e = launch_gqa_decode(a, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "gqa_decode launch");
   return CPATTN_OK;
 }
@@ -488,6 +546,48 @@ int cp_attn_check_device(cudaStream_t stream) {
   if (word == DEV_TIMEOUT) return fail(CPATTN_ERR_DEVICE_TIMEOUT, "a kernel pipeline wait timed out");
   if (word == DEV_LENS_CLAMPED) return fail(CPATTN_ERR_DEVICE_BOUNDS, "decode lens outside [0, Smax] were clamped");
   return fail(CPATTN_ERR_CUDA, "unknown device error %d", word);
+}
+
+int cp_attn_profile_start(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& r : g_prof) {
+    g_ev_pool.push_back(r.a);
+    g_ev_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  g_prof_on = true;
+  return CPATTN_OK;
+}
+
+int cp_attn_profile_stop(cpattn_kernel_stat* stats, int max_stats, int* n_stats) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof_on = false;
+  if (!n_stats) return fail(CPATTN_ERR_INVALID_ARG, "null n_stats");
+  std::vector<cpattn_kernel_stat> agg;
+  for (auto& r : g_prof) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    cpattn_kernel_stat* hit = nullptr;
+    for (auto& x : agg)
+      if (std::string(x.name) == r.name) hit = &x;
+    if (!hit) {
+      cpattn_kernel_stat z{};
+      snprintf(z.name, sizeof(z.name), "%s", r.name);
+      agg.push_back(z);
+      hit = &agg.back();
+    }
+    hit->launches += 1;
+    hit->total_ms += ms;
+    g_ev_pool.push_back(r.a);
+    g_ev_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  *n_stats = (int)agg.size();
+  for (int i = 0; i < (int)agg.size() && i < max_stats && stats; ++i) stats[i] = agg[i];
+  return CPATTN_OK;
 }
 
 const char* cp_attn_last_error(void) { return g_last_error.c_str(); }

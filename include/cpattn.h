@@ -141,6 +141,23 @@ int cp_lb_positions(int S, int cp, int load_balance, int* pos_host);
  */
 int cp_attn_tile_counts(int S, int cp, int load_balance, long long* per_shard_host);
 
+/*
+ * Kernel timing for profiling and benchmarks.  Between profile_start and
+ * profile_stop every kernel the library launches is bracketed by two CUDA
+ * events recorded on its own stream.  profile_stop waits for those events
+ * and fills `stats` (host array of max_stats entries, may be NULL) with one
+ * entry per kernel name: launch count and summed device milliseconds;
+ * *n_stats receives the number of distinct kernels.  Adds about two event
+ * records per launch; off by default.
+ */
+typedef struct {
+  char name[32];
+  int launches;
+  double total_ms;
+} cpattn_kernel_stat;
+int cp_attn_profile_start(void);
+int cp_attn_profile_stop(cpattn_kernel_stat* stats, int max_stats, int* n_stats);
+
 /* Synchronise `stream`, then read and clear the device error word. */
 int cp_attn_check_device(cudaStream_t stream);
 
