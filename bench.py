@@ -482,15 +482,20 @@ def measure_e2e(args, w, step, inputs, outputs, f_step, world, dev):
 
 
 def measure_decode(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
-    """Decode alone, L2 flushed (a 512 MB write) before every timed launch."""
+    """Decode alone, L2 flushed before every timed launch: a 512 MB write,
+    then a 512 MB read of another buffer so that the written lines are
+    already back in HBM (no write-back traffic inside the timed launch)."""
     import torch
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=q.device)
+    flush_rd = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=q.device)
+    sink = torch.empty((), dtype=torch.float32, device=q.device)
     out = torch.empty_like(q)
     for _ in range(3):
         cpattn.gqa_decode(q, kc, vc, lens, out)
     ts = []
     for _ in range(iters):
         flush.zero_()
+        torch.sum(flush_rd, dim=0, out=sink)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         cpattn.gqa_decode(q, kc, vc, lens, out)
@@ -502,7 +507,7 @@ def measure_decode(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
     by = decode_bytes(lens_host)
     gbs = by / (med / 1e3) / 1e9
     return {"us": med * 1e3, "kv_bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
-            "l2": "flushed before each launch"}
+            "l2": "flushed before each launch (512 MB write + 512 MB read)"}
 
 
 def measure_shards(w, q, k, v, cpattn, iters=5):

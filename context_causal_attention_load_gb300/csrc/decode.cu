@@ -3,20 +3,22 @@
 // "Add Pallas GPU decode attention in Maxtext inference" (MaxText pull
 // request 1066), Description: decode attention (one new query token per
 // sequence against the KV cache) through a grouped-query kernel.  Here one
-// CTA owns (batch b, KV head g, a split of 256 cache positions) and serves
-// all Hq/Hkv query heads of the group from a single read of those K/V rows,
-// so the cache is streamed from HBM exactly once.  Partial results
-// (running max m, sum l, unnormalised o) of the splits of one (b, g) are
-// merged by the last CTA to finish (an arrival counter per (b, g), reset by
-// that CTA), so the whole decode is one launch.
+// CTA owns (batch b, KV head g, a split of 128 cache positions) and serves
+// all G = Hq/Hkv query heads of the group from a single read of those K/V
+// rows, so the cache is streamed from HBM exactly once.
 //
-// Inside a CTA, 8 warps each take 32 positions:
-//  * scores: lane = position; the lane reads its whole K row (D bf16) and
-//    forms the G dot products against q held in shared memory (broadcast);
-//    warp-shuffle max and sum give the warp's softmax statistics;
-//  * values: lane = D/32 columns; the warp walks its 32 positions, reading
-//    each V row with coalesced loads and accumulating p * v for all G heads;
-//  * the 8 warps' (m, l, o) are merged in shared memory.
+// Streaming: at entry one thread issues two bulk copies (cp.async.bulk) of
+// the split's K rows and V rows into shared memory (up to 64 KB in flight
+// per CTA, several CTAs per SM), so HBM sees deep, register-free
+// concurrency.  Compute, per warp of 32 positions: LPT lanes work on one
+// position (each lane holds D/LPT columns of every head's q in registers),
+// form G partial dot products, reduce them with log2(LPT) shuffles, and
+// update a running (max, sum, o) per lane group with a lazy rescale (o is
+// rescaled only when the maximum grows by more than 8 in the log2 domain).
+// Groups, warps and finally splits are merged with the usual
+// max-rescaled sums; the splits of one (b, g) are merged by the last CTA to
+// finish (an arrival counter per (b, g) that this CTA resets), so the whole
+// decode is one launch.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,36 +26,65 @@ namespace cpattn {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-static_assert(kWarps * 32 == kDecodeSplit, "one position per thread");
+static_assert(kWarps * 32 == kDecodeSplit, "32 positions per warp");
+
+template <int D, int GMAX>
+struct DecCfg {
+  // lanes per position: keep q and o at 64 registers per lane
+  static constexpr int LPT0 = D * GMAX / 64;
+  static constexpr int LPT = LPT0 < 8 ? 8 : (LPT0 > 32 ? 32 : LPT0);
+  static constexpr int DPL = D / LPT;  // columns per lane
+  static constexpr int TPI = 32 / LPT; // positions per warp step
+  static constexpr int NCH = DPL >= 8 ? DPL / 8 : 1;  // 16-byte chunks per lane (DPL >= 8)
+  static_assert(DPL == 4 || DPL % 8 == 0, "lane column split");
+};
 
 template <int D, int GMAX>
 struct DecSmem {
-  float q[GMAX][D];
-  float p[GMAX][kDecodeSplit];
+  __nv_bfloat16 k[kDecodeSplit][D];
+  __nv_bfloat16 v[kDecodeSplit][D];
   float wm[kWarps][GMAX];
   float wl[kWarps][GMAX];
   float wo[kWarps][GMAX][D];
   float cm[GMAX];
   float cl[GMAX];
+  uint64_t bar;
   int last;
 };
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+// the lane's columns: NCH chunks of 8 (chunk sub + j*LPT), or 4 columns when DPL == 4
+template <int D, int GMAX>
+__device__ __forceinline__ int col_of(int sub, int j) {
+  using C = DecCfg<D, GMAX>;
+  if constexpr (C::DPL == 4) return sub * 4 + j;
+  else return (sub + (j >> 3) * C::LPT) * 8 + (j & 7);
 }
-__device__ __forceinline__ float warp_sum(float v) {
+
+template <int D, int GMAX>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* row, int sub, float (&x)[DecCfg<D, GMAX>::DPL]) {
+  using C = DecCfg<D, GMAX>;
+  if constexpr (C::DPL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(row + sub * 4);
+    x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+  } else {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+    for (int j = 0; j < C::NCH; ++j) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row + (sub + j * C::LPT) * 8);
+      x[8 * j + 0] = bf16lo(u.x); x[8 * j + 1] = bf16hi(u.x);
+      x[8 * j + 2] = bf16lo(u.y); x[8 * j + 3] = bf16hi(u.y);
+      x[8 * j + 4] = bf16lo(u.z); x[8 * j + 5] = bf16hi(u.z);
+      x[8 * j + 6] = bf16lo(u.w); x[8 * j + 7] = bf16hi(u.w);
+    }
+  }
 }
 
 template <int D, int GMAX>
 __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, float scale_log2) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  using C = DecCfg<D, GMAX>;
+  constexpr int LPT = C::LPT, DPL = C::DPL, TPI = C::TPI;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   auto& sm = *reinterpret_cast<DecSmem<D, GMAX>*>(smem_raw);
   const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv;
@@ -66,130 +97,120 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
     len = len < 0 ? 0 : a.Smax;
   }
   const int nsplit = (len + kDecodeSplit - 1) / kDecodeSplit;
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out);
+  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q) + ((size_t)b * a.Hq + (size_t)g * G) * D;
+  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.Hq + (size_t)g * G) * D;
 
   if (len == 0) {  // empty cache: the output is defined as zero
     if (sp == 0)
-      for (int i = tid; i < G * D; i += kThreads)
-        og[((size_t)b * a.Hq + (size_t)g * G) * D + i] = __float2bfloat16(0.f);
+      for (int i = tid; i < G * D; i += kThreads) og[i] = __float2bfloat16(0.f);
     return;
   }
   if (sp >= nsplit) return;
 
-  // q of the group, pre-scaled into the log2 domain
-  for (int i = tid; i < GMAX * D; i += kThreads) {
-    int h = i / D;
-    float x = 0.f;
-    if (h < G) x = __bfloat162float(qg[((size_t)b * a.Hq + (size_t)g * G) * D + i]) * scale_log2;
-    sm.q[h][i - h * D] = x;
-  }
-  __syncthreads();
-
-  const size_t row_base = ((size_t)b * a.Hkv + g) * (size_t)a.Smax;
   const int t0 = sp * kDecodeSplit;
-  const int wt0 = t0 + warp * 32;  // first position of this warp
+  const int n = len - t0 < kDecodeSplit ? len - t0 : kDecodeSplit;
+  const size_t row0 = ((size_t)b * a.Hkv + g) * (size_t)a.Smax + t0;
+  volatile int abort_flag = 0;
+  const Abort ab{&abort_flag, a.err};
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = (uint32_t)n * D * 2;
+    mbar_expect_tx(&sm.bar, 2 * bytes);
+    bulk_load(&sm.k[0][0], static_cast<const __nv_bfloat16*>(a.kc) + row0 * D, bytes, &sm.bar);
+    bulk_load(&sm.v[0][0], static_cast<const __nv_bfloat16*>(a.vc) + row0 * D, bytes, &sm.bar);
+  }
 
-  // ---- scores: lane = position ---------------------------------------------
-  {
-    const int t = wt0 + lane;
-    const bool valid = t < len;
-    float s[GMAX];
+  // q of the group in registers, pre-scaled into the log2 domain
+  const int sub = lane % LPT;     // column slot within the position's lanes
+  const int grp = lane / LPT;     // position slot within the warp step
+  float qr[GMAX][DPL];
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) s[h] = 0.f;
-    if (valid) {
-      const uint4* kr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.kc) +
-                                                       (row_base + t) * D);
-      constexpr int NV = D / 8;
-      uint4 kv[NV];
+  for (int h = 0; h < GMAX; ++h)
 #pragma unroll
-      for (int i = 0; i < NV; ++i) kv[i] = __ldg(kr + i);
+    for (int j = 0; j < DPL; ++j)
+      qr[h][j] = h < G ? __bfloat162float(qg[h * D + col_of<D, GMAX>(sub, j)]) * scale_log2 : 0.f;
+
+  float o[GMAX][DPL];
+  float m[GMAX], l[GMAX];
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const uint32_t w[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
+  for (int h = 0; h < GMAX; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float k0 = bf16lo(w[j]), k1 = bf16hi(w[j]);
+    for (int j = 0; j < DPL; ++j) o[h][j] = 0.f;
+  }
+  __syncthreads();  // barrier initialised before anyone waits on it
+  const bool ok = mbar_wait(&sm.bar, 0, ab);
+
+  const int wbase = warp * 32;
+  if (ok && wbase < n) {
+    const int steps = (min(32, n - wbase) + TPI - 1) / TPI;
+    for (int it = 0; it < steps; ++it) {
+      const int tt = wbase + it * TPI + grp;  // position within the split
+      const bool valid = tt < n;
+      float kx[DPL];
+      load_row<D, GMAX>(&sm.k[valid ? tt : 0][0], sub, kx);
+      float s[GMAX];
 #pragma unroll
-          for (int h = 0; h < GMAX; ++h) {
-            if (h < G) {
-              const float2 qq = *reinterpret_cast<const float2*>(&sm.q[h][i * 8 + j * 2]);
-              s[h] = fmaf(qq.x, k0, s[h]);
-              s[h] = fmaf(qq.y, k1, s[h]);
-            }
-          }
+      for (int h = 0; h < GMAX; ++h) {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) acc = fmaf(qr[h][j], kx[j], acc);
+        s[h] = acc;
+      }
+#pragma unroll
+      for (int off = 1; off < LPT; off <<= 1)
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
+      float vx[DPL];
+      load_row<D, GMAX>(&sm.v[valid ? tt : 0][0], sub, vx);
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (h >= G || !valid) continue;
+        if (s[h] > m[h] + 8.0f) {  // lazy rescale: only when the max grows by > 2^8
+          const float alpha = (m[h] == -INFINITY) ? 0.f : fast_exp2(m[h] - s[h]);
+          l[h] *= alpha;
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) o[h][j] *= alpha;
+          m[h] = s[h];
         }
+        const float p = fast_exp2(s[h] - m[h]);
+        l[h] += p;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) o[h][j] = fmaf(p, vx[j], o[h][j]);
       }
     }
+  }
+  // merge the position groups of the warp (lanes sub, sub+LPT, ...)
+#pragma unroll
+  for (int off = LPT; off < 32; off <<= 1) {
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
-      if (h < G) {
-        float sv = valid ? s[h] : -INFINITY;
-        float m = warp_max(sv);
-        float mref = (m == -INFINITY) ? 0.f : m;
-        float p = valid ? fast_exp2(sv - mref) : 0.f;
-        float l = warp_sum(p);
-        sm.p[h][warp * 32 + lane] = p;
-        if (lane == 0) {
-          sm.wm[warp][h] = m;
-          sm.wl[warp][h] = l;
-        }
+      const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+      const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
+      const float mn = fmaxf(m[h], mo);
+      const float a1 = (m[h] == -INFINITY) ? 0.f : fast_exp2(m[h] - mn);
+      const float a2 = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
+      l[h] = l[h] * a1 + lo * a2;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        const float ov = __shfl_xor_sync(0xffffffffu, o[h][j], off);
+        o[h][j] = o[h][j] * a1 + ov * a2;
       }
+      m[h] = mn;
     }
   }
-  __syncwarp();
-
-  // ---- values: lane = D/32 columns ---------------------------------------------
-  {
-    constexpr int C = D / 32;  // columns per lane: 4 (D=128) or 2 (D=64)
-    float o[GMAX][C];
+  if (grp == 0) {
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h)
+    for (int h = 0; h < GMAX; ++h) {
 #pragma unroll
-      for (int c = 0; c < C; ++c) o[h][c] = 0.f;
-    int n = len - wt0;
-    n = n > 32 ? 32 : n;
-    const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(a.vc) + (row_base + wt0) * D + lane * C;
-    for (int i0 = 0; i0 < n; i0 += 8) {
-      uint32_t raw[8][C / 2];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (i0 + u < n) {
-          if constexpr (C == 4) {
-            uint2 x = __ldg(reinterpret_cast<const uint2*>(vb + (size_t)(i0 + u) * D));
-            raw[u][0] = x.x;
-            raw[u][1] = x.y;
-          } else {
-            raw[u][0] = __ldg(reinterpret_cast<const unsigned int*>(vb + (size_t)(i0 + u) * D));
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < C / 2; ++c) raw[u][c] = 0u;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float vv[C];
-#pragma unroll
-        for (int c = 0; c < C / 2; ++c) {
-          vv[2 * c] = bf16lo(raw[u][c]);
-          vv[2 * c + 1] = bf16hi(raw[u][c]);
-        }
-        const int pi = warp * 32 + i0 + u;
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          if (h < G) {
-            const float p = (i0 + u < n) ? sm.p[h][pi] : 0.f;
-#pragma unroll
-            for (int c = 0; c < C; ++c) o[h][c] = fmaf(p, vv[c], o[h][c]);
-          }
-        }
+      for (int j = 0; j < DPL; ++j) sm.wo[warp][h][col_of<D, GMAX>(sub, j)] = o[h][j];
+      if (sub == 0) {
+        sm.wm[warp][h] = m[h];
+        sm.wl[warp][h] = l[h];
       }
     }
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-      for (int c = 0; c < C; ++c) sm.wo[warp][h][lane * C + c] = o[h][c];
   }
   __syncthreads();
 
@@ -214,7 +235,7 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
     for (int w = 0; w < kWarps; ++w)
       if (sm.wm[w][h] != -INFINITY) acc = fmaf(sm.wo[w][h][d], fast_exp2(sm.wm[w][h] - M), acc);
     if (nsplit == 1) {
-      og[((size_t)b * a.Hq + (size_t)g * G + h) * D + d] = __float2bfloat16(acc / sm.cl[h]);
+      og[i] = __float2bfloat16(acc / sm.cl[h]);
     } else {
       a.part_o[(((size_t)bg * max_split + sp) * GMAX + h) * D + d] = acc;
     }
@@ -256,7 +277,7 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
       const float m2 = __ldcg(a.part_ml + (((size_t)bg * max_split + s2) * GMAX + h) * 2);
       acc = fmaf(__ldcg(a.part_o + (((size_t)bg * max_split + s2) * GMAX + h) * D + d), fast_exp2(m2 - M), acc);
     }
-    og[((size_t)b * a.Hq + (size_t)g * G + h) * D + d] = __float2bfloat16(acc / sm.cl[h]);
+    og[i] = __float2bfloat16(acc / sm.cl[h]);
   }
   if (tid == 0) a.counters[bg] = 0;  // ready for the next launch
 }

@@ -24,11 +24,12 @@ struct DecodeArgs {
   int* counters;    // [B*Hkv]
   int* err;
 };
-constexpr int kDecodeSplit = 256;  // tokens per CTA
+constexpr int kDecodeSplit = 128;  // cache positions per CTA
 int decode_max_split(int Smax);
 size_t decode_part_o_floats(int B, int Hq, int Hkv, int Smax, int D);
 size_t decode_part_ml_floats(int B, int Hq, int Hkv, int Smax);
 cudaError_t launch_gqa_decode(const DecodeArgs& a, cudaStream_t st);
+
 
 // ---- attention ------------------------------------------------------------
 struct AttnShape {
