@@ -507,6 +507,33 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
   return CPATTN_OK;
 }
 
+int gqa_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* lens, void* out, int B,
+                       int Hq, int Hkv, int Smax, int D, cudaStream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Smax < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, Hq, Hkv, Smax must be >= 1");
+  if (Hq % Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Hq / Hkv > 16) return fail(CPATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16", Hq / Hkv);
+  if (D != 64 && D != 128) return fail(CPATTN_ERR_UNSUPPORTED, "decode head dim %d not in {64, 128}", D);
+  if (!lens) return fail(CPATTN_ERR_INVALID_ARG, "null lens");
+  int rc = check_ptrs({q, kcache, vcache, out});
+  if (rc) return rc;
+  const size_t need = noalloc_decode_bytes(B, Hq, Hkv, Smax, D);
+  if (need > noalloc_decode_limit())
+    return fail(CPATTN_ERR_INVALID_ARG,
+                "gqa_decode_noalloc: this shape needs %zu bytes of scratch, the fixed array holds %zu "
+                "(use gqa_decode, or fewer sequences / a shorter cache)",
+                need, noalloc_decode_limit());
+  int dev = 0, major = 0, minor = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(CPATTN_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device is sm_%d%d", major, minor);
+  e = launch_gqa_decode_noalloc(q, kcache, vcache, lens, out, B, Hq, Hkv, Smax, D, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gqa_decode_noalloc");
+  return CPATTN_OK;
+}
+
 int cp_lb_positions(int S, int cp, int load_balance, int* pos_host) {
   if (!pos_host) return fail(CPATTN_ERR_INVALID_ARG, "null pos_host");
   if (S < 1 || cp < 1) return fail(CPATTN_ERR_INVALID_ARG, "S and cp must be >= 1");

@@ -19,6 +19,8 @@
 // max-rescaled sums; the splits of one (b, g) are merged by the last CTA to
 // finish (an arrival counter per (b, g) that this CTA resets), so the whole
 // decode is one launch.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -320,6 +322,70 @@ size_t decode_part_ml_floats(int B, int Hq, int Hkv, int Smax) {
 cudaError_t launch_gqa_decode(const DecodeArgs& a, cudaStream_t st) {
   if (a.D == 128) return launch_d<128>(a, st);
   return launch_d<64>(a, st);
+}
+
+// ---------------------------------------------------------------------------
+// Decode without any allocation by the library.
+//
+// Some callers cannot let a library call cudaMalloc: code running under an
+// allocator that owns all device memory (a caching allocator or a memory pool
+// sized up front), real-time serving loops that must not hit the driver's
+// allocation path or its implicit synchronisation, and processes that have
+// reserved nearly all of HBM for the KV cache.  For them the split partials
+// and arrival counters of the decode live in this fixed, statically sized
+// device array instead of library-allocated scratch.  Every GPU that loads
+// the library holds the array until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kNoAllocHeader = 256;                    // error word
+
+static __device__ __align__(256) unsigned char cpattn_noalloc_scratch[kNoAllocScratchBytes];
+
+static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t noalloc_decode_bytes(int B, int Hq, int Hkv, int Smax, int D) {
+  return kNoAllocHeader + round256((size_t)B * Hkv * sizeof(int)) +
+         round256(decode_part_ml_floats(B, Hq, Hkv, Smax) * sizeof(float)) +
+         round256(decode_part_o_floats(B, Hq, Hkv, Smax, D) * sizeof(float));
+}
+size_t noalloc_decode_limit() { return kNoAllocScratchBytes; }
+
+// Device address of the array, looked up once per device with that device
+// current (in host code the array's name is only a host-side stand-in).
+constexpr int kMaxDevices = 64;
+static unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+static std::mutex g_noalloc_mu;
+
+cudaError_t noalloc_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, cpattn_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_gqa_decode_noalloc(const void* q, const void* kc, const void* vc, const int* lens, void* out,
+                                      int B, int Hq, int Hkv, int Smax, int D, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  unsigned char* base = nullptr;
+  if ((e = noalloc_scratch(dev, &base)) != cudaSuccess) return e;
+  unsigned char* p = base + kNoAllocHeader;
+  int* counters = reinterpret_cast<int*>(p);
+  p += round256((size_t)B * Hkv * sizeof(int));
+  float* ml = reinterpret_cast<float*>(p);
+  p += round256(decode_part_ml_floats(B, Hq, Hkv, Smax) * sizeof(float));
+  float* po = reinterpret_cast<float*>(p);
+  // the array keeps whatever the previous call left: the counters must start at zero
+  if ((e = cudaMemsetAsync(counters, 0, (size_t)B * Hkv * sizeof(int), st)) != cudaSuccess) return e;
+  DecodeArgs a{q, kc, vc, lens, out, B, Hq, Hkv, Smax, D, po, ml, counters, reinterpret_cast<int*>(base)};
+  return launch_gqa_decode(a, st);
 }
 
 }  // namespace cpattn

@@ -29,7 +29,11 @@ int decode_max_split(int Smax);
 size_t decode_part_o_floats(int B, int Hq, int Hkv, int Smax, int D);
 size_t decode_part_ml_floats(int B, int Hq, int Hkv, int Smax);
 cudaError_t launch_gqa_decode(const DecodeArgs& a, cudaStream_t st);
-
+// allocation-free decode: scratch in a fixed static device array
+size_t noalloc_decode_bytes(int B, int Hq, int Hkv, int Smax, int D);
+size_t noalloc_decode_limit();
+cudaError_t launch_gqa_decode_noalloc(const void* q, const void* kc, const void* vc, const int* lens, void* out,
+                                      int B, int Hq, int Hkv, int Smax, int D, cudaStream_t st);
 
 // ---- attention ------------------------------------------------------------
 struct AttnShape {

@@ -128,6 +128,32 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
 int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out,
                int B, int Hq, int Hkv, int Smax, int D, cudaStream_t stream);
 
+/*
+ * gqa_decode without any allocation by the library (the pages have no
+ * counterpart; this exists for callers that must not let a library
+ * allocate device memory: code whose memory is owned by a caching
+ * allocator or a pool sized up front, serving loops that must avoid the
+ * driver's allocation path and its implicit synchronisation, processes
+ * that keep nearly all of HBM for their KV cache).
+ * Same arguments, layouts and results as gqa_decode.  The split partials
+ * and arrival counters live in one fixed 8 MiB device array inside the
+ * library (every GPU that loads the library holds it until the process
+ * exits); the caller still passes all inputs and outputs.  A shape whose
+ * scratch does not fit is rejected with CPATTN_ERR_INVALID_ARG before any
+ * launch (about B*Hkv*ceil(Smax/128)*G'*(D+2)*4 bytes, G' = Hq/Hkv rounded
+ * up to a power of two; the decode workload B=24, Hkv=8, Smax=2048, G=4,
+ * D=128 needs 3.2 MiB).
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Every
+ * call shares the one array and each call clears the counters it uses, so
+ * calls whose executions overlap on the GPU (different streams, or several
+ * host threads) race: serialise them.  lens outside [0, Smax] are clamped
+ * as in gqa_decode; the flag goes to the array's own error word and is not
+ * reported by cp_attn_check_device.
+ */
+int gqa_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* lens,
+                       void* out, int B, int Hq, int Hkv, int Smax, int D, cudaStream_t stream);
+
 /* ---- helpers ---------------------------------------------------------- */
 
 /* pos(j) for j in [0, S) into pos_host (host array of S ints). */
