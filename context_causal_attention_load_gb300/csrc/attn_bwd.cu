@@ -40,7 +40,8 @@ __device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
 }
 
 // ============================================================================
-// preprocess: lse_l2 = lse*log2(e) (+inf past S), delta = rowsum(dO*O) (0 past S)
+// preprocess: -lse*log2(e) (-inf past S) and -rowsum(dO*O) (0 past S), stored
+// negated so the element-wise warps apply them with one fused multiply-add;
 // layout [B, Hq, Spad]; one warp per (b, s, h) row
 // ============================================================================
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     const size_t o_idx = ((size_t)b * sh.Hq + h) * Spad + s;
     if (s >= sh.S) {
       if (lane == 0) {
-        lse_l2[o_idx] = INFINITY;
+        lse_l2[o_idx] = -INFINITY;
         delta[o_idx] = 0.f;
       }
       continue;
@@ -74,8 +75,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
-      delta[o_idx] = acc;
-      lse_l2[o_idx] = lse[((size_t)b * sh.Hq + h) * sh.S + s] * 1.4426950408889634f;
+      delta[o_idx] = -acc;
+      lse_l2[o_idx] = -lse[((size_t)b * sh.Hq + h) * sh.S + s] * 1.4426950408889634f;
     }
   }
 }
@@ -338,16 +339,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
           tmem_ld32(tmem + lane_base + C::T_DP + buf * BQ + g * HC, dp);
           tmem_ld_wait();
           uint32_t pk[16], dk[16];
+          const uint64_t sl2x2 = f2pack(sl2, sl2);
+          const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse_s);  // -lse*log2e pairs
+          const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(del_s);  // -D pairs
 #pragma unroll
           for (int c = 0; c < HC; c += 2) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse_s[c]));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse_s[c + 1]));
+            float p0, p1;
+            f2unpack(f2fma(f2pack_u(sv[c], sv[c + 1]), sl2x2, nl2[c >> 1]), p0, p1);
+            p0 = fast_exp2(p0);
+            p1 = fast_exp2(p1);
             if (!full) {
               p0 = (kpos <= qp_s[c]) ? p0 : 0.f;
               p1 = (kpos <= qp_s[c + 1]) ? p1 : 0.f;
             }
-            const float d0 = p0 * (__uint_as_float(dp[c]) - del_s[c]);
-            const float d1 = p1 * (__uint_as_float(dp[c + 1]) - del_s[c + 1]);
+            const uint64_t p2 = f2pack(p0, p1);
+            float d0, d1;
+            f2unpack(f2mul(p2, f2add(f2pack_u(dp[c], dp[c + 1]), nd2[c >> 1])), d0, d1);
             pk[c >> 1] = pack_bf16(p0, p1);
             dk[c >> 1] = pack_bf16(d0, d1);
           }
@@ -623,8 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       const bool qvalid = qslot < pm.S;
       const int qpos = qvalid ? pm.pos(qslot) : -1;
       const size_t vo = ((size_t)u.b * a.sh.Hq + u.h) * a.Spad + qslot;
-      const float lse2 = a.lse_l2[vo];
-      const float del = a.delta[vo];
+      const float nlse2 = a.lse_l2[vo];  // -lse*log2e
+      const float ndel = a.delta[vo];    // -D
       int qmin, qmax;
       pm.range(u.t * TK, u.t * TK + TK, qmin, qmax);
       int i = 0;
@@ -644,15 +651,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         tmem_ld32(tmem + lane_base + C::T_DP + buf * BK + g * HC, dp);
         tmem_ld_wait();
         uint32_t dk[16];
+        const uint64_t sl2x2 = f2pack(sl2, sl2);
+        const uint64_t nl2 = f2pack(nlse2, nlse2);
+        const uint64_t nd2 = f2pack(ndel, ndel);
 #pragma unroll
         for (int c = 0; c < HC; c += 2) {
-          float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse2));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2));
+          float p0, p1;
+          f2unpack(f2fma(f2pack_u(sv[c], sv[c + 1]), sl2x2, nl2), p0, p1);
+          p0 = fast_exp2(p0);
+          p1 = fast_exp2(p1);
           if (!full) {
             p0 = (kp_s[c] <= qpos) ? p0 : 0.f;
             p1 = (kp_s[c + 1] <= qpos) ? p1 : 0.f;
           }
-          dk[c >> 1] = pack_bf16(p0 * (__uint_as_float(dp[c]) - del), p1 * (__uint_as_float(dp[c + 1]) - del));
+          float d0, d1;
+          f2unpack(f2mul(f2pack(p0, p1), f2add(f2pack_u(dp[c], dp[c + 1]), nd2)), d0, d1);
+          dk[c >> 1] = pack_bf16(d0, d1);
         }
         tmem_st16(tmem + lane_base + C::T_S + buf * BK + g * (HC / 2), dk);
         tmem_st_wait();

@@ -16,12 +16,17 @@
 // the same number of tiles).  Units are sorted heaviest first on the host
 // and dealt to the CTAs in snake order.
 //
-// CTA = 10 warps, one CTA per SM (all 512 TMEM columns):
+// CTA = 12 warps, one CTA per SM (all 512 TMEM columns):
 //   warps 0-3  softmax group 0 (query tile 0, one thread per row)
 //   warps 4-7  softmax group 1 (query tile 1)
 //   warp  8    TMA producer: Q tiles, then K and V tiles into two rings
 //   warp  9    MMA issuer (one thread): S_t = Q_t K^T into TMEM, and
 //              O_t += P_t V with P_t read straight from TMEM
+//   warps 10-11 idle (they complete the third warpgroup)
+// setmaxnreg moves registers from the producer/MMA warpgroup (120 each) to
+// the softmax warpgroups (192 each), so a thread holds its row's 128
+// scores in registers: one TMEM load wait per tile, then max, exp2 and the
+// packed-bf16 P, with fp32 pair (f32x2) arithmetic.
 // TMEM columns: [t*256, t*256+128) = S_t, overwritten in place by P_t as
 // packed bf16 (64 columns); [t*256+128, t*256+128+Dv) = O_t.
 // The MMA thread interleaves the groups (PV_0, QK_0', PV_1, QK_1'), so one
@@ -36,7 +41,11 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // key rows per tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168;  // 65536 / 384, rounded down to a multiple of 8
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsOther = 120;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split");
 
 template <int DQK, int DV>
 struct FwdCfg {
@@ -121,12 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ncta = gridDim.x, cta = blockIdx.x;
-
+  // each role's code sits under its own setmaxnreg, so the compiler
+  // allocates it against that role's register budget
+  if (warp >= 8) {
+  regs_dec<kRegsOther>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if ((tid & 31) == 0) {
       int ks = 0, kph = 0, vs = 0, vph = 0, qph = 0;
-      int kiss[4] = {-1, -1, -1, -1}, viss[4] = {-1, -1, -1, -1}, qiss = -1;  // parity of last issue
+      int nk = 0, nv = 0, nq = 0;  // loads issued into each ring
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int ui = unit_index(r, cta, ncta);
@@ -138,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           qph ^= 1;
         }
         mbar_expect_tx(&bar.q_full, (has1 ? 2 : 1) * C::Q_BYTES);
-        qiss = r & 1;
+        ++nq;
         for (int bx = 0; bx < DQK / 64; ++bx)
           tma_load_4d(smem + C::OFF_Q + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h0, u.t0 * BM, u.b);
         if (has1)
@@ -149,14 +161,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0; kt = next_kv_tile(pm, BN, kt, bound)) {
           if (!(ok = mbar_wait(&bar.k_empty[ks], kph ^ 1, ab))) break;
           mbar_expect_tx(&bar.k_full[ks], C::K_BYTES);
-          kiss[ks] = kph;
+          ++nk;
           for (int bx = 0; bx < DQK / 64; ++bx)
             tma_load_4d(smem + C::OFF_K + ks * C::K_BYTES + bx * BN * 128, &a.tk, &bar.k_full[ks], bx * 64,
                         u.hkv, kt * BN, u.b);
           if (++ks == C::NK) { ks = 0; kph ^= 1; }
           if (!(ok = mbar_wait(&bar.v_empty[vs], vph ^ 1, ab))) break;
           mbar_expect_tx(&bar.v_full[vs], C::V_BYTES);
-          viss[vs] = vph;
+          ++nv;
           for (int bx = 0; bx < DV / 64; ++bx)
             tma_load_4d(smem + C::OFF_V + vs * C::V_BYTES + bx * BN * 128, &a.tv, &bar.v_full[vs], bx * 64,
                         u.hkv, kt * BN, u.b);
@@ -167,11 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // let the copies already issued land (bounded) before the CTA exits
         volatile int own = 0;
         const Abort quiet{&own, a.err};
-        for (int i = 0; i < C::NK; ++i)
-          if (kiss[i] >= 0) mbar_wait(&bar.k_full[i], kiss[i], quiet);
-        for (int i = 0; i < C::NV; ++i)
-          if (viss[i] >= 0) mbar_wait(&bar.v_full[i], viss[i], quiet);
-        if (qiss >= 0) mbar_wait(&bar.q_full, qiss, quiet);
+        // slot i received its last load as load number i + NK*n; that load
+        // completes phase n of the slot's barrier
+        for (int i = 0; i < C::NK && i < nk; ++i) mbar_wait(&bar.k_full[i], ((nk - 1 - i) / C::NK) & 1, quiet);
+        for (int i = 0; i < C::NV && i < nv; ++i) mbar_wait(&bar.v_full[i], ((nv - 1 - i) / C::NV) & 1, quiet);
+        if (nq > 0) mbar_wait(&bar.q_full, (nq - 1) & 1, quiet);
       }
     }
   } else if (warp == 9) {
@@ -186,24 +198,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       int pph[2] = {0, 0};
       bool ok = true;
 
+      // descriptors advance by adding byte offsets / 16 to the start-address field
       auto issue_qk = [&](int t, int kslot) {
         const uint32_t d = tmem + t * 256;
-#pragma unroll
+        const uint64_t ad0 = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+        const uint64_t bd0 = sdesc_sw128(sK + kslot * C::K_BYTES, 16, 1024);
+#pragma unroll 1
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sQ + t * C::Q_BYTES + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + kslot * C::K_BYTES + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;  // BM == BN
+          mma_ss(d, ad0 + off, bd0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int vslot, bool acc) {
         const uint32_t d = tmem + t * 256 + 128;
         const uint32_t p = tmem + t * 256;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(sV + vslot * C::V_BYTES + kk * 16 * 128, BN * 128, 1024);
-          mma_ts(d, p + kk * 8, bd, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-        }
+        const uint64_t bd0 = sdesc_sw128(sV + vslot * C::V_BYTES, BN * 128, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(d, p + kk * 8, bd0 + ((kk * 16 * 128) >> 4), IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       };
 
       for (int r = 0; ok; ++r) {
@@ -261,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mma_commit(&bar.done);
       mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
     }
+  }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax groups
     const int t = warp >> 2;          // group
     const int row = tid & 127;        // query row in tile == TMEM lane
@@ -310,38 +324,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         sph ^= 1;
         tc_fence_after();
         float rowsum = 0.f;
-        if (cls == 0) {
-          uint32_t z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0u;
-          tmem_st32(tS + 0, z);
-          tmem_st32(tS + 32, z);
-        } else {
-          // pass 1: row maximum (masked), 32 columns at a time
-          float mx = -INFINITY;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t sr[32];
-            tmem_ld32(tS + q4 * 32, sr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float v = (cls == 1 && kp[q4 * 32 + i] > qpos) ? -INFINITY : __uint_as_float(sr[i]);
-              mx = fmaxf(mx, v);
-            }
-          }
-          mx *= sl2;
-          const float m_new = fmaxf(m, mx);
+        // online-softmax bookkeeping shared by both paths: lazy rescale of O
+        // (in TMEM) and l when the row maximum grows by more than 2^8
+        auto update_max = [&](float mx) {
+          const float m_new = fmaxf(m, mx * sl2);
           const bool need = (m == -INFINITY) ? (m_new != -INFINITY) : (m_new > m + 8.0f);
           if (__any_sync(0xffffffffu, need && j > 0)) {
             const float alpha = (need && m != -INFINITY) ? fast_exp2(m - m_new) : (need ? 0.f : 1.0f);
+            const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll 1
             for (int c0 = 0; c0 < DV; c0 += 32) {
               uint32_t o[32];
               tmem_ld32(tO + c0, o);
               tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              for (int i = 0; i < 32; i += 2) {
+                float x0, x1;
+                f2unpack(f2mul(f2pack_u(o[i], o[i + 1]), a2), x0, x1);
+                o[i] = __float_as_uint(x0);
+                o[i + 1] = __float_as_uint(x1);
+              }
               tmem_st32(tO + c0, o);
             }
             tmem_st_wait();
@@ -350,10 +352,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             l = (m == -INFINITY) ? 0.f : l * fast_exp2(m - m_new);
             m = m_new;
           }
-          const float mref = (m == -INFINITY) ? 0.f : m;
-          // pass 2: P = exp2(s*scale*log2e - m) as packed bf16; packed
-          // columns [16q, 16q+16) overwrite S columns already read
+          return (m == -INFINITY) ? 0.f : m;
+        };
+        const uint64_t sl2x2 = f2pack(sl2, sl2);
+        if (cls == 0) {
+          uint32_t z[32];
 #pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0u;
+          tmem_st32(tS + 0, z);
+          tmem_st32(tS + 32, z);
+        } else if (cls == 1) {
+          // diagonal / ragged tile: mask with the key-position table, two
+          // passes over TMEM 32 columns at a time
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t sr[32];
+            tmem_ld32(tS + q4 * 32, sr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (kp[q4 * 32 + i] <= qpos) mx = fmaxf(mx, __uint_as_float(sr[i]));
+          }
+          const float mref = update_max(mx);
+          const uint64_t negm2 = f2pack(-mref, -mref);
+          uint64_t sum2 = f2pack(0.f, 0.f);
+#pragma unroll 1
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t sr[32];
             tmem_ld32(tS + q4 * 32, sr);
@@ -361,23 +385,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), sl2, -mref));
-              float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -mref));
-              if (cls == 1) {
-                p0 = kp[q4 * 32 + 2 * i] > qpos ? 0.f : p0;
-                p1 = kp[q4 * 32 + 2 * i + 1] > qpos ? 0.f : p1;
-              }
-              rowsum += p0 + p1;
-              pk[i] = pack_bf16(p0, p1);
+              float x0, x1;
+              f2unpack(f2fma(f2pack_u(sr[2 * i], sr[2 * i + 1]), sl2x2, negm2), x0, x1);
+              x0 = kp[q4 * 32 + 2 * i] <= qpos ? fast_exp2(x0) : 0.f;
+              x1 = kp[q4 * 32 + 2 * i + 1] <= qpos ? fast_exp2(x1) : 0.f;
+              sum2 = f2add(sum2, f2pack(x0, x1));
+              pk[i] = pack_bf16(x0, x1);
             }
             tmem_st16(tS + q4 * 16, pk);
           }
-          if (cls == 1) {
-            mbar_arrive(&bar.kpos[t]);  // table read; it may be rewritten
-            ok = mbar_wait(&bar.kpos[t], kbph, ab);
-            kbph ^= 1;
-            if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          float r0, r1;
+          f2unpack(sum2, r0, r1);
+          rowsum = r0 + r1;
+          tmem_st_wait();
+          mbar_arrive(&bar.kpos[t]);  // table read; it may be rewritten
+          ok = mbar_wait(&bar.kpos[t], kbph, ab);
+          kbph ^= 1;
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        } else {
+          // every key visible: the row's 128 scores stay in registers
+          uint32_t sr[4][32];
+          tmem_ld32(tS + 0, sr[0]);
+          tmem_ld32(tS + 32, sr[1]);
+          tmem_ld32(tS + 64, sr[2]);
+          tmem_ld32(tS + 96, sr[3]);
+          tmem_ld_wait();
+          float mx4[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float v = __uint_as_float(sr[q4][0]);
+#pragma unroll
+            for (int i = 1; i < 31; i += 2)
+              v = fmax3(v, __uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1]));
+            mx4[q4] = fmaxf(v, __uint_as_float(sr[q4][31]));
           }
+          const float mref = update_max(fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]));
+          const uint64_t negm2 = f2pack(-mref, -mref);
+          uint64_t sum2 = f2pack(0.f, 0.f);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              f2unpack(f2fma(f2pack_u(sr[q4][2 * i], sr[q4][2 * i + 1]), sl2x2, negm2), x0, x1);
+              x0 = fast_exp2(x0);
+              x1 = fast_exp2(x1);
+              sum2 = f2add(sum2, f2pack(x0, x1));
+              pk[i] = pack_bf16(x0, x1);
+            }
+            tmem_st16(tS + q4 * 16, pk);
+          }
+          float r0, r1;
+          f2unpack(sum2, r0, r1);
+          rowsum = r0 + r1;
         }
         tmem_st_wait();
         tc_fence_before();
@@ -392,19 +453,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       __nv_bfloat16* orow = outp + (((size_t)u.b * pm.S + (qvalid ? qslot : 0)) * a.sh.Hq + h) * DV;
-#pragma unroll 1
-      for (int c0 = 0; c0 < DV; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c0, o);
+      {
+        uint32_t o[DV / 32][32];
+#pragma unroll
+        for (int c = 0; c < DV / 32; ++c) tmem_ld32(tO + c * 32, o[c]);
         tmem_ld_wait();
-        uint32_t pkd[16];
+        const uint64_t il2 = f2pack(inv_l, inv_l);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pkd[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (qvalid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t pkd[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2unpack(f2mul(f2pack_u(o[c][2 * i], o[c][2 * i + 1]), il2), x0, x1);
+            pkd[i] = pack_bf16(x0, x1);
+          }
+          if (qvalid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          }
         }
       }
       if (qvalid) {
@@ -426,6 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 template <int DQK, int DV>
 cudaError_t launch_t(const FwdArgs& a, int grid, cudaStream_t st) {
   auto kern = attn_fwd_kernel<DQK, DV>;
+  // setmaxnreg.inc only succeeds if the launch reserved kRegsLaunch per thread
+  cudaFuncAttributes fa;
+  cudaError_t e0 = cudaFuncGetAttributes(&fa, kern);
+  if (e0 != cudaSuccess) return e0;
+  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   // more than half of an SM's shared memory: one CTA per SM, so the CTA's
   // 512-column TMEM allocation never waits for a neighbour
   const int smem = FwdCfg<DQK, DV>::SMEM > 120 * 1024 ? FwdCfg<DQK, DV>::SMEM : 120 * 1024;

@@ -67,8 +67,8 @@ struct BwdUnit {  // dk/dv unit: one key tile of one KV head; dq unit: one query
 };
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;  // dq kernel uses 128-row boxes; dkdv uses BQ-row boxes for q/do
-  const float* lse_l2;          // [B, Hq, Spad] lse * log2(e), +inf in padding
-  const float* delta;           // [B, Hq, Spad] rowsum(dout*out), 0 in padding
+  const float* lse_l2;          // [B, Hq, Spad] -lse * log2(e), -inf in padding
+  const float* delta;           // [B, Hq, Spad] -rowsum(dout*out), 0 in padding
   void* dq;
   void* dk;
   void* dv;
