@@ -314,16 +314,8 @@ def run_ours(args, w, wname):
     cpattn.load()
 
     B, S, Hq, Hkv, Dqk, Dv, cp, lb = (w[k] for k in ("B", "S", "Hq", "Hkv", "Dqk", "Dv", "cp", "lb"))
-    g = torch.Generator(device=dev).manual_seed(args.seed + 1000 * rank)
-
-    def randn(*shape, scale=1.0):
-        x = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
-        return (x * scale).to(torch.bfloat16) if scale != 1.0 else x.to(torch.bfloat16)
-
-    q = randn(B, S, Hq, Dqk, scale=w["q_scale"])
-    k = randn(B, S, Hkv, Dqk)
-    v = randn(B, S, Hkv, Dv)
-    dout = randn(B, S, Hq, Dv)
+    q, k, v, dout = synth.attention_inputs_device(B, S, Hq, Hkv, Dqk, Dv, seed=args.seed + 1000 * rank,
+                                                  q_scale=w["q_scale"], device=dev)
     D = DECODE
     dq_, dkc, dvc, dlens = synth.decode_inputs(D["B"], D["Hq"], D["Hkv"], D["D"], D["Smax"], D["lo"], D["hi"],
                                                seed=args.seed + 4)

@@ -10,7 +10,7 @@
 #include <tuple>
 #include <vector>
 
-#include "../../include/cpattn.h"
+#include "cpattn.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -86,7 +86,6 @@ struct DevState {
   std::map<std::vector<int>, DevBuf<BwdUnit>> bwd_units;
   DevBuf<float> bwd_stats;  // lse_l2 then delta
   DevBuf<float> dec_o, dec_ml;
-  DevBuf<int> dec_cnt;
 };
 
 std::mutex g_mu;
@@ -495,9 +494,7 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
   if ((rc = need_sm103(*ds))) return rc;
   if ((rc = ensure(ds->dec_o, decode_part_o_floats(B, Hq, Hkv, Smax, D), stream, false))) return rc;
   if ((rc = ensure(ds->dec_ml, decode_part_ml_floats(B, Hq, Hkv, Smax), stream, false))) return rc;
-  if ((rc = ensure(ds->dec_cnt, (size_t)B * Hkv, stream, true))) return rc;
-  DecodeArgs a{q, kcache, vcache, lens, out, B, Hq, Hkv, Smax, D, ds->dec_o.ptr, ds->dec_ml.ptr, ds->dec_cnt.ptr,
-               ds->err};
+  DecodeArgs a{q, kcache, vcache, lens, out, B, Hq, Hkv, Smax, D, ds->dec_o.ptr, ds->dec_ml.ptr, ds->err};
   cudaError_t e;
   {
     ProfScope ps("gqa_decode", stream);
@@ -632,7 +629,6 @@ int cp_attn_release(void) {
   cudaFree(s.bwd_stats.ptr);
   cudaFree(s.dec_o.ptr);
   cudaFree(s.dec_ml.ptr);
-  cudaFree(s.dec_cnt.ptr);
   cudaFree(s.err);
   g_dev.erase(it);
   return CPATTN_OK;

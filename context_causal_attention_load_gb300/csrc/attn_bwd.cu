@@ -39,6 +39,13 @@ __device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
   return r * ncta + ((r & 1) ? (ncta - 1 - cta) : cta);
 }
 
+// Two element-wise groups each own HC consecutive columns of a row; a group
+// packs the bf16 pairs of column c into its own range, so packed column of c
+// is (c / HC) * HC + (c % HC) / 2.  The TS MMAs read 16 columns (8 packed)
+// per k-step, never straddling two groups.
+template <int HC>
+__host__ __device__ constexpr int packed_col(int c) { return (c / HC) * HC + (c % HC) / 2; }
+
 // ============================================================================
 // preprocess: -lse*log2(e) (-inf past S) and -rowsum(dO*O) (0 past S), stored
 // negated so the element-wise warps apply them with one fused multiply-add;
@@ -84,10 +91,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 // ============================================================================
 // dK / dV
 // ============================================================================
-template <int DQK, int DV, int NBUF>
+template <int DQK, int DV, int BQ_, int NBUF>
 struct KvCfg {
-  static constexpr int BQ = 64;
-  static constexpr int NQ = DQK == 192 ? 3 : 4;  // query stages
+  static constexpr int BQ = BQ_;
+  static constexpr int NQ = BQ_ == 128 ? (DQK == 64 ? 4 : 2) : (DQK == 192 ? 3 : 4);  // query stages
   static constexpr int K_BYTES = TK * DQK * 2;
   static constexpr int V_BYTES = TK * DV * 2;
   static constexpr int QT_BYTES = BQ * DQK * 2;
@@ -122,9 +129,9 @@ struct KvBars {
   uint64_t done;
 };
 
-template <int DQK, int DV, int NBUF>
+template <int DQK, int DV, int BQ_, int NBUF>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
-  using C = KvCfg<DQK, DV, NBUF>;
+  using C = KvCfg<DQK, DV, BQ_, NBUF>;
   constexpr int BQ = C::BQ;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -214,30 +221,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       int ewph[2] = {0, 0};
       bool ok = true;
 
+      // descriptors: base computed once, k-steps add byte offsets / 16 to
+      // the start-address field (keeps the single issuing thread fast)
+      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dV0 = sdesc_sw128(sV, 16, 1024);
       auto issue_sdp = [&](int buf, int stage) {
         const uint32_t st = sSt + stage * C::STAGE;
+        const uint64_t dQ0 = sdesc_sw128(st + C::ST_Q, 16, 1024), dO0 = sdesc_sw128(st + C::ST_DO, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sK + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(st + C::ST_Q + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + C::T_S + buf * BQ, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_ss(tmem + C::T_S + buf * BQ, dK0 + (((kk >> 2) * (TK * 128) + (kk & 3) * 32) >> 4),
+                 dQ0 + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sV + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(st + C::ST_DO + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + C::T_DP + buf * BQ, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_ss(tmem + C::T_DP + buf * BQ, dV0 + (((kk >> 2) * (TK * 128) + (kk & 3) * 32) >> 4),
+                 dO0 + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
       };
       auto issue_acc = [&](int buf, int stage, bool acc) {
         const uint32_t st = sSt + stage * C::STAGE;
+        const uint64_t bdo0 = sdesc_sw128(st + C::ST_DO, BQ * 128, 1024);
+        const uint64_t bq0 = sdesc_sw128(st + C::ST_Q, BQ * 128, 1024);
+        // dV chain, then dK chain (one accumulator at a time)
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint64_t bdo = sdesc_sw128(st + C::ST_DO + kk * 16 * 128, BQ * 128, 1024);
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + buf * BQ + kk * 8, bdo, IDESC_DV, (acc || kk > 0) ? 1u : 0u);
-          const uint64_t bq = sdesc_sw128(st + C::ST_Q + kk * 16 * 128, BQ * 128, 1024);
-          mma_ts(tmem + C::T_DK, tmem + C::T_DP + buf * BQ + kk * 8, bq, IDESC_DK, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + buf * BQ + packed_col<BQ / 2>(kk * 16), bdo0 + ((kk * 16 * 128) >> 4),
+                 IDESC_DV, (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::T_DK, tmem + C::T_DP + buf * BQ + packed_col<BQ / 2>(kk * 16), bq0 + ((kk * 16 * 128) >> 4),
+                 IDESC_DK, (acc || kk > 0) ? 1u : 0u);
       };
 
       for (int r = 0; ok; ++r) {
@@ -303,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     const int g = warp >> 2;              // column half
     const int row = tid & 127;            // key row == TMEM lane
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    constexpr int HC = BQ / 2;            // query columns per group (32)
+    constexpr int HC = BQ / 2;            // query columns per group
     const float sl2 = a.scale_log2;
     int qs = 0, qph = 0, acc_ph = 0;
     int sdph[2] = {0, 0};
@@ -328,38 +339,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
           sdph[buf] ^= 1;
           tc_fence_after();
           const unsigned char* st = smem + C::OFF_ST + qs * C::STAGE;
-          const float* lse_s = reinterpret_cast<const float*>(st + C::ST_LSE) + g * HC;
-          const float* del_s = reinterpret_cast<const float*>(st + C::ST_DEL) + g * HC;
-          const int* qp_s = reinterpret_cast<const int*>(st + C::ST_POS) + g * HC;
           int qmin, qmax;
           pm.range(qt * BQ, qt * BQ + BQ, qmin, qmax);
           const bool full = (kmax <= qmin) && k_inside;
-          uint32_t sv[32], dp[32];
-          tmem_ld32(tmem + lane_base + C::T_S + buf * BQ + g * HC, sv);
-          tmem_ld32(tmem + lane_base + C::T_DP + buf * BQ + g * HC, dp);
-          tmem_ld_wait();
-          uint32_t pk[16], dk[16];
           const uint64_t sl2x2 = f2pack(sl2, sl2);
-          const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse_s);  // -lse*log2e pairs
-          const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(del_s);  // -D pairs
+#pragma unroll 1
+          for (int c0 = g * HC; c0 < (g + 1) * HC; c0 += 32) {
+            const float* lse_s = reinterpret_cast<const float*>(st + C::ST_LSE) + c0;
+            const float* del_s = reinterpret_cast<const float*>(st + C::ST_DEL) + c0;
+            const int* qp_s = reinterpret_cast<const int*>(st + C::ST_POS) + c0;
+            uint32_t sv[32], dp[32];
+            tmem_ld32(tmem + lane_base + C::T_S + buf * BQ + c0, sv);
+            tmem_ld32(tmem + lane_base + C::T_DP + buf * BQ + c0, dp);
+            tmem_ld_wait();
+            uint32_t pk[16], dk[16];
+            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse_s);  // -lse*log2e pairs
+            const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(del_s);  // -D pairs
 #pragma unroll
-          for (int c = 0; c < HC; c += 2) {
-            float p0, p1;
-            f2unpack(f2fma(f2pack_u(sv[c], sv[c + 1]), sl2x2, nl2[c >> 1]), p0, p1);
-            p0 = fast_exp2(p0);
-            p1 = fast_exp2(p1);
-            if (!full) {
-              p0 = (kpos <= qp_s[c]) ? p0 : 0.f;
-              p1 = (kpos <= qp_s[c + 1]) ? p1 : 0.f;
+            for (int c = 0; c < 32; c += 2) {
+              float p0, p1;
+              f2unpack(f2fma(f2pack_u(sv[c], sv[c + 1]), sl2x2, nl2[c >> 1]), p0, p1);
+              p0 = fast_exp2(p0);
+              p1 = fast_exp2(p1);
+              if (!full) {
+                p0 = (kpos <= qp_s[c]) ? p0 : 0.f;
+                p1 = (kpos <= qp_s[c + 1]) ? p1 : 0.f;
+              }
+              const uint64_t p2 = f2pack(p0, p1);
+              float d0, d1;
+              f2unpack(f2mul(p2, f2add(f2pack_u(dp[c], dp[c + 1]), nd2[c >> 1])), d0, d1);
+              pk[c >> 1] = pack_bf16(p0, p1);
+              dk[c >> 1] = pack_bf16(d0, d1);
             }
-            const uint64_t p2 = f2pack(p0, p1);
-            float d0, d1;
-            f2unpack(f2mul(p2, f2add(f2pack_u(dp[c], dp[c + 1]), nd2[c >> 1])), d0, d1);
-            pk[c >> 1] = pack_bf16(p0, p1);
-            dk[c >> 1] = pack_bf16(d0, d1);
+            // packed bf16 pairs stay inside this group's own column range (they
+            // overwrite S / dP columns this thread has already read)
+            tmem_st16(tmem + lane_base + C::T_S + buf * BQ + packed_col<HC>(c0), pk);
+            tmem_st16(tmem + lane_base + C::T_DP + buf * BQ + packed_col<HC>(c0), dk);
           }
-          tmem_st16(tmem + lane_base + C::T_S + buf * BQ + g * (HC / 2), pk);
-          tmem_st16(tmem + lane_base + C::T_DP + buf * BQ + g * (HC / 2), dk);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&bar.ew_full[buf]);
@@ -421,10 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 // ============================================================================
 // dQ
 // ============================================================================
-template <int DQK, int DV>
+template <int DQK, int DV, int BK_, int NSB_, int NDPB_>
 struct QCfg {
-  static constexpr int BK = 64;
-  static constexpr int NS = DQK == 192 ? 3 : 4;  // key/value stages
+  static constexpr int BK = BK_;      // key rows per step
+  static constexpr int NSB = NSB_;    // S / dS TMEM buffers
+  static constexpr int NDPB = NDPB_;  // dP TMEM buffers
+  static constexpr int NS = BK_ == 128 ? 2 : (DQK == 192 ? 3 : 4);  // key/value stages
   static constexpr int Q_BYTES = TK * DQK * 2;
   static constexpr int DO_BYTES = TK * DV * 2;
   static constexpr int K_BYTES = BK * DQK * 2;
@@ -440,9 +458,9 @@ struct QCfg {
   static constexpr int OFF_MISC = OFF_BAR + 256;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static constexpr int T_S = 0;        // S / dS (bf16), buffer b at b*BK
-  static constexpr int T_DP = 2 * BK;  // dP
-  static constexpr int T_DQ = 4 * BK;
+  static constexpr int T_S = 0;                 // S / dS (bf16), buffer b at b*BK
+  static constexpr int T_DP = NSB * BK;         // dP, buffer b at T_DP + b*BK
+  static constexpr int T_DQ = (NSB + NDPB) * BK;
   static_assert(T_DQ + DQK <= 512, "TMEM budget");
 };
 
@@ -454,9 +472,9 @@ struct QBars {
   uint64_t done;
 };
 
-template <int DQK, int DV>
+template <int DQK, int DV, int BK_, int NSB, int NDPB>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
-  using C = QCfg<DQK, DV>;
+  using C = QCfg<DQK, DV, BK_, NSB, NDPB>;
   constexpr int BK = C::BK;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -545,28 +563,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       int ks = 0, kph = 0, qph = 0;
       int ewph[2] = {0, 0};
       bool ok = true;
-      auto issue_sdp = [&](int buf, int stage) {
-        const uint32_t st = sSt + stage * C::STAGE;
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dO0 = sdesc_sw128(sDO, 16, 1024);
+      auto issue_s = [&](int i, int stage) {  // S_i = Q K_i^T
+        const uint64_t dK0 = sdesc_sw128(sSt + stage * C::STAGE + C::ST_K, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(st + C::ST_K + (kk >> 2) * (BK * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + C::T_S + buf * BK, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sDO + (kk >> 2) * (TK * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(st + C::ST_V + (kk >> 2) * (BK * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + C::T_DP + buf * BK, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_ss(tmem + C::T_S + (i % NSB) * BK, dQ0 + (((kk >> 2) * (TK * 128) + (kk & 3) * 32) >> 4),
+                 dK0 + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
       };
-      auto issue_dq = [&](int buf, int stage, bool acc) {
-        const uint32_t st = sSt + stage * C::STAGE;
+      auto issue_dp = [&](int i, int stage) {  // dP_i = dO V_i^T
+        const uint64_t dV0 = sdesc_sw128(sSt + stage * C::STAGE + C::ST_V, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(st + C::ST_K + kk * 16 * 128, BK * 128, 1024);
-          mma_ts(tmem + C::T_DQ, tmem + C::T_S + buf * BK + kk * 8, bd, IDESC_DQ, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_ss(tmem + C::T_DP + (i % NDPB) * BK, dO0 + (((kk >> 2) * (TK * 128) + (kk & 3) * 32) >> 4),
+                 dV0 + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
+      };
+      auto issue_dq = [&](int i, int stage, bool acc) {  // dQ += dS_i K_i
+        const uint64_t bd0 = sdesc_sw128(sSt + stage * C::STAGE + C::ST_K, BK * 128, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_ts(tmem + C::T_DQ, tmem + C::T_S + (i % NSB) * BK + packed_col<BK / 2>(kk * 16), bd0 + ((kk * 16 * 128) >> 4),
+                 IDESC_DQ, (acc || kk > 0) ? 1u : 0u);
       };
       for (int r = 0; ok; ++r) {
         const int ui = unit_index(r, cta, ncta);
@@ -580,28 +597,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         int cur_stage = ks;
         if (!(ok = mbar_wait(&bar.kv_full[ks], kph, ab))) break;
         tc_fence_after();
-        issue_sdp(0, ks);
+        issue_s(0, ks);
+        issue_dp(0, ks);
         mma_commit(&bar.sd_full[0]);
         if (++ks == C::NS) { ks = 0; kph ^= 1; }
+        // Step i: S_{i+1} / dP_{i+1} go ahead of dQ_i when they have a
+        // buffer of their own (NSB / NDPB == 2); otherwise they follow dQ_i,
+        // whose reads of dS_i they would overwrite (tcgen05 MMAs from one
+        // thread execute in order).
         for (int i = 0; ok; ++i) {
           const int nkt = next_kv_tile(pm, BK, kt, bound);
           const int next_stage = ks;
           if (nkt >= 0) {
             if (!(ok = mbar_wait(&bar.kv_full[ks], kph, ab))) break;
             tc_fence_after();
-            issue_sdp((i + 1) & 1, ks);
-            mma_commit(&bar.sd_full[(i + 1) & 1]);
-            if (++ks == C::NS) { ks = 0; kph ^= 1; }
+            if (NSB == 2) issue_s(i + 1, ks);
+            if (NDPB == 2) issue_dp(i + 1, ks);
+            if (NSB == 2 && NDPB == 2) mma_commit(&bar.sd_full[(i + 1) & 1]);
           } else {
             mma_commit(&bar.q_empty);  // every S/dP MMA (the readers of Q and dO) is already issued
           }
-          const int buf = i & 1;
-          if (!(ok = mbar_wait(&bar.ew_full[buf], ewph[buf], ab))) break;
-          ewph[buf] ^= 1;
+          if (!(ok = mbar_wait(&bar.ew_full[i & 1], ewph[i & 1], ab))) break;
+          ewph[i & 1] ^= 1;
           tc_fence_after();
-          issue_dq(buf, cur_stage, i > 0);
+          issue_dq(i, cur_stage, i > 0);
           mma_commit(&bar.kv_empty[cur_stage]);
           if (nkt < 0) break;
+          if (NSB == 1) issue_s(i + 1, next_stage);
+          if (NDPB == 1) issue_dp(i + 1, next_stage);
+          if (NSB == 1 || NDPB == 1) mma_commit(&bar.sd_full[(i + 1) & 1]);
+          if (++ks == C::NS) { ks = 0; kph ^= 1; }
           cur_stage = next_stage;
           kt = nkt;
         }
@@ -642,33 +667,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         sdph[buf] ^= 1;
         tc_fence_after();
-        const int* kp_s = reinterpret_cast<const int*>(smem + C::OFF_ST + ks * C::STAGE + C::ST_POS) + g * HC;
         int kmin, kmax;
         pm.range(kt * BK, kt * BK + BK, kmin, kmax);
         const bool full = (kmax <= qmin) && (kt * BK + BK <= pm.S);
-        uint32_t sv[32], dp[32];
-        tmem_ld32(tmem + lane_base + C::T_S + buf * BK + g * HC, sv);
-        tmem_ld32(tmem + lane_base + C::T_DP + buf * BK + g * HC, dp);
-        tmem_ld_wait();
-        uint32_t dk[16];
         const uint64_t sl2x2 = f2pack(sl2, sl2);
         const uint64_t nl2 = f2pack(nlse2, nlse2);
         const uint64_t nd2 = f2pack(ndel, ndel);
+        const uint32_t tS = tmem + lane_base + C::T_S + (i % NSB) * BK;
+        const uint32_t tP = tmem + lane_base + C::T_DP + (i % NDPB) * BK;
+#pragma unroll 1
+        for (int c0 = g * HC; c0 < (g + 1) * HC; c0 += 32) {
+          const int* kp_s = reinterpret_cast<const int*>(smem + C::OFF_ST + ks * C::STAGE + C::ST_POS) + c0;
+          uint32_t sv[32], dp[32];
+          tmem_ld32(tS + c0, sv);
+          tmem_ld32(tP + c0, dp);
+          tmem_ld_wait();
+          uint32_t dk[16];
 #pragma unroll
-        for (int c = 0; c < HC; c += 2) {
-          float p0, p1;
-          f2unpack(f2fma(f2pack_u(sv[c], sv[c + 1]), sl2x2, nl2), p0, p1);
-          p0 = fast_exp2(p0);
-          p1 = fast_exp2(p1);
-          if (!full) {
-            p0 = (kp_s[c] <= qpos) ? p0 : 0.f;
-            p1 = (kp_s[c + 1] <= qpos) ? p1 : 0.f;
+          for (int c = 0; c < 32; c += 2) {
+            float p0, p1;
+            f2unpack(f2fma(f2pack_u(sv[c], sv[c + 1]), sl2x2, nl2), p0, p1);
+            p0 = fast_exp2(p0);
+            p1 = fast_exp2(p1);
+            if (!full) {
+              p0 = (kp_s[c] <= qpos) ? p0 : 0.f;
+              p1 = (kp_s[c + 1] <= qpos) ? p1 : 0.f;
+            }
+            float d0, d1;
+            f2unpack(f2mul(f2pack(p0, p1), f2add(f2pack_u(dp[c], dp[c + 1]), nd2)), d0, d1);
+            dk[c >> 1] = pack_bf16(d0, d1);
           }
-          float d0, d1;
-          f2unpack(f2mul(f2pack(p0, p1), f2add(f2pack_u(dp[c], dp[c + 1]), nd2)), d0, d1);
-          dk[c >> 1] = pack_bf16(d0, d1);
+          // dS as packed bf16 inside this group's own column range
+          tmem_st16(tS + packed_col<HC>(c0), dk);
         }
-        tmem_st16(tmem + lane_base + C::T_S + buf * BK + g * (HC / 2), dk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar.ew_full[buf]);
@@ -722,6 +753,10 @@ cudaError_t launch_k(K kern, int smem, int grid, const BwdArgs& a, cudaStream_t 
 
 }  // namespace
 
+// Measured on GB300: 64-row steps with double-buffered S/dP (the element-wise
+// work of one step overlaps the MMAs of the next, and four load stages keep
+// the TMA copies off the critical path) beat 128-row steps, whose wider MMAs
+// do not pay for the lost overlap and the shallower two-stage load ring.
 int bwd_dkdv_q_tile(int) { return 64; }
 int bwd_dq_kv_tile(int) { return 64; }
 
@@ -737,15 +772,18 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
 }
 
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, int grid, cudaStream_t st) {
-  if (a.sh.Dqk == 64) return launch_k(attn_bwd_dkdv_kernel<64, 64, 2>, KvCfg<64, 64, 2>::SMEM, grid, a, st);
-  if (a.sh.Dqk == 128) return launch_k(attn_bwd_dkdv_kernel<128, 128, 2>, KvCfg<128, 128, 2>::SMEM, grid, a, st);
-  return launch_k(attn_bwd_dkdv_kernel<192, 128, 1>, KvCfg<192, 128, 1>::SMEM, grid, a, st);
+  if (a.sh.Dqk == 64) return launch_k(attn_bwd_dkdv_kernel<64, 64, 64, 2>, KvCfg<64, 64, 64, 2>::SMEM, grid, a, st);
+  if (a.sh.Dqk == 128)
+    return launch_k(attn_bwd_dkdv_kernel<128, 128, 64, 2>, KvCfg<128, 128, 64, 2>::SMEM, grid, a, st);
+  // MLA: dK needs 192 TMEM columns, so S^T / dP^T are single-buffered
+  return launch_k(attn_bwd_dkdv_kernel<192, 128, 64, 1>, KvCfg<192, 128, 64, 1>::SMEM, grid, a, st);
 }
 
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, int grid, cudaStream_t st) {
-  if (a.sh.Dqk == 64) return launch_k(attn_bwd_dq_kernel<64, 64>, QCfg<64, 64>::SMEM, grid, a, st);
-  if (a.sh.Dqk == 128) return launch_k(attn_bwd_dq_kernel<128, 128>, QCfg<128, 128>::SMEM, grid, a, st);
-  return launch_k(attn_bwd_dq_kernel<192, 128>, QCfg<192, 128>::SMEM, grid, a, st);
+  if (a.sh.Dqk == 64) return launch_k(attn_bwd_dq_kernel<64, 64, 64, 2, 2>, QCfg<64, 64, 64, 2, 2>::SMEM, grid, a, st);
+  if (a.sh.Dqk == 128)
+    return launch_k(attn_bwd_dq_kernel<128, 128, 64, 2, 2>, QCfg<128, 128, 64, 2, 2>::SMEM, grid, a, st);
+  return launch_k(attn_bwd_dq_kernel<192, 128, 64, 2, 2>, QCfg<192, 128, 64, 2, 2>::SMEM, grid, a, st);
 }
 
 }  // namespace cpattn

@@ -9,9 +9,8 @@ namespace cpattn {
 cudaError_t launch_lb_permute(const void* src, void* dst, int B, int S, long long row_bytes, int cp,
                               int inverse, int num_sms, cudaStream_t st);
 
-// split-K decode: scratch = partial (o, m, l) per split and one counter per
-// (batch, kv head); counters must be zero before the first launch and are
-// left zero by every launch.
+// split-K decode: scratch = partial (o, m, l) per 128-position slice; a
+// second kernel merges the slices of each (batch, kv head).
 struct DecodeArgs {
   const void* q;
   const void* kc;
@@ -21,7 +20,6 @@ struct DecodeArgs {
   int B, Hq, Hkv, Smax, D;
   float* part_o;    // [B*Hkv][max_split][G][D]
   float* part_ml;   // [B*Hkv][max_split][G][2]
-  int* counters;    // [B*Hkv]
   int* err;
 };
 constexpr int kDecodeSplit = 128;  // cache positions per CTA

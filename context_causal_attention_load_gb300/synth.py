@@ -9,7 +9,7 @@ very same bf16 values.
 
 import torch
 
-__all__ = ["attention_inputs", "decode_inputs", "to_f64"]
+__all__ = ["attention_inputs", "attention_inputs_device", "decode_inputs", "to_f64"]
 
 
 def _normal(shape, seed, scale=1.0):
@@ -28,6 +28,23 @@ def attention_inputs(B, S, Hq, Hkv, Dqk, Dv, seed=0, q_scale=1.0):
     k = _normal((B, S, Hkv, Dqk), seed + 1)
     v = _normal((B, S, Hkv, Dv), seed + 2)
     dout = _normal((B, S, Hq, Dv), seed + 3)
+    return q, k, v, dout
+
+
+def attention_inputs_device(B, S, Hq, Hkv, Dqk, Dv, seed=0, q_scale=1.0, device="cuda"):
+    """Same shapes and distributions as ``attention_inputs`` but drawn by a
+    seeded generator on the GPU (for workloads too large to draw on the host;
+    the values differ from the host draw of the same seed)."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+
+    def draw(shape, scale=1.0):
+        x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+        return (x * scale).to(torch.bfloat16) if scale != 1.0 else x.to(torch.bfloat16)
+
+    q = draw((B, S, Hq, Dqk), q_scale)
+    k = draw((B, S, Hkv, Dqk))
+    v = draw((B, S, Hkv, Dv))
+    dout = draw((B, S, Hq, Dv))
     return q, k, v, dout
 
 

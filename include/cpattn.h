@@ -136,7 +136,7 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
  * driver's allocation path and its implicit synchronisation, processes
  * that keep nearly all of HBM for their KV cache).
  * Same arguments, layouts and results as gqa_decode.  The split partials
- * and arrival counters live in one fixed 8 MiB device array inside the
+ * live in one fixed 8 MiB device array inside the
  * library (every GPU that loads the library holds it until the process
  * exits); the caller still passes all inputs and outputs.  A shape whose
  * scratch does not fit is rejected with CPATTN_ERR_INVALID_ARG before any
@@ -145,9 +145,10 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
  * D=128 needs 3.2 MiB).
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  Every
- * call shares the one array and each call clears the counters it uses, so
- * calls whose executions overlap on the GPU (different streams, or several
- * host threads) race: serialise them.  lens outside [0, Smax] are clamped
+ * call shares the one array (each call writes every entry it later reads,
+ * so nothing an earlier call left behind is used), and calls whose
+ * executions overlap on the GPU (different streams, or several host
+ * threads) race on it: serialise them.  lens outside [0, Smax] are clamped
  * as in gqa_decode; the flag goes to the array's own error word and is not
  * reported by cp_attn_check_device.
  */

@@ -180,6 +180,8 @@ def test_bwd_parity(cfg):
     (3, 8, 8, 128, 300, 1, 300),          # G = 1, ragged splits
     (4, 16, 1, 64, 700, 200, 700),        # G = 16, D = 64
     (2, 6, 2, 128, 512, 255, 257),        # G = 3, around a split boundary
+    (2, 16, 1, 128, 640, 300, 640),       # G = 16, D = 128 (two-stage ring)
+    (1, 2, 1, 128, 128, 128, 128),        # one slice: no merge pass
 ])
 def test_decode_parity(cfg):
     B, Hq, Hkv, D, Smax, lo, hi = cfg
