@@ -2,25 +2,23 @@
 //
 // "Add Pallas GPU decode attention in Maxtext inference" (MaxText pull
 // request 1066), Description: decode attention (one new query token per
-// sequence against the KV cache) through a grouped-query kernel.  Work is
-// cut into items (batch b, KV head g, a slice of 128 cache positions); an
-// item serves all G = Hq/Hkv query heads of the group from a single read
-// of its K/V rows, so the cache is streamed from HBM exactly once.
+// sequence against the KV cache) through a grouped-query kernel.  A CTA owns
+// an item (batch b, KV head g, a slice of kDecodeSplit cache positions) and
+// serves all G = Hq/Hkv query heads of the group from a single read of its
+// K/V rows, so the cache is streamed from HBM exactly once.
 //
-// Streaming: the main kernel is persistent, one CTA per SM walking items
-// cta, cta + grid, ...  A producer warp keeps several items in flight with
-// bulk copies (cp.async.bulk) of the item's K rows, V rows and the group's q
-// into a shared-memory ring (about 197 KB per SM for D = 128), so HBM sees
-// deep, continuous, register-free concurrency while two groups of four
-// compute warps take alternate items.  Compute, per warp of 32 positions: LPT lanes
-// work on one position (each lane holds D/LPT columns of every head's q in
-// registers), form G partial dot products, reduce them with log2(LPT)
-// shuffles, and update a running (max, sum, o) per lane group with a lazy
-// rescale (o is rescaled only when the maximum grows by more than 8 in the
-// log2 domain).  Lane groups and warps are merged in the CTA; an item that
-// covers a whole sequence writes the output, otherwise it writes its
-// partial (m, l, o) and a second, small kernel merges the slices of each
-// (b, g).  No atomics, no fences on the streaming path.
+// Streaming: small CTAs (one warp per 32 positions), several resident per
+// SM.  At entry one thread issues bulk copies (cp.async.bulk) of the
+// slice's K rows with the group's q, and of its V rows, on two mbarriers, so
+// the score pass starts as soon as K lands while V is still in flight.
+// Compute, per warp of 32 positions: LPT lanes work on one position (each
+// lane holds D/LPT columns of every head's q in registers) and form G
+// partial dot products reduced with log2(LPT) shuffles.  The CTA's maximum
+// per head is agreed before any exponential, so the value pass needs no
+// rescaling and the lane groups' partial sums merge by plain addition in
+// shared memory.  An item covering a whole sequence writes the output;
+// otherwise it writes (o, m, l) and a second, small kernel merges the slices
+// of each (b, g).  No atomics, no fences.
 #include <mutex>
 
 #include "common.cuh"
@@ -30,42 +28,33 @@ namespace cpattn {
 
 namespace {
 
-constexpr int kGroupWarps = 4;                     // one item per group, 32 positions per warp
-constexpr int kGroups = 2;                         // groups take alternate items
-constexpr int kComputeWarps = kGroups * kGroupWarps;
-constexpr int kThreads = (kComputeWarps + 1) * 32; // + one producer warp
-static_assert(kGroupWarps * 32 == kDecodeSplit, "32 positions per warp");
+constexpr int kWarps = kDecodeSplit / 32;  // one warp per 32 positions
+constexpr int kThreads = kWarps * 32;
 
 template <int D, int GMAX>
 struct DecCfg {
   // lanes per position: keep q and o at 64 registers per lane
   static constexpr int LPT0 = D * GMAX / 64;
   static constexpr int LPT = LPT0 < 8 ? 8 : (LPT0 > 32 ? 32 : LPT0);
-  static constexpr int DPL = D / LPT;  // columns per lane
-  static constexpr int TPI = 32 / LPT; // positions per warp step
+  static constexpr int DPL = D / LPT;   // columns per lane
+  static constexpr int TPI = 32 / LPT;  // positions per warp step
+  static constexpr int NSTEP = 32 / TPI;
   static constexpr int NCH = DPL >= 8 ? DPL / 8 : 1;  // 16-byte chunks per lane (DPL >= 8)
   static_assert(DPL == 4 || DPL % 8 == 0, "lane column split");
-  // ring depth: as many items as fit next to the merge buffers
-  static constexpr int STAGE_BYTES = 2 * kDecodeSplit * D * 2 + GMAX * D * 2;
-  static constexpr int MERGE_BYTES = kComputeWarps * GMAX * (D + 2) * 4 + 1024;
-  static constexpr int NST0 = (225 * 1024 - MERGE_BYTES) / STAGE_BYTES;
-  static constexpr int NST = NST0 > 6 ? 6 : NST0;
-  static_assert(NST >= 2, "ring of at least two items");
 };
 
 template <int D, int GMAX>
 struct DecSmem {
-  static constexpr int kStages = DecCfg<D, GMAX>::NST;
-  __nv_bfloat16 k[kStages][kDecodeSplit][D];
-  __nv_bfloat16 v[kStages][kDecodeSplit][D];
-  __nv_bfloat16 q[kStages][GMAX][D];
-  float wo[kComputeWarps][GMAX][D];
-  float wm[kComputeWarps][GMAX];
-  float wl[kComputeWarps][GMAX];
-  float cm[kGroups][GMAX];
-  float cl[kGroups][GMAX];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  using C = DecCfg<D, GMAX>;
+  // K then V; after the value pass the pair is reused for the lane groups' sums
+  __nv_bfloat16 k[kDecodeSplit][D];
+  __nv_bfloat16 v[kDecodeSplit][D];
+  __nv_bfloat16 q[GMAX][D];
+  float sc[kDecodeSplit][GMAX];  // scores (log2 domain), -inf past the cache length
+  float wm[kWarps][GMAX];
+  float lsum[kWarps][C::TPI][GMAX];
+  uint64_t bar_k, bar_v;
+  static_assert(kWarps * C::TPI * GMAX * D * 4 <= 2 * kDecodeSplit * D * 2, "partial sums fit over K and V");
 };
 
 // the lane's columns: NCH chunks of 8 (chunk sub + j*LPT), or 4 columns when DPL == 4
@@ -94,238 +83,173 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* row, int sub, floa
   }
 }
 
-// work item i = ((b * Hkv + g) * max_split + sp): kind 0 skip, 1 empty cache
-// (write zeros), 2 attend over positions [sp*128, min(len, sp*128+128))
-struct Item {
-  int kind, b, g, sp, len, nsplit;
-};
-__device__ __forceinline__ Item decode_item(const DecodeArgs& a, int i, int max_split, bool flag_errors) {
-  Item it;
-  const int bg = i / max_split;
-  it.sp = i - bg * max_split;
-  it.b = bg / a.Hkv;
-  it.g = bg - it.b * a.Hkv;
-  int len = a.lens[it.b];
-  if (len < 0 || len > a.Smax) {
-    if (flag_errors && it.sp == 0 && it.g == 0) atomicExch(a.err, DEV_LENS_CLAMPED);
-    len = len < 0 ? 0 : a.Smax;
-  }
-  it.len = len;
-  it.nsplit = (len + kDecodeSplit - 1) / kDecodeSplit;
-  it.kind = len == 0 ? (it.sp == 0 ? 1 : 0) : (it.sp < it.nsplit ? 2 : 0);
-  return it;
-}
-
-__device__ __forceinline__ void group_sync(int grp) { named_bar(1 + grp, kGroupWarps * 32); }
-
-// Persistent: each CTA walks items cta, cta + grid, ...; the producer warp
-// keeps up to kStages slices in flight while the compute warps consume.
 template <int D, int GMAX>
-__global__ void __launch_bounds__(kThreads, 1) gqa_decode_kernel(DecodeArgs a, float scale_log2, int max_split) {
+__global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, float scale_log2) {
   using C = DecCfg<D, GMAX>;
-  constexpr int LPT = C::LPT, DPL = C::DPL, TPI = C::TPI, kStages = C::NST;
+  constexpr int LPT = C::LPT, DPL = C::DPL, TPI = C::TPI, NSTEP = C::NSTEP;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   auto& sm = *reinterpret_cast<DecSmem<D, GMAX>*>(smem_raw);
-  static_assert(sizeof(DecSmem<D, GMAX>) <= 232448, "shared memory budget");
+  const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int max_split = gridDim.x;
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int total = a.B * a.Hkv * max_split;
-  const int ncta = gridDim.x, cta = blockIdx.x;
+
+  int len = a.lens[b];
+  if (len < 0 || len > a.Smax) {
+    if (sp == 0 && g == 0 && tid == 0) atomicExch(a.err, DEV_LENS_CLAMPED);
+    len = len < 0 ? 0 : a.Smax;
+  }
+  const int nsplit = (len + kDecodeSplit - 1) / kDecodeSplit;
+  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.Hq + (size_t)g * G) * D;
+  if (len == 0) {  // empty cache: the output is defined as zero
+    if (sp == 0)
+      for (int x = tid; x < G * D; x += kThreads) og[x] = __float2bfloat16(0.f);
+    return;
+  }
+  if (sp >= nsplit) return;
+
+  const int t0 = sp * kDecodeSplit;
+  const int n = min(kDecodeSplit, len - t0);
   volatile int abort_flag = 0;
   const Abort ab{&abort_flag, a.err};
-
   if (tid == 0) {
-    for (int s2 = 0; s2 < kStages; ++s2) {
-      mbar_init(&sm.full[s2], 1);
-      mbar_init(&sm.empty[s2], kGroupWarps * 32);
-    }
+    mbar_init(&sm.bar_k, 1);
+    mbar_init(&sm.bar_v, 1);
     fence_mbar_init();
+    const size_t row0 = ((size_t)b * a.Hkv + g) * (size_t)a.Smax + t0;
+    const uint32_t bytes = (uint32_t)n * D * 2, qbytes = (uint32_t)G * D * 2;
+    mbar_expect_tx(&sm.bar_k, bytes + qbytes);
+    bulk_load(&sm.k[0][0], static_cast<const __nv_bfloat16*>(a.kc) + row0 * D, bytes, &sm.bar_k);
+    bulk_load(&sm.q[0][0], static_cast<const __nv_bfloat16*>(a.q) + ((size_t)b * a.Hq + (size_t)g * G) * D, qbytes,
+              &sm.bar_k);
+    mbar_expect_tx(&sm.bar_v, bytes);
+    bulk_load(&sm.v[0][0], static_cast<const __nv_bfloat16*>(a.vc) + row0 * D, bytes, &sm.bar_v);
   }
-  __syncthreads();
+  __syncthreads();  // barriers initialised before anyone waits on them
 
-  if (warp == kComputeWarps) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      int st = 0, ph = 0;
-      for (int i = cta; i < total; i += ncta) {
-        const Item it = decode_item(a, i, max_split, true);
-        if (it.kind != 2) continue;
-        if (!mbar_wait(&sm.empty[st], ph ^ 1, ab)) break;
-        const int t0 = it.sp * kDecodeSplit;
-        const int n = min(kDecodeSplit, it.len - t0);
-        const uint32_t bytes = (uint32_t)n * D * 2;
-        const size_t row0 = ((size_t)it.b * a.Hkv + it.g) * (size_t)a.Smax + t0;
-        const uint32_t qbytes = (uint32_t)G * D * 2;
-        mbar_expect_tx(&sm.full[st], 2 * bytes + qbytes);
-        bulk_load(&sm.k[st][0][0], static_cast<const __nv_bfloat16*>(a.kc) + row0 * D, bytes, &sm.full[st]);
-        bulk_load(&sm.v[st][0][0], static_cast<const __nv_bfloat16*>(a.vc) + row0 * D, bytes, &sm.full[st]);
-        bulk_load(&sm.q[st][0][0], static_cast<const __nv_bfloat16*>(a.q) + ((size_t)it.b * a.Hq + (size_t)it.g * G) * D,
-                  qbytes, &sm.full[st]);
-        if (++st == kStages) { st = 0; ph ^= 1; }
-      }
+  const int sub = lane % LPT;  // column slot within the position's lanes
+  const int grp = lane / LPT;  // position slot within the warp step
+  const int wbase = warp * 32;
+  // ---- score pass (K) -------------------------------------------------------
+  float mx[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) mx[h] = -INFINITY;
+  const bool okk = mbar_wait(&sm.bar_k, 0, ab);
+  {
+    uint64_t q2[GMAX][DPL / 2];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      float x[DPL];
+      load_row<D, GMAX>(&sm.q[h < G ? h : 0][0], sub, x);
+#pragma unroll
+      for (int j = 0; j < DPL / 2; ++j)
+        q2[h][j] = h < G ? f2pack(x[2 * j] * scale_log2, x[2 * j + 1] * scale_log2) : f2pack(0.f, 0.f);
     }
-  } else {
-    // ---------------------------------------------------------- compute warps
-    // Group gi (warps 4gi .. 4gi+3) takes every other loaded item.  Control
-    // flow is uniform inside a group (a failed wait only skips arithmetic),
-    // so its named barrier always completes.
-    const int gi = warp / kGroupWarps;
-    const int gw = warp % kGroupWarps;     // warp within the group
-    const int gt = tid - gi * kGroupWarps * 32;
-    const int sub = lane % LPT;            // column slot within the position's lanes
-    const int grp = lane / LPT;            // position slot within the warp step
-    int nload = 0;                         // loaded items seen so far (ring index)
-    for (int i = cta; i < total; i += ncta) {
-      const Item it = decode_item(a, i, max_split, false);
-      if (it.kind == 0) continue;
-      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + ((size_t)it.b * a.Hq + (size_t)it.g * G) * D;
-      if (it.kind == 1) {  // empty cache: the output is defined as zero
-        if (gi == 0)
-          for (int x = gt; x < G * D; x += kGroupWarps * 32) og[x] = __float2bfloat16(0.f);
-        continue;
-      }
-      const int n_item = nload++;
-      if ((n_item % kGroups) != gi) continue;
-      const int st = n_item % kStages;
-      const int ph = (n_item / kStages) & 1;
-      const int t0 = it.sp * kDecodeSplit;
-      const int n = min(kDecodeSplit, it.len - t0);
-      const bool ok = mbar_wait(&sm.full[st], ph, ab);
-      // q of the group (bulk-copied with the slice) as fp32 pairs, pre-scaled to log2
-      uint64_t q2[GMAX][DPL / 2];
+#pragma unroll 4
+    for (int st = 0; st < NSTEP; ++st) {
+      const int tt = wbase + st * TPI + grp;
+      const bool valid = okk && tt < n;
+      float kx[DPL];
+      load_row<D, GMAX>(&sm.k[valid ? tt : 0][0], sub, kx);
+      float sv[GMAX];
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
-        float x[DPL];
-        load_row<D, GMAX>(&sm.q[st][h < G ? h : 0][0], sub, x);
+        uint64_t acc = f2pack(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < DPL / 2; ++j)
-          q2[h][j] = h < G ? f2pack(x[2 * j] * scale_log2, x[2 * j + 1] * scale_log2) : f2pack(0.f, 0.f);
+        for (int j = 0; j < DPL / 2; ++j) acc = f2fma(q2[h][j], f2pack(kx[2 * j], kx[2 * j + 1]), acc);
+        float a0, a1;
+        f2unpack(acc, a0, a1);
+        sv[h] = a0 + a1;
       }
-      uint64_t o2[GMAX][DPL / 2];
-      float m[GMAX], l[GMAX];
+#pragma unroll
+      for (int off = 1; off < LPT; off <<= 1)
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) sv[h] += __shfl_xor_sync(0xffffffffu, sv[h], off);
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
-#pragma unroll
-        for (int j = 0; j < DPL / 2; ++j) o2[h][j] = f2pack(0.f, 0.f);
+        sv[h] = valid ? sv[h] : -INFINITY;
+        mx[h] = fmaxf(mx[h], sv[h]);
+        if (sub == (h % LPT)) sm.sc[tt][h] = sv[h];  // one writer per (position, head)
       }
-      const int wbase = gw * 32;
-      if (ok && wbase < n) {
-        const int steps = (min(32, n - wbase) + TPI - 1) / TPI;
-        for (int s3 = 0; s3 < steps; ++s3) {
-          const int tt = wbase + s3 * TPI + grp;  // position within the slice
-          const bool valid = tt < n;
-          float kx[DPL];
-          load_row<D, GMAX>(&sm.k[st][valid ? tt : 0][0], sub, kx);
-          float s[GMAX];
-#pragma unroll
-          for (int h = 0; h < GMAX; ++h) {
-            uint64_t acc = f2pack(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < DPL / 2; ++j) acc = f2fma(q2[h][j], f2pack(kx[2 * j], kx[2 * j + 1]), acc);
-            float a0, a1;
-            f2unpack(acc, a0, a1);
-            s[h] = a0 + a1;
-          }
-#pragma unroll
-          for (int off = 1; off < LPT; off <<= 1)
-#pragma unroll
-            for (int h = 0; h < GMAX; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
-          float vx[DPL];
-          load_row<D, GMAX>(&sm.v[st][valid ? tt : 0][0], sub, vx);
-#pragma unroll
-          for (int h = 0; h < GMAX; ++h) {
-            if (h >= G || !valid) continue;
-            if (s[h] > m[h] + 8.0f) {  // lazy rescale: only when the max grows by > 2^8
-              const float alpha = (m[h] == -INFINITY) ? 0.f : fast_exp2(m[h] - s[h]);
-              l[h] *= alpha;
-              const uint64_t a2 = f2pack(alpha, alpha);
-#pragma unroll
-              for (int j = 0; j < DPL / 2; ++j) o2[h][j] = f2mul(o2[h][j], a2);
-              m[h] = s[h];
-            }
-            const float p = fast_exp2(s[h] - m[h]);
-            l[h] += p;
-            const uint64_t p2 = f2pack(p, p);
-#pragma unroll
-            for (int j = 0; j < DPL / 2; ++j) o2[h][j] = f2fma(p2, f2pack(vx[2 * j], vx[2 * j + 1]), o2[h][j]);
-          }
-        }
-      }
-      mbar_arrive(&sm.empty[st]);  // this thread is done with the slice
-      // merge the position groups of the warp (lanes sub, sub+LPT, ...)
-#pragma unroll
-      for (int off = LPT; off < 32; off <<= 1) {
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
-          const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
-          const float mn = fmaxf(m[h], mo);
-          const float a1 = (m[h] == -INFINITY) ? 0.f : fast_exp2(m[h] - mn);
-          const float a2 = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
-          l[h] = l[h] * a1 + lo * a2;
-#pragma unroll
-          for (int j = 0; j < DPL / 2; ++j) {
-            float x0, x1;
-            f2unpack(o2[h][j], x0, x1);
-            const float y0 = __shfl_xor_sync(0xffffffffu, x0, off);
-            const float y1 = __shfl_xor_sync(0xffffffffu, x1, off);
-            o2[h][j] = f2pack(x0 * a1 + y0 * a2, x1 * a1 + y1 * a2);
-          }
-          m[h] = mn;
-        }
-      }
-      if (grp == 0) {
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-#pragma unroll
-          for (int j = 0; j < DPL / 2; ++j) {
-            float x0, x1;
-            f2unpack(o2[h][j], x0, x1);
-            sm.wo[warp][h][col_of<D, GMAX>(sub, 2 * j)] = x0;
-            sm.wo[warp][h][col_of<D, GMAX>(sub, 2 * j + 1)] = x1;
-          }
-          if (sub == 0) {
-            sm.wm[warp][h] = m[h];
-            sm.wl[warp][h] = l[h];
-          }
-        }
-      }
-      group_sync(gi);
-      // ---- merge the group's warps --------------------------------------
-      const int w0 = gi * kGroupWarps;
-      if (gt < GMAX) {
-        const int h = gt;
-        float M = -INFINITY;
-        for (int w = 0; w < kGroupWarps; ++w) M = fmaxf(M, sm.wm[w0 + w][h]);
-        float L = 0.f;
-        for (int w = 0; w < kGroupWarps; ++w)
-          if (sm.wm[w0 + w][h] != -INFINITY) L += sm.wl[w0 + w][h] * fast_exp2(sm.wm[w0 + w][h] - M);
-        sm.cm[gi][h] = M;
-        sm.cl[gi][h] = L;
-      }
-      group_sync(gi);
-      const int bg = it.b * a.Hkv + it.g;
-      for (int x = gt; x < G * D; x += kGroupWarps * 32) {
-        const int h = x / D, d = x - h * D;
-        const float M = sm.cm[gi][h];
-        float acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kGroupWarps; ++w)
-          if (sm.wm[w0 + w][h] != -INFINITY) acc = fmaf(sm.wo[w0 + w][h][d], fast_exp2(sm.wm[w0 + w][h] - M), acc);
-        if (it.nsplit == 1) og[x] = __float2bfloat16(acc / sm.cl[gi][h]);
-        else a.part_o[(((size_t)bg * max_split + it.sp) * GMAX + h) * D + d] = acc;
-      }
-      if (it.nsplit > 1 && gt < G) {
-        float* ml = a.part_ml + (((size_t)bg * max_split + it.sp) * GMAX + gt) * 2;
-        ml[0] = sm.cm[gi][gt];
-        ml[1] = sm.cl[gi][gt];
-      }
-      group_sync(gi);  // the group's merge buffers are rewritten by its next item
     }
   }
+  // ---- the CTA agrees on one maximum per head ---------------------------------
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) sm.wm[warp][h] = mx[h];
   __syncthreads();
+  float M[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    M[h] = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M[h] = fmaxf(M[h], sm.wm[w][h]);
+  }
+  // ---- value pass (V) -------------------------------------------------------
+  uint64_t o2[GMAX][DPL / 2];
+  float l[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    l[h] = 0.f;
+#pragma unroll
+    for (int j = 0; j < DPL / 2; ++j) o2[h][j] = f2pack(0.f, 0.f);
+  }
+  const bool okv = mbar_wait(&sm.bar_v, 0, ab);
+#pragma unroll 4
+  for (int st = 0; st < NSTEP; ++st) {
+    const int tt = wbase + st * TPI + grp;
+    const bool valid = okv && tt < n;
+    float vx[DPL];
+    load_row<D, GMAX>(&sm.v[valid ? tt : 0][0], sub, vx);
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      const float p = valid ? fast_exp2(sm.sc[tt][h] - M[h]) : 0.f;
+      l[h] += p;
+      const uint64_t p2 = f2pack(p, p);
+#pragma unroll
+      for (int j = 0; j < DPL / 2; ++j) o2[h][j] = f2fma(p2, f2pack(vx[2 * j], vx[2 * j + 1]), o2[h][j]);
+    }
+  }
+  __syncthreads();  // K and V are dead: their space takes the partial sums
+  float* part = reinterpret_cast<float*>(&sm.k[0][0]);  // [kWarps][TPI][GMAX][D]
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    float* dst = part + ((size_t)(warp * TPI + grp) * GMAX + h) * D;
+#pragma unroll
+    for (int j = 0; j < DPL / 2; ++j) {
+      float x0, x1;
+      f2unpack(o2[h][j], x0, x1);
+      dst[col_of<D, GMAX>(sub, 2 * j)] = x0;
+      dst[col_of<D, GMAX>(sub, 2 * j + 1)] = x1;
+    }
+    if (sub == 0) sm.lsum[warp][grp][h] = l[h];
+  }
+  __syncthreads();
+  const int bg = b * a.Hkv + g;
+  for (int x = tid; x < G * D; x += kThreads) {
+    const int h = x / D, d = x - h * D;
+    float acc = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps * TPI; ++w) {
+      acc += part[((size_t)w * GMAX + h) * D + d];
+      L += sm.lsum[w / TPI][w % TPI][h];
+    }
+    if (nsplit == 1) {
+      og[x] = __float2bfloat16(acc / L);
+    } else {
+      a.part_o[(((size_t)bg * max_split + sp) * GMAX + h) * D + d] = acc;
+      if (d == 0) {
+        float* ml = a.part_ml + (((size_t)bg * max_split + sp) * GMAX + h) * 2;
+        ml[0] = M[h];
+        ml[1] = L;
+      }
+    }
+  }
 }
 
 // merge the slices of every (b, g) that has more than one: one CTA per (b, g)
@@ -370,14 +294,9 @@ cudaError_t launch_dg(const DecodeArgs& a, cudaStream_t st) {
   auto kern = gqa_decode_kernel<D, GMAX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int max_split = decode_max_split(a.Smax);
-  const long long items = (long long)a.B * a.Hkv * max_split;
-  const int grid = (int)(items < sms ? items : sms);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
-  kern<<<grid, kThreads, smem, st>>>(a, scale_log2, max_split);
+  kern<<<dim3(max_split, a.Hkv, a.B), kThreads, smem, st>>>(a, scale_log2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (max_split > 1) {
     gqa_decode_combine_kernel<D, GMAX><<<a.B * a.Hkv, 128, 0, st>>>(a, max_split);
