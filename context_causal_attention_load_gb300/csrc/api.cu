@@ -55,6 +55,30 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+// bf16 tensor map with 128-byte swizzle and zero fill past the extents
+// (dims[0] innermost; strides in bytes for dims 1..rank-1)
+int cpattn::encode_bf16_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
+                             const unsigned long long* strides, const unsigned* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return -1;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i > 0) st[i - 1] = strides[i - 1];
+  }
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, st, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+namespace {
+
 // [B, S, H, D] bf16 tensor seen as 4-D {D, H, S, B}; box = 64 columns x rows
 // (128-byte rows, 128-byte swizzle, zero fill past S)
 int make_tmap(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, int rows) {
@@ -494,7 +518,10 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
   if ((rc = need_sm103(*ds))) return rc;
   if ((rc = ensure(ds->dec_o, decode_part_o_floats(B, Hq, Hkv, Smax, D), stream, false))) return rc;
   if ((rc = ensure(ds->dec_ml, decode_part_ml_floats(B, Hq, Hkv, Smax), stream, false))) return rc;
-  DecodeArgs a{q, kcache, vcache, lens, out, B, Hq, Hkv, Smax, D, ds->dec_o.ptr, ds->dec_ml.ptr, ds->err};
+  DecodeArgs a{};
+  a.q = q; a.kc = kcache; a.vc = vcache; a.lens = lens; a.out = out;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Smax = Smax; a.D = D;
+  a.part_o = ds->dec_o.ptr; a.part_ml = ds->dec_ml.ptr; a.err = ds->err;
   cudaError_t e;
   {
     ProfScope ps("gqa_decode", stream);

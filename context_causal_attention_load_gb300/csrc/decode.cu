@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
   auto& sm = *reinterpret_cast<DecSmem<D, GMAX>*>(smem_raw);
   const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int max_split = gridDim.x;
+  asm volatile("griddepcontrol.launch_dependents;");  // the merge grid may be scheduled now
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -252,9 +253,315 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
   }
 }
 
-// merge the slices of every (b, g) that has more than one: one CTA per (b, g)
+// ---------------------------------------------------------------------------
+// Tensor-core decode for D = 128.  Per item (b, g, 128-position slice):
+//   S^T = K Q^T  : M = 128 positions, N = 16 head columns, K = 128 dims
+//   O^T = V^T P^T: M = 128 dims,      N = 16 head columns, K = 128 positions
+// so an item is 16 tcgen05 MMAs instead of thousands of FMAs.  The group's
+// G <= 16 heads are the N columns (columns past G are computed and ignored;
+// their P rows stay zero).  Persistent: one CTA per SM; only slices that hold
+// positions are items, numbered densely and dealt round-robin so every CTA
+// gets the same count to within one.  Warp 0 streams K, V and q with TMA
+// through a 3-stage ring, warp 1 issues the MMAs, and two softmax groups
+// (warps 2-5 and 6-9; one thread per position for the scores, per dim for the
+// output) take alternate items, so one group's reductions overlap the other's.
+// S, O (TMEM), P (shared memory) and the group barriers are indexed by item
+// parity.
+// ---------------------------------------------------------------------------
+namespace tcd {
+constexpr int D = 128;
+constexpr int NH = 16;                 // head columns of the MMAs
+constexpr int ROWS = kDecodeSplit;     // positions per item
+constexpr int NST = 3;                 // ring stages
+constexpr int K_BYTES = ROWS * D * 2;  // two 64-column boxes
+constexpr int V_BYTES = ROWS * D * 2;
+constexpr int Q_BYTES = NH * D * 2;    // two boxes of 16 rows
+constexpr int STAGE = K_BYTES + V_BYTES + Q_BYTES;
+constexpr int P_BYTES = NH * ROWS * 2;  // P^T as [head][position], two boxes of 64 positions
+constexpr int OFF_P = NST * STAGE;
+constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int OFF_RED = OFF_BAR + 256;  // per group: float rmax[4][NH], rsum[4][NH]
+constexpr int OFF_MISC = OFF_RED + 2 * 2 * 4 * NH * 4;
+constexpr int OFF_LENS = OFF_MISC + 64;
+constexpr int MAX_B = 1024;             // batch rows staged in shared memory
+constexpr int OFF_PRE = OFF_LENS + MAX_B * 4;
+constexpr int SMEM = OFF_PRE + (MAX_B + 1) * 4 + 1024;
+constexpr int kThreadsTc = 320;
+static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(SMEM <= 232448, "shared memory budget");
+static_assert(ROWS == 128, "one position per softmax thread");
+struct Bars {
+  uint64_t full[NST], empty[NST];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t done;
+};
+}  // namespace tcd
+
+// dense item j -> (b, g, slice): pre[b] = items of rows before b (Hkv slices
+// per 128 positions), pre[B] = the total
+struct Item {
+  int b, g, sp, len, nsplit;
+};
+__device__ __forceinline__ Item loaded_item(int j, const int* pre, const int* lens, int B, int Hkv) {
+  int lo = 0, hi = B - 1;  // largest b with pre[b] <= j (never a row without items)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= j) lo = mid;
+    else hi = mid - 1;
+  }
+  Item it;
+  it.b = lo;
+  it.len = lens[lo];
+  it.nsplit = (it.len + kDecodeSplit - 1) / kDecodeSplit;
+  const int r = j - pre[lo];
+  it.g = r / it.nsplit;
+  it.sp = r - it.g * it.nsplit;
+  return it;
+}
+
+template <int GMAX>
+__global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const __grid_constant__ DecodeArgs a,
+                                                                         float scale_log2, int max_split) {
+  using namespace tcd;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars& bar = *reinterpret_cast<Bars*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 16);
+  int* lens_s = reinterpret_cast<int*>(smem + OFF_LENS);
+  int* pre = reinterpret_cast<int*>(smem + OFF_PRE);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.Hq / a.Hkv;
+  const int ncta = gridDim.x, cta = blockIdx.x;
+  const Abort ab{abort_flag, a.err};
+  asm volatile("griddepcontrol.launch_dependents;");  // the merge grid may be scheduled now
+
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.s_full[i], 1); mbar_init(&bar.p_full[i], 128); mbar_init(&bar.o_full[i], 1); }
+    mbar_init(&bar.done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // stage (and validate) the lengths; rows with an empty cache get zeros here
+  for (int bb = tid; bb < a.B; bb += kThreadsTc) {
+    const int l = a.lens[bb];
+    if ((l < 0 || l > a.Smax) && cta == 0) atomicExch(a.err, DEV_LENS_CLAMPED);
+    lens_s[bb] = l < 0 ? 0 : (l > a.Smax ? a.Smax : l);
+  }
+  // P rows of heads past G are never written again: zero both P buffers once
+  for (int i = tid; i < 2 * P_BYTES / 16; i += kThreadsTc)
+    reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix of items per row: each lane scans a run of rows
+    const int per = (a.B + 31) / 32, b0 = lane * per, b1 = min(a.B, b0 + per);
+    int run = 0;
+    for (int bb = b0; bb < b1; ++bb) run += (lens_s[bb] + kDecodeSplit - 1) / kDecodeSplit * a.Hkv;
+    int inc = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    int acc = inc - run;
+    for (int bb = b0; bb < b1; ++bb) {
+      pre[bb] = acc;
+      acc += (lens_s[bb] + kDecodeSplit - 1) / kDecodeSplit * a.Hkv;
+    }
+    if (lane == 31) pre[a.B] = inc;
+  } else {
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out);
+    for (int bb = cta; bb < a.B; bb += ncta)
+      if (lens_s[bb] == 0)
+        for (int x = tid - 32; x < a.Hq * D; x += kThreadsTc - 32) ob[(size_t)bb * a.Hq * D + x] = __float2bfloat16(0.f);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, 64); tmem_relinquish(); }
+  if (warp == 0 && lane == 0) { prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tq); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S_b at cols 16b, O_b at 32 + 16b
+  const int total = pre[a.B];
+  const int n_items = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // this CTA's items k: j = cta + k*ncta
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      for (int k = 0; k < n_items; ++k) {
+        const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
+        const int st = k % NST;
+        if (!mbar_wait(&bar.empty[st], ((k / NST) & 1) ^ 1, ab)) break;
+        unsigned char* sb = smem + st * STAGE;
+        mbar_expect_tx(&bar.full[st], STAGE);
+        const int t0 = it.sp * ROWS;
+        for (int bx = 0; bx < 2; ++bx) {
+          tma_load_4d(sb + bx * (ROWS * 128), &a.tk, &bar.full[st], bx * 64, t0, it.g, it.b);
+          tma_load_3d(sb + K_BYTES + V_BYTES + bx * (NH * 128), &a.tq, &bar.full[st], bx * 64, it.g * G, it.b);
+        }
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_4d(sb + K_BYTES + bx * (ROWS * 128), &a.tv, &bar.full[st], bx * 64, t0, it.g, it.b);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, NH, 0, 0);   // K (K-major) x q (K-major)
+      constexpr uint32_t IDESC_O = idesc_bf16(128, NH, 1, 0);   // V^T (MN-major) x P^T (K-major)
+      const uint32_t s0 = smem_u32(smem);
+      auto issue_s = [&](int k) {
+        const uint32_t sb = s0 + (k % NST) * STAGE;
+        const uint64_t ak = sdesc_sw128(sb, 16, 1024), bq = sdesc_sw128(sb + K_BYTES + V_BYTES, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + (k & 1) * 16, ak + (((kk >> 2) * (ROWS * 128) + (kk & 3) * 32) >> 4),
+                 bq + (((kk >> 2) * (NH * 128) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
+        mma_commit(&bar.s_full[k & 1]);
+      };
+      auto issue_o = [&](int k) {
+        const uint32_t sb = s0 + (k % NST) * STAGE;
+        const uint64_t av = sdesc_sw128(sb + K_BYTES, ROWS * 128, 1024);
+        const uint64_t bp = sdesc_sw128(s0 + OFF_P + (k & 1) * P_BYTES, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < ROWS / 16; ++kk)
+          mma_ss(tmem + 32 + (k & 1) * 16, av + ((kk * 16 * 128) >> 4),
+                 bp + (((kk >> 2) * (NH * 128) + (kk & 3) * 32) >> 4), IDESC_O, kk > 0 ? 1u : 0u);
+        mma_commit(&bar.o_full[k & 1]);
+        mma_commit(&bar.empty[k % NST]);
+      };
+      bool ok = true;
+      // scores of the first two items, then: O(k) once group k&1 has written
+      // P(k); S(k+2) into the buffer that group has finished reading
+      for (int k = 0; k < 2 && k < n_items && ok; ++k) {
+        if (!(ok = mbar_wait(&bar.full[k % NST], (k / NST) & 1, ab))) break;
+        tc_fence_after();
+        issue_s(k);
+      }
+      for (int k = 0; ok && k < n_items; ++k) {
+        if (!(ok = mbar_wait(&bar.p_full[k & 1], (k >> 1) & 1, ab))) break;
+        tc_fence_after();
+        issue_o(k);
+        if (k + 2 < n_items) {
+          if (!(ok = mbar_wait(&bar.full[(k + 2) % NST], ((k + 2) / NST) & 1, ab))) break;
+          tc_fence_after();
+          issue_s(k + 2);
+        }
+      }
+      mma_commit(&bar.done);
+      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+    }
+  } else {
+    // ---------------------------------------------------------- softmax + epilogue
+    // group gi takes items k = gi, gi + 2, ...; thread = TMEM lane = position
+    // (scores) and = dim (output); control flow is uniform over the group's
+    // 128 threads, so its named barrier completes.  rmax is rewritten only
+    // after the group's next first barrier, rsum after its second, and every
+    // thread reaches those after reading both for this item.
+    const int gi = (warp - 2) >> 2;
+    const int wq = warp & 3;            // TMEM lane quarter of this warp
+    const int r = wq * 32 + lane;       // position / dim handled by this thread
+    const uint32_t lane_base = uint32_t(wq * 32) << 16;
+    float* rmax = reinterpret_cast<float*>(smem + OFF_RED) + gi * 2 * 4 * NH;
+    float* rsum = rmax + 4 * NH;
+    __nv_bfloat16* ogb = static_cast<__nv_bfloat16*>(a.out);
+    for (int k = gi; k < n_items; k += 2) {
+      const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
+      __nv_bfloat16* og = ogb + ((size_t)it.b * a.Hq + (size_t)it.g * G) * D;
+      const int buf = k & 1;
+      const uint32_t par = (k >> 1) & 1;
+      const int n = min(ROWS, it.len - it.sp * ROWS);
+      // a failed wait (abort or timeout) runs on: the named barriers need every thread
+      mbar_wait(&bar.s_full[buf], par, ab);
+      tc_fence_after();
+      uint32_t sr[16];
+      tmem_ld16(tmem + lane_base + buf * 16, sr);
+      tmem_ld_wait();
+      float sv[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h)
+        sv[h] = (h < G && r < n) ? __uint_as_float(sr[h]) * scale_log2 : -INFINITY;
+      // max over the item's positions, per head
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        float m = sv[h];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) rmax[wq * NH + h] = m;
+      }
+      named_bar(1 + gi, 128);
+      float M[GMAX], p[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        M[h] = fmaxf(fmaxf(rmax[h], rmax[NH + h]), fmaxf(rmax[2 * NH + h], rmax[3 * NH + h]));
+        p[h] = (h < G && r < n) ? fast_exp2(sv[h] - M[h]) : 0.f;
+      }
+      // P^T[head][position] in the K-major 128-byte-swizzled layout of the MMA's B operand
+      {
+        unsigned char* pb = smem + OFF_P + buf * P_BYTES + (r >> 6) * (NH * 128);
+        const int chunk = (r & 63) >> 3;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+          if (h < G)
+            *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + ((chunk ^ (h & 7)) << 4) + (r & 7) * 2) =
+                __float2bfloat16(p[h]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.p_full[buf]);
+      // the denominators while the tensor core forms O
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        float l = p[h];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (lane == 0) rsum[wq * NH + h] = l;
+      }
+      named_bar(1 + gi, 128);
+      float L[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) L[h] = (rsum[h] + rsum[NH + h]) + (rsum[2 * NH + h] + rsum[3 * NH + h]);
+      // output: thread r owns dim r of every head
+      mbar_wait(&bar.o_full[buf], par, ab);
+      tc_fence_after();
+      uint32_t orr[16];
+      tmem_ld16(tmem + lane_base + 32 + buf * 16, orr);
+      tmem_ld_wait();
+      const int bg = it.b * a.Hkv + it.g;
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (h >= G) continue;
+        const float o = __uint_as_float(orr[h]);
+        if (it.nsplit == 1) {
+          og[h * D + r] = __float2bfloat16(o / L[h]);
+        } else {
+          a.part_o[(((size_t)bg * max_split + it.sp) * GMAX + h) * D + r] = o;
+          if (r == 0) {
+            float* ml = a.part_ml + (((size_t)bg * max_split + it.sp) * GMAX + h) * 2;
+            ml[0] = M[h];
+            ml[1] = L[h];
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+// merge the slices of every (b, g) that has more than one: one CTA of
+// kCombineThreads per (b, g).  Warp w reduces the maxima and denominators of
+// head w (lanes over slices); each thread then owns one or more outputs and
+// keeps sixteen slices' loads in flight (a chain of dependent global loads
+// here costs more than the attention itself).
+constexpr int kCombineThreads = 512;
 template <int D, int GMAX>
-__global__ void __launch_bounds__(128) gqa_decode_combine_kernel(DecodeArgs a, int max_split) {
+__global__ void __launch_bounds__(kCombineThreads) gqa_decode_combine_kernel(DecodeArgs a, int max_split) {
   const int bg = blockIdx.x;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int G = a.Hq / a.Hkv;
@@ -262,30 +569,66 @@ __global__ void __launch_bounds__(128) gqa_decode_combine_kernel(DecodeArgs a, i
   len = len < 0 ? 0 : (len > a.Smax ? a.Smax : len);
   const int nsplit = (len + kDecodeSplit - 1) / kDecodeSplit;
   if (nsplit <= 1) return;
+  // launched early (programmatic dependent launch): the partials are
+  // complete and visible once the attention grid has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float cm[GMAX], cl[GMAX];
-  const int tid = threadIdx.x;
-  if (tid < G) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* ml0 = a.part_ml + (size_t)bg * max_split * GMAX * 2;
+  const float* po = a.part_o + (size_t)bg * max_split * GMAX * D;
+  for (int h = warp; h < G; h += kCombineThreads / 32) {
     float M = -INFINITY;
-    for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, a.part_ml[(((size_t)bg * max_split + s2) * GMAX + tid) * 2]);
+    for (int s2 = lane; s2 < nsplit; s2 += 32) M = fmaxf(M, ml0[(s2 * GMAX + h) * 2]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
-    for (int s2 = 0; s2 < nsplit; ++s2) {
-      const float* ml = a.part_ml + (((size_t)bg * max_split + s2) * GMAX + tid) * 2;
-      L += ml[1] * fast_exp2(ml[0] - M);
+    for (int s2 = lane; s2 < nsplit; s2 += 32) {
+      const float* ml = ml0 + (s2 * GMAX + h) * 2;
+      L = fmaf(ml[1], fast_exp2(ml[0] - M), L);
     }
-    cm[tid] = M;
-    cl[tid] = L;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+      cm[h] = M;
+      cl[h] = L;
+    }
   }
   __syncthreads();
   __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.Hq + (size_t)g * G) * D;
-  for (int x = tid; x < G * D; x += 128) {
+  for (int x = tid; x < G * D; x += kCombineThreads) {
     const int h = x / D, d = x - h * D;
+    const float M = cm[h];
     float acc = 0.f;
-    for (int s2 = 0; s2 < nsplit; ++s2) {
-      const float m2 = a.part_ml[(((size_t)bg * max_split + s2) * GMAX + h) * 2];
-      acc = fmaf(a.part_o[(((size_t)bg * max_split + s2) * GMAX + h) * D + d], fast_exp2(m2 - cm[h]), acc);
+    for (int s0 = 0; s0 < nsplit; s0 += 16) {
+      float o[16], m[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const bool in = s0 + j < nsplit;
+        o[j] = in ? po[((size_t)(s0 + j) * GMAX + h) * D + d] : 0.f;
+        m[j] = in ? ml0[((s0 + j) * GMAX + h) * 2] : M;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc = fmaf(o[j], fast_exp2(m[j] - M), acc);
     }
     og[x] = __float2bfloat16(acc / cl[h]);
   }
+}
+
+// the merge grid may be scheduled while the attention grid still runs (its
+// CTAs are small and wait in griddepcontrol.wait), hiding its launch latency
+template <int D, int GMAX>
+cudaError_t launch_combine(const DecodeArgs& a, int max_split, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.Hkv);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_decode_combine_kernel<D, GMAX>, a, max_split);
 }
 
 template <int D, int GMAX>
@@ -298,11 +641,33 @@ cudaError_t launch_dg(const DecodeArgs& a, cudaStream_t st) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
   kern<<<dim3(max_split, a.Hkv, a.B), kThreads, smem, st>>>(a, scale_log2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (max_split > 1) {
-    gqa_decode_combine_kernel<D, GMAX><<<a.B * a.Hkv, 128, 0, st>>>(a, max_split);
-    e = cudaGetLastError();
-  }
-  return e;
+  return max_split > 1 ? launch_combine<D, GMAX>(a, max_split, st) : cudaSuccess;
+}
+
+template <int GMAX>
+cudaError_t launch_tc(const DecodeArgs& a0, cudaStream_t st) {
+  DecodeArgs a = a0;
+  const unsigned long long D = 128;
+  unsigned long long kd[4] = {D, (unsigned long long)a.Smax, (unsigned long long)a.Hkv, (unsigned long long)a.B};
+  unsigned long long ks[3] = {D * 2, (unsigned long long)a.Smax * D * 2, (unsigned long long)a.Hkv * a.Smax * D * 2};
+  unsigned kb[4] = {64, (unsigned)tcd::ROWS, 1, 1};
+  unsigned long long qd[3] = {D, (unsigned long long)a.Hq, (unsigned long long)a.B};
+  unsigned long long qs[2] = {D * 2, (unsigned long long)a.Hq * D * 2};
+  unsigned qb[3] = {64, (unsigned)tcd::NH, 1};
+  if (encode_bf16_tmap(&a.tk, a.kc, 4, kd, ks, kb) || encode_bf16_tmap(&a.tv, a.vc, 4, kd, ks, kb) ||
+      encode_bf16_tmap(&a.tq, a.q, 3, qd, qs, qb))
+    return cudaErrorInvalidValue;
+  auto kern = gqa_decode_tc_kernel<GMAX>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tcd::SMEM);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int max_split = decode_max_split(a.Smax);
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
+  kern<<<sms, tcd::kThreadsTc, tcd::SMEM, st>>>(a, scale_log2, max_split);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return max_split > 1 ? launch_combine<128, GMAX>(a, max_split, st) : cudaSuccess;
 }
 
 template <int D>
@@ -329,7 +694,14 @@ size_t decode_part_ml_floats(int B, int Hq, int Hkv, int Smax) {
 }
 
 cudaError_t launch_gqa_decode(const DecodeArgs& a, cudaStream_t st) {
-  if (a.D == 128) return launch_d<128>(a, st);
+  if (a.D == 128 && a.B <= tcd::MAX_B) {  // tensor-core path
+    const int G = a.Hq / a.Hkv;
+    if (G <= 1) return launch_tc<1>(a, st);
+    if (G <= 2) return launch_tc<2>(a, st);
+    if (G <= 4) return launch_tc<4>(a, st);
+    if (G <= 8) return launch_tc<8>(a, st);
+    return launch_tc<16>(a, st);
+  }
   return launch_d<64>(a, st);
 }
 
@@ -341,7 +713,7 @@ cudaError_t launch_gqa_decode(const DecodeArgs& a, cudaStream_t st) {
 // sized up front), real-time serving loops that must not hit the driver's
 // allocation path or its implicit synchronisation, and processes that have
 // reserved nearly all of HBM for the KV cache.  For them the split partials
-// and arrival counters of the decode live in this fixed, statically sized
+// of the decode and its error word live in this fixed, statically sized
 // device array instead of library-allocated scratch.  Every GPU that loads
 // the library holds the array until the process exits.
 // ---------------------------------------------------------------------------
@@ -388,9 +760,12 @@ cudaError_t launch_gqa_decode_noalloc(const void* q, const void* kc, const void*
   float* ml = reinterpret_cast<float*>(p);
   p += round256(decode_part_ml_floats(B, Hq, Hkv, Smax) * sizeof(float));
   float* po = reinterpret_cast<float*>(p);
-  // every slice partial the merge reads is written by the same launch
-  // pair, so nothing left in the array by an earlier call is ever read
-  DecodeArgs a{q, kc, vc, lens, out, B, Hq, Hkv, Smax, D, po, ml, reinterpret_cast<int*>(base)};
+  // every slice partial the merge reads is written by the same call, so
+  // nothing left in the array by an earlier call is ever read
+  DecodeArgs a{};
+  a.q = q; a.kc = kc; a.vc = vc; a.lens = lens; a.out = out;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Smax = Smax; a.D = D;
+  a.part_o = po; a.part_ml = ml; a.err = reinterpret_cast<int*>(base);
   return launch_gqa_decode(a, st);
 }
 

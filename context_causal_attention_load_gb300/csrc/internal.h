@@ -11,7 +11,12 @@ cudaError_t launch_lb_permute(const void* src, void* dst, int B, int S, long lon
 
 // split-K decode: scratch = partial (o, m, l) per 128-position slice; a
 // second kernel merges the slices of each (batch, kv head).
+// bf16 tiled tensor map, 128-byte swizzle (returns 0 on success)
+int encode_bf16_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
+                     const unsigned long long* strides, const unsigned* box);
+
 struct DecodeArgs {
+  CUtensorMap tk, tv, tq;  // used by the tensor-core path (D = 128)
   const void* q;
   const void* kc;
   const void* vc;

@@ -136,13 +136,13 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
  * driver's allocation path and its implicit synchronisation, processes
  * that keep nearly all of HBM for their KV cache).
  * Same arguments, layouts and results as gqa_decode.  The split partials
- * live in one fixed 8 MiB device array inside the
- * library (every GPU that loads the library holds it until the process
- * exits); the caller still passes all inputs and outputs.  A shape whose
- * scratch does not fit is rejected with CPATTN_ERR_INVALID_ARG before any
- * launch (about B*Hkv*ceil(Smax/128)*G'*(D+2)*4 bytes, G' = Hq/Hkv rounded
- * up to a power of two; the decode workload B=24, Hkv=8, Smax=2048, G=4,
- * D=128 needs 3.2 MiB).
+ * live in one fixed 8 MiB device array inside the library (every GPU that
+ * loads the library holds it until the process exits); the caller still
+ * passes all inputs and outputs.  A shape whose scratch does not fit is
+ * rejected with CPATTN_ERR_INVALID_ARG before any launch (about
+ * B*Hkv*ceil(Smax/128)*G'*(D+2)*4 bytes, G' = Hq/Hkv rounded up to a power
+ * of two; the decode workload B=24, Hkv=8, Smax=2048, G=4, D=128 needs
+ * 3.2 MiB).
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  Every
  * call shares the one array (each call writes every entry it later reads,

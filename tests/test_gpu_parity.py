@@ -182,6 +182,7 @@ def test_bwd_parity(cfg):
     (2, 6, 2, 128, 512, 255, 257),        # G = 3, around a split boundary
     (2, 16, 1, 128, 640, 300, 640),       # G = 16, D = 128 (two-stage ring)
     (1, 2, 1, 128, 128, 128, 128),        # one slice: no merge pass
+    (2, 8, 2, 128, 4500, 2100, 4500),     # 17-36 slices: the merge runs in chunks of 16
 ])
 def test_decode_parity(cfg):
     B, Hq, Hkv, D, Smax, lo, hi = cfg
@@ -191,7 +192,7 @@ def test_decode_parity(cfg):
     cp_.check_device()
     ref = O.gqa_decode(_f64(q), _f64(kc), _f64(vc), lens.numpy())
     assert_close_out(_f64(out), ref, "decode %s" % (cfg,))
-    # a second call reuses the split counters
+    # a second call reuses the arrival counts (and must give the same bits)
     out2 = cp_.gqa_decode(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda())
     assert torch.equal(out2, out)
 
