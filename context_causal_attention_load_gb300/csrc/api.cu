@@ -95,6 +95,22 @@ int make_tmap(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, int r
   return CPATTN_OK;
 }
 
+// [B, S, H, D] fp32 tensor as 4-D {D, H, S, B}; box = 32 columns (128 bytes) x
+// rows, 128-byte swizzle (the fused backward's dQ reduce-add target)
+int make_tmap_f32(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4, (cuuint64_t)S * H * D * 4};
+  cuuint32_t box[4] = {32, 1, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (%d)", (int)r);
+  return CPATTN_OK;
+}
+
 // ---- per-device state ---------------------------------------------------------
 template <typename T>
 struct DevBuf {
@@ -109,6 +125,7 @@ struct DevState {
   std::map<std::vector<int>, DevBuf<FwdUnit>> fwd_units;
   std::map<std::vector<int>, DevBuf<BwdUnit>> bwd_units;
   DevBuf<float> bwd_stats;  // lse_l2 then delta
+  DevBuf<float> dq_acc;     // fused backward's fp32 dQ accumulator
   DevBuf<float> dec_o, dec_ml;
 };
 
@@ -452,13 +469,17 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   const int Spad = (S + kTile - 1) / kTile * kTile;
   const size_t nstat = (size_t)B * Hq * Spad;
   if ((rc = ensure(ds->bwd_stats, 2 * nstat, stream, false))) return rc;
+  const bool fused = bwd_fused_supported(Dqk, Dv);
+  const size_t nacc = (size_t)B * S * Hq * Dqk;
+  if (fused && (rc = ensure(ds->dq_acc, nacc, stream, false))) return rc;
   DevBuf<BwdUnit>* u_kv;
-  DevBuf<BwdUnit>* u_q;
+  DevBuf<BwdUnit>* u_q = nullptr;
   if ((rc = bwd_units_cached(*ds, sh, 0, &u_kv))) return rc;
-  if ((rc = bwd_units_cached(*ds, sh, 1, &u_q))) return rc;
+  if (!fused && (rc = bwd_units_cached(*ds, sh, 1, &u_q))) return rc;
   BwdArgs a;
   a.lse_l2 = ds->bwd_stats.ptr;
   a.delta = ds->bwd_stats.ptr + nstat;
+  a.dq_acc = fused ? ds->dq_acc.ptr : nullptr;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
@@ -470,10 +491,31 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   cudaError_t e;
   {
     ProfScope ps("bwd_preprocess", stream);
-    e = launch_bwd_preprocess(out, dout, lse, const_cast<float*>(a.lse_l2), const_cast<float*>(a.delta), sh, Spad,
-                              stream);
+    e = launch_bwd_preprocess(out, dout, lse, const_cast<float*>(a.lse_l2), const_cast<float*>(a.delta), a.dq_acc,
+                              sh, Spad, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
+  if (fused) {
+    // one kernel: 128-row key tiles, 128-row query steps; dQ through the fp32 accumulator
+    if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, 128))) return rc;
+    if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, 128))) return rc;
+    if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, 128))) return rc;
+    if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
+    if ((rc = make_tmap_f32(&a.tdq, a.dq_acc, B, S, Hq, Dqk, 128))) return rc;
+    a.units = u_kv->ptr;
+    a.n_units = (int)u_kv->n;
+    {
+      ProfScope ps("attn_bwd_fused", stream);
+      e = launch_attn_bwd_fused(a, (int)std::min<size_t>(u_kv->n, (size_t)ds->num_sms), stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "fused bwd launch");
+    {
+      ProfScope ps("bwd_dq_round", stream);
+      e = launch_bwd_dq_round(a.dq_acc, dq, (long long)nacc, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "dq rounding launch");
+    return CPATTN_OK;
+  }
   // dk/dv: key tiles of 128 rows, query/dout boxes of BQ rows
   const int BQ = bwd_dkdv_q_tile(Dqk);
   if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, BQ))) return rc;
@@ -596,6 +638,7 @@ int cp_attn_check_device(cudaStream_t stream) {
   cudaMemset(ds->err, 0, sizeof(int));
   if (word == DEV_TIMEOUT) return fail(CPATTN_ERR_DEVICE_TIMEOUT, "a kernel pipeline wait timed out");
   if (word == DEV_LENS_CLAMPED) return fail(CPATTN_ERR_DEVICE_BOUNDS, "decode lens outside [0, Smax] were clamped");
+  if (word == DEV_SMEM_ALIGN) return fail(CPATTN_ERR_CUDA, "a kernel's shared memory was not 1024-byte aligned");
   return fail(CPATTN_ERR_CUDA, "unknown device error %d", word);
 }
 

@@ -35,26 +35,17 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int TK = 128;  // key rows per dk/dv unit; query rows per dq unit
 
-__device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
-  return r * ncta + ((r & 1) ? (ncta - 1 - cta) : cta);
-}
-
-// Two element-wise groups each own HC consecutive columns of a row; a group
-// packs the bf16 pairs of column c into its own range, so packed column of c
-// is (c / HC) * HC + (c % HC) / 2.  The TS MMAs read 16 columns (8 packed)
-// per k-step, never straddling two groups.
-template <int HC>
-__host__ __device__ constexpr int packed_col(int c) { return (c / HC) * HC + (c % HC) / 2; }
 
 // ============================================================================
 // preprocess: -lse*log2(e) (-inf past S) and -rowsum(dO*O) (0 past S), stored
 // negated so the element-wise warps apply them with one fused multiply-add;
-// layout [B, Hq, Spad]; one warp per (b, s, h) row
+// layout [B, Hq, Spad]; one warp per (b, s, h) row.  With dq_acc, also zeroes
+// the row of the fused kernel's fp32 dQ accumulator.
 // ============================================================================
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse, float* lse_l2,
-                                                             float* delta, AttnShape sh, int Spad) {
+                                                             float* delta, float* dq_acc, AttnShape sh, int Spad) {
   const long long nrows = (long long)sh.B * Spad * sh.Hq;
   const int lane = threadIdx.x & 31;
   for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nrows;
@@ -72,6 +63,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
       continue;
     }
     const size_t base = (((size_t)b * sh.S + s) * sh.Hq + h) * sh.Dv;
+    if (dq_acc) {
+      float4* z = reinterpret_cast<float4*>(dq_acc + (((size_t)b * sh.S + s) * sh.Hq + h) * sh.Dqk);
+      for (int i = lane; i < sh.Dqk / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float acc = 0.f;
     for (int d = lane * 2; d < sh.Dv; d += 64) {
       const uint32_t a = *reinterpret_cast<const uint32_t*>(out + base + d);
@@ -761,13 +756,13 @@ int bwd_dkdv_q_tile(int) { return 64; }
 int bwd_dq_kv_tile(int) { return 64; }
 
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, float* lse_l2, float* delta,
-                                  const AttnShape& sh, int Spad, cudaStream_t st) {
+                                  float* dq_acc, const AttnShape& sh, int Spad, cudaStream_t st) {
   const long long rows = (long long)sh.B * Spad * sh.Hq;
   long long blocks = (rows * 32 + 255) / 256;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
   bwd_preprocess_kernel<<<(int)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
-                                                     static_cast<const __nv_bfloat16*>(dout), lse, lse_l2, delta, sh,
-                                                     Spad);
+                                                     static_cast<const __nv_bfloat16*>(dout), lse, lse_l2, delta, dq_acc,
+                                                     sh, Spad);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,587 @@
+// Fused flash backward for equal query/key and value head dims (64 or 128).
+//
+// Same gradient as the two-kernel backward (the textbook gradient of
+// out = softmax(scale q k^T + mask) v under the reordered causal mask), but
+// in one pass: a CTA owns a 128-row key tile of one KV head and walks every
+// (query head of the group, 128-row query tile) that sees it.  Per step, on
+// tcgen05 with 128-wide N throughout:
+//   S^T  = K Q^T            (TMEM, key lanes)  -> P^T  (bf16, in place)
+//   dP^T = V dO^T           (TMEM, key lanes)  -> dS^T (bf16, in place) and
+//                                                 dS    (bf16, shared memory)
+//   dV  += P^T dO,  dK += dS^T Q               (TMEM accumulators)
+//   dQ_step = dS K          (TMEM, query lanes, in dP's columns)
+// and dQ_step is scaled and added into an fp32 dQ accumulator in global
+// memory with TMA reduce-add (so S and dP are formed once, not twice as in
+// the dQ kernel of the two-kernel path).  The accumulator is zeroed by the
+// preprocess kernel and rounded to bf16 by a final pass.
+//
+// MMA order per step j:  dP_j, dV_j, S_{j+1}, dK_j, dQ_j; the element-wise
+// warps run P_{j+1} while dK_j and dQ_j execute, read dQ_j out of TMEM, then
+// form dS_{j+1} while dV_{j+1} and S_{j+2} execute.  TMEM (512 columns): S/P
+// 128, dP/dS/dQ 128, dV D, dK D.  Tensor-core MMAs from one thread execute
+// in issue order, so an MMA may overwrite TMEM columns an earlier one reads.
+//
+// Shared memory (D = 128, 226 KiB): K and V tiles (resident per unit), two
+// stages each of Q and dO with the per-row -lse*log2(e) and -D vectors, and
+// one dS tile.  dQ_step (128 x D fp32) is staged for the reduce in the dS
+// tile and, for D = 128, in the step's dO stage (both dead by then).
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int kThreadsF = 352;  // warps 0-7 element-wise (two column halves), 8 TMA producer, 9 MMA issuer,
+                                // 10 dQ reducer
+constexpr int kRows = 128;      // key rows per unit, query rows per step
+
+template <int D>
+struct FCfg {
+  static constexpr int TILE = kRows * D * 2;  // D/64 boxes of 128 rows x 128 B
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;   // stage s at OFF_Q + s*TILE
+  static constexpr int OFF_DO = 4 * TILE;  // stage s at OFF_DO + s*TILE
+  static constexpr int OFF_DS = 6 * TILE;  // dS as two query halves x 128 key rows x 128 B
+  static constexpr int DS_BYTES = 2 * kRows * 128;
+  static constexpr int OFF_VEC = OFF_DS + DS_BYTES;  // stage s: lse[128] then delta[128] (fp32)
+  static constexpr int VEC_BYTES = 2 * kRows * 4;
+  static constexpr int OFF_BAR = OFF_VEC + 2 * VEC_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int SMEM = OFF_MISC + 64;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(TILE % 1024 == 0 && OFF_DS % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  // TMEM columns
+  static constexpr int T_S = 0;
+  static constexpr int T_DP = 128;
+  static constexpr int T_DV = 256;
+  static constexpr int T_DK = 256 + D;
+  static_assert(T_DK + D <= 512, "TMEM budget");
+  static constexpr int NBOX = D / 32;  // fp32 dQ boxes of 32 columns x 128 rows (16 KiB)
+};
+
+struct FBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+  uint64_t s_full, p_full, dp_full, dst_full, dss_full, dq_full, dq_free, staged, ds_free;
+  uint64_t acc_full, done;
+};
+
+// this thread's bulk async-groups, all but the newest N, have read their sources
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// P for this thread's 64 query columns of one step: scores from TMEM (t_s),
+// p = exp2(s * scale*log2e - lse*log2e), zeroed where the key's position is
+// past the query's (MASKED steps only; positions walked slot by slot from
+// slot0), kept in fp32 for dS and stored back to TMEM (t_pk) as packed bf16
+template <bool MASKED>
+__device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* lse_s, uint64_t sl2x2,
+                                     float (&p)[64], int kpos, const PosMap& pm, int slot0) {
+  int ck = 0, ct = 0, cbase = 0;  // memory chunk, offset in it, first position of the chunk
+  if (MASKED && pm.lb) {
+    ck = slot0 / pm.c;
+    ct = slot0 - ck * pm.c;
+    cbase = pm.chunk_of(ck) * pm.c;
+  }
+  auto next_qpos = [&](int slot) {
+    int q = -1;
+    if (slot < pm.S) {
+      if (!pm.lb) {
+        q = slot;
+      } else {
+        q = cbase + ct;
+        if (++ct == pm.c) {
+          ++ck;
+          ct = 0;
+          cbase = pm.chunk_of(ck) * pm.c;
+        }
+      }
+    }
+    return q;
+  };
+  uint32_t sv[2][32];
+  tmem_ld32(t_s, sv[0]);
+  tmem_ld32(t_s + 32, sv[1]);
+  tmem_ld_wait();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse_s + 32 * h);
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      float p0, p1;
+      f2unpack(f2fma(f2pack_u(sv[h][c], sv[h][c + 1]), sl2x2, nl2[c >> 1]), p0, p1);
+      p0 = fast_exp2(p0);
+      p1 = fast_exp2(p1);
+      if (MASKED) {
+        const int q0 = next_qpos(slot0 + 32 * h + c);
+        const int q1 = next_qpos(slot0 + 32 * h + c + 1);
+        p0 = kpos <= q0 ? p0 : 0.f;
+        p1 = kpos <= q1 ? p1 : 0.f;
+      }
+      p[32 * h + c] = p0;
+      p[32 * h + c + 1] = p1;
+      pk[c >> 1] = pack_bf16(p0, p1);
+    }
+    tmem_st16(t_pk + 16 * h, pk);
+  }
+}
+
+// (query head, query tile) steps of a key-tile unit
+struct StepWalk {
+  int h_end, kmin;
+  __device__ __forceinline__ bool next(const PosMap& pm, int& hq, int& qt) const {
+    qt = next_q_tile(pm, kRows, qt, kmin);
+    if (qt >= 0) return true;
+    if (++hq >= h_end) return false;
+    qt = next_q_tile(pm, kRows, -1, kmin);
+    return qt >= 0;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __grid_constant__ BwdArgs a) {
+  using C = FCfg<D>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // every offset below assumes a 1024-byte aligned base (no slack is left for
+  // aligning by hand); a misaligned base is reported and the CTA does nothing
+  if (smem_u32(smem) & 1023u) {
+    if (tid == 0) atomicExch(a.err, DEV_SMEM_ALIGN);
+    return;
+  }
+  FBars& bar = *reinterpret_cast<FBars*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  const PosMap pm = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb);
+  const Abort ab{abort_flag, a.err};
+  const int G = a.sh.Hq / a.sh.Hkv;
+  const int ncta = gridDim.x, cta = blockIdx.x;
+
+  if (tid == 0) {
+    mbar_init(&bar.kv_full, 1);
+    mbar_init(&bar.kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.q_full[i], 1);
+      mbar_init(&bar.q_empty[i], 1);
+      mbar_init(&bar.do_full[i], 1);
+      mbar_init(&bar.do_empty[i], 1);
+    }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.p_full, 256);
+    mbar_init(&bar.dp_full, 1);
+    mbar_init(&bar.dst_full, 256);
+    mbar_init(&bar.dss_full, 256);
+    mbar_init(&bar.dq_full, 1);
+    mbar_init(&bar.dq_free, 256);
+    mbar_init(&bar.staged, 256);
+    mbar_init(&bar.ds_free, 1);
+    mbar_init(&bar.acc_full, 1);
+    mbar_init(&bar.done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tdo); prefetch_tmap(&a.tdq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int gs = 0;  // global step index: stage gs & 1, ring phase (gs >> 1) & 1
+      bool ok = true;
+      for (int r = 0, uc = 0; ok; ++r) {
+        const int ui = unit_index(r, cta, ncta);
+        if (ui >= a.n_units) break;
+        const BwdUnit u = a.units[ui];
+        int kmin, kmax;
+        pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
+        const StepWalk w{u.h * G + G, kmin};
+        int hq = u.h * G, qt = -1;
+        if (!w.next(pm, hq, qt)) continue;  // every role skips a unit no query sees
+        if (!(ok = mbar_wait(&bar.kv_empty, (uc & 1) ^ 1, ab))) break;
+        mbar_expect_tx(&bar.kv_full, 2 * C::TILE);
+        for (int bx = 0; bx < D / 64; ++bx) {
+          tma_load_4d(smem + C::OFF_K + bx * kRows * 128, &a.tk, &bar.kv_full, bx * 64, u.h, u.t * kRows, u.b);
+          tma_load_4d(smem + C::OFF_V + bx * kRows * 128, &a.tv, &bar.kv_full, bx * 64, u.h, u.t * kRows, u.b);
+        }
+        do {
+          const int st = gs & 1;
+          const uint32_t ph = ((gs >> 1) & 1) ^ 1;
+          if (!(ok = mbar_wait(&bar.q_empty[st], ph, ab))) break;
+          mbar_expect_tx(&bar.q_full[st], C::TILE + C::VEC_BYTES);
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_load_4d(smem + C::OFF_Q + st * C::TILE + bx * kRows * 128, &a.tq, &bar.q_full[st], bx * 64, hq,
+                        qt * kRows, u.b);
+          const size_t vo = ((size_t)u.b * a.sh.Hq + hq) * a.Spad + (size_t)qt * kRows;
+          unsigned char* vec = smem + C::OFF_VEC + st * C::VEC_BYTES;
+          bulk_load(vec, a.lse_l2 + vo, kRows * 4, &bar.q_full[st]);
+          bulk_load(vec + kRows * 4, a.delta + vo, kRows * 4, &bar.q_full[st]);
+          if (!(ok = mbar_wait(&bar.do_empty[st], ph, ab))) break;
+          mbar_expect_tx(&bar.do_full[st], C::TILE);
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_load_4d(smem + C::OFF_DO + st * C::TILE + bx * kRows * 128, &a.tdo, &bar.do_full[st], bx * 64, hq,
+                        qt * kRows, u.b);
+          ++gs;
+        } while (w.next(pm, hq, qt));
+        ++uc;
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, kRows, 0, 0);  // S^T, dP^T: K-major x K-major
+      constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, 0, 1);    // P^T / dS^T (TMEM) x dO / Q (MN-major)
+      constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, 1, 1);     // dS (MN-major) x K (MN-major)
+      const uint32_t s0 = smem_u32(smem);
+      const uint64_t dK_k = sdesc_sw128(s0 + C::OFF_K, 16, 1024);          // K as K-major A
+      const uint64_t dV_k = sdesc_sw128(s0 + C::OFF_V, 16, 1024);          // V as K-major A
+      const uint64_t dK_mn = sdesc_sw128(s0 + C::OFF_K, kRows * 128, 1024);  // K as MN-major B
+      const uint64_t dS_mn = sdesc_sw128(s0 + C::OFF_DS, kRows * 128, 1024); // dS as MN-major A
+      auto kstep = [](int kk) { return (uint64_t)((((kk >> 2) * (kRows * 128)) + (kk & 3) * 32) >> 4); };
+      auto issue_s = [&](int st) {
+        const uint64_t bq = sdesc_sw128(s0 + C::OFF_Q + st * C::TILE, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::T_S, dK_k + kstep(kk), bq + kstep(kk), IDESC_S, kk > 0 ? 1u : 0u);
+        mma_commit(&bar.s_full);
+      };
+      auto issue_dp = [&](int st) {
+        const uint64_t bo = sdesc_sw128(s0 + C::OFF_DO + st * C::TILE, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::T_DP, dV_k + kstep(kk), bo + kstep(kk), IDESC_S, kk > 0 ? 1u : 0u);
+        mma_commit(&bar.dp_full);
+      };
+      auto issue_dv = [&](int st, bool acc) {
+        const uint64_t bo = sdesc_sw128(s0 + C::OFF_DO + st * C::TILE, kRows * 128, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + packed_col<64>(kk * 16), bo + ((kk * 16 * 128) >> 4), IDESC_ACC,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      auto issue_dk = [&](int st, bool acc) {
+        const uint64_t bq = sdesc_sw128(s0 + C::OFF_Q + st * C::TILE, kRows * 128, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          mma_ts(tmem + C::T_DK, tmem + C::T_DP + packed_col<64>(kk * 16), bq + ((kk * 16 * 128) >> 4), IDESC_ACC,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      auto issue_dq = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          mma_ss(tmem + C::T_DP, dS_mn + ((kk * 16 * 128) >> 4), dK_mn + ((kk * 16 * 128) >> 4), IDESC_DQ,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&bar.dq_full);
+      };
+
+      int gs = 0;
+      bool ok = true;
+      for (int r = 0, uc = 0; ok; ++r) {
+        const int ui = unit_index(r, cta, ncta);
+        if (ui >= a.n_units) break;
+        const BwdUnit u = a.units[ui];
+        int kmin, kmax;
+        pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
+        const StepWalk w{u.h * G + G, kmin};
+        int hq = u.h * G, qt = -1;
+        if (!w.next(pm, hq, qt)) continue;
+        if (!(ok = mbar_wait(&bar.kv_full, uc & 1, ab))) break;
+        tc_fence_after();
+        // prologue: S and dP of the unit's first step
+        if (!(ok = mbar_wait(&bar.q_full[gs & 1], (gs >> 1) & 1, ab))) break;
+        tc_fence_after();
+        issue_s(gs & 1);
+        if (gs > 0 && !(ok = mbar_wait(&bar.dq_free, (gs - 1) & 1, ab))) break;  // dQ of the last step read out
+        if (!(ok = mbar_wait(&bar.do_full[gs & 1], (gs >> 1) & 1, ab))) break;
+        tc_fence_after();
+        issue_dp(gs & 1);
+        for (int j = 0; ok; ++j, ++gs) {
+          const int st = gs & 1;
+          const bool more = w.next(pm, hq, qt);
+          if (!(ok = mbar_wait(&bar.p_full, gs & 1, ab))) break;
+          tc_fence_after();
+          issue_dv(st, j > 0);
+          if (more) {
+            if (!(ok = mbar_wait(&bar.q_full[st ^ 1], ((gs + 1) >> 1) & 1, ab))) break;
+            tc_fence_after();
+            issue_s(st ^ 1);
+          }
+          if (!(ok = mbar_wait(&bar.dst_full, gs & 1, ab))) break;
+          tc_fence_after();
+          issue_dk(st, j > 0);
+          mma_commit(&bar.q_empty[st]);  // Q_j (S_j, dK_j) and its vectors are done
+          if (!(ok = mbar_wait(&bar.dss_full, gs & 1, ab))) break;
+          tc_fence_after();
+          issue_dq();
+          if (!more) break;
+          if (!(ok = mbar_wait(&bar.dq_free, gs & 1, ab))) break;
+          if (!(ok = mbar_wait(&bar.do_full[st ^ 1], ((gs + 1) >> 1) & 1, ab))) break;
+          tc_fence_after();
+          issue_dp(st ^ 1);
+        }
+        if (!ok) break;
+        ++gs;
+        mma_commit(&bar.acc_full);
+        mma_commit(&bar.kv_empty);  // K (last read by dQ) and V are done
+        ++uc;
+      }
+      mma_commit(&bar.done);
+      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dQ reducer
+    // adds each staged dQ tile into the fp32 accumulator; the boxes in the dS
+    // space go first, in their own bulk group, because the next dS waits on them
+    if (lane == 0) {
+      int gs = 0;
+      for (int r = 0;; ++r) {
+        const int ui = unit_index(r, cta, ncta);
+        if (ui >= a.n_units) break;
+        const BwdUnit u = a.units[ui];
+        int kmin, kmax;
+        pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
+        const StepWalk w{u.h * G + G, kmin};
+        int hq = u.h * G, qt = -1;
+        if (!w.next(pm, hq, qt)) continue;
+        do {
+          mbar_wait(&bar.staged, gs & 1, ab);  // runs on after an abort: the staging is garbage, the waits bounded
+#pragma unroll
+          for (int box = 0; box < C::NBOX; ++box) {
+            const unsigned char* bb = box < 2 ? smem + C::OFF_DS + box * (kRows * 128)
+                                              : smem + C::OFF_DO + (gs & 1) * C::TILE + (box - 2) * (kRows * 128);
+            tma_reduce_add_4d(bb, &a.tdq, box * 32, hq, qt * kRows, u.b);
+            if (box == 1) bulk_commit_group();
+          }
+          if (C::NBOX > 2) {
+            bulk_commit_group();
+            bulk_wait_read<1>();
+          } else {
+            bulk_wait_read<0>();
+          }
+          mbar_arrive(&bar.ds_free);  // the dS tile (staging space) may be rewritten
+          bulk_wait_read<0>();
+          mbar_arrive(&bar.do_empty[gs & 1]);  // the dO stage (staging space) may be reloaded
+          ++gs;
+        } while (w.next(pm, hq, qt));
+      }
+      bulk_wait_all();  // every dQ reduce has landed before the CTA retires
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise warps
+    // Group g (warps 4g..4g+3) owns query columns [64g, 64g+64) of S^T/dP^T
+    // (thread = key row = TMEM lane) and dQ columns [gD/2, (g+1)D/2) (thread =
+    // query row).  A failed wait (abort or timeout) runs on with whatever is in
+    // TMEM, so every role walks all of its steps and every wait stays bounded.
+    const int g = warp >> 2;
+    const int row = ((warp & 3) << 5) + lane;  // TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const uint64_t sl2x2 = f2pack(a.scale_log2, a.scale_log2);
+    int gs = 0;
+    bool have_prev = false;
+
+    // dQ of global step gsr: TMEM -> registers (frees the columns for the next
+    // dP) -> scaled fp32 tile in shared memory for the reducer warp (the dS
+    // tile and, for D = 128, the step's dO stage; boxes of 32 columns, 128-byte
+    // swizzle)
+    auto readout = [&](int gsr) {
+      mbar_wait(&bar.dq_full, gsr & 1, ab);
+      tc_fence_after();
+      constexpr int NC = D / 2 / 32;  // 32-column chunks per group
+      uint32_t o[NC][32];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) tmem_ld32(tmem + lane_base + C::T_DP + g * (D / 2) + c * 32, o[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar.dq_free);
+      const float sc = a.scale;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int box = g * NC + c;
+        unsigned char* bb = box < 2 ? smem + C::OFF_DS + box * (kRows * 128)
+                                    : smem + C::OFF_DO + (gsr & 1) * C::TILE + (box - 2) * (kRows * 128);
+        unsigned char* rp = bb + row * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          float4 v;
+          v.x = sc * __uint_as_float(o[c][4 * ch + 0]);
+          v.y = sc * __uint_as_float(o[c][4 * ch + 1]);
+          v.z = sc * __uint_as_float(o[c][4 * ch + 2]);
+          v.w = sc * __uint_as_float(o[c][4 * ch + 3]);
+          *reinterpret_cast<float4*>(rp + ((ch ^ (row & 7)) << 4)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar.staged);
+    };
+
+    for (int r = 0, uc = 0;; ++r) {
+      const int ui = unit_index(r, cta, ncta);
+      if (ui >= a.n_units) break;
+      const BwdUnit u = a.units[ui];
+      const int kslot = u.t * kRows + row;
+      const bool kvalid = kslot < pm.S;
+      const int kpos = kvalid ? pm.pos(kslot) : 0x7fffffff;
+      int kmin, kmax;
+      pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
+      const bool k_inside = u.t * kRows + kRows <= pm.S;
+      const StepWalk w{u.h * G + G, kmin};
+      int hq = u.h * G, qt = -1;
+      if (!w.next(pm, hq, qt)) continue;
+      do {
+        const int st = gs & 1;
+        // ---- P into TMEM as bf16 (fp32 copy kept for dS)
+        mbar_wait(&bar.s_full, gs & 1, ab);
+        mbar_wait(&bar.q_full[st], (gs >> 1) & 1, ab);
+        tc_fence_after();
+        int qmin, qmax;
+        pm.range(qt * kRows, qt * kRows + kRows, qmin, qmax);
+        const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * C::VEC_BYTES) + g * 64;
+        const float* del_s = lse_s + kRows;
+        float p[64];
+        const uint32_t t_s = tmem + lane_base + C::T_S + g * 64;
+        const uint32_t t_pk = tmem + lane_base + C::T_S + packed_col<64>(g * 64);
+        if ((kmax <= qmin) && k_inside)
+          ew_p<false>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, 0);
+        else
+          ew_p<true>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, qt * kRows + g * 64);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar.p_full);
+        // ---- dQ of the previous step
+        if (have_prev) readout(gs - 1);
+        // ---- dS = P * (dP - D): bf16 into TMEM (for dK), then shared memory (for dQ)
+        mbar_wait(&bar.dp_full, gs & 1, ab);
+        tc_fence_after();
+        uint32_t dp[2][32], dk[2][16];
+        tmem_ld32(tmem + lane_base + C::T_DP + g * 64, dp[0]);
+        tmem_ld32(tmem + lane_base + C::T_DP + g * 64 + 32, dp[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(del_s + 32 * h);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float d0, d1;
+            f2unpack(f2mul(f2pack(p[32 * h + c], p[32 * h + c + 1]), f2add(f2pack_u(dp[h][c], dp[h][c + 1]), nd2[c >> 1])),
+                     d0, d1);
+            dk[h][c >> 1] = pack_bf16(d0, d1);
+          }
+          tmem_st16(tmem + lane_base + C::T_DP + packed_col<64>(g * 64 + 32 * h), dk[h]);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar.dst_full);
+        if (gs > 0) mbar_wait(&bar.ds_free, (gs - 1) & 1, ab);  // the previous dQ tile left the dS space
+        unsigned char* dsr = smem + C::OFF_DS + g * (kRows * 128) + row * 128;  // this key row of query half g
+#pragma unroll
+        for (int chunk = 0; chunk < 8; ++chunk)  // 8 query columns per 16-byte chunk
+          *reinterpret_cast<uint4*>(dsr + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(dk[chunk >> 2][4 * (chunk & 3)], dk[chunk >> 2][4 * (chunk & 3) + 1],
+                         dk[chunk >> 2][4 * (chunk & 3) + 2], dk[chunk >> 2][4 * (chunk & 3) + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.dss_full);
+        have_prev = true;
+        ++gs;
+      } while (w.next(pm, hq, qt));
+      // the unit's last dQ, then dV and scale*dK of this key tile
+      readout(gs - 1);
+      have_prev = false;
+      mbar_wait(&bar.acc_full, uc & 1, ab);
+      tc_fence_after();
+      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) +
+                           (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * D;
+      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) +
+                           (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * D;
+      const float sc = a.scale;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float f = which ? sc : 1.f;
+        __nv_bfloat16* dst0 = which ? dkp : dvp;
+#pragma unroll 1
+        for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + (which ? C::T_DK : C::T_DV) + c0, o);
+          tmem_ld_wait();
+          if (kvalid) {
+            uint4* dst = reinterpret_cast<uint4*>(dst0 + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pack_bf16(f * __uint_as_float(o[8 * v4 + 0]), f * __uint_as_float(o[8 * v4 + 1])),
+                                   pack_bf16(f * __uint_as_float(o[8 * v4 + 2]), f * __uint_as_float(o[8 * v4 + 3])),
+                                   pack_bf16(f * __uint_as_float(o[8 * v4 + 4]), f * __uint_as_float(o[8 * v4 + 5])),
+                                   pack_bf16(f * __uint_as_float(o[8 * v4 + 6]), f * __uint_as_float(o[8 * v4 + 7])));
+          }
+        }
+      }
+      tc_fence_before();
+      ++uc;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dq (bf16, [B, S, Hq, D]) = the fp32 accumulator; 8 elements per thread
+__global__ void __launch_bounds__(256) bwd_dq_round_kernel(const float* __restrict__ acc, __nv_bfloat16* dq, long long n8) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+    const float4 x = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i);
+    const float4 y = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y),
+                                                 pack_bf16(y.z, y.w));
+  }
+}
+
+template <int D>
+cudaError_t launch_fused(const BwdArgs& a, int grid, cudaStream_t st) {
+  auto kern = attn_bwd_fused_kernel<D>;
+  // more than half of an SM's shared memory: one CTA per SM, so the CTA's
+  // 512-column TMEM allocation never waits for a neighbour
+  int smem = FCfg<D>::SMEM;
+  if (smem < 120 * 1024) smem = 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreadsF, smem, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    cudaFuncAttributes fa{};
+    cudaFuncGetAttributes(&fa, kern);
+    fprintf(stderr, "attn_bwd_fused<%d>: %s (regs %d, max threads %d, smem %d)\n", D, cudaGetErrorString(e),
+            fa.numRegs, fa.maxThreadsPerBlock, smem);
+  }
+  return e;
+}
+
+}  // namespace
+
+bool bwd_fused_supported(int Dqk, int Dv) { return Dqk == Dv && (Dqk == 64 || Dqk == 128); }
+
+cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st) {
+  return a.sh.Dqk == 64 ? launch_fused<64>(a, grid, st) : launch_fused<128>(a, grid, st);
+}
+
+cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, cudaStream_t st) {
+  const long long n8 = n / 8;  // n is a multiple of 64 (head dim)
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  bwd_dq_round_kernel<<<(int)blocks, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(dq), n8);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

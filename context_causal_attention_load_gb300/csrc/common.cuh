@@ -25,6 +25,7 @@ enum : int {
   DEV_OK = 0,
   DEV_TIMEOUT = 1,      // a bounded mbarrier wait ran out
   DEV_LENS_CLAMPED = 2, // gqa_decode saw lens[b] outside [0, Smax]
+  DEV_SMEM_ALIGN = 3,   // dynamic shared memory not 1024-byte aligned (kernel did nothing)
 };
 
 constexpr int kMaxPieces = 64;
@@ -357,6 +358,35 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// r-th unit of CTA `cta` in a snake deal over ncta CTAs of a work list sorted
+// by decreasing cost (even rounds left to right, odd rounds right to left)
+__device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
+  return r * ncta + ((r & 1) ? (ncta - 1 - cta) : cta);
+}
+
+// Two element-wise groups each own HC consecutive TMEM columns of a row; a
+// group packs the bf16 pairs of column c into its own range, so the packed
+// column of c is (c / HC) * HC + (c % HC) / 2.  TS MMAs read 16 columns (8
+// packed) per k-step, never straddling two groups.
+template <int HC>
+__host__ __device__ constexpr int packed_col(int c) { return (c / HC) * HC + (c % HC) / 2; }
+
+// TMA reduce-add of a tile from shared memory into global memory (element
+// type of the tensor map), tracked by the issuing thread's bulk async-group
+__device__ __forceinline__ void tma_reduce_add_4d(const void* src, const CUtensorMap* map, int c0, int c1, int c2,
+                                                  int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk groups have finished reading their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and their writes are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // named barrier among `count` threads
 __device__ __forceinline__ void named_bar(int id, int count) {

@@ -70,6 +70,8 @@ struct BwdUnit {  // dk/dv unit: one key tile of one KV head; dq unit: one query
 };
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;  // dq kernel uses 128-row boxes; dkdv uses BQ-row boxes for q/do
+  CUtensorMap tdq;              // fused kernel: fp32 dQ accumulator, 32-column x 128-row boxes
+  float* dq_acc;                // fused kernel: [B, S, Hq, Dqk] fp32, zeroed by the preprocess
   const float* lse_l2;          // [B, Hq, Spad] -lse * log2(e), -inf in padding
   const float* delta;           // [B, Hq, Spad] -rowsum(dout*out), 0 in padding
   void* dq;
@@ -84,7 +86,12 @@ struct BwdArgs {
   int* err;
 };
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, float* lse_l2,
-                                  float* delta, const AttnShape& sh, int Spad, cudaStream_t st);
+                                  float* delta, float* dq_acc, const AttnShape& sh, int Spad, cudaStream_t st);
+// fused backward (one kernel for dK, dV and dQ, the latter through an fp32
+// accumulator) for Dqk == Dv in {64, 128}
+bool bwd_fused_supported(int Dqk, int Dv);
+cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, cudaStream_t st);
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, int grid, cudaStream_t st);
 int bwd_dkdv_q_tile(int Dqk);  // query rows per step of the dk/dv kernel
