@@ -49,7 +49,7 @@ struct FCfg {
   static constexpr int OFF_VEC = OFF_DS + DS_BYTES;  // stage s: lse[128] then delta[128] (fp32)
   static constexpr int VEC_BYTES = 2 * kRows * 4;
   static constexpr int OFF_BAR = OFF_VEC + 2 * VEC_BYTES;
-  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int OFF_MISC = OFF_BAR + 256;  // TMEM address, abort flag, StepInfo[2] at +32
   static constexpr int SMEM = OFF_MISC + 64;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TILE % 1024 == 0 && OFF_DS % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -60,6 +60,13 @@ struct FCfg {
   static constexpr int T_DK = 256 + D;
   static_assert(T_DK + D <= 512, "TMEM budget");
   static constexpr int NBOX = D / 32;  // fp32 dQ boxes of 32 columns x 128 rows (16 KiB)
+};
+
+// what the producer publishes with each Q stage: the step's query head and
+// tile, and whether it is the last step of its unit (walking the steps costs
+// a chain of integer divisions; only the producer, which runs ahead, pays it)
+struct StepInfo {
+  int hq, qt, last, pad;
 };
 
 struct FBars {
@@ -158,6 +165,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
   FBars& bar = *reinterpret_cast<FBars*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  volatile StepInfo* info = reinterpret_cast<volatile StepInfo*>(smem + C::OFF_MISC + 32);
   const PosMap pm = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb);
   const Abort ab{abort_flag, a.err};
   const int G = a.sh.Hq / a.sh.Hkv;
@@ -215,11 +223,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           tma_load_4d(smem + C::OFF_K + bx * kRows * 128, &a.tk, &bar.kv_full, bx * 64, u.h, u.t * kRows, u.b);
           tma_load_4d(smem + C::OFF_V + bx * kRows * 128, &a.tv, &bar.kv_full, bx * 64, u.h, u.t * kRows, u.b);
         }
+        bool more;
         do {
+          int nhq = hq, nqt = qt;
+          more = w.next(pm, nhq, nqt);
           const int st = gs & 1;
           const uint32_t ph = ((gs >> 1) & 1) ^ 1;
           if (!(ok = mbar_wait(&bar.q_empty[st], ph, ab))) break;
-          mbar_expect_tx(&bar.q_full[st], C::TILE + C::VEC_BYTES);
+          info[st].hq = hq;
+          info[st].qt = qt;
+          info[st].last = more ? 0 : 1;
+          mbar_expect_tx(&bar.q_full[st], C::TILE + C::VEC_BYTES);  // (release: the info is visible to q_full's waiters)
           for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d(smem + C::OFF_Q + st * C::TILE + bx * kRows * 128, &a.tq, &bar.q_full[st], bx * 64, hq,
                         qt * kRows, u.b);
@@ -233,7 +247,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
             tma_load_4d(smem + C::OFF_DO + st * C::TILE + bx * kRows * 128, &a.tdo, &bar.do_full[st], bx * 64, hq,
                         qt * kRows, u.b);
           ++gs;
-        } while (w.next(pm, hq, qt));
+          hq = nhq;
+          qt = nqt;
+        } while (more);
         ++uc;
       }
     }
@@ -301,6 +317,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         // prologue: S and dP of the unit's first step
         if (!(ok = mbar_wait(&bar.q_full[gs & 1], (gs >> 1) & 1, ab))) break;
         tc_fence_after();
+        bool more = !info[gs & 1].last;
         issue_s(gs & 1);
         if (gs > 0 && !(ok = mbar_wait(&bar.dq_free, (gs - 1) & 1, ab))) break;  // dQ of the last step read out
         if (!(ok = mbar_wait(&bar.do_full[gs & 1], (gs >> 1) & 1, ab))) break;
@@ -308,13 +325,14 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         issue_dp(gs & 1);
         for (int j = 0; ok; ++j, ++gs) {
           const int st = gs & 1;
-          const bool more = w.next(pm, hq, qt);
+          const bool this_more = more;
           if (!(ok = mbar_wait(&bar.p_full, gs & 1, ab))) break;
           tc_fence_after();
           issue_dv(st, j > 0);
-          if (more) {
+          if (this_more) {
             if (!(ok = mbar_wait(&bar.q_full[st ^ 1], ((gs + 1) >> 1) & 1, ab))) break;
             tc_fence_after();
+            more = !info[st ^ 1].last;
             issue_s(st ^ 1);
           }
           if (!(ok = mbar_wait(&bar.dst_full, gs & 1, ab))) break;
@@ -324,7 +342,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           if (!(ok = mbar_wait(&bar.dss_full, gs & 1, ab))) break;
           tc_fence_after();
           issue_dq();
-          if (!more) break;
+          if (!this_more) break;
           if (!(ok = mbar_wait(&bar.dq_free, gs & 1, ab))) break;
           if (!(ok = mbar_wait(&bar.do_full[st ^ 1], ((gs + 1) >> 1) & 1, ab))) break;
           tc_fence_after();
@@ -435,15 +453,20 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       int kmin, kmax;
       pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
       const bool k_inside = u.t * kRows + kRows <= pm.S;
-      const StepWalk w{u.h * G + G, kmin};
-      int hq = u.h * G, qt = -1;
-      if (!w.next(pm, hq, qt)) continue;
+      {
+        const StepWalk w{u.h * G + G, kmin};
+        int hq = u.h * G, qt = -1;
+        if (!w.next(pm, hq, qt)) continue;
+      }
+      bool last;
       do {
         const int st = gs & 1;
         // ---- P into TMEM as bf16 (fp32 copy kept for dS)
         mbar_wait(&bar.s_full, gs & 1, ab);
         mbar_wait(&bar.q_full[st], (gs >> 1) & 1, ab);
         tc_fence_after();
+        const int qt = info[st].qt;
+        last = info[st].last != 0;
         int qmin, qmax;
         pm.range(qt * kRows, qt * kRows + kRows, qmin, qmax);
         const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * C::VEC_BYTES) + g * 64;
@@ -493,7 +516,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         mbar_arrive(&bar.dss_full);
         have_prev = true;
         ++gs;
-      } while (w.next(pm, hq, qt));
+      } while (!last);
       // the unit's last dQ, then dV and scale*dK of this key tile
       readout(gs - 1);
       have_prev = false;
