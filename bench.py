@@ -46,6 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "attn_fwd": "attn_fwd.cu", "attn_fwd_shard": "attn_fwd.cu", "attn_bwd_dkdv": "attn_bwd.cu",
     "attn_bwd_dq": "attn_bwd.cu", "bwd_preprocess": "attn_bwd.cu", "gqa_decode": "decode.cu",
+    "attn_bwd_fused": "attn_bwd_fused.cu", "bwd_dq_round": "attn_bwd_fused.cu",
     "lb_permute": "permute.cu", "lb_unpermute": "permute.cu",
 }
 
@@ -67,12 +68,15 @@ def flops_bwd(w):
 
 
 def kernel_flops(name, w):
-    """Algorithmic FLOPs of one launch of each attention kernel.  The dk/dv
-    kernel owns the S and dP recomputes plus dV and dK; the dq kernel is
-    credited only with dQ (its own S/dP recompute is extra work)."""
+    """Algorithmic FLOPs of one launch of each attention kernel.  The fused
+    backward does all five backward products (S and dP recomputes, dV, dK,
+    dQ); in the two-kernel backward the dk/dv kernel owns the S and dP
+    recomputes plus dV and dK, and the dq kernel is credited only with dQ (its
+    own S/dP recompute is extra work)."""
     p = pairs(w)
     return {
         "attn_fwd": 2.0 * p * (w["Dqk"] + w["Dv"]),
+        "attn_bwd_fused": 2.0 * p * (3 * w["Dqk"] + 2 * w["Dv"]),
         "attn_bwd_dkdv": 2.0 * p * (2 * w["Dqk"] + 2 * w["Dv"]),
         "attn_bwd_dq": 2.0 * p * w["Dqk"],
     }.get(name)
