@@ -108,7 +108,10 @@ int cp_attn_fwd_shard(const void* q, const void* k, const void* v, void* out, fl
  * dk/dv sum over the query heads of a group and over all shards (the
  * transpose of the K/V all-gather).  q, k, v, out, lse, dout: device
  * inputs (out and lse as written by cp_attn_fwd); dq, dk, dv: device
- * outputs (overwritten).  Constraints as cp_attn_fwd.
+ * outputs (overwritten).  Constraints as cp_attn_fwd.  With Dqk == Dv
+ * (64 or 128) dq is summed in an fp32 scratch buffer of B*S*Hq*Dqk floats
+ * (library-owned, grown on demand) by reduce-adds whose order varies, so
+ * dq may differ in its last bits between calls; dk, dv are repeatable.
  */
 int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
@@ -142,7 +145,7 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
  * rejected with CPATTN_ERR_INVALID_ARG before any launch (about
  * B*Hkv*ceil(Smax/128)*G'*(D+2)*4 bytes, G' = Hq/Hkv rounded up to a power
  * of two; the decode workload B=24, Hkv=8, Smax=2048, G=4, D=128 needs
- * 3.2 MiB).
+ * 6.1 MiB).
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  Every
  * call shares the one array (each call writes every entry it later reads,
