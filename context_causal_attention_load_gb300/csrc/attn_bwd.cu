@@ -39,46 +39,45 @@ constexpr int TK = 128;  // key rows per dk/dv unit; query rows per dq unit
 // ============================================================================
 // preprocess: -lse*log2(e) (-inf past S) and -rowsum(dO*O) (0 past S), stored
 // negated so the element-wise warps apply them with one fused multiply-add;
-// layout [B, Hq, Spad]; one warp per (b, s, h) row.  With dq_acc, also zeroes
-// the row of the fused kernel's fp32 dQ accumulator.
+// layout [B, Hq, Spad].  LPR = Dv/8 lanes per (b, h, s) row, each with one
+// 16-byte load of out and of dout; rows go in output order (s fastest), so
+// the row statistics are written and lse read contiguously.  With dq_acc,
+// also zeroes the row of the fused kernel's fp32 dQ accumulator.
 // ============================================================================
+template <int LPR>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse, float* lse_l2,
                                                              float* delta, float* dq_acc, AttnShape sh, int Spad) {
-  const long long nrows = (long long)sh.B * Spad * sh.Hq;
-  const int lane = threadIdx.x & 31;
-  for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nrows;
-       w += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const int h = int(w % sh.Hq);
-    const long long bs = w / sh.Hq;
-    const int s = int(bs % Spad);
-    const int b = int(bs / Spad);
-    const size_t o_idx = ((size_t)b * sh.Hq + h) * Spad + s;
-    if (s >= sh.S) {
-      if (lane == 0) {
-        lse_l2[o_idx] = -INFINITY;
-        delta[o_idx] = 0.f;
-      }
-      continue;
-    }
-    const size_t base = (((size_t)b * sh.S + s) * sh.Hq + h) * sh.Dv;
-    if (dq_acc) {
-      float4* z = reinterpret_cast<float4*>(dq_acc + (((size_t)b * sh.S + s) * sh.Hq + h) * sh.Dqk);
-      for (int i = lane; i < sh.Dqk / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+  const long long nrows = (long long)sh.B * sh.Hq * Spad;
+  const int sub = threadIdx.x % LPR;
+  const unsigned gmask = ((1u << LPR) - 1u) << ((threadIdx.x & 31) & ~(LPR - 1));  // this row's lanes
+  const long long stride = (long long)gridDim.x * blockDim.x / LPR;
+  for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / LPR; r < nrows; r += stride) {
+    const int s = int(r % Spad);
+    const long long bh = r / Spad;
+    const int h = int(bh % sh.Hq);
+    const int b = int(bh / sh.Hq);
+    const bool valid = s < sh.S;
     float acc = 0.f;
-    for (int d = lane * 2; d < sh.Dv; d += 64) {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(out + base + d);
-      const uint32_t g = *reinterpret_cast<const uint32_t*>(dout + base + d);
-      acc = fmaf(bf16lo(a), bf16lo(g), acc);
-      acc = fmaf(bf16hi(a), bf16hi(g), acc);
+    if (valid) {
+      const size_t row = ((size_t)b * sh.S + s) * sh.Hq + h;
+      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(out + row * sh.Dv) + sub);
+      const uint4 g = __ldcs(reinterpret_cast<const uint4*>(dout + row * sh.Dv) + sub);
+      acc = fmaf(bf16lo(a.x), bf16lo(g.x), fmaf(bf16hi(a.x), bf16hi(g.x), acc));
+      acc = fmaf(bf16lo(a.y), bf16lo(g.y), fmaf(bf16hi(a.y), bf16hi(g.y), acc));
+      acc = fmaf(bf16lo(a.z), bf16lo(g.z), fmaf(bf16hi(a.z), bf16hi(g.z), acc));
+      acc = fmaf(bf16lo(a.w), bf16lo(g.w), fmaf(bf16hi(a.w), bf16hi(g.w), acc));
+      if (dq_acc) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + row * sh.Dqk);
+        for (int c = sub; c < sh.Dqk / 4; c += LPR) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      delta[o_idx] = -acc;
-      lse_l2[o_idx] = -lse[((size_t)b * sh.Hq + h) * sh.S + s] * 1.4426950408889634f;
+    for (int o = LPR / 2; o; o >>= 1) acc += __shfl_xor_sync(gmask, acc, o);
+    if (sub == 0) {
+      delta[r] = -acc;
+      lse_l2[r] = valid ? -lse[bh * sh.S + s] * 1.4426950408889634f : -INFINITY;
     }
   }
 }
@@ -758,11 +757,12 @@ int bwd_dq_kv_tile(int) { return 64; }
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, float* lse_l2, float* delta,
                                   float* dq_acc, const AttnShape& sh, int Spad, cudaStream_t st) {
   const long long rows = (long long)sh.B * Spad * sh.Hq;
-  long long blocks = (rows * 32 + 255) / 256;
-  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  bwd_preprocess_kernel<<<(int)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
-                                                     static_cast<const __nv_bfloat16*>(dout), lse, lse_l2, delta, dq_acc,
-                                                     sh, Spad);
+  const int lpr = sh.Dv / 8;  // Dv is 64 or 128
+  long long blocks = (rows * lpr + 255) / 256;
+  if (blocks > 152LL * 64) blocks = 152LL * 64;
+  auto kern = lpr == 16 ? bwd_preprocess_kernel<16> : bwd_preprocess_kernel<8>;
+  kern<<<(int)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
+                                    lse, lse_l2, delta, dq_acc, sh, Spad);
   return cudaGetLastError();
 }
 
