@@ -261,8 +261,10 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
 // G <= 16 heads are the N columns (columns past G are computed and ignored;
 // their P rows stay zero).  Persistent: one CTA per SM; only slices that hold
 // positions are items, numbered densely and dealt round-robin so every CTA
-// gets the same count to within one.  Warp 0 streams K, V and q with TMA
-// through a 3-stage ring, warp 1 issues the MMAs, and two softmax groups
+// gets the same count to within one.  Warp 0 streams K and q with TMA through
+// one 3-stage ring and warp 10 streams V through another (K is freed as soon
+// as the scores are formed, so more of the next items' bytes are in flight
+// while the softmax runs), warp 1 issues the MMAs, and two softmax groups
 // (warps 2-5 and 6-9; one thread per position for the scores, per dim for the
 // output) take alternate items, so one group's reductions overlap the other's.
 // S, O (TMEM), P (shared memory) and the group barriers are indexed by item
@@ -272,13 +274,15 @@ namespace tcd {
 constexpr int D = 128;
 constexpr int NH = 16;                 // head columns of the MMAs
 constexpr int ROWS = kDecodeSplit;     // positions per item
-constexpr int NST = 3;                 // ring stages
+constexpr int NK = 3;                  // K (+q) ring stages: freed once the scores are formed
+constexpr int NV = 3;                  // V ring stages: freed once the output is formed
 constexpr int K_BYTES = ROWS * D * 2;  // two 64-column boxes
 constexpr int V_BYTES = ROWS * D * 2;
 constexpr int Q_BYTES = NH * D * 2;    // two boxes of 16 rows
-constexpr int STAGE = K_BYTES + V_BYTES + Q_BYTES;
+constexpr int KSTAGE = K_BYTES + Q_BYTES;
 constexpr int P_BYTES = NH * ROWS * 2;  // P^T as [head][position], two boxes of 64 positions
-constexpr int OFF_P = NST * STAGE;
+constexpr int OFF_V = NK * KSTAGE;
+constexpr int OFF_P = OFF_V + NV * V_BYTES;
 constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
 constexpr int OFF_RED = OFF_BAR + 256;  // per group: float rmax[4][NH], rsum[4][NH]
 constexpr int OFF_MISC = OFF_RED + 2 * 2 * 4 * NH * 4;
@@ -286,12 +290,12 @@ constexpr int OFF_LENS = OFF_MISC + 64;
 constexpr int MAX_B = 1024;             // batch rows staged in shared memory
 constexpr int OFF_PRE = OFF_LENS + MAX_B * 4;
 constexpr int SMEM = OFF_PRE + (MAX_B + 1) * 4 + 1024;
-constexpr int kThreadsTc = 320;
-static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+constexpr int kThreadsTc = 352;
+static_assert(KSTAGE % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM <= 232448, "shared memory budget");
 static_assert(ROWS == 128, "one position per softmax thread");
 struct Bars {
-  uint64_t full[NST], empty[NST];
+  uint64_t kfull[NK], kempty[NK], vfull[NV], vempty[NV];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t done;
 };
@@ -336,22 +340,28 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
   const Abort ab{abort_flag, a.err};
   asm volatile("griddepcontrol.launch_dependents;");  // the merge grid may be scheduled now
 
+  // set-up that reads no input overlaps the previous kernel in the stream
+  // (this grid is launched as a programmatic dependent)
   if (tid == 0) {
-    for (int i = 0; i < NST; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
+    for (int i = 0; i < NK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
+    for (int i = 0; i < NV; ++i) { mbar_init(&bar.vfull[i], 1); mbar_init(&bar.vempty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&bar.s_full[i], 1); mbar_init(&bar.p_full[i], 128); mbar_init(&bar.o_full[i], 1); }
     mbar_init(&bar.done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == 1) { tmem_alloc(tmem_slot, 64); tmem_relinquish(); }
+  if (warp == 0 && lane == 0) { prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tq); }
+  // P rows of heads past G are never written again: zero both P buffers once
+  for (int i = tid; i < 2 * P_BYTES / 16; i += kThreadsTc)
+    reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs written by earlier kernels are visible
   // stage (and validate) the lengths; rows with an empty cache get zeros here
   for (int bb = tid; bb < a.B; bb += kThreadsTc) {
     const int l = a.lens[bb];
     if ((l < 0 || l > a.Smax) && cta == 0) atomicExch(a.err, DEV_LENS_CLAMPED);
     lens_s[bb] = l < 0 ? 0 : (l > a.Smax ? a.Smax : l);
   }
-  // P rows of heads past G are never written again: zero both P buffers once
-  for (int i = tid; i < 2 * P_BYTES / 16; i += kThreadsTc)
-    reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   __syncthreads();
   if (warp == 0) {  // exclusive prefix of items per row: each lane scans a run of rows
@@ -376,8 +386,6 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
       if (lens_s[bb] == 0)
         for (int x = tid - 32; x < a.Hq * D; x += kThreadsTc - 32) ob[(size_t)bb * a.Hq * D + x] = __float2bfloat16(0.f);
   }
-  if (warp == 1) { tmem_alloc(tmem_slot, 64); tmem_relinquish(); }
-  if (warp == 0 && lane == 0) { prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tq); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -386,21 +394,31 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
   const int n_items = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // this CTA's items k: j = cta + k*ncta
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------- TMA producer: K and q
     if (lane == 0) {
       for (int k = 0; k < n_items; ++k) {
         const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
-        const int st = k % NST;
-        if (!mbar_wait(&bar.empty[st], ((k / NST) & 1) ^ 1, ab)) break;
-        unsigned char* sb = smem + st * STAGE;
-        mbar_expect_tx(&bar.full[st], STAGE);
-        const int t0 = it.sp * ROWS;
+        const int st = k % NK;
+        if (!mbar_wait(&bar.kempty[st], ((k / NK) & 1) ^ 1, ab)) break;
+        unsigned char* sb = smem + st * KSTAGE;
+        mbar_expect_tx(&bar.kfull[st], KSTAGE);
         for (int bx = 0; bx < 2; ++bx) {
-          tma_load_4d(sb + bx * (ROWS * 128), &a.tk, &bar.full[st], bx * 64, t0, it.g, it.b);
-          tma_load_3d(sb + K_BYTES + V_BYTES + bx * (NH * 128), &a.tq, &bar.full[st], bx * 64, it.g * G, it.b);
+          tma_load_4d(sb + bx * (ROWS * 128), &a.tk, &bar.kfull[st], bx * 64, it.sp * ROWS, it.g, it.b);
+          tma_load_3d(sb + K_BYTES + bx * (NH * 128), &a.tq, &bar.kfull[st], bx * 64, it.g * G, it.b);
         }
+      }
+    }
+  } else if (warp == 10) {
+    // ---------------------------------------------------------- TMA producer: V
+    if (lane == 0) {
+      for (int k = 0; k < n_items; ++k) {
+        const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
+        const int st = k % NV;
+        if (!mbar_wait(&bar.vempty[st], ((k / NV) & 1) ^ 1, ab)) break;
+        unsigned char* sb = smem + OFF_V + st * V_BYTES;
+        mbar_expect_tx(&bar.vfull[st], V_BYTES);
         for (int bx = 0; bx < 2; ++bx)
-          tma_load_4d(sb + K_BYTES + bx * (ROWS * 128), &a.tv, &bar.full[st], bx * 64, t0, it.g, it.b);
+          tma_load_4d(sb + bx * (ROWS * 128), &a.tv, &bar.vfull[st], bx * 64, it.sp * ROWS, it.g, it.b);
       }
     }
   } else if (warp == 1) {
@@ -410,39 +428,41 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
       constexpr uint32_t IDESC_O = idesc_bf16(128, NH, 1, 0);   // V^T (MN-major) x P^T (K-major)
       const uint32_t s0 = smem_u32(smem);
       auto issue_s = [&](int k) {
-        const uint32_t sb = s0 + (k % NST) * STAGE;
-        const uint64_t ak = sdesc_sw128(sb, 16, 1024), bq = sdesc_sw128(sb + K_BYTES + V_BYTES, 16, 1024);
+        const uint32_t sb = s0 + (k % NK) * KSTAGE;
+        const uint64_t ak = sdesc_sw128(sb, 16, 1024), bq = sdesc_sw128(sb + K_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + (k & 1) * 16, ak + (((kk >> 2) * (ROWS * 128) + (kk & 3) * 32) >> 4),
                  bq + (((kk >> 2) * (NH * 128) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
         mma_commit(&bar.s_full[k & 1]);
+        mma_commit(&bar.kempty[k % NK]);
       };
       auto issue_o = [&](int k) {
-        const uint32_t sb = s0 + (k % NST) * STAGE;
-        const uint64_t av = sdesc_sw128(sb + K_BYTES, ROWS * 128, 1024);
+        const uint32_t sb = s0 + OFF_V + (k % NV) * V_BYTES;
+        const uint64_t av = sdesc_sw128(sb, ROWS * 128, 1024);
         const uint64_t bp = sdesc_sw128(s0 + OFF_P + (k & 1) * P_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < ROWS / 16; ++kk)
           mma_ss(tmem + 32 + (k & 1) * 16, av + ((kk * 16 * 128) >> 4),
                  bp + (((kk >> 2) * (NH * 128) + (kk & 3) * 32) >> 4), IDESC_O, kk > 0 ? 1u : 0u);
         mma_commit(&bar.o_full[k & 1]);
-        mma_commit(&bar.empty[k % NST]);
+        mma_commit(&bar.vempty[k % NV]);
       };
       bool ok = true;
       // scores of the first two items, then: O(k) once group k&1 has written
       // P(k); S(k+2) into the buffer that group has finished reading
       for (int k = 0; k < 2 && k < n_items && ok; ++k) {
-        if (!(ok = mbar_wait(&bar.full[k % NST], (k / NST) & 1, ab))) break;
+        if (!(ok = mbar_wait(&bar.kfull[k % NK], (k / NK) & 1, ab))) break;
         tc_fence_after();
         issue_s(k);
       }
       for (int k = 0; ok && k < n_items; ++k) {
         if (!(ok = mbar_wait(&bar.p_full[k & 1], (k >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait(&bar.vfull[k % NV], (k / NV) & 1, ab))) break;
         tc_fence_after();
         issue_o(k);
         if (k + 2 < n_items) {
-          if (!(ok = mbar_wait(&bar.full[(k + 2) % NST], ((k + 2) / NST) & 1, ab))) break;
+          if (!(ok = mbar_wait(&bar.kfull[(k + 2) % NK], ((k + 2) / NK) & 1, ab))) break;
           tc_fence_after();
           issue_s(k + 2);
         }
@@ -555,10 +575,10 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
 }
 
 // merge the slices of every (b, g) that has more than one: one CTA of
-// kCombineThreads per (b, g).  Warp w reduces the maxima and denominators of
-// head w (lanes over slices); each thread then owns one or more outputs and
-// keeps sixteen slices' loads in flight (a chain of dependent global loads
-// here costs more than the attention itself).
+// kCombineThreads per (b, g); each thread owns output elements and loads the
+// (max, sum, partial) of sixteen slices at a time, all in flight together,
+// merging chunks of slices online (a chain of dependent global loads here
+// would cost more than the attention itself)
 constexpr int kCombineThreads = 512;
 template <int D, int GMAX>
 __global__ void __launch_bounds__(kCombineThreads) gqa_decode_combine_kernel(DecodeArgs a, int max_split) {
@@ -572,45 +592,38 @@ __global__ void __launch_bounds__(kCombineThreads) gqa_decode_combine_kernel(Dec
   // launched early (programmatic dependent launch): the partials are
   // complete and visible once the attention grid has finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float cm[GMAX], cl[GMAX];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float* ml0 = a.part_ml + (size_t)bg * max_split * GMAX * 2;
   const float* po = a.part_o + (size_t)bg * max_split * GMAX * D;
-  for (int h = warp; h < G; h += kCombineThreads / 32) {
-    float M = -INFINITY;
-    for (int s2 = lane; s2 < nsplit; s2 += 32) M = fmaxf(M, ml0[(s2 * GMAX + h) * 2]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int s2 = lane; s2 < nsplit; s2 += 32) {
-      const float* ml = ml0 + (s2 * GMAX + h) * 2;
-      L = fmaf(ml[1], fast_exp2(ml[0] - M), L);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) {
-      cm[h] = M;
-      cl[h] = L;
-    }
-  }
-  __syncthreads();
   __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.Hq + (size_t)g * G) * D;
-  for (int x = tid; x < G * D; x += kCombineThreads) {
+  for (int x = threadIdx.x; x < G * D; x += kCombineThreads) {
     const int h = x / D, d = x - h * D;
-    const float M = cm[h];
-    float acc = 0.f;
+    float M = -INFINITY, L = 0.f, acc = 0.f;
     for (int s0 = 0; s0 < nsplit; s0 += 16) {
-      float o[16], m[16];
+      float o[16], m[16], l[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const bool in = s0 + j < nsplit;
+        const float* ml = ml0 + ((size_t)(s0 + j) * GMAX + h) * 2;
         o[j] = in ? po[((size_t)(s0 + j) * GMAX + h) * D + d] : 0.f;
-        m[j] = in ? ml0[((s0 + j) * GMAX + h) * 2] : M;
+        m[j] = in ? ml[0] : -INFINITY;
+        l[j] = in ? ml[1] : 0.f;
       }
+      float mc = m[0];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc = fmaf(o[j], fast_exp2(m[j] - M), acc);
+      for (int j = 1; j < 16; ++j) mc = fmaxf(mc, m[j]);
+      const float mn = fmaxf(M, mc);  // finite: every chunk holds at least one slice
+      const float f = fast_exp2(M - mn);
+      acc *= f;
+      L *= f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float w = fast_exp2(m[j] - mn);  // 0 for slices past nsplit
+        acc = fmaf(o[j], w, acc);
+        L = fmaf(l[j], w, L);
+      }
+      M = mn;
     }
-    og[x] = __float2bfloat16(acc / cl[h]);
+    og[x] = __float2bfloat16(acc / L);
   }
 }
 
@@ -665,8 +678,17 @@ cudaError_t launch_tc(const DecodeArgs& a0, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int max_split = decode_max_split(a.Smax);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
-  kern<<<sms, tcd::kThreadsTc, tcd::SMEM, st>>>(a, scale_log2, max_split);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(tcd::kThreadsTc);
+  cfg.dynamicSmemBytes = tcd::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // its set-up overlaps the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, kern, a, scale_log2, max_split)) != cudaSuccess) return e;
   return max_split > 1 ? launch_combine<128, GMAX>(a, max_split, st) : cudaSuccess;
 }
 
