@@ -74,11 +74,6 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier area");
 
-__device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
-  // snake order over the heaviest-first list
-  return r * ncta + ((r & 1) ? (ncta - 1 - cta) : cta);
-}
-
 __device__ __forceinline__ int kv_bound(const PosMap& pm, const FwdUnit& u) {
   int mn, mx, mx2 = -1;
   pm.range(u.t0 * BM, u.t0 * BM + BM, mn, mx);
@@ -95,6 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   int* kpos_s = reinterpret_cast<int*>(smem + C::OFF_POS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  // per K stage: 1 if the tile in it is its unit's last (the producer walks the
+  // tiles, a chain of integer divisions, so the MMA thread does not have to)
+  volatile int* klast = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 32);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -158,8 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tma_load_4d(smem + C::OFF_Q + C::Q_BYTES + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h1,
                         u.t1 * BM, u.b);
         const int bound = kv_bound(pm, u);
-        for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0; kt = next_kv_tile(pm, BN, kt, bound)) {
+        for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0;) {
+          const int nkt = next_kv_tile(pm, BN, kt, bound);
           if (!(ok = mbar_wait(&bar.k_empty[ks], kph ^ 1, ab))) break;
+          klast[ks] = nkt < 0 ? 1 : 0;  // published with the tile (the arrive below releases it)
           mbar_expect_tx(&bar.k_full[ks], C::K_BYTES);
           ++nk;
           for (int bx = 0; bx < DQK / 64; ++bx)
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tma_load_4d(smem + C::OFF_V + vs * C::V_BYTES + bx * BN * 128, &a.tv, &bar.v_full[vs], bx * 64,
                         u.hkv, kt * BN, u.b);
           if (++vs == C::NV) { vs = 0; vph ^= 1; }
+          kt = nkt;
         }
       }
       if (!ok) {
@@ -223,14 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (ui >= a.n_units) break;
         const FwdUnit u = a.units[ui];
         const bool has1 = u.h1 >= 0;
-        const int bound = kv_bound(pm, u);
         if (!(ok = mbar_wait(&bar.q_full, qph, ab))) break;
         qph ^= 1;
         tc_fence_after();
-        int kt = next_kv_tile(pm, BN, -1, bound);
         // prologue: S_0 and S_1 of the first key tile
         if (!(ok = mbar_wait(&bar.k_full[ks], kph, ab))) break;
         tc_fence_after();
+        bool last = klast[ks] != 0;
         issue_qk(0, ks);
         mma_commit(&bar.s_full[0]);
         if (has1) {
@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mma_commit(&bar.k_empty[ks]);
         if (++ks == C::NK) { ks = 0; kph ^= 1; }
         for (int j = 0; ok; ++j) {
-          const int nkt = next_kv_tile(pm, BN, kt, bound);
-          if (nkt < 0) mma_commit(&bar.q_empty);  // every QK of this unit is issued
+          const bool more = !last;
+          if (!more) mma_commit(&bar.q_empty);  // every QK of this unit is issued
           if (!(ok = mbar_wait(&bar.v_full[vs], vph, ab))) break;
           bool knext = false;
           for (int t = 0; t < (has1 ? 2 : 1); ++t) {
@@ -249,11 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             pph[t] ^= 1;
             tc_fence_after();
             issue_pv(t, vs, j > 0);
-            if (nkt < 0) mma_commit(&bar.o_full[t]);
-            if (nkt >= 0) {
+            if (!more) mma_commit(&bar.o_full[t]);
+            if (more) {
               if (!knext) {
                 if (!(ok = mbar_wait(&bar.k_full[ks], kph, ab))) break;
                 tc_fence_after();
+                last = klast[ks] != 0;
                 knext = true;
               }
               issue_qk(t, ks);
@@ -263,10 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (!ok) break;
           mma_commit(&bar.v_empty[vs]);
           if (++vs == C::NV) { vs = 0; vph ^= 1; }
-          if (nkt < 0) break;
+          if (!more) break;
           mma_commit(&bar.k_empty[ks]);
           if (++ks == C::NK) { ks = 0; kph ^= 1; }
-          kt = nkt;
         }
       }
       // wait for every issued MMA before TMEM is released
