@@ -60,6 +60,7 @@ def load(path=None):
         "cp_attn_fwd": [_P, _P, _P, _P, _P] + [_I] * 8 + [_P],
         "cp_attn_fwd_shard": [_P, _P, _P, _P, _P] + [_I] * 9 + [_P],
         "cp_attn_bwd": [_P] * 9 + [_I] * 8 + [_P],
+        "cp_attn_bwd_shard": [_P] * 9 + [_I] * 9 + [_P, _P, _P],
         "gqa_decode": [_P] * 5 + [_I] * 5 + [_P],
         "cp_lb_positions": [_I, _I, _I, ctypes.POINTER(ctypes.c_int)],
         "cp_attn_tile_counts": [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)],
@@ -173,6 +174,26 @@ def attn_bwd(q, k, v, out, lse, dout, cp, load_balance=True, dq=None, dk=None, d
                             _stream(q))
     _check(rc)
     return dq, dk, dv
+
+
+def attn_bwd_shard(q, k, v, out, lse, dout, cp, shard, load_balance=True, dq=None, dk_part=None, dv_part=None,
+                   dk=None, dv=None):
+    """Backward work of one shard: dq (bf16, the shard's rows; zero elsewhere)
+    and this shard's fp32 contributions dk_part, dv_part (optionally also
+    rounded into bf16 dk, dv)."""
+    B, S, Hq, Hkv, Dqk, Dv = _shape(q, k, v)
+    _need(out, torch.bfloat16, "out", 4)
+    _need(dout, torch.bfloat16, "dout", 4)
+    _need(lse, torch.float32, "lse", 3)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk_part = torch.empty(k.shape, dtype=torch.float32, device=k.device) if dk_part is None else dk_part
+    dv_part = torch.empty(v.shape, dtype=torch.float32, device=v.device) if dv_part is None else dv_part
+    rc = load().cp_attn_bwd_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                  _ptr(dk) if dk is not None else None, _ptr(dv) if dv is not None else None,
+                                  B, Hq, Hkv, S, Dqk, Dv, cp, int(bool(load_balance)), int(shard),
+                                  _ptr(dk_part), _ptr(dv_part), _stream(q))
+    _check(rc)
+    return dq, dk_part, dv_part
 
 
 def gqa_decode(q, kcache, vcache, lens, out=None):

@@ -455,14 +455,14 @@ int cp_attn_fwd_shard(const void* q, const void* k, const void* v, void* out, fl
   return fwd_impl(q, k, v, out, lse, sh, shard, stream);
 }
 
-int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
-                void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int cp,
-                int load_balance, cudaStream_t stream) {
+namespace {
+// shard < 0: the whole backward; else only query slots [shard*S/cp, (shard+1)*S/cp)
+// take part and dk/dv (optional, bf16) and dk_part/dv_part (fp32) get their partial sums
+int bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int cp,
+             int load_balance, int shard, float* dk_part, float* dv_part, cudaStream_t stream) {
   AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
-  int rc = check_attn(sh);
-  if (rc) return rc;
-  if ((rc = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv}))) return rc;
-  std::lock_guard<std::mutex> lk(g_mu);
+  int rc;
   DevState* ds;
   if ((rc = get_state(&ds))) return rc;
   if ((rc = need_sm103(*ds))) return rc;
@@ -470,6 +470,7 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   const size_t nstat = (size_t)B * Hq * Spad;
   if ((rc = ensure(ds->bwd_stats, 2 * nstat, stream, false))) return rc;
   const bool fused = bwd_fused_supported(Dqk, Dv);
+  if (shard >= 0 && !fused) return fail(CPATTN_ERR_UNSUPPORTED, "per-shard backward needs Dqk == Dv (64 or 128)");
   const size_t nacc = (size_t)B * S * Hq * Dqk;
   if (fused && (rc = ensure(ds->dq_acc, nacc, stream, false))) return rc;
   DevBuf<BwdUnit>* u_kv;
@@ -483,6 +484,10 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.q_lo = shard < 0 ? 0 : shard * (S / cp);
+  a.q_hi = shard < 0 ? S : (shard + 1) * (S / cp);
+  a.dk_part = dk_part;
+  a.dv_part = dv_part;
   a.Spad = Spad;
   a.sh = sh;
   a.scale = (float)(1.0 / std::sqrt((double)Dqk));
@@ -504,6 +509,15 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
     if ((rc = make_tmap_f32(&a.tdq, a.dq_acc, B, S, Hq, Dqk, 128))) return rc;
     a.units = u_kv->ptr;
     a.n_units = (int)u_kv->n;
+    if (shard >= 0) {  // key tiles no query of the shard sees are skipped: their partials are zero
+      const size_t nk = (size_t)B * S * Hkv;
+      cudaError_t ez = cudaSuccess;
+      if (dk_part) ez = cudaMemsetAsync(dk_part, 0, nk * Dqk * sizeof(float), stream);
+      if (ez == cudaSuccess && dv_part) ez = cudaMemsetAsync(dv_part, 0, nk * Dv * sizeof(float), stream);
+      if (ez == cudaSuccess && dk) ez = cudaMemsetAsync(dk, 0, nk * Dqk * 2, stream);
+      if (ez == cudaSuccess && dv) ez = cudaMemsetAsync(dv, 0, nk * Dv * 2, stream);
+      if (ez != cudaSuccess) return cuda_fail(ez, "clearing the shard partials");
+    }
     {
       ProfScope ps("attn_bwd_fused", stream);
       e = launch_attn_bwd_fused(a, (int)std::min<size_t>(u_kv->n, (size_t)ds->num_sms), stream);
@@ -543,6 +557,34 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
   return CPATTN_OK;
+}
+}  // namespace
+
+int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+                void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int cp,
+                int load_balance, cudaStream_t stream) {
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  int rc = check_attn(sh);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv}))) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, Dqk, Dv, cp, load_balance, -1, nullptr,
+                  nullptr, stream);
+}
+
+int cp_attn_bwd_shard(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk,
+                      int Dv, int cp, int load_balance, int shard, float* dk_part, float* dv_part,
+                      cudaStream_t stream) {
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  int rc = check_attn(sh);
+  if (rc) return rc;
+  if (shard < 0 || shard >= cp) return fail(CPATTN_ERR_INVALID_ARG, "shard %d outside [0, %d)", shard, cp);
+  if ((rc = check_ptrs({q, k, v, out, lse, dout, dq, dk_part, dv_part}))) return rc;
+  if ((dk && (rc = check_ptrs({dk}))) || (dv && (rc = check_ptrs({dv})))) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, Dqk, Dv, cp, load_balance, shard, dk_part,
+                  dv_part, stream);
 }
 
 int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out, int B, int Hq,

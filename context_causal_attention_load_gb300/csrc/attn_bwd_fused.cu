@@ -86,9 +86,9 @@ __device__ __forceinline__ void bulk_wait_read() {
 // p = exp2(s * scale*log2e - lse*log2e), zeroed where the key's position is
 // past the query's (MASKED steps only; positions walked slot by slot from
 // slot0), kept in fp32 for dS and stored back to TMEM (t_pk) as packed bf16
-template <bool MASKED>
+template <bool MASKED, bool SHARD>
 __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* lse_s, uint64_t sl2x2,
-                                     float (&p)[64], int kpos, const PosMap& pm, int slot0) {
+                                     float (&p)[64], int kpos, const PosMap& pm, int slot0, int lo, int hi) {
   int ck = 0, ct = 0, cbase = 0;  // memory chunk, offset in it, first position of the chunk
   if (MASKED && pm.lb) {
     ck = slot0 / pm.c;
@@ -109,7 +109,7 @@ __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* l
         }
       }
     }
-    return q;
+    return (!SHARD || (slot >= lo && slot < hi)) ? q : -1;  // rows outside [lo, hi) take no part
   };
   uint32_t sv[2][32];
   tmem_ld32(t_s, sv[0]);
@@ -139,19 +139,32 @@ __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* l
   }
 }
 
-// (query head, query tile) steps of a key-tile unit
+// (query head, query tile) steps of a key-tile unit: the query tiles that
+// see the key tile (and, per shard, hold a slot in [lo, hi))
+template <bool SHARD>
 struct StepWalk {
-  int h_end, kmin;
+  int h_end, kmin, lo, hi;
+  __device__ __forceinline__ int next_tile(const PosMap& pm, int qt) const {
+    if (!SHARD) return next_q_tile(pm, kRows, qt, kmin);
+    for (qt = next_q_tile(pm, kRows, qt, kmin); qt >= 0; qt = next_q_tile(pm, kRows, qt, kmin)) {
+      if (qt * kRows >= hi) return -1;  // tiles come in increasing slot order
+      if (qt * kRows + kRows > lo) return qt;
+    }
+    return -1;
+  }
   __device__ __forceinline__ bool next(const PosMap& pm, int& hq, int& qt) const {
-    qt = next_q_tile(pm, kRows, qt, kmin);
+    qt = next_tile(pm, qt);
     if (qt >= 0) return true;
     if (++hq >= h_end) return false;
-    qt = next_q_tile(pm, kRows, -1, kmin);
+    qt = next_tile(pm, -1);
     return qt >= 0;
   }
 };
 
-template <int D>
+// SHARD: only query slots [a.q_lo, a.q_hi) take part and dk/dv also go out
+// as fp32 partials (a separate instantiation, so the whole backward keeps
+// none of that bookkeeping)
+template <int D, bool SHARD>
 __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __grid_constant__ BwdArgs a) {
   using C = FCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -214,7 +227,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk w{u.h * G + G, kmin};
+        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;  // every role skips a unit no query sees
         if (!(ok = mbar_wait(&bar.kv_empty, (uc & 1) ^ 1, ab))) break;
@@ -309,7 +322,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk w{u.h * G + G, kmin};
+        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;
         if (!(ok = mbar_wait(&bar.kv_full, uc & 1, ab))) break;
@@ -369,7 +382,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk w{u.h * G + G, kmin};
+        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;
         do {
@@ -454,7 +467,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
       const bool k_inside = u.t * kRows + kRows <= pm.S;
       {
-        const StepWalk w{u.h * G + G, kmin};
+        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;
       }
@@ -474,10 +487,11 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         float p[64];
         const uint32_t t_s = tmem + lane_base + C::T_S + g * 64;
         const uint32_t t_pk = tmem + lane_base + C::T_S + packed_col<64>(g * 64);
-        if ((kmax <= qmin) && k_inside)
-          ew_p<false>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, 0);
+        const bool q_inside = !SHARD || (qt * kRows >= a.q_lo && qt * kRows + kRows <= a.q_hi);
+        if ((kmax <= qmin) && k_inside && q_inside)
+          ew_p<false, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, 0, 0, 0);
         else
-          ew_p<true>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, qt * kRows + g * 64);
+          ew_p<true, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, qt * kRows + g * 64, a.q_lo, a.q_hi);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar.p_full);
@@ -522,28 +536,33 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       have_prev = false;
       mbar_wait(&bar.acc_full, uc & 1, ab);
       tc_fence_after();
-      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) +
-                           (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * D;
-      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) +
-                           (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * D;
+      const size_t orow = ((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h;
       const float sc = a.scale;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float f = which ? sc : 1.f;
-        __nv_bfloat16* dst0 = which ? dkp : dvp;
+        __nv_bfloat16* dst0 = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv);
+        float* part0 = which ? a.dk_part : a.dv_part;
 #pragma unroll 1
         for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_base + (which ? C::T_DK : C::T_DV) + c0, o);
           tmem_ld_wait();
-          if (kvalid) {
-            uint4* dst = reinterpret_cast<uint4*>(dst0 + c0);
+          if (kvalid && (!SHARD || dst0)) {
+            uint4* dst = reinterpret_cast<uint4*>(dst0 + orow * D + c0);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
               dst[v4] = make_uint4(pack_bf16(f * __uint_as_float(o[8 * v4 + 0]), f * __uint_as_float(o[8 * v4 + 1])),
                                    pack_bf16(f * __uint_as_float(o[8 * v4 + 2]), f * __uint_as_float(o[8 * v4 + 3])),
                                    pack_bf16(f * __uint_as_float(o[8 * v4 + 4]), f * __uint_as_float(o[8 * v4 + 5])),
                                    pack_bf16(f * __uint_as_float(o[8 * v4 + 6]), f * __uint_as_float(o[8 * v4 + 7])));
+          }
+          if (SHARD && kvalid) {  // per-shard partial, unrounded
+            float4* dst = reinterpret_cast<float4*>(part0 + orow * D + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(f * __uint_as_float(o[4 * v4 + 0]), f * __uint_as_float(o[4 * v4 + 1]),
+                                    f * __uint_as_float(o[4 * v4 + 2]), f * __uint_as_float(o[4 * v4 + 3]));
           }
         }
       }
@@ -571,9 +590,9 @@ __global__ void __launch_bounds__(256) bwd_dq_round_kernel(const float* __restri
   }
 }
 
-template <int D>
+template <int D, bool SHARD>
 cudaError_t launch_fused(const BwdArgs& a, int grid, cudaStream_t st) {
-  auto kern = attn_bwd_fused_kernel<D>;
+  auto kern = attn_bwd_fused_kernel<D, SHARD>;
   // more than half of an SM's shared memory: one CTA per SM, so the CTA's
   // 512-column TMEM allocation never waits for a neighbour
   int smem = FCfg<D>::SMEM;
@@ -596,7 +615,9 @@ cudaError_t launch_fused(const BwdArgs& a, int grid, cudaStream_t st) {
 bool bwd_fused_supported(int Dqk, int Dv) { return Dqk == Dv && (Dqk == 64 || Dqk == 128); }
 
 cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st) {
-  return a.sh.Dqk == 64 ? launch_fused<64>(a, grid, st) : launch_fused<128>(a, grid, st);
+  const bool shard = a.dk_part != nullptr;
+  if (a.sh.Dqk == 64) return shard ? launch_fused<64, true>(a, grid, st) : launch_fused<64, false>(a, grid, st);
+  return shard ? launch_fused<128, true>(a, grid, st) : launch_fused<128, false>(a, grid, st);
 }
 
 cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, cudaStream_t st) {

@@ -72,6 +72,9 @@ struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;  // dq kernel uses 128-row boxes; dkdv uses BQ-row boxes for q/do
   CUtensorMap tdq;              // fused kernel: fp32 dQ accumulator, 32-column x 128-row boxes
   float* dq_acc;                // fused kernel: [B, S, Hq, Dqk] fp32, zeroed by the preprocess
+  int q_lo, q_hi;               // fused kernel: query slots that take part ([0, S) except per shard)
+  float* dk_part;               // fused kernel, per shard: fp32 partial dk/dv (null: none)
+  float* dv_part;
   const float* lse_l2;          // [B, Hq, Spad] -lse * log2(e), -inf in padding
   const float* delta;           // [B, Hq, Spad] -rowsum(dout*out), 0 in padding
   void* dq;

@@ -118,6 +118,24 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
                 int Dqk, int Dv, int cp, int load_balance, cudaStream_t stream);
 
 /*
+ * Backward work of ONE shard (the emulated reduce-scatter made visible):
+ * only the query slots [shard*S/cp, (shard+1)*S/cp) take part.  Arguments as
+ * cp_attn_bwd plus 0 <= shard < cp and two fp32 outputs:
+ *   dq       bf16, device: full gradients on the shard's rows, zero elsewhere;
+ *   dk_part, dv_part  fp32 [B, S, Hkv, Dqk|Dv], device: this shard's
+ *            contribution (summing them over all shards gives dk, dv; keys
+ *            no query of the shard sees get zero);
+ *   dk, dv   bf16, device, may be NULL: the same partial sums rounded.
+ * Requires Dqk == Dv (64 or 128); otherwise CPATTN_ERR_UNSUPPORTED.  Rows of
+ * a 128-row query tile that straddles a shard boundary outside the shard are
+ * masked out, so the partials are exact per shard for any S.
+ */
+int cp_attn_bwd_shard(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
+                      int Dqk, int Dv, int cp, int load_balance, int shard, float* dk_part,
+                      float* dv_part, cudaStream_t stream);
+
+/*
  * Grouped-query decode attention ("Add Pallas GPU decode attention in
  * Maxtext inference", Description: decode attention through a GQA kernel):
  * one query token per sequence against a KV cache.

@@ -170,6 +170,57 @@ def test_bwd_parity(cfg):
         assert_close_grad(_f64(got), want, "%s %s" % (name, cfg))
 
 
+@pytest.mark.parametrize("cfg", [
+    (1, 512, 4, 2, 128, 128, 4, True),    # shards of 128 rows: every tile inside one shard
+    (1, 320, 4, 2, 128, 128, 2, True),    # shards of 160 rows: tiles straddle the boundary
+    (2, 256, 2, 2, 64, 64, 2, True),
+    (1, 384, 2, 1, 128, 128, 3, False),   # natural order
+])
+def test_bwd_shard_partials(cfg):
+    """Per-shard backward against the oracle on that shard's rows; the shards'
+    dk/dv partials add up to the full backward's dk/dv."""
+    B, S, Hq, Hkv, Dqk, Dv, cp, lb = cfg
+    r = _run_fwd(*cfg, seed=13)
+    doutd = r["dout"].cuda()
+    if lb:
+        doutd = cp_.lb_permute(doutd, cp)
+    pos = r["pos"]
+    qs, ks, vs, ds = (O.permute(_f64(x), pos) for x in (r["q"], r["k"], r["v"], r["dout"]))
+    _, dk_full, dv_full = cp_.attn_bwd(r["qd"], r["kd"], r["vd"], r["out"], r["lse"], doutd, cp, lb)
+    dk_sum = torch.zeros(r["kd"].shape, dtype=torch.float64)
+    dv_sum = torch.zeros(r["vd"].shape, dtype=torch.float64)
+    for s in range(cp):
+        dq, dkp, dvp = cp_.attn_bwd_shard(r["qd"], r["kd"], r["vd"], r["out"], r["lse"], doutd, cp, s, lb)
+        torch.cuda.synchronize()
+        cp_.check_device()
+        rows = slice(s * S // cp, (s + 1) * S // cp)
+        dq_s, dk_s, dv_s = O.masked_attention_bwd(qs[:, rows], ks, vs, r["o_ref"][:, rows], r["l_ref"][:, :, rows],
+                                                  ds[:, rows], pos[rows], pos)
+        dqh = _f64(dq)
+        assert_close_grad(dqh[:, rows], dq_s, "dq shard %d %s" % (s, cfg))
+        outside = np.ones(S, bool)
+        outside[rows] = False
+        assert np.all(dqh[:, outside] == 0), "dq outside shard %d" % s
+        assert_close_grad(_f64(dkp), dk_s, "dk part %d %s" % (s, cfg))
+        assert_close_grad(_f64(dvp), dv_s, "dv part %d %s" % (s, cfg))
+        dk_sum += dkp.cpu().double()
+        dv_sum += dvp.cpu().double()
+    assert_close_grad(dk_sum.numpy(), _f64(dk_full), "sum of dk parts %s" % (cfg,))
+    assert_close_grad(dv_sum.numpy(), _f64(dv_full), "sum of dv parts %s" % (cfg,))
+
+
+def test_bwd_shard_mla_unsupported():
+    B, S, H, cp = 1, 256, 1, 2
+    q = torch.zeros(B, S, H, 192, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(B, S, H, 192, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(B, S, H, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(B, S, H, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(B, H, S, dtype=torch.float32, device="cuda")
+    with pytest.raises(cp_.CpAttnError) as e:
+        cp_.attn_bwd_shard(q, k, v, out, lse, out, cp, 0)
+    assert e.value.code == -2
+
+
 # ---------------------------------------------------------------------------
 # decode
 # ---------------------------------------------------------------------------
