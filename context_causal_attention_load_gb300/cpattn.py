@@ -148,10 +148,10 @@ def attn_fwd(q, k, v, cp, load_balance=True, out=None, lse=None, shard=None):
     lib = load()
     if shard is None:
         rc = lib.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, Dqk, Dv,
-                             cp, int(bool(load_balance)), _stream(q))
+                             cp, _lb(load_balance), _stream(q))
     else:
         rc = lib.cp_attn_fwd_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, Dqk,
-                                   Dv, cp, int(bool(load_balance)), int(shard), _stream(q))
+                                   Dv, cp, _lb(load_balance), int(shard), _stream(q))
     _check(rc)
     return out, lse
 
@@ -170,10 +170,20 @@ def attn_bwd(q, k, v, out, lse, dout, cp, load_balance=True, dq=None, dk=None, d
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     rc = load().cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
-                            _ptr(dk), _ptr(dv), B, Hq, Hkv, S, Dqk, Dv, cp, int(bool(load_balance)),
+                            _ptr(dk), _ptr(dv), B, Hq, Hkv, S, Dqk, Dv, cp, _lb(load_balance),
                             _stream(q))
     _check(rc)
     return dq, dk, dv
+
+
+def _lb(load_balance):
+    """0 natural order, 1 tensors in load-balanced slot order, 2 natural-order
+    tensors with the load-balanced schedule (zero-copy); True/False -> 1/0."""
+    if load_balance is True or load_balance is False:
+        return int(load_balance)
+    if load_balance not in (0, 1, 2):
+        raise ValueError("load_balance must be 0, 1 or 2")
+    return int(load_balance)
 
 
 def attn_bwd_shard(q, k, v, out, lse, dout, cp, shard, load_balance=True, dq=None, dk_part=None, dv_part=None,
@@ -190,7 +200,7 @@ def attn_bwd_shard(q, k, v, out, lse, dout, cp, shard, load_balance=True, dq=Non
     dv_part = torch.empty(v.shape, dtype=torch.float32, device=v.device) if dv_part is None else dv_part
     rc = load().cp_attn_bwd_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                                   _ptr(dk) if dk is not None else None, _ptr(dv) if dv is not None else None,
-                                  B, Hq, Hkv, S, Dqk, Dv, cp, int(bool(load_balance)), int(shard),
+                                  B, Hq, Hkv, S, Dqk, Dv, cp, _lb(load_balance), int(shard),
                                   _ptr(dk_part), _ptr(dv_part), _stream(q))
     _check(rc)
     return dq, dk_part, dv_part
@@ -213,13 +223,13 @@ def gqa_decode(q, kcache, vcache, lens, out=None):
 
 def lb_positions(S, cp, load_balance=True):
     arr = (ctypes.c_int * S)()
-    _check(load().cp_lb_positions(S, cp, int(bool(load_balance)), arr))
+    _check(load().cp_lb_positions(S, cp, _lb(load_balance), arr))
     return list(arr)
 
 
 def tile_counts(S, cp, load_balance=True):
     arr = (ctypes.c_longlong * cp)()
-    _check(load().cp_attn_tile_counts(S, cp, int(bool(load_balance)), arr))
+    _check(load().cp_attn_tile_counts(S, cp, _lb(load_balance), arr))
     return list(arr)
 
 

@@ -228,13 +228,19 @@ int upload(DevBuf<T>& b, const std::vector<T>& v) {
 }
 
 // ---- argument checks ------------------------------------------------------
+constexpr int kTile = 128;  // rows per attention tile
+
 int check_attn(const AttnShape& sh) {
   if (sh.B < 1 || sh.S < 1 || sh.Hq < 1 || sh.Hkv < 1 || sh.cp < 1)
     return fail(CPATTN_ERR_INVALID_ARG, "B, S, Hq, Hkv and cp must be >= 1");
   if (sh.Hq % sh.Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", sh.Hq, sh.Hkv);
   if (sh.S % sh.cp) return fail(CPATTN_ERR_INVALID_ARG, "S (%d) must be a multiple of cp (%d)", sh.S, sh.cp);
+  if (sh.lb < 0 || sh.lb > 2) return fail(CPATTN_ERR_INVALID_ARG, "load_balance must be 0, 1 or 2");
   if (sh.lb && sh.S % (2 * sh.cp))
     return fail(CPATTN_ERR_INVALID_ARG, "load balance needs S (%d) to be a multiple of 2*cp (%d)", sh.S, 2 * sh.cp);
+  if (sh.lb == 2 && sh.cp > 1 && (sh.S / (2 * sh.cp)) % kTile)
+    return fail(CPATTN_ERR_UNSUPPORTED, "zero-copy load balance needs the chunk length S/(2cp) = %d to be a multiple of %d",
+                sh.S / (2 * sh.cp), kTile);
   const bool dims_ok = (sh.Dqk == 64 && sh.Dv == 64) || (sh.Dqk == 128 && sh.Dv == 128) ||
                        (sh.Dqk == 192 && sh.Dv == 128);
   if (!dims_ok)
@@ -254,7 +260,6 @@ int check_ptrs(std::initializer_list<const void*> ps) {
 }
 
 // ---- work lists ------------------------------------------------------------
-constexpr int kTile = 128;
 
 int count_kv_tiles(const PosMap& pm, int bound) {
   int n = 0;
@@ -444,14 +449,14 @@ int cp_lb_unpermute(const void* src, void* dst, int B, int S, long long row_byte
 
 int cp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int S,
                 int Dqk, int Dv, int cp, int load_balance, cudaStream_t stream) {
-  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance};
   return fwd_impl(q, k, v, out, lse, sh, -1, stream);
 }
 
 int cp_attn_fwd_shard(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                       int S, int Dqk, int Dv, int cp, int load_balance, int shard, cudaStream_t stream) {
   if (shard < 0) return fail(CPATTN_ERR_INVALID_ARG, "shard must be >= 0");
-  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance};
   return fwd_impl(q, k, v, out, lse, sh, shard, stream);
 }
 
@@ -461,7 +466,7 @@ namespace {
 int bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
              void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int cp,
              int load_balance, int shard, float* dk_part, float* dv_part, cudaStream_t stream) {
-  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance};
   int rc;
   DevState* ds;
   if ((rc = get_state(&ds))) return rc;
@@ -563,7 +568,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
 int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int cp,
                 int load_balance, cudaStream_t stream) {
-  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance};
   int rc = check_attn(sh);
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv}))) return rc;
@@ -576,10 +581,11 @@ int cp_attn_bwd_shard(const void* q, const void* k, const void* v, const void* o
                       const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk,
                       int Dv, int cp, int load_balance, int shard, float* dk_part, float* dv_part,
                       cudaStream_t stream) {
-  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance ? 1 : 0};
+  AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance};
   int rc = check_attn(sh);
   if (rc) return rc;
   if (shard < 0 || shard >= cp) return fail(CPATTN_ERR_INVALID_ARG, "shard %d outside [0, %d)", shard, cp);
+  if (sh.lb == 2) return fail(CPATTN_ERR_UNSUPPORTED, "the per-shard backward takes tensors in slot order (load_balance 0 or 1)");
   if ((rc = check_ptrs({q, k, v, out, lse, dout, dq, dk_part, dv_part}))) return rc;
   if ((dk && (rc = check_ptrs({dk}))) || (dv && (rc = check_ptrs({dv})))) return rc;
   std::lock_guard<std::mutex> lk(g_mu);

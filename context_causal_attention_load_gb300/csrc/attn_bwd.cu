@@ -39,17 +39,18 @@ constexpr int TK = 128;  // key rows per dk/dv unit; query rows per dq unit
 // ============================================================================
 // preprocess: -lse*log2(e) (-inf past S) and -rowsum(dO*O) (0 past S), stored
 // negated so the element-wise warps apply them with one fused multiply-add;
-// layout [B, Hq, Spad].  LPR = Dv/8 lanes per (b, h, s) row, each with one
+// layout [B, Hq, Spad] in slot order.  LPR = Dv/8 lanes per (b, h, s) row, each with one
 // 16-byte load of out and of dout; rows go in output order (s fastest), so
 // the row statistics are written and lse read contiguously.  With dq_acc,
 // also zeroes the row of the fused kernel's fp32 dQ accumulator.
 // ============================================================================
-template <int LPR>
+template <int LPR, bool NAT>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse, float* lse_l2,
                                                              float* delta, float* dq_acc, AttnShape sh, int Spad) {
   const long long nrows = (long long)sh.B * sh.Hq * Spad;
+  const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
   const int sub = threadIdx.x % LPR;
   const unsigned gmask = ((1u << LPR) - 1u) << ((threadIdx.x & 31) & ~(LPR - 1));  // this row's lanes
   const long long stride = (long long)gridDim.x * blockDim.x / LPR;
@@ -59,9 +60,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     const int h = int(bh % sh.Hq);
     const int b = int(bh / sh.Hq);
     const bool valid = s < sh.S;
+    const int mrow = (valid && NAT) ? pm.pos(s) : s;  // memory row of slot s (natural order under zero-copy)
     float acc = 0.f;
     if (valid) {
-      const size_t row = ((size_t)b * sh.S + s) * sh.Hq + h;
+      const size_t row = ((size_t)b * sh.S + mrow) * sh.Hq + h;
       const uint4 a = __ldcs(reinterpret_cast<const uint4*>(out + row * sh.Dv) + sub);
       const uint4 g = __ldcs(reinterpret_cast<const uint4*>(dout + row * sh.Dv) + sub);
       acc = fmaf(bf16lo(a.x), bf16lo(g.x), fmaf(bf16hi(a.x), bf16hi(g.x), acc));
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     for (int o = LPR / 2; o; o >>= 1) acc += __shfl_xor_sync(gmask, acc, o);
     if (sub == 0) {
       delta[r] = -acc;
-      lse_l2[r] = valid ? -lse[bh * sh.S + s] * 1.4426950408889634f : -INFINITY;
+      lse_l2[r] = valid ? -lse[bh * sh.S + mrow] * 1.4426950408889634f : -INFINITY;
     }
   }
 }
@@ -168,9 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         if (ok) {
           mbar_expect_tx(&bar.kv_full, C::K_BYTES + C::V_BYTES);
           for (int bx = 0; bx < DQK / 64; ++bx)
-            tma_load_4d(smem + C::OFF_K + bx * TK * 128, &a.tk, &bar.kv_full, bx * 64, u.h, u.t * TK, u.b);
+            tma_load_4d(smem + C::OFF_K + bx * TK * 128, &a.tk, &bar.kv_full, bx * 64, u.h, pm.row(u.t * TK), u.b);
           for (int bx = 0; bx < DV / 64; ++bx)
-            tma_load_4d(smem + C::OFF_V + bx * TK * 128, &a.tv, &bar.kv_full, bx * 64, u.h, u.t * TK, u.b);
+            tma_load_4d(smem + C::OFF_V + bx * TK * 128, &a.tv, &bar.kv_full, bx * 64, u.h, pm.row(u.t * TK), u.b);
         }
       }
       kvph ^= 1;
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
           if (lane == 0) {
             mbar_expect_tx(&bar.q_full[qs], C::QT_BYTES + C::DO_BYTES + 2 * C::VEC_BYTES);
             for (int bx = 0; bx < DQK / 64; ++bx)
-              tma_load_4d(st + C::ST_Q + bx * BQ * 128, &a.tq, &bar.q_full[qs], bx * 64, hq, qt * BQ, u.b);
+              tma_load_4d(st + C::ST_Q + bx * BQ * 128, &a.tq, &bar.q_full[qs], bx * 64, hq, pm.row(qt * BQ), u.b);
             for (int bx = 0; bx < DV / 64; ++bx)
-              tma_load_4d(st + C::ST_DO + bx * BQ * 128, &a.tdo, &bar.q_full[qs], bx * 64, hq, qt * BQ, u.b);
+              tma_load_4d(st + C::ST_DO + bx * BQ * 128, &a.tdo, &bar.q_full[qs], bx * 64, hq, pm.row(qt * BQ), u.b);
             const size_t vo = ((size_t)u.b * a.sh.Hq + hq) * a.Spad + (size_t)qt * BQ;
             bulk_load(st + C::ST_LSE, a.lse_l2 + vo, C::VEC_BYTES, &bar.q_full[qs]);
             bulk_load(st + C::ST_DEL, a.delta + vo, C::VEC_BYTES, &bar.q_full[qs]);
@@ -382,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       acc_ph ^= 1;
       tc_fence_after();
-      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) + (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * DV;
-      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) + (((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h) * DQK;
+      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) + (((size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0)) * a.sh.Hkv + u.h) * DV;
+      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) + (((size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0)) * a.sh.Hkv + u.h) * DQK;
 #pragma unroll 1
       for (int c0 = g * (DV / 2); c0 < (g + 1) * (DV / 2); c0 += 32) {
         uint32_t o[32];
@@ -518,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         if (ok) {
           mbar_expect_tx(&bar.q_full, C::Q_BYTES + C::DO_BYTES);
           for (int bx = 0; bx < DQK / 64; ++bx)
-            tma_load_4d(smem + C::OFF_Q + bx * TK * 128, &a.tq, &bar.q_full, bx * 64, u.h, u.t * TK, u.b);
+            tma_load_4d(smem + C::OFF_Q + bx * TK * 128, &a.tq, &bar.q_full, bx * 64, u.h, pm.row(u.t * TK), u.b);
           for (int bx = 0; bx < DV / 64; ++bx)
-            tma_load_4d(smem + C::OFF_DO + bx * TK * 128, &a.tdo, &bar.q_full, bx * 64, u.h, u.t * TK, u.b);
+            tma_load_4d(smem + C::OFF_DO + bx * TK * 128, &a.tdo, &bar.q_full, bx * 64, u.h, pm.row(u.t * TK), u.b);
         }
       }
       qph ^= 1;
@@ -539,9 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         if (lane == 0) {
           mbar_expect_tx(&bar.kv_full[ks], C::K_BYTES + C::V_BYTES);
           for (int bx = 0; bx < DQK / 64; ++bx)
-            tma_load_4d(st + C::ST_K + bx * BK * 128, &a.tk, &bar.kv_full[ks], bx * 64, hkv, kt * BK, u.b);
+            tma_load_4d(st + C::ST_K + bx * BK * 128, &a.tk, &bar.kv_full[ks], bx * 64, hkv, pm.row(kt * BK), u.b);
           for (int bx = 0; bx < DV / 64; ++bx)
-            tma_load_4d(st + C::ST_V + bx * BK * 128, &a.tv, &bar.kv_full[ks], bx * 64, hkv, kt * BK, u.b);
+            tma_load_4d(st + C::ST_V + bx * BK * 128, &a.tv, &bar.kv_full[ks], bx * 64, hkv, pm.row(kt * BK), u.b);
         }
         if (++ks == C::NS) { ks = 0; kph ^= 1; }
       }
@@ -704,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       acc_ph ^= 1;
       tc_fence_after();
-      __nv_bfloat16* dqp = static_cast<__nv_bfloat16*>(a.dq) + (((size_t)u.b * pm.S + (qvalid ? qslot : 0)) * a.sh.Hq + u.h) * DQK;
+      __nv_bfloat16* dqp = static_cast<__nv_bfloat16*>(a.dq) + (((size_t)u.b * pm.S + (qvalid ? pm.row(qslot) : 0)) * a.sh.Hq + u.h) * DQK;
       const float sc = a.scale;
 #pragma unroll 1
       for (int c0 = g * (DQK / 2); c0 < (g + 1) * (DQK / 2); c0 += 32) {
@@ -760,7 +762,9 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
   const int lpr = sh.Dv / 8;  // Dv is 64 or 128
   long long blocks = (rows * lpr + 255) / 256;
   if (blocks > 152LL * 64) blocks = 152LL * 64;
-  auto kern = lpr == 16 ? bwd_preprocess_kernel<16> : bwd_preprocess_kernel<8>;
+  const bool nat = PosMap::make(sh.S, sh.cp, sh.lb).lb == 2;
+  auto kern = lpr == 16 ? (nat ? bwd_preprocess_kernel<16, true> : bwd_preprocess_kernel<16, false>)
+                        : (nat ? bwd_preprocess_kernel<8, true> : bwd_preprocess_kernel<8, false>);
   kern<<<(int)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
                                     lse, lse_l2, delta, dq_acc, sh, Spad);
   return cudaGetLastError();

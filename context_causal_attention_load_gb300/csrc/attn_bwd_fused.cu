@@ -161,10 +161,16 @@ struct StepWalk {
   }
 };
 
+// memory row of slot `slot`: natural-order tensors (NAT, load_balance 2) keep
+// slot j at row pos(j); permuted or natural tensors without the reorder at row j
+template <bool NAT>
+__device__ __forceinline__ int mem_row(const PosMap& pm, int slot) { return NAT ? pm.pos(slot) : slot; }
+
 // SHARD: only query slots [a.q_lo, a.q_hi) take part and dk/dv also go out
-// as fp32 partials (a separate instantiation, so the whole backward keeps
-// none of that bookkeeping)
-template <int D, bool SHARD>
+// as fp32 partials.  NAT: tensors in natural order (zero-copy load balance).
+// Each is its own instantiation, so the plain backward keeps none of that
+// bookkeeping in its code.
+template <int D, bool SHARD, bool NAT>
 __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __grid_constant__ BwdArgs a) {
   using C = FCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -233,8 +239,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         if (!(ok = mbar_wait(&bar.kv_empty, (uc & 1) ^ 1, ab))) break;
         mbar_expect_tx(&bar.kv_full, 2 * C::TILE);
         for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_4d(smem + C::OFF_K + bx * kRows * 128, &a.tk, &bar.kv_full, bx * 64, u.h, u.t * kRows, u.b);
-          tma_load_4d(smem + C::OFF_V + bx * kRows * 128, &a.tv, &bar.kv_full, bx * 64, u.h, u.t * kRows, u.b);
+          tma_load_4d(smem + C::OFF_K + bx * kRows * 128, &a.tk, &bar.kv_full, bx * 64, u.h, mem_row<NAT>(pm, u.t * kRows), u.b);
+          tma_load_4d(smem + C::OFF_V + bx * kRows * 128, &a.tv, &bar.kv_full, bx * 64, u.h, mem_row<NAT>(pm, u.t * kRows), u.b);
         }
         bool more;
         do {
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           mbar_expect_tx(&bar.q_full[st], C::TILE + C::VEC_BYTES);  // (release: the info is visible to q_full's waiters)
           for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d(smem + C::OFF_Q + st * C::TILE + bx * kRows * 128, &a.tq, &bar.q_full[st], bx * 64, hq,
-                        qt * kRows, u.b);
+                        mem_row<NAT>(pm, qt * kRows), u.b);
           const size_t vo = ((size_t)u.b * a.sh.Hq + hq) * a.Spad + (size_t)qt * kRows;
           unsigned char* vec = smem + C::OFF_VEC + st * C::VEC_BYTES;
           bulk_load(vec, a.lse_l2 + vo, kRows * 4, &bar.q_full[st]);
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           mbar_expect_tx(&bar.do_full[st], C::TILE);
           for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d(smem + C::OFF_DO + st * C::TILE + bx * kRows * 128, &a.tdo, &bar.do_full[st], bx * 64, hq,
-                        qt * kRows, u.b);
+                        mem_row<NAT>(pm, qt * kRows), u.b);
           ++gs;
           hq = nhq;
           qt = nqt;
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           for (int box = 0; box < C::NBOX; ++box) {
             const unsigned char* bb = box < 2 ? smem + C::OFF_DS + box * (kRows * 128)
                                               : smem + C::OFF_DO + (gs & 1) * C::TILE + (box - 2) * (kRows * 128);
-            tma_reduce_add_4d(bb, &a.tdq, box * 32, hq, qt * kRows, u.b);
+            tma_reduce_add_4d(bb, &a.tdq, box * 32, hq, mem_row<NAT>(pm, qt * kRows), u.b);
             if (box == 1) bulk_commit_group();
           }
           if (C::NBOX > 2) {
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       have_prev = false;
       mbar_wait(&bar.acc_full, uc & 1, ab);
       tc_fence_after();
-      const size_t orow = ((size_t)u.b * pm.S + (kvalid ? kslot : 0)) * a.sh.Hkv + u.h;
+      const size_t orow = ((size_t)u.b * pm.S + (kvalid ? mem_row<NAT>(pm, kslot) : 0)) * a.sh.Hkv + u.h;
       const float sc = a.scale;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -590,9 +596,9 @@ __global__ void __launch_bounds__(256) bwd_dq_round_kernel(const float* __restri
   }
 }
 
-template <int D, bool SHARD>
+template <int D, bool SHARD, bool NAT>
 cudaError_t launch_fused(const BwdArgs& a, int grid, cudaStream_t st) {
-  auto kern = attn_bwd_fused_kernel<D, SHARD>;
+  auto kern = attn_bwd_fused_kernel<D, SHARD, NAT>;
   // more than half of an SM's shared memory: one CTA per SM, so the CTA's
   // 512-column TMEM allocation never waits for a neighbour
   int smem = FCfg<D>::SMEM;
@@ -615,9 +621,14 @@ cudaError_t launch_fused(const BwdArgs& a, int grid, cudaStream_t st) {
 bool bwd_fused_supported(int Dqk, int Dv) { return Dqk == Dv && (Dqk == 64 || Dqk == 128); }
 
 cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st) {
-  const bool shard = a.dk_part != nullptr;
-  if (a.sh.Dqk == 64) return shard ? launch_fused<64, true>(a, grid, st) : launch_fused<64, false>(a, grid, st);
-  return shard ? launch_fused<128, true>(a, grid, st) : launch_fused<128, false>(a, grid, st);
+  const bool shard = a.dk_part != nullptr;  // (the per-shard call does not take natural-order tensors)
+  const bool nat = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb).lb == 2;
+  if (a.sh.Dqk == 64) {
+    if (shard) return launch_fused<64, true, false>(a, grid, st);
+    return nat ? launch_fused<64, false, true>(a, grid, st) : launch_fused<64, false, false>(a, grid, st);
+  }
+  if (shard) return launch_fused<128, true, false>(a, grid, st);
+  return nat ? launch_fused<128, false, true>(a, grid, st) : launch_fused<128, false, false>(a, grid, st);
 }
 
 cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, cudaStream_t st) {

@@ -150,11 +150,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mbar_expect_tx(&bar.q_full, (has1 ? 2 : 1) * C::Q_BYTES);
         ++nq;
         for (int bx = 0; bx < DQK / 64; ++bx)
-          tma_load_4d(smem + C::OFF_Q + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h0, u.t0 * BM, u.b);
+          tma_load_4d(smem + C::OFF_Q + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h0, pm.row(u.t0 * BM), u.b);
         if (has1)
           for (int bx = 0; bx < DQK / 64; ++bx)
             tma_load_4d(smem + C::OFF_Q + C::Q_BYTES + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h1,
-                        u.t1 * BM, u.b);
+                        pm.row(u.t1 * BM), u.b);
         const int bound = kv_bound(pm, u);
         for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0;) {
           const int nkt = next_kv_tile(pm, BN, kt, bound);
@@ -164,14 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ++nk;
           for (int bx = 0; bx < DQK / 64; ++bx)
             tma_load_4d(smem + C::OFF_K + ks * C::K_BYTES + bx * BN * 128, &a.tk, &bar.k_full[ks], bx * 64,
-                        u.hkv, kt * BN, u.b);
+                        u.hkv, pm.row(kt * BN), u.b);
           if (++ks == C::NK) { ks = 0; kph ^= 1; }
           if (!(ok = mbar_wait(&bar.v_empty[vs], vph ^ 1, ab))) break;
           mbar_expect_tx(&bar.v_full[vs], C::V_BYTES);
           ++nv;
           for (int bx = 0; bx < DV / 64; ++bx)
             tma_load_4d(smem + C::OFF_V + vs * C::V_BYTES + bx * BN * 128, &a.tv, &bar.v_full[vs], bx * 64,
-                        u.hkv, kt * BN, u.b);
+                        u.hkv, pm.row(kt * BN), u.b);
           if (++vs == C::NV) { vs = 0; vph ^= 1; }
           kt = nkt;
         }
@@ -452,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       oph ^= 1;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-      __nv_bfloat16* orow = outp + (((size_t)u.b * pm.S + (qvalid ? qslot : 0)) * a.sh.Hq + h) * DV;
+      const int qrow = qvalid ? pm.row(qslot) : 0;  // memory row of this query
+      __nv_bfloat16* orow = outp + (((size_t)u.b * pm.S + qrow) * a.sh.Hq + h) * DV;
       {
         uint32_t o[DV / 32][32];
 #pragma unroll
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       if (qvalid) {
         const float lse = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-        a.lse[((size_t)u.b * a.sh.Hq + h) * pm.S + qslot] = lse;
+        a.lse[((size_t)u.b * a.sh.Hq + h) * pm.S + qrow] = lse;
       }
     }
   }

@@ -36,17 +36,21 @@ constexpr int kMaxPieces = 64;
 struct PosMap {
   int S;   // sequence length
   int cp;  // number of shards
-  int lb;  // 1: load-balance reorder applied; 0: natural order
+  int lb;  // 0: natural order; 1: tensors in load-balanced slot order; 2: tensors in
+           // natural order, load-balanced schedule (slot j lives at memory row pos(j))
   int c;   // chunk length S/(2cp) (only meaningful when lb)
 
-  CPATTN_HD static PosMap make(int S_, int cp_, int lb_) {
+  CPATTN_HD static PosMap make(int S_, int cp_, int load_balance) {
     PosMap m;
     m.S = S_;
     m.cp = cp_;
-    m.lb = (lb_ && cp_ > 1) ? 1 : 0;
+    m.lb = (load_balance && cp_ > 1) ? (load_balance == 2 ? 2 : 1) : 0;
     m.c = m.lb ? S_ / (2 * cp_) : S_;
     return m;
   }
+  // memory row of slot j (a whole tile of slots is contiguous in memory when
+  // the chunk length is a multiple of the tile)
+  CPATTN_HD int row(int slot) const { return lb == 2 ? pos(slot) : slot; }
   // original chunk held by memory chunk k
   CPATTN_HD int chunk_of(int k) const {
     int s = k >> 1;

@@ -126,7 +126,8 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
  *            contribution (summing them over all shards gives dk, dv; keys
  *            no query of the shard sees get zero);
  *   dk, dv   bf16, device, may be NULL: the same partial sums rounded.
- * Requires Dqk == Dv (64 or 128); otherwise CPATTN_ERR_UNSUPPORTED.  Rows of
+ * Requires Dqk == Dv (64 or 128) and load_balance 0 or 1; otherwise
+ * CPATTN_ERR_UNSUPPORTED.  Rows of
  * a 128-row query tile that straddles a shard boundary outside the shard are
  * masked out, so the partials are exact per shard for any S.
  */

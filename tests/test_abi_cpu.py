@@ -77,6 +77,13 @@ def test_bad_arguments_are_rejected_on_host():
     assert "aligned" in _err()
     assert lib.cp_attn_fwd_shard(*args, 1, 4, 4, 256, 128, 128, 2, 1, 2, None) == -1
     assert lib.cp_attn_bwd(*([P] * 9), 1, 4, 4, 256, 64, 128, 2, 1, None) == -2
+    # load_balance outside {0, 1, 2}; zero-copy needs whole 128-row tiles per chunk
+    assert lib.cp_attn_fwd(*args, 1, 4, 4, 256, 128, 128, 2, 3, None) == -1
+    assert lib.cp_attn_fwd(*args, 1, 4, 4, 320, 128, 128, 2, 2, None) == -2
+    assert "zero-copy" in _err()
+    assert lib.cp_attn_bwd(*([P] * 9), 1, 4, 4, 768, 128, 128, 2, 2, None) == -2
+    # per-shard backward: shard out of range
+    assert lib.cp_attn_bwd_shard(*([P] * 9), 1, 4, 4, 256, 128, 128, 2, 1, 2, P, P, None) == -1
     # decode: group too large, bad head dim, null lens
     assert lib.gqa_decode(P, P, P, P, P, 1, 64, 2, 128, 128, None) == -2
     assert lib.gqa_decode(P, P, P, P, P, 1, 8, 2, 128, 96, None) == -2

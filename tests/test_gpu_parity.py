@@ -221,6 +221,43 @@ def test_bwd_shard_mla_unsupported():
     assert e.value.code == -2
 
 
+@pytest.mark.parametrize("cfg", [
+    # B, S, Hq, Hkv, Dqk, Dv, cp: chunk lengths S/(2cp) of 128, 512 and 256 rows
+    (1, 1024, 4, 2, 128, 128, 4),
+    (2, 2048, 2, 2, 64, 64, 2),
+    (1, 1024, 2, 2, 192, 128, 2),
+])
+def test_zero_copy_matches_permuted_path(cfg):
+    """load_balance=2: natural-order tensors, load-balanced schedule.  out,
+    lse, dk and dv are bit-identical to permute -> attend -> unpermute (the
+    same tiles in the same order); dq agrees to its reduction order; all of
+    them against the oracle on the natural-order inputs."""
+    B, S, Hq, Hkv, Dqk, Dv, cp = cfg
+    q, k, v, dout = synth.attention_inputs(B, S, Hq, Hkv, Dqk, Dv, seed=17)
+    qd, kd, vd, dd = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    out2, lse2 = cp_.attn_fwd(qd, kd, vd, cp, 2)
+    dq2, dk2, dv2 = cp_.attn_bwd(qd, kd, vd, out2, lse2, dd, cp, 2)
+    torch.cuda.synchronize()
+    cp_.check_device()
+    perm = [cp_.lb_permute(x, cp) for x in (qd, kd, vd, dd)]
+    out1, lse1 = cp_.attn_fwd(*perm[:3], cp, 1)
+    dq1, dk1, dv1 = cp_.attn_bwd(*perm[:3], out1, lse1, perm[3], cp, 1)
+    torch.cuda.synchronize()
+    pos = torch.from_numpy(O.lb_positions(S, cp, True)).long()
+    lse1_nat = torch.empty_like(lse1)
+    lse1_nat[:, :, pos.cuda()] = lse1
+    assert torch.equal(out2, cp_.lb_unpermute(out1, cp))
+    assert torch.equal(lse2, lse1_nat)
+    assert torch.equal(dk2, cp_.lb_unpermute(dk1, cp))
+    assert torch.equal(dv2, cp_.lb_unpermute(dv1, cp))
+    assert_close_grad(_f64(dq2), _f64(cp_.lb_unpermute(dq1, cp)), "dq zero-copy vs permuted")
+    o_ref, l_ref = O.causal_attention_fwd(_f64(q), _f64(k), _f64(v))
+    assert_close_out(_f64(out2), o_ref, "zero-copy out")
+    g_ref = O.causal_attention_bwd(_f64(q), _f64(k), _f64(v), o_ref, l_ref, _f64(dout))
+    for got, want, name in zip((dq2, dk2, dv2), g_ref, ("dq", "dk", "dv")):
+        assert_close_grad(_f64(got), want, "zero-copy %s %s" % (name, cfg))
+
+
 # ---------------------------------------------------------------------------
 # decode
 # ---------------------------------------------------------------------------
