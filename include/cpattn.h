@@ -85,9 +85,17 @@ int cp_lb_unpermute(const void* src, void* dst, int B, int S, long long row_byte
  * MHA and MLA head layouts).
  *   out = softmax(scale * q k^T + mask) v,  lse = ln sum exp(scale q k^T).
  * q, k, v: device inputs; out, lse: device outputs (overwritten).
- * Requires B >= 1, S >= 1, Hkv >= 1, Hq % Hkv == 0, S % cp == 0 and, with
- * load_balance = 1, S % (2*cp) == 0.  (Dqk, Dv) in {(64,64), (128,128),
- * (192,128)}.  Runs on tcgen05 tensor cores; needs an sm_103 GPU.
+ * load_balance: 0 = natural token order, no reorder; 1 = q, k, v (and out,
+ * lse) in the load-balanced slot order that cp_lb_permute produces; 2 =
+ * zero-copy: q, k, v, out, lse in natural token order, work split and mask
+ * as for 1 (each 128-row tile of slots is read from and written to the rows
+ * of its original positions, so no permute is needed; the same for
+ * cp_attn_bwd's dout, dq, dk, dv).
+ * Requires B >= 1, S >= 1, Hkv >= 1, Hq % Hkv == 0, S % cp == 0, with
+ * load_balance 1 or 2 S % (2*cp) == 0, and with 2 (cp > 1) a chunk length
+ * S/(2*cp) that is a multiple of 128 (else CPATTN_ERR_UNSUPPORTED).
+ * (Dqk, Dv) in {(64,64), (128,128), (192,128)}.  Runs on tcgen05 tensor
+ * cores; needs an sm_103 GPU.
  */
 int cp_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
                 int Hkv, int S, int Dqk, int Dv, int cp, int load_balance, cudaStream_t stream);
