@@ -59,6 +59,22 @@ def decode_inputs(B, Hq, Hkv, D, Smax, len_lo, len_hi, seed=0):
     return q, kc, vc, lens
 
 
+def decode_inputs_int8(B, Hq, Hkv, D, Smax, len_lo, len_hi, seed=0):
+    """q [B,Hq,D] bf16; int8 caches kq/vq [B,Hkv,Smax,D] uniform in
+    [-127, 127]; fp32 scales kscale/vscale [B,Hkv,Smax] uniform in
+    [0.008, 0.016] (cached values then span about +-2); lens [B] int32
+    uniform in [len_lo, len_hi]."""
+    q = _normal((B, Hq, D), seed)
+    g = torch.Generator(device="cpu").manual_seed(int(seed) + 11)
+    kq = torch.randint(-127, 128, (B, Hkv, Smax, D), generator=g, dtype=torch.int32).to(torch.int8)
+    vq = torch.randint(-127, 128, (B, Hkv, Smax, D), generator=g, dtype=torch.int32).to(torch.int8)
+    ks = 0.008 + 0.008 * torch.rand((B, Hkv, Smax), generator=g, dtype=torch.float32)
+    vs = 0.008 + 0.008 * torch.rand((B, Hkv, Smax), generator=g, dtype=torch.float32)
+    gl = torch.Generator(device="cpu").manual_seed(int(seed) + 4)
+    lens = torch.randint(int(len_lo), int(len_hi) + 1, (B,), generator=gl, dtype=torch.int32)
+    return q, kq, vq, ks, vs, lens
+
+
 def to_f64(t):
     """bf16/float torch tensor -> float64 NumPy array (exact upcast)."""
     return t.detach().to("cpu").to(torch.float64).numpy()

@@ -38,6 +38,11 @@ Maxtext inference" (#1066)):
 * ``gqa_decode`` -- one query token per sequence against a KV cache,
   grouped-query heads ("Add Pallas GPU decode attention", Description:
   ``pallas_decode_attention.gqa`` replaces dot-product decode attention).
+* ``gqa_decode_int8`` -- the same against an int8-quantised KV cache (the
+  inference setup of "rename context to context_autoregressive", Tests, runs
+  with ``quantize_kvcache=True``): each cached vector is stored as int8
+  values times one float scale per (batch, KV head, position); it is
+  dequantised exactly and then decoded as above.
 
 Readings where the pages are silent (each one listed in the design notes):
 scale = 1/sqrt(Dqk); query head h uses KV head floor(h / (Hq/Hkv)); lse is the
@@ -57,7 +62,7 @@ __all__ = [
     "masked_attention_fwd", "masked_attention_bwd",
     "causal_attention_fwd", "causal_attention_bwd",
     "cp_attention_fwd", "cp_attention_bwd",
-    "shard_pair_counts", "gqa_decode",
+    "shard_pair_counts", "gqa_decode", "gqa_decode_int8",
 ]
 
 _ROW_BLOCK = 512
@@ -289,3 +294,12 @@ def gqa_decode(q, kcache, vcache, lens, scale=None):
             p = np.exp(s)
             out[b, h] = (p @ vc[b, g, :n, :]) / p.sum()
     return out
+
+
+def gqa_decode_int8(q, kq, vq, kscale, vscale, lens, scale=None):
+    """Decode against an int8 KV cache: kq/vq int8 [B,Hkv,Smax,D] and
+    kscale/vscale [B,Hkv,Smax]; the cached key (value) vector at position t is
+    kq[b,g,t,:] * kscale[b,g,t].  Dequantised in float64, then ``gqa_decode``."""
+    k = np.asarray(kq, np.float64) * np.asarray(kscale, np.float64)[..., None]
+    v = np.asarray(vq, np.float64) * np.asarray(vscale, np.float64)[..., None]
+    return gqa_decode(q, k, v, lens, scale)

@@ -428,3 +428,57 @@ def test_decode_zero_length_is_zero():
                        _rand((2, 1, 3, 4), rng), np.array([0, 3]))
     assert np.all(out[0] == 0)
     assert np.any(out[1] != 0)
+
+
+# ---------------------------------------------------------------------------
+# int8 KV-cache decode
+# ---------------------------------------------------------------------------
+
+def _int8_case(seed, B=2, Hq=4, Hkv=2, D=8, Smax=6):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, D))
+    kq = rng.integers(-127, 128, (B, Hkv, Smax, D))
+    vq = rng.integers(-127, 128, (B, Hkv, Smax, D))
+    ks = rng.uniform(0.008, 0.016, (B, Hkv, Smax))
+    vs = rng.uniform(0.008, 0.016, (B, Hkv, Smax))
+    lens = np.array([Smax, 3][:B])
+    return q, kq, vq, ks, vs, lens
+
+
+def test_decode_int8_brute_force():
+    """Element by element: dequantise each cached value, score, softmax, sum."""
+    q, kq, vq, ks, vs, lens = _int8_case(31)
+    B, Hq, D = q.shape
+    Hkv = kq.shape[1]
+    G = Hq // Hkv
+    got = O.gqa_decode_int8(q, kq, vq, ks, vs, lens)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            sc = []
+            for t in range(int(lens[b])):
+                acc = 0.0
+                for d in range(D):
+                    acc += q[b, h, d] * (float(kq[b, g, t, d]) * ks[b, g, t])
+                sc.append(acc / math.sqrt(D))
+            m = max(sc)
+            w = [math.exp(x - m) for x in sc]
+            for d in range(D):
+                num = sum(w[t] * float(vq[b, g, t, d]) * vs[b, g, t] for t in range(len(w)))
+                assert abs(got[b, h, d] - num / sum(w)) < 1e-12
+
+
+def test_decode_int8_value_scale_is_linear():
+    q, kq, vq, ks, vs, lens = _int8_case(32)
+    a = O.gqa_decode_int8(q, kq, vq, ks, vs, lens)
+    b = O.gqa_decode_int8(q, kq, vq, ks, 3.0 * vs, lens)
+    np.testing.assert_allclose(b, 3.0 * a, rtol=1e-12, atol=1e-14)
+
+
+def test_decode_int8_key_scale_acts_like_query_scale():
+    """A common factor on every key scale multiplies the scores, exactly as the
+    same factor on the query does."""
+    q, kq, vq, ks, vs, lens = _int8_case(33)
+    a = O.gqa_decode_int8(q, kq, vq, 2.5 * ks, vs, lens)
+    b = O.gqa_decode_int8(2.5 * q, kq, vq, ks, vs, lens)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
