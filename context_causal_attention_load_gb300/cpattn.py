@@ -62,6 +62,7 @@ def load(path=None):
         "cp_attn_bwd": [_P] * 9 + [_I] * 8 + [_P],
         "cp_attn_bwd_shard": [_P] * 9 + [_I] * 9 + [_P, _P, _P],
         "gqa_decode": [_P] * 5 + [_I] * 5 + [_P],
+        "gqa_decode_int8": [_P] * 7 + [_I] * 5 + [_P],
         "cp_lb_positions": [_I, _I, _I, ctypes.POINTER(ctypes.c_int)],
         "cp_attn_tile_counts": [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)],
         "cp_attn_check_device": [_P],
@@ -253,3 +254,21 @@ def profile_stop():
     n = ctypes.c_int(0)
     _check(load().cp_attn_profile_stop(arr, 64, ctypes.byref(n)))
     return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(min(n.value, 64))}
+
+
+def gqa_decode_int8(q, kq, vq, kscale, vscale, lens, out=None):
+    """q [B,Hq,D] bf16, kq/vq [B,Hkv,Smax,D] int8, kscale/vscale [B,Hkv,Smax]
+    fp32, lens [B] int32 -> out [B,Hq,D] bf16."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kq, torch.int8, "kcache", 4)
+    _need(vq, torch.int8, "vcache", 4)
+    _need(kscale, torch.float32, "kscale", 3)
+    _need(vscale, torch.float32, "vscale", 3)
+    _need(lens, torch.int32, "lens", 1)
+    B, Hq, D = q.shape
+    Hkv, Smax = kq.shape[1], kq.shape[2]
+    out = torch.empty_like(q) if out is None else out
+    rc = load().gqa_decode_int8(_ptr(q), _ptr(kq), _ptr(vq), _ptr(kscale), _ptr(vscale), _ptr(lens), _ptr(out),
+                                B, Hq, Hkv, Smax, D, _stream(q))
+    _check(rc)
+    return out

@@ -61,6 +61,11 @@ EncodeTiledFn encode_fn() {
 // (dims[0] innermost; strides in bytes for dims 1..rank-1)
 int cpattn::encode_bf16_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
                              const unsigned long long* strides, const unsigned* box) {
+  return encode_tmap(m, ptr, rank, dims, strides, box, 2);
+}
+
+int cpattn::encode_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
+                        const unsigned long long* strides, const unsigned* box, int elem_bytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return -1;
   cuuint64_t d[5], st[4];
@@ -71,7 +76,8 @@ int cpattn::encode_bf16_tmap(CUtensorMap* m, const void* ptr, int rank, const un
     es[i] = 1;
     if (i > 0) st[i - 1] = strides[i - 1];
   }
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, st, bx, es,
+  CUresult r = fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                  const_cast<void*>(ptr), d, st, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -1;
@@ -618,6 +624,37 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
     e = launch_gqa_decode(a, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "gqa_decode launch");
+  return CPATTN_OK;
+}
+
+int gqa_decode_int8(const void* q, const void* kcache, const void* vcache, const float* kscale,
+                    const float* vscale, const int* lens, void* out, int B, int Hq, int Hkv, int Smax, int D,
+                    cudaStream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Smax < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, Hq, Hkv, Smax must be >= 1");
+  if (Hq % Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Hq / Hkv > 16) return fail(CPATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16", Hq / Hkv);
+  if (D != 128) return fail(CPATTN_ERR_UNSUPPORTED, "int8 decode head dim %d is not 128", D);
+  if (B > decode_int8_max_batch()) return fail(CPATTN_ERR_UNSUPPORTED, "int8 decode batch %d > %d", B, decode_int8_max_batch());
+  if (!lens || !kscale || !vscale) return fail(CPATTN_ERR_INVALID_ARG, "null lens or scales");
+  int rc = check_ptrs({q, kcache, vcache, out});
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds;
+  if ((rc = get_state(&ds))) return rc;
+  if ((rc = need_sm103(*ds))) return rc;
+  if ((rc = ensure(ds->dec_o, decode_part_o_floats(B, Hq, Hkv, Smax, D), stream, false))) return rc;
+  if ((rc = ensure(ds->dec_ml, decode_part_ml_floats(B, Hq, Hkv, Smax), stream, false))) return rc;
+  DecodeArgs a{};
+  a.q = q; a.kc = kcache; a.vc = vcache; a.lens = lens; a.out = out;
+  a.kscale = kscale; a.vscale = vscale;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Smax = Smax; a.D = D;
+  a.part_o = ds->dec_o.ptr; a.part_ml = ds->dec_ml.ptr; a.err = ds->err;
+  cudaError_t e;
+  {
+    ProfScope ps("gqa_decode_int8", stream);
+    e = launch_gqa_decode(a, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gqa_decode_int8 launch");
   return CPATTN_OK;
 }
 

@@ -21,6 +21,8 @@
 // of each (b, g).  No atomics, no fences.
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -270,36 +272,90 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
 // S, O (TMEM), P (shared memory) and the group barriers are indexed by item
 // parity.
 // ---------------------------------------------------------------------------
-namespace tcd {
-constexpr int D = 128;
-constexpr int NH = 16;                 // head columns of the MMAs
-constexpr int ROWS = kDecodeSplit;     // positions per item
-constexpr int NK = 3;                  // K (+q) ring stages: freed once the scores are formed
-constexpr int NV = 3;                  // V ring stages: freed once the output is formed
-constexpr int K_BYTES = ROWS * D * 2;  // two 64-column boxes
-constexpr int V_BYTES = ROWS * D * 2;
-constexpr int Q_BYTES = NH * D * 2;    // two boxes of 16 rows
-constexpr int KSTAGE = K_BYTES + Q_BYTES;
-constexpr int P_BYTES = NH * ROWS * 2;  // P^T as [head][position], two boxes of 64 positions
-constexpr int OFF_V = NK * KSTAGE;
-constexpr int OFF_P = OFF_V + NV * V_BYTES;
-constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-constexpr int OFF_RED = OFF_BAR + 256;  // per group: float rmax[4][NH], rsum[4][NH]
-constexpr int OFF_MISC = OFF_RED + 2 * 2 * 4 * NH * 4;
-constexpr int OFF_LENS = OFF_MISC + 64;
-constexpr int MAX_B = 1024;             // batch rows staged in shared memory
-constexpr int OFF_PRE = OFF_LENS + MAX_B * 4;
-constexpr int SMEM = OFF_PRE + (MAX_B + 1) * 4 + 1024;
-constexpr int kThreadsTc = 352;
-static_assert(KSTAGE % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(SMEM <= 232448, "shared memory budget");
-static_assert(ROWS == 128, "one position per softmax thread");
-struct Bars {
+// INT8: the cache holds int8 vectors with one fp32 scale per (b, g,
+// position).  TMA stages each item's int8 K (with the bf16 q rows) and int8
+// V; eight converter warps turn them into fp16 tiles (int8 is exact in fp16,
+// so the conversion is exact and needs no multiply) and the MMAs run as fp16
+// x fp16 -> fp32.  The scales are folded in by the softmax threads, one
+// position each: the key scale into the scores, the value scale into P.  The
+// staging costs shared memory: two stages per ring instead of three.
+template <bool INT8>
+struct TcCfg {
+  static constexpr int D = 128;
+  static constexpr int NH = 16;                 // head columns of the MMAs
+  static constexpr int ROWS = kDecodeSplit;     // positions per item
+  static constexpr int NK = INT8 ? 2 : 3;       // K (+q) ring stages: freed once the scores are formed
+  static constexpr int NV = INT8 ? 2 : 3;       // V ring stages: freed once the output is formed
+  static constexpr int NS = 2;                  // int8 staging stages per tensor
+  static constexpr int K_BYTES = ROWS * D * 2;  // two 64-column boxes
+  static constexpr int V_BYTES = ROWS * D * 2;
+  static constexpr int Q_BYTES = NH * D * 2;    // two boxes of 16 rows
+  static constexpr int KSTAGE = K_BYTES + Q_BYTES;
+  static constexpr int S8_BYTES = ROWS * D;     // one int8 tile: 128 rows x 128 bytes
+  static constexpr int KS_STAGE = S8_BYTES + Q_BYTES;  // int8 K tile + the item's bf16 q rows
+  static constexpr int P_BYTES = NH * ROWS * 2;  // P^T as [head][position], two boxes of 64 positions
+  static constexpr int OFF_V = NK * KSTAGE;
+  static constexpr int OFF_KS = OFF_V + NV * V_BYTES;              // int8 K staging
+  static constexpr int OFF_VS = OFF_KS + (INT8 ? NS * KS_STAGE : 0);  // int8 V staging
+  static constexpr int OFF_P = OFF_VS + (INT8 ? NS * S8_BYTES : 0);
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_RED = OFF_BAR + 256;  // per group: float rmax[4][NH], rsum[4][NH]
+  static constexpr int OFF_MISC = OFF_RED + 2 * 2 * 4 * NH * 4;
+  static constexpr int OFF_LENS = OFF_MISC + 64;
+  static constexpr int MAX_B = 1024;             // batch rows staged in shared memory
+  static constexpr int OFF_PRE = OFF_LENS + MAX_B * 4;
+  static constexpr int SMEM = OFF_PRE + (MAX_B + 1) * 4 + 1024;
+  static constexpr int kThreads = INT8 ? 608 : 352;  // + warps 11-14 converting K, 15-18 converting V
+  static_assert(KSTAGE % 1024 == 0 && OFF_V % 1024 == 0 && OFF_KS % 1024 == 0 && OFF_VS % 1024 == 0 &&
+                    OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(ROWS == 128, "one position per softmax / converter thread");
+};
+template <int NK, int NV>
+struct TcBars {
   uint64_t kfull[NK], kempty[NK], vfull[NV], vempty[NV];
+  uint64_t ksfull[2], ksempty[2], vsfull[2], vsempty[2];  // int8 staging
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t done;
 };
+namespace tcd {
+constexpr int MAX_B = TcCfg<false>::MAX_B;
 }  // namespace tcd
+
+// one cached int8 row (128 values, staged with a 128-byte swizzle) to fp16
+// row r of a K-major, 128-byte-swizzled tile of two 64-column boxes, exactly:
+// the biased byte b = x + 128 in the mantissa of fp16 1024 is 1024 + b, and
+// subtracting 1152 leaves x
+__device__ __forceinline__ void int8_row_to_f16(const unsigned char* stg, unsigned char* tile, int r) {
+  const uint32_t nmagic = 0xE480E480u;  // fp16x2 (-1152, -1152)
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // 16 values per 16-byte chunk
+    const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
+    const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // fp16 pairs (1024 + b0, 1024 + b1) and (1024 + b2, 1024 + b3)
+      const uint32_t lo = __byte_perm(wv[i], 0x64646464u, 0x5140);
+      const uint32_t hi = __byte_perm(wv[i], 0x64646464u, 0x7362);
+      uint32_t x;
+      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(lo), "r"(nmagic));
+      o[2 * i] = x;
+      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(hi), "r"(nmagic));
+      o[2 * i + 1] = x;
+    }
+    unsigned char* box = tile + (c >> 2) * (128 * 128) + r * 128;
+    const int cc = 2 * (c & 3);
+    *reinterpret_cast<uint4*>(box + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(box + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// instruction descriptor, kind::f16 with fp16 A/B and fp32 accumulation
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
 
 // dense item j -> (b, g, slice): pre[b] = items of rows before b (Hkv slices
 // per 128 positions), pre[B] = the total
@@ -323,10 +379,15 @@ __device__ __forceinline__ Item loaded_item(int j, const int* pre, const int* le
   return it;
 }
 
-template <int GMAX>
-__global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const __grid_constant__ DecodeArgs a,
-                                                                         float scale_log2, int max_split) {
-  using namespace tcd;
+template <int GMAX, bool INT8>
+__global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel(const __grid_constant__ DecodeArgs a,
+                                                                                float scale_log2, int max_split) {
+  using C = TcCfg<INT8>;
+  constexpr int D = C::D, NH = C::NH, ROWS = C::ROWS, NK = C::NK, NV = C::NV, K_BYTES = C::K_BYTES;
+  constexpr int KSTAGE = C::KSTAGE, V_BYTES = C::V_BYTES, P_BYTES = C::P_BYTES, OFF_V = C::OFF_V, OFF_P = C::OFF_P;
+  constexpr int OFF_BAR = C::OFF_BAR, OFF_RED = C::OFF_RED, OFF_MISC = C::OFF_MISC, OFF_LENS = C::OFF_LENS;
+  constexpr int OFF_PRE = C::OFF_PRE, kThreadsTc = C::kThreads;
+  using Bars = TcBars<NK, NV>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bar = *reinterpret_cast<Bars*>(smem + OFF_BAR);
@@ -343,8 +404,13 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
   // set-up that reads no input overlaps the previous kernel in the stream
   // (this grid is launched as a programmatic dependent)
   if (tid == 0) {
-    for (int i = 0; i < NK; ++i) { mbar_init(&bar.kfull[i], 1); mbar_init(&bar.kempty[i], 1); }
-    for (int i = 0; i < NV; ++i) { mbar_init(&bar.vfull[i], 1); mbar_init(&bar.vempty[i], 1); }
+    // int8: a K or V stage completes when its 128 converter threads have written it
+    for (int i = 0; i < NK; ++i) { mbar_init(&bar.kfull[i], INT8 ? 128 : 1); mbar_init(&bar.kempty[i], 1); }
+    for (int i = 0; i < NV; ++i) { mbar_init(&bar.vfull[i], INT8 ? 128 : 1); mbar_init(&bar.vempty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.ksfull[i], 1); mbar_init(&bar.ksempty[i], 128);
+      mbar_init(&bar.vsfull[i], 1); mbar_init(&bar.vsempty[i], 128);
+    }
     for (int i = 0; i < 2; ++i) { mbar_init(&bar.s_full[i], 1); mbar_init(&bar.p_full[i], 128); mbar_init(&bar.o_full[i], 1); }
     mbar_init(&bar.done, 1);
     *abort_flag = 0;
@@ -394,10 +460,20 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
   const int n_items = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // this CTA's items k: j = cta + k*ncta
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer: K and q
+    // ---------------------------------------------------------- TMA producer: K and q (int8: K staging)
     if (lane == 0) {
       for (int k = 0; k < n_items; ++k) {
         const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
+        if (INT8) {
+          const int st = k % C::NS;
+          if (!mbar_wait(&bar.ksempty[st], ((k / C::NS) & 1) ^ 1, ab)) break;
+          unsigned char* sb = smem + C::OFF_KS + st * C::KS_STAGE;
+          mbar_expect_tx(&bar.ksfull[st], C::KS_STAGE);
+          tma_load_4d(sb, &a.tk, &bar.ksfull[st], 0, it.sp * ROWS, it.g, it.b);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_3d(sb + C::S8_BYTES + bx * (NH * 128), &a.tq, &bar.ksfull[st], bx * 64, it.g * G, it.b);
+          continue;
+        }
         const int st = k % NK;
         if (!mbar_wait(&bar.kempty[st], ((k / NK) & 1) ^ 1, ab)) break;
         unsigned char* sb = smem + st * KSTAGE;
@@ -409,10 +485,17 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
       }
     }
   } else if (warp == 10) {
-    // ---------------------------------------------------------- TMA producer: V
+    // ---------------------------------------------------------- TMA producer: V (int8: V staging)
     if (lane == 0) {
       for (int k = 0; k < n_items; ++k) {
         const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
+        if (INT8) {
+          const int st = k % C::NS;
+          if (!mbar_wait(&bar.vsempty[st], ((k / C::NS) & 1) ^ 1, ab)) break;
+          mbar_expect_tx(&bar.vsfull[st], C::S8_BYTES);
+          tma_load_4d(smem + C::OFF_VS + st * C::S8_BYTES, &a.tv, &bar.vsfull[st], 0, it.sp * ROWS, it.g, it.b);
+          continue;
+        }
         const int st = k % NV;
         if (!mbar_wait(&bar.vempty[st], ((k / NV) & 1) ^ 1, ab)) break;
         unsigned char* sb = smem + OFF_V + st * V_BYTES;
@@ -421,11 +504,58 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
           tma_load_4d(sb + bx * (ROWS * 128), &a.tv, &bar.vfull[st], bx * 64, it.sp * ROWS, it.g, it.b);
       }
     }
+  } else if (INT8 && warp >= 11) {
+    // ---------------------------------------------------------- int8 -> fp16 converters
+    // warps 11-14 convert K (and the item's q rows, bf16 -> fp16), warps 15-18
+    // convert V; thread r owns row r.  A failed wait runs on (the tiles are
+    // then garbage and the error word is set)
+    const bool is_v = warp >= 15;
+    const int r = tid - (is_v ? 480 : 352);
+    for (int k = 0; k < n_items; ++k) {
+      const int ss = k % C::NS;
+      const uint32_t sph = (k / C::NS) & 1;
+      if (!is_v) {
+        const int kst = k % NK;
+        mbar_wait(&bar.kempty[kst], ((k / NK) & 1) ^ 1, ab);
+        mbar_wait(&bar.ksfull[ss], sph, ab);
+        const unsigned char* sb = smem + C::OFF_KS + ss * C::KS_STAGE;
+        unsigned char* kb = smem + kst * KSTAGE;
+        int8_row_to_f16(sb, kb, r);
+        // q: 16 rows x 128 bf16 in two swizzled boxes; thread r converts 16 values in place order
+        {
+          const uint4 u0 = reinterpret_cast<const uint4*>(sb + C::S8_BYTES)[2 * r];
+          const uint4 u1 = reinterpret_cast<const uint4*>(sb + C::S8_BYTES)[2 * r + 1];
+          const uint32_t in[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float x0 = bf16lo(in[i]), x1 = bf16hi(in[i]);
+            uint32_t h;
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+            o[i] = h;
+          }
+          reinterpret_cast<uint4*>(kb + K_BYTES)[2 * r] = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(kb + K_BYTES)[2 * r + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.ksempty[ss]);
+        mbar_arrive(&bar.kfull[kst]);
+      } else {
+        const int vst = k % NV;
+        mbar_wait(&bar.vempty[vst], ((k / NV) & 1) ^ 1, ab);
+        mbar_wait(&bar.vsfull[ss], sph, ab);
+        int8_row_to_f16(smem + C::OFF_VS + ss * C::S8_BYTES, smem + OFF_V + vst * V_BYTES, r);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.vsempty[ss]);
+        mbar_arrive(&bar.vfull[vst]);
+      }
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16(128, NH, 0, 0);   // K (K-major) x q (K-major)
-      constexpr uint32_t IDESC_O = idesc_bf16(128, NH, 1, 0);   // V^T (MN-major) x P^T (K-major)
+      // K (K-major) x q (K-major); V^T (MN-major) x P^T (K-major); fp16 operands for the int8 cache
+      constexpr uint32_t IDESC_S = INT8 ? idesc_f16(128, NH, 0, 0) : idesc_bf16(128, NH, 0, 0);
+      constexpr uint32_t IDESC_O = INT8 ? idesc_f16(128, NH, 1, 0) : idesc_bf16(128, NH, 1, 0);
       const uint32_t s0 = smem_u32(smem);
       auto issue_s = [&](int k) {
         const uint32_t sb = s0 + (k % NK) * KSTAGE;
@@ -490,6 +620,13 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
       const int buf = k & 1;
       const uint32_t par = (k >> 1) & 1;
       const int n = min(ROWS, it.len - it.sp * ROWS);
+      float ksc = 1.f, vsc = 1.f;  // int8 cache: this position's scales, fetched while the scores form
+      if (INT8) {
+        const int t = it.sp * ROWS + r;
+        const size_t so = ((size_t)it.b * a.Hkv + it.g) * a.Smax + t;
+        ksc = t < a.Smax ? a.kscale[so] : 0.f;
+        vsc = t < a.Smax ? a.vscale[so] : 0.f;
+      }
       // a failed wait (abort or timeout) runs on: the named barriers need every thread
       mbar_wait(&bar.s_full[buf], par, ab);
       tc_fence_after();
@@ -499,7 +636,7 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
       float sv[GMAX];
 #pragma unroll
       for (int h = 0; h < GMAX; ++h)
-        sv[h] = (h < G && r < n) ? __uint_as_float(sr[h]) * scale_log2 : -INFINITY;
+        sv[h] = (h < G && r < n) ? __uint_as_float(sr[h]) * (scale_log2 * ksc) : -INFINITY;
       // max over the item's positions, per head
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
@@ -521,9 +658,13 @@ __global__ void __launch_bounds__(tcd::kThreadsTc, 1) gqa_decode_tc_kernel(const
         const int chunk = (r & 63) >> 3;
 #pragma unroll
         for (int h = 0; h < GMAX; ++h)
-          if (h < G)
-            *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + ((chunk ^ (h & 7)) << 4) + (r & 7) * 2) =
-                __float2bfloat16(p[h]);
+          if (h < G) {
+            unsigned short* dst = reinterpret_cast<unsigned short*>(pb + h * 128 + ((chunk ^ (h & 7)) << 4) + (r & 7) * 2);
+            if (INT8)
+              *dst = __half_as_ushort(__float2half_rn(p[h] * vsc));  // value scale folded into P (fp16)
+            else
+              *dst = __bfloat16_as_ushort(__float2bfloat16(p[h]));
+          }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -657,21 +798,22 @@ cudaError_t launch_dg(const DecodeArgs& a, cudaStream_t st) {
   return max_split > 1 ? launch_combine<D, GMAX>(a, max_split, st) : cudaSuccess;
 }
 
-template <int GMAX>
+template <int GMAX, bool INT8>
 cudaError_t launch_tc(const DecodeArgs& a0, cudaStream_t st) {
+  using C = TcCfg<INT8>;
   DecodeArgs a = a0;
-  const unsigned long long D = 128;
+  const unsigned long long D = 128, eb = INT8 ? 1 : 2;  // bytes per cached element
   unsigned long long kd[4] = {D, (unsigned long long)a.Smax, (unsigned long long)a.Hkv, (unsigned long long)a.B};
-  unsigned long long ks[3] = {D * 2, (unsigned long long)a.Smax * D * 2, (unsigned long long)a.Hkv * a.Smax * D * 2};
-  unsigned kb[4] = {64, (unsigned)tcd::ROWS, 1, 1};
+  unsigned long long ks[3] = {D * eb, (unsigned long long)a.Smax * D * eb, (unsigned long long)a.Hkv * a.Smax * D * eb};
+  unsigned kb[4] = {INT8 ? 128u : 64u, (unsigned)C::ROWS, 1, 1};  // 128-byte rows either way
   unsigned long long qd[3] = {D, (unsigned long long)a.Hq, (unsigned long long)a.B};
   unsigned long long qs[2] = {D * 2, (unsigned long long)a.Hq * D * 2};
-  unsigned qb[3] = {64, (unsigned)tcd::NH, 1};
-  if (encode_bf16_tmap(&a.tk, a.kc, 4, kd, ks, kb) || encode_bf16_tmap(&a.tv, a.vc, 4, kd, ks, kb) ||
-      encode_bf16_tmap(&a.tq, a.q, 3, qd, qs, qb))
+  unsigned qb[3] = {64, (unsigned)C::NH, 1};
+  if (encode_tmap(&a.tk, a.kc, 4, kd, ks, kb, (int)eb) || encode_tmap(&a.tv, a.vc, 4, kd, ks, kb, (int)eb) ||
+      encode_tmap(&a.tq, a.q, 3, qd, qs, qb, 2))
     return cudaErrorInvalidValue;
-  auto kern = gqa_decode_tc_kernel<GMAX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tcd::SMEM);
+  auto kern = gqa_decode_tc_kernel<GMAX, INT8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -680,8 +822,8 @@ cudaError_t launch_tc(const DecodeArgs& a0, cudaStream_t st) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
-  cfg.blockDim = dim3(tcd::kThreadsTc);
-  cfg.dynamicSmemBytes = tcd::SMEM;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // its set-up overlaps the previous kernel
@@ -690,6 +832,16 @@ cudaError_t launch_tc(const DecodeArgs& a0, cudaStream_t st) {
   cfg.numAttrs = 1;
   if ((e = cudaLaunchKernelEx(&cfg, kern, a, scale_log2, max_split)) != cudaSuccess) return e;
   return max_split > 1 ? launch_combine<128, GMAX>(a, max_split, st) : cudaSuccess;
+}
+
+template <bool INT8>
+cudaError_t launch_tc_g(const DecodeArgs& a, cudaStream_t st) {
+  const int G = a.Hq / a.Hkv;
+  if (G <= 1) return launch_tc<1, INT8>(a, st);
+  if (G <= 2) return launch_tc<2, INT8>(a, st);
+  if (G <= 4) return launch_tc<4, INT8>(a, st);
+  if (G <= 8) return launch_tc<8, INT8>(a, st);
+  return launch_tc<16, INT8>(a, st);
 }
 
 template <int D>
@@ -716,16 +868,13 @@ size_t decode_part_ml_floats(int B, int Hq, int Hkv, int Smax) {
 }
 
 cudaError_t launch_gqa_decode(const DecodeArgs& a, cudaStream_t st) {
-  if (a.D == 128 && a.B <= tcd::MAX_B) {  // tensor-core path
-    const int G = a.Hq / a.Hkv;
-    if (G <= 1) return launch_tc<1>(a, st);
-    if (G <= 2) return launch_tc<2>(a, st);
-    if (G <= 4) return launch_tc<4>(a, st);
-    if (G <= 8) return launch_tc<8>(a, st);
-    return launch_tc<16>(a, st);
-  }
+  if (a.kscale) return launch_tc_g<true>(a, st);  // int8 cache (D = 128, B <= 1024 checked by the caller)
+  if (a.D == 128 && a.B <= tcd::MAX_B) return launch_tc_g<false>(a, st);  // tensor-core path
+  if (a.D == 128) return launch_d<128>(a, st);
   return launch_d<64>(a, st);
 }
+
+int decode_int8_max_batch() { return tcd::MAX_B; }
 
 // ---------------------------------------------------------------------------
 // Decode without any allocation by the library.

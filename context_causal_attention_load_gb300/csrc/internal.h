@@ -12,6 +12,10 @@ cudaError_t launch_lb_permute(const void* src, void* dst, int B, int S, long lon
 // split-K decode: scratch = partial (o, m, l) per 128-position slice; a
 // second kernel merges the slices of each (batch, kv head).
 // bf16 tiled tensor map, 128-byte swizzle (returns 0 on success)
+int decode_int8_max_batch();
+// tensor map with 128-byte swizzle and zero fill; elem_bytes 2 (bf16) or 1 (int8 as bytes)
+int encode_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
+                const unsigned long long* strides, const unsigned* box, int elem_bytes);
 int encode_bf16_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
                      const unsigned long long* strides, const unsigned* box);
 
@@ -23,6 +27,8 @@ struct DecodeArgs {
   const int* lens;
   void* out;
   int B, Hq, Hkv, Smax, D;
+  const float* kscale;  // int8 cache only: [B, Hkv, Smax] per-position scales (null: bf16 cache)
+  const float* vscale;
   float* part_o;    // [B*Hkv][max_split][G][D]
   float* part_ml;   // [B*Hkv][max_split][G][2]
   int* err;

@@ -159,6 +159,21 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
                int B, int Hq, int Hkv, int Smax, int D, cudaStream_t stream);
 
 /*
+ * gqa_decode against an int8-quantised KV cache (the inference setup of
+ * "rename context to context_autoregressive", Tests, runs with
+ * quantize_kvcache=True): kcache/vcache int8 [B, Hkv, Smax, D], device, with
+ * one fp32 scale per (batch, KV head, position) in kscale/vscale [B, Hkv,
+ * Smax], device; the cached vector at position t is int8 values * scale.
+ * The kernel dequantises each vector to bf16 (one rounding) and then runs
+ * the tensor-core decode, reading half the bytes of the bf16 cache.  Other
+ * arguments, layouts, results and error behaviour as gqa_decode.  Requires
+ * D == 128, B <= 1024, Hq % Hkv == 0, Hq/Hkv <= 16.
+ */
+int gqa_decode_int8(const void* q, const void* kcache, const void* vcache, const float* kscale,
+                    const float* vscale, const int* lens, void* out, int B, int Hq, int Hkv, int Smax,
+                    int D, cudaStream_t stream);
+
+/*
  * gqa_decode without any allocation by the library (the pages have no
  * counterpart; this exists for callers that must not let a library
  * allocate device memory: code whose memory is owned by a caching

@@ -88,3 +88,6 @@ def test_bad_arguments_are_rejected_on_host():
     assert lib.gqa_decode(P, P, P, P, P, 1, 64, 2, 128, 128, None) == -2
     assert lib.gqa_decode(P, P, P, P, P, 1, 8, 2, 128, 96, None) == -2
     assert lib.gqa_decode(P, P, P, None, P, 1, 8, 2, 128, 128, None) == -1
+    # int8 decode: head dim, null scales
+    assert lib.gqa_decode_int8(P, P, P, P, P, P, P, 1, 8, 2, 128, 64, None) == -2
+    assert lib.gqa_decode_int8(P, P, P, None, P, P, P, 1, 8, 2, 128, 128, None) == -1

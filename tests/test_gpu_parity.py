@@ -308,3 +308,40 @@ def test_decode_bad_lengths_are_flagged():
     ref = O.gqa_decode(_f64(q), _f64(kc), _f64(vc), np.array([256, 10]))
     assert_close_out(_f64(out), ref, "clamped decode")
     cp_.check_device()  # the flag was cleared
+
+
+# ---------------------------------------------------------------------------
+# int8 KV-cache decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [
+    # B, Hq, Hkv, D, Smax, lo, hi
+    (24, 32, 8, 128, 2048, 1024, 2048),   # the decode workload with an int8 cache
+    (3, 8, 8, 128, 300, 1, 300),          # G = 1, cache length not a multiple of 128
+    (2, 16, 1, 128, 640, 300, 640),       # G = 16
+    (1, 2, 1, 128, 128, 128, 128),        # one slice: no merge pass
+])
+def test_decode_int8_parity(cfg):
+    B, Hq, Hkv, D, Smax, lo, hi = cfg
+    q, kq, vq, ks, vs, lens = synth.decode_inputs_int8(B, Hq, Hkv, D, Smax, lo, hi, seed=41)
+    out = cp_.gqa_decode_int8(q.cuda(), kq.cuda(), vq.cuda(), ks.cuda(), vs.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref = O.gqa_decode_int8(_f64(q), kq.numpy(), vq.numpy(), ks.numpy().astype(np.float64),
+                            vs.numpy().astype(np.float64), lens.numpy())
+    assert_close_out(_f64(out), ref, "int8 decode %s" % (cfg,))
+    out2 = cp_.gqa_decode_int8(q.cuda(), kq.cuda(), vq.cuda(), ks.cuda(), vs.cuda(), lens.cuda())
+    assert torch.equal(out2, out)
+
+
+def test_decode_int8_edge_lengths():
+    B, Hq, Hkv, D, Smax = 5, 8, 2, 128, 1024
+    q, kq, vq, ks, vs, _ = synth.decode_inputs_int8(B, Hq, Hkv, D, Smax, 1, 1, seed=42)
+    lens = torch.tensor([0, 1, 256, 257, 1024], dtype=torch.int32)
+    out = cp_.gqa_decode_int8(q.cuda(), kq.cuda(), vq.cuda(), ks.cuda(), vs.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref = O.gqa_decode_int8(_f64(q), kq.numpy(), vq.numpy(), ks.numpy().astype(np.float64),
+                            vs.numpy().astype(np.float64), lens.numpy())
+    assert torch.all(out[0] == 0)
+    assert_close_out(_f64(out), ref, "int8 decode edge lengths")
