@@ -436,6 +436,7 @@ def run_ours(args, w, wname):
                                   (out_n if lb else out_p, dq_n if lb else dq_p, dk_n if lb else dk_p,
                                    dv_n if lb else dv_p, dec_out), f_step, world, dev)
         line["decode"] = measure_decode(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
+        line["decode_int8"] = measure_decode_int8(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
         line["shards"] = measure_shards(w, qp if lb else q, kp if lb else k, vp if lb else v, cpattn)
         if lb and (w["S"] // (2 * w["cp"])) % 128 == 0:
             line["zero_copy"] = measure_zero_copy(args, w, (q, k, v, dout), (dq_, dkc, dvc, dlens), dec_out, f_step,
@@ -543,6 +544,42 @@ def measure_zero_copy(args, w, inputs, dec_inputs, dec_out, f_step, ms_step, wor
     return {"ms_per_step": ms, "value": aggregate_throughput(f_step, ms / 1e3, world) / 1e12, "unit": "TFLOP/s",
             "steps": n, "saved_ms_vs_permuted_step": ms_step - ms,
             "what": "fwd + bwd with load_balance=2 (natural-order tensors, balanced schedule) + decode"}
+
+
+def measure_decode_int8(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
+    """The decode workload against an int8 cache of the same shape (values
+    drawn on the device, one fp32 scale per position and KV head), timed like
+    ``measure_decode``; bytes are the int8 K/V plus their scales."""
+    import torch
+    g = torch.Generator(device=q.device).manual_seed(7)
+    kq = torch.randint(-127, 128, kc.shape, generator=g, device=q.device, dtype=torch.int32).to(torch.int8)
+    vq = torch.randint(-127, 128, vc.shape, generator=g, device=q.device, dtype=torch.int32).to(torch.int8)
+    ks = 0.008 + 0.008 * torch.rand(kc.shape[:3], generator=g, device=q.device)
+    vs = 0.008 + 0.008 * torch.rand(vc.shape[:3], generator=g, device=q.device)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=q.device)
+    flush_rd = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=q.device)
+    sink = torch.empty((), dtype=torch.float32, device=q.device)
+    out = torch.empty_like(q)
+    for _ in range(3):
+        cpattn.gqa_decode_int8(q, kq, vq, ks, vs, lens, out)
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        torch.sum(flush_rd, dim=0, out=sink)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        cpattn.gqa_decode_int8(q, kq, vq, ks, vs, lens, out)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    med = ts[len(ts) // 2]
+    n = int(sum(int(x) for x in lens_host))
+    by = n * DECODE["Hkv"] * DECODE["D"] * 2 + n * DECODE["Hkv"] * 4 * 2
+    gbs = by / (med / 1e3) / 1e9
+    return {"us": med * 1e3, "kv_bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "bf16_equivalent_gbs": decode_bytes(lens_host) / (med / 1e3) / 1e9,
+            "l2": "flushed before each launch (512 MB write + 512 MB read)"}
 
 
 def measure_shards(w, q, k, v, cpattn, iters=5):
