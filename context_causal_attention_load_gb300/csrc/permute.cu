@@ -7,46 +7,40 @@
 // c*row bytes, so the gather is 2cp*B block copies.  One launch streams all
 // of them with 16-byte (or the widest aligned) vectors, every warp reading
 // and writing consecutive addresses: a pure HBM copy, 2 bytes moved per
-// byte of tensor.
+// byte of tensor, with no per-element index arithmetic.
 #include "common.cuh"
 #include "internal.h"
 
 namespace cpattn {
 
+// blockIdx.y + gridDim.y * blockIdx.z = b * nchunk + k: memory chunk k of
+// batch b, which holds original chunk chunk_of(k); the CTAs along x stream
+// it.  Both block bases are computed once per CTA, so the inner loop is a
+// plain strided copy.
 template <typename V, int UNROLL>
 __global__ void __launch_bounds__(256) lb_permute_kernel(const V* __restrict__ src, V* __restrict__ dst,
-                                                         long long chunk_vecs, int nchunk, int cp,
-                                                         long long total, int inverse) {
+                                                         long long chunk_vecs, int nchunk, int cp, long long nblk,
+                                                         int inverse) {
+  const long long blk = blockIdx.y + (long long)gridDim.y * blockIdx.z;
+  if (blk >= nblk) return;
+  const long long b = blk / nchunk;
+  const int k = int(blk - b * nchunk);
+  const int s = k >> 1;
+  const int ch = (k & 1) ? (2 * cp - 1 - s) : s;
+  const long long slot_base = blk * chunk_vecs;
+  const long long pos_base = (b * nchunk + ch) * chunk_vecs;
+  // permute: dst[slot] = src[pos];  unpermute: dst[pos] = src[slot]
+  const V* sp = src + (inverse ? slot_base : pos_base);
+  V* dp = dst + (inverse ? pos_base : slot_base);
   const long long stride = (long long)gridDim.x * blockDim.x;
-  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  // each thread moves UNROLL vectors per iteration, spaced by the grid
-  // stride so a warp's accesses stay contiguous
-  for (; i < total; i += stride * UNROLL) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunk_vecs; i += stride * UNROLL) {
     V buf[UNROLL];
-    long long so[UNROLL], dofs[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      long long e = i + u * stride;
-      so[u] = -1;
-      if (e < total) {
-        long long blk = e / chunk_vecs;  // (batch, memory chunk)
-        long long off = e - blk * chunk_vecs;
-        long long b = blk / nchunk;
-        int k = int(blk - b * nchunk);
-        int s = k >> 1;
-        int ch = (k & 1) ? (2 * cp - 1 - s) : s;
-        long long lbpos = (b * nchunk + ch) * chunk_vecs + off;  // original-order block
-        // permute: dst[slot] = src[pos];  unpermute: dst[pos] = src[slot]
-        so[u] = inverse ? e : lbpos;
-        dofs[u] = inverse ? lbpos : e;
-      }
-    }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u)
-      if (so[u] >= 0) buf[u] = __ldcs(src + so[u]);
+      if (i + u * stride < chunk_vecs) buf[u] = __ldcs(sp + i + u * stride);
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u)
-      if (so[u] >= 0) __stcs(dst + dofs[u], buf[u]);
+      if (i + u * stride < chunk_vecs) __stcs(dp + i + u * stride, buf[u]);
   }
 }
 
@@ -54,14 +48,15 @@ template <typename V>
 static cudaError_t launch_v(const void* src, void* dst, long long chunk_bytes, int nchunk, int cp,
                             int B, int inverse, int num_sms, cudaStream_t st) {
   const long long chunk_vecs = chunk_bytes / (long long)sizeof(V);
-  const long long total = chunk_vecs * nchunk * (long long)B;
+  const long long nblk = (long long)nchunk * B;
+  const unsigned gy = (unsigned)(nblk < 65535 ? nblk : 65535), gz = (unsigned)((nblk + gy - 1) / gy);
   constexpr int kUnroll = 4;
-  long long want = (total + 256LL * kUnroll - 1) / (256LL * kUnroll);
-  long long cap = (long long)num_sms * 8;  // 8 resident 256-thread blocks per SM
-  int grid = int(want < cap ? want : cap);
-  if (grid < 1) grid = 1;
-  lb_permute_kernel<V, kUnroll><<<grid, 256, 0, st>>>(static_cast<const V*>(src), static_cast<V*>(dst),
-                                                      chunk_vecs, nchunk, cp, total, inverse);
+  long long want = (chunk_vecs + 256LL * kUnroll - 1) / (256LL * kUnroll);
+  long long cap = ((long long)num_sms * 8 + nblk - 1) / nblk;  // about 8 resident 256-thread blocks per SM
+  int gx = int(want < cap ? want : cap);
+  if (gx < 1) gx = 1;
+  lb_permute_kernel<V, kUnroll><<<dim3(gx, gy, gz), 256, 0, st>>>(static_cast<const V*>(src), static_cast<V*>(dst),
+                                                                  chunk_vecs, nchunk, cp, nblk, inverse);
   return cudaGetLastError();
 }
 
