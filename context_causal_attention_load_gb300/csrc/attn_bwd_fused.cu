@@ -85,10 +85,12 @@ __device__ __forceinline__ void bulk_wait_read() {
 // P for this thread's 64 query columns of one step: scores from TMEM (t_s),
 // p = exp2(s * scale*log2e - lse*log2e), zeroed where the key's position is
 // past the query's (MASKED steps only; positions walked slot by slot from
-// slot0), kept in fp32 for dS and stored back to TMEM (t_pk) as packed bf16
-template <bool MASKED, bool SHARD>
+// slot0), kept in fp32 for dS and stored back to TMEM (t_pk) as packed bf16;
+// mid() runs after the first 32 columns
+template <bool MASKED, bool SHARD, typename Mid>
 __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* lse_s, uint64_t sl2x2,
-                                     float (&p)[64], int kpos, const PosMap& pm, int slot0, int lo, int hi) {
+                                     float (&p)[64], int kpos, const PosMap& pm, int slot0, int lo, int hi,
+                                     Mid&& mid) {
   int ck = 0, ct = 0, cbase = 0;  // memory chunk, offset in it, first position of the chunk
   if (MASKED && pm.lb) {
     ck = slot0 / pm.c;
@@ -136,6 +138,7 @@ __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* l
       pk[c >> 1] = pack_bf16(p0, p1);
     }
     tmem_st16(t_pk + 16 * h, pk);
+    if (h == 0) mid();  // between the halves: a chance to take the previous dQ out early
   }
 }
 
@@ -494,15 +497,23 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const uint32_t t_s = tmem + lane_base + C::T_S + g * 64;
         const uint32_t t_pk = tmem + lane_base + C::T_S + packed_col<64>(g * 64);
         const bool q_inside = !SHARD || (qt * kRows >= a.q_lo && qt * kRows + kRows <= a.q_hi);
+        // the previous step's dQ: read out as soon as it is ready (checked, warp by
+        // warp, halfway through P), since the tensor core's next dP waits on it
+        bool ro_pending = have_prev;
+        auto mid = [&]() {
+          if (ro_pending && __all_sync(0xffffffffu, mbar_try(smem_u32(&bar.dq_full), (gs - 1) & 1))) {
+            readout(gs - 1);
+            ro_pending = false;
+          }
+        };
         if ((kmax <= qmin) && k_inside && q_inside)
-          ew_p<false, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, 0, 0, 0);
+          ew_p<false, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, 0, 0, 0, mid);
         else
-          ew_p<true, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, qt * kRows + g * 64, a.q_lo, a.q_hi);
+          ew_p<true, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, qt * kRows + g * 64, a.q_lo, a.q_hi, mid);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar.p_full);
-        // ---- dQ of the previous step
-        if (have_prev) readout(gs - 1);
+        if (ro_pending) readout(gs - 1);
         // ---- dS = P * (dP - D): bf16 into TMEM (for dK), then shared memory (for dQ)
         mbar_wait(&bar.dp_full, gs & 1, ab);
         tc_fence_after();
