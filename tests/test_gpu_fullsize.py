@@ -6,7 +6,9 @@ checks:
   * dk and dv exactly on the last 64 key positions of one KV head (only the
     64 query rows per head at those positions see them);
   * identities that hold at any size: sum_j dk_j = 0 and
-    sum_j dv_j = sum_i dout_i per KV head."""
+    sum_j dv_j = sum_i dout_i per KV head;
+  * the zero-copy mode (natural-order tensors, load_balance=2) against the
+    permuted run: out, lse, dk, dv bit-identical, dq to its reduction order."""
 
 import math
 
@@ -46,7 +48,6 @@ def test_fullsize_parity(name):
     q, k, v, dout = synth.attention_inputs_device(B, S, Hq, Hkv, Dqk, Dv, seed=101, q_scale=qs)
     # load-balanced order on the GPU, exactly as the bench step does it
     qp, kp, vp, dp = (cpattn.lb_permute(x, cp) for x in (q, k, v, dout))
-    del q, dout
     out, lse = cpattn.attn_fwd(qp, kp, vp, cp, True)
     dq, dk, dv = cpattn.attn_bwd(qp, kp, vp, out, lse, dp, cp, True)
     torch.cuda.synchronize()
@@ -99,3 +100,16 @@ def test_fullsize_parity(name):
     vsum = dv32.sum(dim=1)
     rel = float(((vsum - dsum).norm() / dsum.norm()))
     assert rel < 5e-3, "%s: sum dv != sum dout (rel %.2e)" % (name, rel)
+
+    # ---- zero-copy load balance: the same tiles on natural-order tensors ----
+    out_z, lse_z = cpattn.attn_fwd(q, k, v, cp, 2)
+    dq_z, dk_z, dv_z = cpattn.attn_bwd(q, k, v, out_z, lse_z, dout, cp, 2)
+    torch.cuda.synchronize()
+    cpattn.check_device()
+    assert torch.equal(out_z, cpattn.lb_unpermute(out, cp)), "%s zero-copy out" % name
+    assert torch.equal(lse_z[:, :, torch.from_numpy(pos).long().cuda()], lse), "%s zero-copy lse" % name
+    assert torch.equal(dk_z, cpattn.lb_unpermute(dk, cp)), "%s zero-copy dk" % name
+    assert torch.equal(dv_z, cpattn.lb_unpermute(dv, cp)), "%s zero-copy dv" % name
+    dq_n = cpattn.lb_unpermute(dq, cp).float()
+    rel = float((dq_z.float() - dq_n).norm() / dq_n.norm())
+    assert rel < 1e-3, "%s zero-copy dq differs beyond its reduction order (rel %.2e)" % (name, rel)
