@@ -199,12 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       int pph[2] = {0, 0};
       bool ok = true;
 
-      // descriptors advance by adding byte offsets / 16 to the start-address field
+      // descriptors advance by adding byte offsets / 16 to the start-address field;
+      // the issue loops are unrolled: the MMA queue is shallow, so every
+      // instruction this thread spends between MMAs shows as tensor-pipe idle
       auto issue_qk = [&](int t, int kslot) {
         const uint32_t d = tmem + t * 256;
         const uint64_t ad0 = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
         const uint64_t bd0 = sdesc_sw128(sK + kslot * C::K_BYTES, 16, 1024);
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;  // BM == BN
           mma_ss(d, ad0 + off, bd0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t d = tmem + t * 256 + 128;
         const uint32_t p = tmem + t * 256;
         const uint64_t bd0 = sdesc_sw128(sV + vslot * C::V_BYTES, BN * 128, 1024);
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(d, p + kk * 8, bd0 + ((kk * 16 * 128) >> 4), IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       };
