@@ -536,7 +536,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     if (e != cudaSuccess) return cuda_fail(e, "fused bwd launch");
     {
       ProfScope ps("bwd_dq_round", stream);
-      e = launch_bwd_dq_round(a.dq_acc, dq, (long long)nacc, stream);
+      e = launch_bwd_dq_round(a.dq_acc, dq, (long long)nacc, a.scale, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "dq rounding launch");
     return CPATTN_OK;

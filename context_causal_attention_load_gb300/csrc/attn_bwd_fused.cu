@@ -16,15 +16,19 @@
 // preprocess kernel and rounded to bf16 by a final pass.
 //
 // MMA order per step j:  dP_j, dV_j, S_{j+1}, dK_j, dQ_j; the element-wise
-// warps run P_{j+1} while dK_j and dQ_j execute, read dQ_j out of TMEM, then
-// form dS_{j+1} while dV_{j+1} and S_{j+2} execute.  TMEM (512 columns): S/P
-// 128, dP/dS/dQ 128, dV D, dK D.  Tensor-core MMAs from one thread execute
-// in issue order, so an MMA may overwrite TMEM columns an earlier one reads.
+// warps run P_{j+1} while dK_j and dQ_j execute, then form dS_{j+1} while
+// dV_{j+1} and S_{j+2} execute.  dQ_j is taken out of TMEM by a warpgroup of
+// its own the moment it is complete, because dP_{j+1} needs its columns and
+// the tensor core waits for them.  TMEM (512 columns): S/P 128, dP/dS/dQ
+// 128, dV D, dK D.  Tensor-core MMAs from one thread execute in issue order,
+// so an MMA may overwrite TMEM columns an earlier one reads.
 //
 // Shared memory (D = 128, 226 KiB): K and V tiles (resident per unit), two
 // stages each of Q and dO with the per-row -lse*log2(e) and -D vectors, and
 // one dS tile.  dQ_step (128 x D fp32) is staged for the reduce in the dS
-// tile and, for D = 128, in the step's dO stage (both dead by then).
+// tile and, for D = 128, in the step's dO stage (both dead by then; the Q
+// stage is not, since S_{j+1} reads the other one and Q_{j+2} must land in
+// this one by the next step).
 #include <cstdio>
 
 #include "common.cuh"
@@ -33,8 +37,16 @@
 namespace cpattn {
 namespace {
 
-constexpr int kThreadsF = 352;  // warps 0-7 element-wise (two column halves), 8 TMA producer, 9 MMA issuer,
-                                // 10 dQ reducer
+// warps 0-7 element-wise (two column halves), 8 TMA producer, 9 MMA issuer,
+// 10 dQ reducer, 11 idle, 12-15 dQ read-out.  setmaxnreg moves registers from
+// warpgroup 2 (producer, MMA, reducer) and warpgroup 3 (read-out) to the
+// element-wise warpgroups.
+constexpr int kThreadsF = 512;
+constexpr int kRegsLaunchF = 128;  // 65536 / 512
+constexpr int kRegsEw = 152;
+constexpr int kRegsWg2 = 112;
+constexpr int kRegsWg3 = 96;
+static_assert(256 * kRegsEw + 128 * kRegsWg2 + 128 * kRegsWg3 <= kThreadsF * kRegsLaunchF, "register split");
 constexpr int kRows = 128;      // key rows per unit, query rows per step
 
 template <int D>
@@ -85,12 +97,10 @@ __device__ __forceinline__ void bulk_wait_read() {
 // P for this thread's 64 query columns of one step: scores from TMEM (t_s),
 // p = exp2(s * scale*log2e - lse*log2e), zeroed where the key's position is
 // past the query's (MASKED steps only; positions walked slot by slot from
-// slot0), kept in fp32 for dS and stored back to TMEM (t_pk) as packed bf16;
-// mid() runs after the first 32 columns
-template <bool MASKED, bool SHARD, typename Mid>
+// slot0), kept in fp32 for dS and stored back to TMEM (t_pk) as packed bf16
+template <bool MASKED, bool SHARD>
 __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* lse_s, uint64_t sl2x2,
-                                     float (&p)[64], int kpos, const PosMap& pm, int slot0, int lo, int hi,
-                                     Mid&& mid) {
+                                     float (&p)[64], int kpos, const PosMap& pm, int slot0, int lo, int hi) {
   int ck = 0, ct = 0, cbase = 0;  // memory chunk, offset in it, first position of the chunk
   if (MASKED && pm.lb) {
     ck = slot0 / pm.c;
@@ -138,7 +148,6 @@ __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* l
       pk[c >> 1] = pack_bf16(p0, p1);
     }
     tmem_st16(t_pk + 16 * h, pk);
-    if (h == 0) mid();  // between the halves: a chance to take the previous dQ out early
   }
 }
 
@@ -208,8 +217,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     mbar_init(&bar.dst_full, 256);
     mbar_init(&bar.dss_full, 256);
     mbar_init(&bar.dq_full, 1);
-    mbar_init(&bar.dq_free, 256);
-    mbar_init(&bar.staged, 256);
+    mbar_init(&bar.dq_free, 128);
+    mbar_init(&bar.staged, 128);
     mbar_init(&bar.ds_free, 1);
     mbar_init(&bar.acc_full, 1);
     mbar_init(&bar.done, 1);
@@ -225,6 +234,70 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  auto dq_readout = [&]() {
+    // ------------------------------------------------------------ dQ read-out
+    // dQ_j (query rows = TMEM lanes, D fp32 columns in dP's space): TMEM ->
+    // registers -> shared memory for the reducer (the dS tile and, for
+    // D = 128, the step's dO stage; boxes of 32 columns, 128-byte swizzle),
+    // each 32-column chunk staged while the next load is in flight; the
+    // columns are released as soon as the last load is done.  Both spaces are
+    // dead once dQ_j is complete: dS_j and dO_j were last read by MMAs that
+    // precede it.  The tile goes out unscaled (the final rounding pass applies
+    // the softmax scale).
+    const int qd = warp & 3;
+    const int row = (qd << 5) + lane;  // query row of the tile == TMEM lane
+    const uint32_t t_dq = tmem + (uint32_t(qd * 32) << 16) + C::T_DP;
+    auto stage = [&](int gsr, int c, const uint32_t (&o)[32]) {
+      unsigned char* bb = c < 2 ? smem + C::OFF_DS + c * (kRows * 128)
+                                : smem + C::OFF_DO + (gsr & 1) * C::TILE + (c - 2) * (kRows * 128);
+      unsigned char* rp = bb + row * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(rp + ((ch ^ (row & 7)) << 4)) =
+            make_uint4(o[4 * ch + 0], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
+    };
+    int gs = 0;
+    for (int r = 0;; ++r) {
+      const int ui = unit_index(r, cta, ncta);
+      if (ui >= a.n_units) break;
+      const BwdUnit u = a.units[ui];
+      int kmin, kmax;
+      pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
+      const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
+      int hq = u.h * G, qt = -1;
+      if (!w.next(pm, hq, qt)) continue;
+      do {
+        mbar_wait(&bar.dq_full, gs & 1, ab);  // runs on after an abort: the staging is garbage, the waits bounded
+        tc_fence_after();
+        uint32_t o[2][32];
+        tmem_ld32(t_dq, o[0]);
+        tmem_ld32(t_dq + 32, o[1]);
+        tmem_ld_wait();
+        if (C::NBOX > 2) {
+          stage(gs, 0, o[0]);
+          tmem_ld32(t_dq + 64, o[0]);
+          stage(gs, 1, o[1]);
+          tmem_ld32(t_dq + 96, o[1]);
+          tmem_ld_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.dq_free);
+        stage(gs, C::NBOX - 2, o[0]);
+        stage(gs, C::NBOX - 1, o[1]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.staged);
+        ++gs;
+      } while (w.next(pm, hq, qt));
+    }
+  };
+
+  // each role's code sits under its own setmaxnreg, so the compiler
+  // allocates it against that role's register budget
+  if (warp >= 12) {
+  regs_dec<kRegsWg3>();
+  dq_readout();
+  } else if (warp >= 8) {
+  regs_dec<kRegsWg2>();
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -417,7 +490,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       }
       bulk_wait_all();  // every dQ reduce has landed before the CTA retires
     }
+  }
   } else {
+    regs_inc<kRegsEw>();
     // ------------------------------------------------------------ element-wise warps
     // Group g (warps 4g..4g+3) owns query columns [64g, 64g+64) of S^T/dP^T
     // (thread = key row = TMEM lane) and dQ columns [gD/2, (g+1)D/2) (thread =
@@ -428,42 +503,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const uint64_t sl2x2 = f2pack(a.scale_log2, a.scale_log2);
     int gs = 0;
-    bool have_prev = false;
-
-    // dQ of global step gsr: TMEM -> registers (frees the columns for the next
-    // dP) -> scaled fp32 tile in shared memory for the reducer warp (the dS
-    // tile and, for D = 128, the step's dO stage; boxes of 32 columns, 128-byte
-    // swizzle)
-    auto readout = [&](int gsr) {
-      mbar_wait(&bar.dq_full, gsr & 1, ab);
-      tc_fence_after();
-      constexpr int NC = D / 2 / 32;  // 32-column chunks per group
-      uint32_t o[NC][32];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) tmem_ld32(tmem + lane_base + C::T_DP + g * (D / 2) + c * 32, o[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bar.dq_free);
-      const float sc = a.scale;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const int box = g * NC + c;
-        unsigned char* bb = box < 2 ? smem + C::OFF_DS + box * (kRows * 128)
-                                    : smem + C::OFF_DO + (gsr & 1) * C::TILE + (box - 2) * (kRows * 128);
-        unsigned char* rp = bb + row * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          float4 v;
-          v.x = sc * __uint_as_float(o[c][4 * ch + 0]);
-          v.y = sc * __uint_as_float(o[c][4 * ch + 1]);
-          v.z = sc * __uint_as_float(o[c][4 * ch + 2]);
-          v.w = sc * __uint_as_float(o[c][4 * ch + 3]);
-          *reinterpret_cast<float4*>(rp + ((ch ^ (row & 7)) << 4)) = v;
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bar.staged);
-    };
 
     for (int r = 0, uc = 0;; ++r) {
       const int ui = unit_index(r, cta, ncta);
@@ -497,23 +536,13 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const uint32_t t_s = tmem + lane_base + C::T_S + g * 64;
         const uint32_t t_pk = tmem + lane_base + C::T_S + packed_col<64>(g * 64);
         const bool q_inside = !SHARD || (qt * kRows >= a.q_lo && qt * kRows + kRows <= a.q_hi);
-        // the previous step's dQ: read out as soon as it is ready (checked, warp by
-        // warp, halfway through P), since the tensor core's next dP waits on it
-        bool ro_pending = have_prev;
-        auto mid = [&]() {
-          if (ro_pending && __all_sync(0xffffffffu, mbar_try(smem_u32(&bar.dq_full), (gs - 1) & 1))) {
-            readout(gs - 1);
-            ro_pending = false;
-          }
-        };
         if ((kmax <= qmin) && k_inside && q_inside)
-          ew_p<false, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, 0, 0, 0, mid);
+          ew_p<false, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, 0, 0, 0);
         else
-          ew_p<true, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, qt * kRows + g * 64, a.q_lo, a.q_hi, mid);
+          ew_p<true, SHARD>(t_s, t_pk, lse_s, sl2x2, p, kpos, pm, qt * kRows + g * 64, a.q_lo, a.q_hi);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar.p_full);
-        if (ro_pending) readout(gs - 1);
         // ---- dS = P * (dP - D): bf16 into TMEM (for dK), then shared memory (for dQ)
         mbar_wait(&bar.dp_full, gs & 1, ab);
         tc_fence_after();
@@ -545,12 +574,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
                          dk[chunk >> 2][4 * (chunk & 3) + 2], dk[chunk >> 2][4 * (chunk & 3) + 3]);
         fence_proxy_async_smem();
         mbar_arrive(&bar.dss_full);
-        have_prev = true;
         ++gs;
       } while (!last);
-      // the unit's last dQ, then dV and scale*dK of this key tile
-      readout(gs - 1);
-      have_prev = false;
+      // dV and scale*dK of this key tile
       mbar_wait(&bar.acc_full, uc & 1, ab);
       tc_fence_after();
       const size_t orow = ((size_t)u.b * pm.S + (kvalid ? mem_row<NAT>(pm, kslot) : 0)) * a.sh.Hkv + u.h;
@@ -597,13 +623,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
   }
 }
 
-// dq (bf16, [B, S, Hq, D]) = the fp32 accumulator; 8 elements per thread
-__global__ void __launch_bounds__(256) bwd_dq_round_kernel(const float* __restrict__ acc, __nv_bfloat16* dq, long long n8) {
+// dq (bf16, [B, S, Hq, D]) = scale * the fp32 accumulator; 8 elements per thread
+__global__ void __launch_bounds__(256) bwd_dq_round_kernel(const float* __restrict__ acc, __nv_bfloat16* dq, long long n8,
+                                                           float scale) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const float4 x = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i);
     const float4 y = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
-    reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y),
-                                                 pack_bf16(y.z, y.w));
+    reinterpret_cast<uint4*>(dq)[i] =
+        make_uint4(pack_bf16(scale * x.x, scale * x.y), pack_bf16(scale * x.z, scale * x.w),
+                   pack_bf16(scale * y.x, scale * y.y), pack_bf16(scale * y.z, scale * y.w));
   }
 }
 
@@ -614,7 +642,12 @@ cudaError_t launch_fused(const BwdArgs& a, int grid, cudaStream_t st) {
   // 512-column TMEM allocation never waits for a neighbour
   int smem = FCfg<D>::SMEM;
   if (smem < 120 * 1024) smem = 120 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // setmaxnreg.inc only succeeds if the launch reserved kRegsLaunchF per thread
+  cudaFuncAttributes fa0;
+  cudaError_t e = cudaFuncGetAttributes(&fa0, kern);
+  if (e != cudaSuccess) return e;
+  if (fa0.numRegs != kRegsLaunchF) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreadsF, smem, st>>>(a);
   e = cudaGetLastError();
@@ -642,11 +675,11 @@ cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st) {
   return nat ? launch_fused<128, false, true>(a, grid, st) : launch_fused<128, false, false>(a, grid, st);
 }
 
-cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, cudaStream_t st) {
+cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, float scale, cudaStream_t st) {
   const long long n8 = n / 8;  // n is a multiple of 64 (head dim)
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152LL * 16) blocks = 152LL * 16;
-  bwd_dq_round_kernel<<<(int)blocks, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(dq), n8);
+  bwd_dq_round_kernel<<<(int)blocks, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(dq), n8, scale);
   return cudaGetLastError();
 }
 

@@ -100,7 +100,7 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
 // accumulator) for Dqk == Dv in {64, 128}
 bool bwd_fused_supported(int Dqk, int Dv);
 cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st);
-cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, cudaStream_t st);
+cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, float scale, cudaStream_t st);
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, int grid, cudaStream_t st);
 int bwd_dkdv_q_tile(int Dqk);  // query rows per step of the dk/dv kernel
