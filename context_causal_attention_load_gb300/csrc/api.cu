@@ -294,10 +294,11 @@ std::vector<FwdUnit> build_fwd_units(const AttnShape& sh, int shard) {
   for (int qt = 0; qt < nqt; ++qt) qmax[qt] = tile_max_pos(pm, qt, kTile);
   std::vector<std::pair<long long, FwdUnit>> w;
   auto add = [&](int b, int hkv, int h0, int t0, int h1, int t1) {
-    FwdUnit u{b, h0, h1, t0, t1, hkv, 0, 0};
     int bound = qmax[t0];
     if (h1 >= 0) bound = std::max(bound, qmax[t1]);
-    long long cost = (long long)count_kv_tiles(pm, bound) * (h1 >= 0 ? 2 : 1);
+    const int nkv = count_kv_tiles(pm, bound);
+    FwdUnit u{b, h0, h1, t0, t1, hkv, nkv, 0};
+    long long cost = (long long)nkv * (h1 >= 0 ? 2 : 1);
     w.push_back({cost, u});
   };
   // tiles of one head paired with their neighbour in the same memory chunk

@@ -19,7 +19,8 @@
 // CTA = 12 warps, one CTA per SM (all 512 TMEM columns):
 //   warps 0-3  softmax group 0 (query tile 0, one thread per row)
 //   warps 4-7  softmax group 1 (query tile 1)
-//   warp  8    TMA producer: Q tiles, then K and V tiles into two rings
+//   warp  8    TMA producer: Q tiles, then one ring stage per key step
+//              (K of the unit's first tile alone, then V_j with K_{j+1})
 //   warp  9    MMA issuer (one thread): S_t = Q_t K^T into TMEM, and
 //              O_t += P_t V with P_t read straight from TMEM
 //   warps 10-11 idle (they complete the third warpgroup)
@@ -47,10 +48,14 @@ constexpr int kRegsSoftmax = 192;
 constexpr int kRegsOther = 120;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split");
 
+// Ring of NK stages: stage g holds K in slot g % NK and V in slot g % NV
+// (NV < NK only where shared memory has no room for a second V slot; then a
+// stage's V waits for the previous stage instead of the one NK back).
 template <int DQK, int DV>
 struct FwdCfg {
   static constexpr int NK = DQK == 192 ? 2 : (DQK == 64 ? 4 : 2);
   static constexpr int NV = DQK == 192 ? 1 : (DQK == 64 ? 4 : 2);
+  static_assert(NV == NK || NV == 1, "stage ring");
   static constexpr int Q_BYTES = BM * DQK * 2;
   static constexpr int K_BYTES = BN * DQK * 2;
   static constexpr int V_BYTES = BN * DV * 2;
@@ -66,8 +71,7 @@ struct FwdCfg {
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4];
-  uint64_t v_full[4], v_empty[4];
+  uint64_t kv_full[4], kv_empty[4];  // per ring stage
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t kpos[2];  // per softmax group: key-position table written
   uint64_t done;
@@ -90,9 +94,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   int* kpos_s = reinterpret_cast<int*>(smem + C::OFF_POS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
-  // per K stage: 1 if the tile in it is its unit's last (the producer walks the
-  // tiles, a chain of integer divisions, so the MMA thread does not have to)
-  volatile int* klast = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 32);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -102,8 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (tid == 0) {
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_empty, 1);
-    for (int i = 0; i < C::NK; ++i) { mbar_init(&bar.k_full[i], 1); mbar_init(&bar.k_empty[i], 1); }
-    for (int i = 0; i < C::NV; ++i) { mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_empty[i], 1); }
+    for (int i = 0; i < C::NK; ++i) { mbar_init(&bar.kv_full[i], 1); mbar_init(&bar.kv_empty[i], 1); }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar.s_full[t], 1);
       mbar_init(&bar.p_full[t], 128);
@@ -135,9 +135,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if ((tid & 31) == 0) {
-      int ks = 0, kph = 0, vs = 0, vph = 0, qph = 0;
-      int nk = 0, nv = 0, nq = 0;  // loads issued into each ring
+      int qph = 0;
+      int ng = 0, nq = 0;  // ring stages and Q loads issued
       bool ok = true;
+      // claim ring stage ng for `bytes` of loads (its K slot, and its V slot
+      // when it carries V, must have been released)
+      auto claim = [&](bool with_v, uint32_t bytes) {
+        const int i = ng % C::NK;
+        if (ng >= C::NK && !(ok = mbar_wait(&bar.kv_empty[i], ((ng / C::NK) & 1) ^ 1, ab))) return false;
+        if (C::NV == 1 && with_v && ng >= 1) {
+          const int pg = ng - 1;  // the stage before holds the one V slot
+          if (!(ok = mbar_wait(&bar.kv_empty[pg % C::NK], (pg / C::NK) & 1, ab))) return false;
+        }
+        mbar_expect_tx(&bar.kv_full[i], bytes);
+        return true;
+      };
+      auto load_k = [&](int kt, const FwdUnit& u) {
+        const int i = ng % C::NK;
+        for (int bx = 0; bx < DQK / 64; ++bx)
+          tma_load_4d(smem + C::OFF_K + i * C::K_BYTES + bx * BN * 128, &a.tk, &bar.kv_full[i], bx * 64, u.hkv,
+                      pm.row(kt * BN), u.b);
+      };
+      auto load_v = [&](int kt, const FwdUnit& u) {
+        const int i = ng % C::NK, vi = ng % C::NV;
+        for (int bx = 0; bx < DV / 64; ++bx)
+          tma_load_4d(smem + C::OFF_V + vi * C::V_BYTES + bx * BN * 128, &a.tv, &bar.kv_full[i], bx * 64, u.hkv,
+                      pm.row(kt * BN), u.b);
+      };
       for (int r = 0; ok; ++r) {
         const int ui = unit_index(r, cta, ncta);
         if (ui >= a.n_units) break;
@@ -156,23 +180,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tma_load_4d(smem + C::OFF_Q + C::Q_BYTES + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h1,
                         pm.row(u.t1 * BM), u.b);
         const int bound = kv_bound(pm, u);
-        for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0;) {
+        int kt = next_kv_tile(pm, BN, -1, bound);
+        // prologue stage: the first K tile
+        if (!claim(false, C::K_BYTES)) break;
+        load_k(kt, u);
+        ++ng;
+        // step j: V_j and, unless it is the last, K_{j+1}
+        while (kt >= 0) {
           const int nkt = next_kv_tile(pm, BN, kt, bound);
-          if (!(ok = mbar_wait(&bar.k_empty[ks], kph ^ 1, ab))) break;
-          klast[ks] = nkt < 0 ? 1 : 0;  // published with the tile (the arrive below releases it)
-          mbar_expect_tx(&bar.k_full[ks], C::K_BYTES);
-          ++nk;
-          for (int bx = 0; bx < DQK / 64; ++bx)
-            tma_load_4d(smem + C::OFF_K + ks * C::K_BYTES + bx * BN * 128, &a.tk, &bar.k_full[ks], bx * 64,
-                        u.hkv, pm.row(kt * BN), u.b);
-          if (++ks == C::NK) { ks = 0; kph ^= 1; }
-          if (!(ok = mbar_wait(&bar.v_empty[vs], vph ^ 1, ab))) break;
-          mbar_expect_tx(&bar.v_full[vs], C::V_BYTES);
-          ++nv;
-          for (int bx = 0; bx < DV / 64; ++bx)
-            tma_load_4d(smem + C::OFF_V + vs * C::V_BYTES + bx * BN * 128, &a.tv, &bar.v_full[vs], bx * 64,
-                        u.hkv, pm.row(kt * BN), u.b);
-          if (++vs == C::NV) { vs = 0; vph ^= 1; }
+          if (!claim(true, C::V_BYTES + (nkt >= 0 ? C::K_BYTES : 0))) break;
+          load_v(kt, u);
+          if (nkt >= 0) load_k(nkt, u);
+          ++ng;
           kt = nkt;
         }
       }
@@ -180,10 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // let the copies already issued land (bounded) before the CTA exits
         volatile int own = 0;
         const Abort quiet{&own, a.err};
-        // slot i received its last load as load number i + NK*n; that load
-        // completes phase n of the slot's barrier
-        for (int i = 0; i < C::NK && i < nk; ++i) mbar_wait(&bar.k_full[i], ((nk - 1 - i) / C::NK) & 1, quiet);
-        for (int i = 0; i < C::NV && i < nv; ++i) mbar_wait(&bar.v_full[i], ((nv - 1 - i) / C::NV) & 1, quiet);
+        // stage g's loads complete phase g / NK of its barrier
+        for (int g = ng - 1; g >= 0 && g >= ng - C::NK; --g) mbar_wait(&bar.kv_full[g % C::NK], (g / C::NK) & 1, quiet);
         if (nq > 0) mbar_wait(&bar.q_full, (nq - 1) & 1, quiet);
       }
     }
@@ -195,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sK = smem_u32(smem + C::OFF_K);
       const uint32_t sV = smem_u32(smem + C::OFF_V);
-      int ks = 0, kph = 0, vs = 0, vph = 0, qph = 0;
+      int qph = 0;
       int pph[2] = {0, 0};
       bool ok = true;
 
@@ -221,54 +238,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mma_ts(d, p + kk * 8, bd0 + ((kk * 16 * 128) >> 4), IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       };
 
+      int g = 0;  // ring stage
       for (int r = 0; ok; ++r) {
         const int ui = unit_index(r, cta, ncta);
         if (ui >= a.n_units) break;
         const FwdUnit u = a.units[ui];
         const bool has1 = u.h1 >= 0;
+        const int nt = has1 ? 2 : 1;
         if (!(ok = mbar_wait(&bar.q_full, qph, ab))) break;
         qph ^= 1;
         tc_fence_after();
-        // prologue: S_0 and S_1 of the first key tile
-        if (!(ok = mbar_wait(&bar.k_full[ks], kph, ab))) break;
+        // prologue stage: S_0 and S_1 of the first key tile
+        if (!(ok = mbar_wait(&bar.kv_full[g % C::NK], (g / C::NK) & 1, ab))) break;
         tc_fence_after();
-        bool last = klast[ks] != 0;
-        issue_qk(0, ks);
-        mma_commit(&bar.s_full[0]);
-        if (has1) {
-          issue_qk(1, ks);
-          mma_commit(&bar.s_full[1]);
+        for (int t = 0; t < nt; ++t) {
+          issue_qk(t, g % C::NK);
+          mma_commit(&bar.s_full[t]);
         }
-        mma_commit(&bar.k_empty[ks]);
-        if (++ks == C::NK) { ks = 0; kph ^= 1; }
-        for (int j = 0; ok; ++j) {
-          const bool more = !last;
+        mma_commit(&bar.kv_empty[g % C::NK]);
+        ++g;
+        for (int j = 0; ok; ++j, ++g) {
+          const bool more = j + 1 < u.nkv;
           if (!more) mma_commit(&bar.q_empty);  // every QK of this unit is issued
-          if (!(ok = mbar_wait(&bar.v_full[vs], vph, ab))) break;
-          bool knext = false;
-          for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+          if (!(ok = mbar_wait(&bar.kv_full[g % C::NK], (g / C::NK) & 1, ab))) break;
+          for (int t = 0; t < nt; ++t) {
             if (!(ok = mbar_wait(&bar.p_full[t], pph[t], ab))) break;
             pph[t] ^= 1;
             tc_fence_after();
-            issue_pv(t, vs, j > 0);
-            if (!more) mma_commit(&bar.o_full[t]);
-            if (more) {
-              if (!knext) {
-                if (!(ok = mbar_wait(&bar.k_full[ks], kph, ab))) break;
-                tc_fence_after();
-                last = klast[ks] != 0;
-                knext = true;
-              }
-              issue_qk(t, ks);
+            issue_pv(t, g % C::NV, j > 0);
+            if (!more) {
+              mma_commit(&bar.o_full[t]);
+            } else {
+              issue_qk(t, g % C::NK);
               mma_commit(&bar.s_full[t]);
             }
           }
           if (!ok) break;
-          mma_commit(&bar.v_empty[vs]);
-          if (++vs == C::NV) { vs = 0; vph ^= 1; }
-          if (!more) break;
-          mma_commit(&bar.k_empty[ks]);
-          if (++ks == C::NK) { ks = 0; kph ^= 1; }
+          mma_commit(&bar.kv_empty[g % C::NK]);
+          if (!more) {
+            ++g;
+            break;
+          }
         }
       }
       // wait for every issued MMA before TMEM is released

@@ -55,7 +55,8 @@ struct FwdUnit {
   int h0, h1;   // query heads of the two tiles; h1 < 0: single tile
   int t0, t1;   // query tile indices (128-slot tiles)
   int hkv;
-  int pad0, pad1;
+  int nkv;      // key tiles the unit walks (each step holds one)
+  int pad;
 };
 
 struct FwdArgs {
