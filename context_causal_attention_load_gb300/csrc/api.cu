@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <map>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -124,12 +125,20 @@ struct DevBuf {
   size_t n = 0;
 };
 
+// a work list dealt out to ncta CTAs: CTA c runs units [off[c], off[c+1])
+template <typename U>
+struct UnitPlan {
+  DevBuf<U> units;
+  DevBuf<int> off;
+  int ncta = 0;
+};
+
 struct DevState {
   int num_sms = 0;
   int cc_major = 0, cc_minor = 0;
   int* err = nullptr;  // device error word
-  std::map<std::vector<int>, DevBuf<FwdUnit>> fwd_units;
-  std::map<std::vector<int>, DevBuf<BwdUnit>> bwd_units;
+  std::map<std::vector<int>, UnitPlan<FwdUnit>> fwd_units;
+  std::map<std::vector<int>, UnitPlan<BwdUnit>> bwd_units;
   DevBuf<float> bwd_stats;  // lse_l2 then delta
   DevBuf<float> dq_acc;     // fused backward's fp32 dQ accumulator
   DevBuf<float> dec_o, dec_ml;
@@ -233,6 +242,38 @@ int upload(DevBuf<T>& b, const std::vector<T>& v) {
   return CPATTN_OK;
 }
 
+// Deal a work list out to min(units, num_sms) CTAs: units by decreasing cost,
+// each to the CTA with the least cost so far (longest processing time first);
+// every CTA runs its units heaviest first.  The cost of a unit is its steps
+// plus a fixed per-unit overhead measured in steps (pipeline fill and drain,
+// epilogue), so many small units are not mistaken for little work.
+template <typename U>
+int upload_plan(std::vector<std::pair<long long, U>> w, int num_sms, UnitPlan<U>& plan) {
+  std::stable_sort(w.begin(), w.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+  const int ncta = (int)std::min<size_t>(w.size(), (size_t)std::max(1, num_sms));
+  std::vector<std::vector<U>> lists(ncta);
+  using Load = std::pair<long long, int>;  // (cost so far, CTA): ties go to the lower CTA
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> pq;
+  for (int c = 0; c < ncta; ++c) pq.push({0, c});
+  for (const auto& cu : w) {
+    const Load top = pq.top();
+    pq.pop();
+    lists[top.second].push_back(cu.second);
+    pq.push({top.first + cu.first, top.second});
+  }
+  std::vector<U> units;
+  std::vector<int> off(ncta + 1, 0);
+  for (int c = 0; c < ncta; ++c) {
+    off[c] = (int)units.size();
+    units.insert(units.end(), lists[c].begin(), lists[c].end());
+  }
+  off[ncta] = (int)units.size();
+  int rc = upload(plan.units, units);
+  if (!rc) rc = upload(plan.off, off);
+  plan.ncta = ncta;
+  return rc;
+}
+
 // ---- argument checks ------------------------------------------------------
 constexpr int kTile = 128;  // rows per attention tile
 
@@ -283,8 +324,9 @@ int tile_min_pos(const PosMap& pm, int t, int T) {
   return mn;
 }
 
-// forward units: pairs of 128-row query tiles sharing a KV head, heaviest first
-std::vector<FwdUnit> build_fwd_units(const AttnShape& sh, int shard) {
+// forward units: pairs of 128-row query tiles sharing a KV head, with their
+// cost (query tiles x (key steps + 4 steps of per-unit overhead))
+std::vector<std::pair<long long, FwdUnit>> build_fwd_units(const AttnShape& sh, int shard) {
   const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
   const int nqt = (sh.S + kTile - 1) / kTile;
   const int G = sh.Hq / sh.Hkv;
@@ -298,7 +340,7 @@ std::vector<FwdUnit> build_fwd_units(const AttnShape& sh, int shard) {
     if (h1 >= 0) bound = std::max(bound, qmax[t1]);
     const int nkv = count_kv_tiles(pm, bound);
     FwdUnit u{b, h0, h1, t0, t1, hkv, nkv, 0};
-    long long cost = (long long)nkv * (h1 >= 0 ? 2 : 1);
+    const long long cost = (long long)(nkv + 4) * (h1 >= 0 ? 2 : 1);
     w.push_back({cost, u});
   };
   // tiles of one head paired with their neighbour in the same memory chunk
@@ -325,20 +367,17 @@ std::vector<FwdUnit> build_fwd_units(const AttnShape& sh, int shard) {
           if (in_shard(qt)) add(b, hkv, h_first + i, qt, h_first + i + 1, qt);
       if (i < G) pair_rows(b, hkv, h_first + i);
     }
-  std::stable_sort(w.begin(), w.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
-  std::vector<FwdUnit> out(w.size());
-  for (size_t i = 0; i < w.size(); ++i) out[i] = w[i].second;
-  return out;
+  return w;
 }
 
-int fwd_units_cached(DevState& ds, const AttnShape& sh, int shard, DevBuf<FwdUnit>** out) {
+int fwd_units_cached(DevState& ds, const AttnShape& sh, int shard, UnitPlan<FwdUnit>** out) {
   std::vector<int> key{sh.B, sh.Hq, sh.Hkv, sh.S, sh.cp, sh.lb, shard};
   auto it = ds.fwd_units.find(key);
   if (it == ds.fwd_units.end()) {
-    DevBuf<FwdUnit> buf;
-    int rc = upload(buf, build_fwd_units(sh, shard));
+    UnitPlan<FwdUnit> plan;
+    int rc = upload_plan(build_fwd_units(sh, shard), ds.num_sms, plan);
     if (rc) return rc;
-    it = ds.fwd_units.emplace(key, buf).first;
+    it = ds.fwd_units.emplace(key, plan).first;
   }
   *out = &it->second;
   return CPATTN_OK;
@@ -346,8 +385,9 @@ int fwd_units_cached(DevState& ds, const AttnShape& sh, int shard, DevBuf<FwdUni
 
 // backward units.  kind 0: dk/dv, one 128-row key tile of a KV head, cost =
 // query tiles (of BQ rows, all heads of the group) that see it.  kind 1: dq,
-// one 128-row query tile of a query head, cost = key tiles it sees.
-int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, DevBuf<BwdUnit>** out) {
+// one 128-row query tile of a query head, cost = key tiles it sees.  Both
+// plus 3 steps of per-unit overhead.
+int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, UnitPlan<BwdUnit>** out) {
   std::vector<int> key{kind, sh.B, sh.Hq, sh.Hkv, sh.S, sh.cp, sh.lb, sh.Dqk};
   auto it = ds.bwd_units.find(key);
   if (it == ds.bwd_units.end()) {
@@ -361,7 +401,7 @@ int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, DevBuf<BwdUnit
         long long n = 0;
         for (int qt = next_q_tile(pm, BQ, -1, bound); qt >= 0; qt = next_q_tile(pm, BQ, qt, bound)) ++n;
         for (int b = 0; b < sh.B; ++b)
-          for (int g = 0; g < sh.Hkv; ++g) w.push_back({n, BwdUnit{b, g, kt, 0}});
+          for (int g = 0; g < sh.Hkv; ++g) w.push_back({n + 3, BwdUnit{b, g, kt, 0}});
       }
     } else {
       const int BK = bwd_dq_kv_tile(sh.Dqk);
@@ -370,16 +410,13 @@ int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, DevBuf<BwdUnit
         long long n = 0;
         for (int kt = next_kv_tile(pm, BK, -1, bound); kt >= 0; kt = next_kv_tile(pm, BK, kt, bound)) ++n;
         for (int b = 0; b < sh.B; ++b)
-          for (int h = 0; h < sh.Hq; ++h) w.push_back({n, BwdUnit{b, h, qt, 0}});
+          for (int h = 0; h < sh.Hq; ++h) w.push_back({n + 3, BwdUnit{b, h, qt, 0}});
       }
     }
-    std::stable_sort(w.begin(), w.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
-    std::vector<BwdUnit> v(w.size());
-    for (size_t i = 0; i < w.size(); ++i) v[i] = w[i].second;
-    DevBuf<BwdUnit> buf;
-    int rc = upload(buf, v);
+    UnitPlan<BwdUnit> plan;
+    int rc = upload_plan(std::move(w), ds.num_sms, plan);
     if (rc) return rc;
-    it = ds.bwd_units.emplace(key, buf).first;
+    it = ds.bwd_units.emplace(key, plan).first;
   }
   *out = &it->second;
   return CPATTN_OK;
@@ -418,21 +455,22 @@ int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
   DevState* ds;
   if ((rc = get_state(&ds))) return rc;
   if ((rc = need_sm103(*ds))) return rc;
-  DevBuf<FwdUnit>* units;
-  if ((rc = fwd_units_cached(*ds, sh, shard, &units))) return rc;
-  if (units->n == 0) return CPATTN_OK;
+  UnitPlan<FwdUnit>* plan;
+  if ((rc = fwd_units_cached(*ds, sh, shard, &plan))) return rc;
+  if (plan->units.n == 0) return CPATTN_OK;
   FwdArgs a;
   if ((rc = make_tmap(&a.tq, q, sh.B, sh.S, sh.Hq, sh.Dqk, 128))) return rc;
   if ((rc = make_tmap(&a.tk, k, sh.B, sh.S, sh.Hkv, sh.Dqk, 128))) return rc;
   if ((rc = make_tmap(&a.tv, v, sh.B, sh.S, sh.Hkv, sh.Dv, 128))) return rc;
   a.out = out;
   a.lse = lse;
-  a.units = units->ptr;
-  a.n_units = (int)units->n;
+  a.units = plan->units.ptr;
+  a.cta_off = plan->off.ptr;
+  a.n_units = (int)plan->units.n;
   a.sh = sh;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.Dqk));
   a.err = ds->err;
-  const int grid = (int)std::min<size_t>(units->n, (size_t)ds->num_sms);
+  const int grid = plan->ncta;
   cudaError_t e;
   {
     ProfScope ps(shard < 0 ? "attn_fwd" : "attn_fwd_shard", st);
@@ -485,8 +523,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   if (shard >= 0 && !fused) return fail(CPATTN_ERR_UNSUPPORTED, "per-shard backward needs Dqk == Dv (64 or 128)");
   const size_t nacc = (size_t)B * S * Hq * Dqk;
   if (fused && (rc = ensure(ds->dq_acc, nacc, stream, false))) return rc;
-  DevBuf<BwdUnit>* u_kv;
-  DevBuf<BwdUnit>* u_q = nullptr;
+  UnitPlan<BwdUnit>* u_kv;
+  UnitPlan<BwdUnit>* u_q = nullptr;
   if ((rc = bwd_units_cached(*ds, sh, 0, &u_kv))) return rc;
   if (!fused && (rc = bwd_units_cached(*ds, sh, 1, &u_q))) return rc;
   BwdArgs a;
@@ -519,8 +557,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, 128))) return rc;
     if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
     if ((rc = make_tmap_f32(&a.tdq, a.dq_acc, B, S, Hq, Dqk, 128))) return rc;
-    a.units = u_kv->ptr;
-    a.n_units = (int)u_kv->n;
+    a.units = u_kv->units.ptr;
+    a.cta_off = u_kv->off.ptr;
+    a.n_units = (int)u_kv->units.n;
     if (shard >= 0) {  // key tiles no query of the shard sees are skipped: their partials are zero
       const size_t nk = (size_t)B * S * Hkv;
       cudaError_t ez = cudaSuccess;
@@ -532,7 +571,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     }
     {
       ProfScope ps("attn_bwd_fused", stream);
-      e = launch_attn_bwd_fused(a, (int)std::min<size_t>(u_kv->n, (size_t)ds->num_sms), stream);
+      e = launch_attn_bwd_fused(a, u_kv->ncta, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "fused bwd launch");
     {
@@ -548,11 +587,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, BQ))) return rc;
   if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, 128))) return rc;
   if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
-  a.units = u_kv->ptr;
-  a.n_units = (int)u_kv->n;
+  a.units = u_kv->units.ptr;
+  a.cta_off = u_kv->off.ptr;
+  a.n_units = (int)u_kv->units.n;
   {
     ProfScope ps("attn_bwd_dkdv", stream);
-    e = launch_attn_bwd_dkdv(a, (int)std::min<size_t>(u_kv->n, (size_t)ds->num_sms), stream);
+    e = launch_attn_bwd_dkdv(a, u_kv->ncta, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dk/dv launch");
   // dq: query tiles of 128 rows, key/value boxes of BK rows
@@ -561,11 +601,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, 128))) return rc;
   if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, BK))) return rc;
   if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, BK))) return rc;
-  a.units = u_q->ptr;
-  a.n_units = (int)u_q->n;
+  a.units = u_q->units.ptr;
+  a.cta_off = u_q->off.ptr;
+  a.n_units = (int)u_q->units.n;
   {
     ProfScope ps("attn_bwd_dq", stream);
-    e = launch_attn_bwd_dq(a, (int)std::min<size_t>(u_q->n, (size_t)ds->num_sms), stream);
+    e = launch_attn_bwd_dq(a, u_q->ncta, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
   return CPATTN_OK;
@@ -780,9 +821,10 @@ int cp_attn_release(void) {
   if (it == g_dev.end()) return CPATTN_OK;
   cudaDeviceSynchronize();
   DevState& s = it->second;
-  for (auto& kv : s.fwd_units) cudaFree(kv.second.ptr);
-  for (auto& kv : s.bwd_units) cudaFree(kv.second.ptr);
+  for (auto& kv : s.fwd_units) { cudaFree(kv.second.units.ptr); cudaFree(kv.second.off.ptr); }
+  for (auto& kv : s.bwd_units) { cudaFree(kv.second.units.ptr); cudaFree(kv.second.off.ptr); }
   cudaFree(s.bwd_stats.ptr);
+  cudaFree(s.dq_acc.ptr);
   cudaFree(s.dec_o.ptr);
   cudaFree(s.dec_ml.ptr);
   cudaFree(s.err);

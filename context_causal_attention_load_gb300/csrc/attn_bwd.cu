@@ -155,15 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ncta = gridDim.x, cta = blockIdx.x;
+  const int cta = blockIdx.x;
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer (whole warp)
     int qs = 0, qph = 0, kvph = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int ui = unit_index(r, cta, ncta);
-      if (ui >= a.n_units) break;
+      const int ui = unit_index(a.cta_off, r, cta);
+      if (ui < 0) break;
       const BwdUnit u = a.units[ui];
       if (lane == 0) {
         ok = mbar_wait(&bar.kv_empty, kvph ^ 1, ab);
@@ -248,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       };
 
       for (int r = 0; ok; ++r) {
-        const int ui = unit_index(r, cta, ncta);
-        if (ui >= a.n_units) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
         const BwdUnit u = a.units[ui];
         if (!(ok = mbar_wait(&bar.kv_full, kvph, ab))) break;
         kvph ^= 1;
@@ -316,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     int sdph[2] = {0, 0};
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int ui = unit_index(r, cta, ncta);
-      if (ui >= a.n_units) break;
+      const int ui = unit_index(a.cta_off, r, cta);
+      if (ui < 0) break;
       const BwdUnit u = a.units[ui];
       const int kslot = u.t * TK + row;
       const bool kvalid = kslot < pm.S;
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ncta = gridDim.x, cta = blockIdx.x;
+  const int cta = blockIdx.x;
 
   auto q_bound = [&](const BwdUnit& u) {
     int mn, mx;
@@ -511,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     int ks = 0, kph = 0, qph = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int ui = unit_index(r, cta, ncta);
-      if (ui >= a.n_units) break;
+      const int ui = unit_index(a.cta_off, r, cta);
+      if (ui < 0) break;
       const BwdUnit u = a.units[ui];
       const int hkv = u.h / G;
       if (lane == 0) {
@@ -582,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
                  IDESC_DQ, (acc || kk > 0) ? 1u : 0u);
       };
       for (int r = 0; ok; ++r) {
-        const int ui = unit_index(r, cta, ncta);
-        if (ui >= a.n_units) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
         const BwdUnit u = a.units[ui];
         const int bound = q_bound(u);
         if (!(ok = mbar_wait(&bar.q_full, qph, ab))) break;
@@ -643,8 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     int sdph[2] = {0, 0};
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int ui = unit_index(r, cta, ncta);
-      if (ui >= a.n_units) break;
+      const int ui = unit_index(a.cta_off, r, cta);
+      if (ui < 0) break;
       const BwdUnit u = a.units[ui];
       const int bound = q_bound(u);
       const int qslot = u.t * TK + row;

@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
   const PosMap pm = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb);
   const Abort ab{abort_flag, a.err};
   const int G = a.sh.Hq / a.sh.Hkv;
-  const int ncta = gridDim.x, cta = blockIdx.x;
+  const int cta = blockIdx.x;
 
   if (tid == 0) {
     mbar_init(&bar.kv_full, 1);
@@ -258,8 +258,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     };
     int gs = 0;
     for (int r = 0;; ++r) {
-      const int ui = unit_index(r, cta, ncta);
-      if (ui >= a.n_units) break;
+      const int ui = unit_index(a.cta_off, r, cta);
+      if (ui < 0) break;
       const BwdUnit u = a.units[ui];
       int kmin, kmax;
       pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       int gs = 0;  // global step index: stage gs & 1, ring phase (gs >> 1) & 1
       bool ok = true;
       for (int r = 0, uc = 0; ok; ++r) {
-        const int ui = unit_index(r, cta, ncta);
-        if (ui >= a.n_units) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
@@ -399,8 +399,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       int gs = 0;
       bool ok = true;
       for (int r = 0, uc = 0; ok; ++r) {
-        const int ui = unit_index(r, cta, ncta);
-        if (ui >= a.n_units) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
@@ -459,8 +459,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     if (lane == 0) {
       int gs = 0;
       for (int r = 0;; ++r) {
-        const int ui = unit_index(r, cta, ncta);
-        if (ui >= a.n_units) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
@@ -505,8 +505,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     int gs = 0;
 
     for (int r = 0, uc = 0;; ++r) {
-      const int ui = unit_index(r, cta, ncta);
-      if (ui >= a.n_units) break;
+      const int ui = unit_index(a.cta_off, r, cta);
+      if (ui < 0) break;
       const BwdUnit u = a.units[ui];
       const int kslot = u.t * kRows + row;
       const bool kvalid = kslot < pm.S;

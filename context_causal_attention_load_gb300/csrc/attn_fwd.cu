@@ -13,8 +13,8 @@
 // head).  Their KV tiles are the union of the tiles either one can see;
 // tiles every row of a query tile can see need no mask, tiles no row can see
 // are skipped (load balancing follows from the reorder: every shard visits
-// the same number of tiles).  Units are sorted heaviest first on the host
-// and dealt to the CTAs in snake order.
+// the same number of tiles).  The host deals the units out to the CTAs,
+// heaviest first, each to the least-loaded CTA; a CTA runs its own list.
 //
 // CTA = 12 warps, one CTA per SM (all 512 TMEM columns):
 //   warps 0-3  softmax group 0 (query tile 0, one thread per row)
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ncta = gridDim.x, cta = blockIdx.x;
+  const int cta = blockIdx.x;
   // each role's code sits under its own setmaxnreg, so the compiler
   // allocates it against that role's register budget
   if (warp >= 8) {
@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                       pm.row(kt * BN), u.b);
       };
       for (int r = 0; ok; ++r) {
-        const int ui = unit_index(r, cta, ncta);
-        if (ui >= a.n_units) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
         const FwdUnit u = a.units[ui];
         const bool has1 = u.h1 >= 0;
         if (r > 0) {
@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
       int g = 0;  // ring stage
       for (int r = 0; ok; ++r) {
-        const int ui = unit_index(r, cta, ncta);
-        if (ui >= a.n_units) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
         const FwdUnit u = a.units[ui];
         const bool has1 = u.h1 >= 0;
         const int nt = has1 ? 2 : 1;
@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
 
     for (int r = 0; ok; ++r) {
-      const int ui = unit_index(r, cta, ncta);
-      if (ui >= a.n_units) break;
+      const int ui = unit_index(a.cta_off, r, cta);
+      if (ui < 0) break;
       const FwdUnit u = a.units[ui];
       if (t == 1 && u.h1 < 0) continue;
       const int h = t ? u.h1 : u.h0;

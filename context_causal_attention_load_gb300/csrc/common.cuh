@@ -363,10 +363,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// r-th unit of CTA `cta` in a snake deal over ncta CTAs of a work list sorted
-// by decreasing cost (even rounds left to right, odd rounds right to left)
-__device__ __forceinline__ int unit_index(int r, int cta, int ncta) {
-  return r * ncta + ((r & 1) ? (ncta - 1 - cta) : cta);
+// r-th unit of CTA `cta`: the host deals the work list out CTA by CTA (CTA c
+// runs units [off[c], off[c+1]) in that order); -1 past the CTA's last unit
+__device__ __forceinline__ int unit_index(const int* __restrict__ off, int r, int cta) {
+  const int ui = off[cta] + r;
+  return ui < off[cta + 1] ? ui : -1;
 }
 
 // Two element-wise groups each own HC consecutive TMEM columns of a row; a

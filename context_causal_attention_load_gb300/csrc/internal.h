@@ -64,6 +64,7 @@ struct FwdArgs {
   void* out;
   float* lse;
   const FwdUnit* units;
+  const int* cta_off;  // CTA c runs units [cta_off[c], cta_off[c+1])
   int n_units;
   AttnShape sh;
   float scale_log2;
@@ -88,6 +89,7 @@ struct BwdArgs {
   void* dk;
   void* dv;
   const BwdUnit* units;
+  const int* cta_off;  // CTA c runs units [cta_off[c], cta_off[c+1])
   int n_units;
   int Spad;
   AttnShape sh;
