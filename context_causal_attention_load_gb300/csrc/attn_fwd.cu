@@ -162,6 +162,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tma_load_4d(smem + C::OFF_V + vi * C::V_BYTES + bx * BN * 128, &a.tv, &bar.kv_full[i], bx * 64, u.hkv,
                       pm.row(kt * BN), u.b);
       };
+      // while a unit's last stage is in flight, its successor's Q tiles and
+      // first K/V tiles go to L2, so the loads at the unit boundary (which
+      // wait for this unit's buffers) hit L2 instead of HBM
+      auto prefetch_unit = [&](int r2) {
+        const int ui2 = unit_index(a.cta_off, r2, cta);
+        if (ui2 < 0) return;
+        const FwdUnit u2 = a.units[ui2];
+        const int kt0 = next_kv_tile(pm, BN, -1, kv_bound(pm, u2));
+        for (int bx = 0; bx < DQK / 64; ++bx) {
+          tma_prefetch_l2_4d(&a.tq, bx * 64, u2.h0, pm.row(u2.t0 * BM), u2.b);
+          if (u2.h1 >= 0) tma_prefetch_l2_4d(&a.tq, bx * 64, u2.h1, pm.row(u2.t1 * BM), u2.b);
+          if (kt0 >= 0) tma_prefetch_l2_4d(&a.tk, bx * 64, u2.hkv, pm.row(kt0 * BN), u2.b);
+        }
+        for (int bx = 0; kt0 >= 0 && bx < DV / 64; ++bx) tma_prefetch_l2_4d(&a.tv, bx * 64, u2.hkv, pm.row(kt0 * BN), u2.b);
+      };
       for (int r = 0; ok; ++r) {
         const int ui = unit_index(a.cta_off, r, cta);
         if (ui < 0) break;
@@ -192,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           load_v(kt, u);
           if (nkt >= 0) load_k(nkt, u);
           ++ng;
+          if (nkt < 0) prefetch_unit(r + 1);
           kt = nkt;
         }
       }
