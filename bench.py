@@ -438,6 +438,15 @@ def run_ours(args, w, wname):
         line["decode"] = measure_decode(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
         line["decode_int8"] = measure_decode_int8(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
         line["shards"] = measure_shards(w, qp if lb else q, kp if lb else k, vp if lb else v, cpattn)
+        # the same shards with four sequences: at one sequence a shard is 256 two-tile units for 152
+        # SMs, so its time is set by how the units pack (the slowest shard has to run two units on
+        # most SMs); with four, the per-shard times show the balance of the work itself
+        w4 = dict(w, B=4 * w["B"])
+        g4 = torch.Generator(device=dev).manual_seed(args.seed + 99)
+        q4, k4, v4 = [torch.randn(w4["B"], w["S"], h, d, device=dev, generator=g4).to(torch.bfloat16)
+                      for h, d in ((w["Hq"], w["Dqk"]), (w["Hkv"], w["Dqk"]), (w["Hkv"], w["Dv"]))]
+        line["shards_4seq"] = measure_shards(w4, q4, k4, v4, cpattn)
+        del q4, k4, v4
         if lb and (w["S"] // (2 * w["cp"])) % 128 == 0:
             line["zero_copy"] = measure_zero_copy(args, w, (q, k, v, dout), (dq_, dkc, dvc, dlens), dec_out, f_step,
                                                   ms_max, world, dev, cpattn)
