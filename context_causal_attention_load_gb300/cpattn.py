@@ -61,6 +61,8 @@ def load(path=None):
         "cp_attn_fwd_shard": [_P, _P, _P, _P, _P] + [_I] * 9 + [_P],
         "cp_attn_bwd": [_P] * 9 + [_I] * 8 + [_P],
         "cp_attn_bwd_shard": [_P] * 9 + [_I] * 9 + [_P, _P, _P],
+        "cp_attn_fwd_mla": [_P] * 6 + [_I] * 5 + [_P],
+        "cp_attn_bwd_mla": [_P] * 11 + [_I] * 5 + [_P],
         "gqa_decode": [_P] * 5 + [_I] * 5 + [_P],
         "gqa_decode_int8": [_P] * 7 + [_I] * 5 + [_P],
         "cp_lb_positions": [_I, _I, _I, ctypes.POINTER(ctypes.c_int)],
@@ -205,6 +207,46 @@ def attn_bwd_shard(q, k, v, out, lse, dout, cp, shard, load_balance=True, dq=Non
                                   _ptr(dk_part), _ptr(dv_part), _stream(q))
     _check(rc)
     return dq, dk_part, dv_part
+
+
+
+def _mla_shapes(q, k_nope, k_rope, v):
+    _need(q, torch.bfloat16, "q", 4)
+    _need(k_nope, torch.bfloat16, "k_nope", 4)
+    _need(k_rope, torch.bfloat16, "k_rope", 3)
+    _need(v, torch.bfloat16, "v", 4)
+    B, S, H, Dqk = q.shape
+    if Dqk != 192 or tuple(k_nope.shape) != (B, S, H, 128) or tuple(k_rope.shape) != (B, S, 64) \
+            or tuple(v.shape) != (B, S, H, 128):
+        raise ValueError("MLA shapes: q [B,S,H,192], k_nope [B,S,H,128], k_rope [B,S,64], v [B,S,H,128]")
+    return B, S, H
+
+
+def attn_fwd_mla(q, k_nope, k_rope, v, cp, load_balance=True, out=None, lse=None):
+    """MLA forward with one rope key per token shared by the heads: out
+    [B,S,H,128] bf16 and lse [B,H,S] fp32 of attention with the per-head key
+    concat(k_nope, k_rope)."""
+    B, S, H = _mla_shapes(q, k_nope, k_rope, v)
+    out = torch.empty(B, S, H, 128, dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(load().cp_attn_fwd_mla(_ptr(q), _ptr(k_nope), _ptr(k_rope), _ptr(v), _ptr(out), _ptr(lse), B, H, S, cp,
+                                  _lb(load_balance), _stream(q)))
+    return out, lse
+
+
+def attn_bwd_mla(q, k_nope, k_rope, v, out, lse, dout, cp, load_balance=True):
+    """dq, dk_nope, dk_rope (summed over heads), dv of sum(out * dout) for
+    ``attn_fwd_mla``."""
+    B, S, H = _mla_shapes(q, k_nope, k_rope, v)
+    _need(out, torch.bfloat16, "out", 4)
+    _need(dout, torch.bfloat16, "dout", 4)
+    _need(lse, torch.float32, "lse", 3)
+    dq, dk_nope, dk_rope, dv = (torch.empty_like(q), torch.empty_like(k_nope), torch.empty_like(k_rope),
+                                torch.empty_like(v))
+    _check(load().cp_attn_bwd_mla(_ptr(q), _ptr(k_nope), _ptr(k_rope), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                  _ptr(dq), _ptr(dk_nope), _ptr(dk_rope), _ptr(dv), B, H, S, cp, _lb(load_balance),
+                                  _stream(q)))
+    return dq, dk_nope, dk_rope, dv
 
 
 def gqa_decode(q, kcache, vcache, lens, out=None):

@@ -141,6 +141,7 @@ struct DevState {
   std::map<std::vector<int>, UnitPlan<BwdUnit>> bwd_units;
   DevBuf<float> bwd_stats;  // lse_l2 then delta
   DevBuf<float> dq_acc;     // fused backward's fp32 dQ accumulator
+  DevBuf<float> rope_acc;   // MLA with shared rope keys: dK's rope columns summed over heads
   DevBuf<float> dec_o, dec_ml;
 };
 
@@ -490,8 +491,10 @@ int permute_impl(const void* src, void* dst, int B, int S, long long row_bytes, 
   return CPATTN_OK;
 }
 
+// k_rope non-null: MLA with one rope key per token shared by the heads (k holds
+// the per-head 128-column nope keys)
 int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, const AttnShape& sh, int shard,
-             cudaStream_t st) {
+             cudaStream_t st, const void* k_rope = nullptr) {
   int rc = check_attn(sh);
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, out, lse}))) return rc;
@@ -503,10 +506,12 @@ int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
   UnitPlan<FwdUnit>* plan;
   if ((rc = fwd_units_cached(*ds, sh, shard, &plan))) return rc;
   if (plan->units.n == 0) return CPATTN_OK;
-  FwdArgs a;
+  FwdArgs a{};
   if ((rc = make_tmap(&a.tq, q, sh.B, sh.S, sh.Hq, sh.Dqk, 128))) return rc;
-  if ((rc = make_tmap(&a.tk, k, sh.B, sh.S, sh.Hkv, sh.Dqk, 128))) return rc;
+  if ((rc = make_tmap(&a.tk, k, sh.B, sh.S, sh.Hkv, k_rope ? 128 : sh.Dqk, 128))) return rc;
   if ((rc = make_tmap(&a.tv, v, sh.B, sh.S, sh.Hkv, sh.Dv, 128))) return rc;
+  if (k_rope && (rc = make_tmap(&a.tkr, k_rope, sh.B, sh.S, 1, 64, 128))) return rc;
+  a.rope_shared = k_rope ? 1 : 0;
   a.out = out;
   a.lse = lse;
   a.units = plan->units.ptr;
@@ -553,9 +558,12 @@ int cp_attn_fwd_shard(const void* q, const void* k, const void* v, void* out, fl
 namespace {
 // shard < 0: the whole backward; else only query slots [shard*S/cp, (shard+1)*S/cp)
 // take part and dk/dv (optional, bf16) and dk_part/dv_part (fp32) get their partial sums
+// k_rope non-null: MLA with shared rope keys (k and dk hold the per-head nope
+// columns, dk_rope the rope gradient summed over heads)
 int bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
              void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int cp,
-             int load_balance, int shard, float* dk_part, float* dv_part, cudaStream_t stream) {
+             int load_balance, int shard, float* dk_part, float* dv_part, cudaStream_t stream,
+             const void* k_rope = nullptr, void* dk_rope = nullptr) {
   AttnShape sh{B, Hq, Hkv, S, Dqk, Dv, cp, load_balance};
   int rc;
   DevState* ds;
@@ -572,7 +580,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   UnitPlan<BwdUnit>* u_q = nullptr;
   if ((rc = bwd_units_cached(*ds, sh, 0, &u_kv))) return rc;
   if (!fused && (rc = bwd_units_cached(*ds, sh, 1, &u_q))) return rc;
-  BwdArgs a;
+  BwdArgs a{};
   a.lse_l2 = ds->bwd_stats.ptr;
   a.delta = ds->bwd_stats.ptr + nstat;
   a.dq_acc = fused ? ds->dq_acc.ptr : nullptr;
@@ -628,10 +636,20 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   }
   // dk/dv: key tiles of 128 rows, query/dout boxes of BQ rows
   const int BQ = bwd_dkdv_q_tile(Dqk);
+  const size_t nrope = (size_t)B * S * 64;
+  if (k_rope) {
+    if ((rc = ensure(ds->rope_acc, nrope, stream, false))) return rc;
+    e = cudaMemsetAsync(ds->rope_acc.ptr, 0, nrope * sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the rope-key gradient");
+    a.rope_shared = 1;
+    a.dk_rope_acc = ds->rope_acc.ptr;
+  }
+  const int kcols = k_rope ? 128 : Dqk;
   if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, BQ))) return rc;
   if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, BQ))) return rc;
-  if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, 128))) return rc;
+  if ((rc = make_tmap(&a.tk, k, B, S, Hkv, kcols, 128))) return rc;
   if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
+  if (k_rope && (rc = make_tmap(&a.tkr, k_rope, B, S, 1, 64, 128))) return rc;
   a.units = u_kv->units.ptr;
   a.cta_off = u_kv->off.ptr;
   a.n_units = (int)u_kv->units.n;
@@ -644,8 +662,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   const int BK = bwd_dq_kv_tile(Dqk);
   if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, 128))) return rc;
   if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, 128))) return rc;
-  if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, BK))) return rc;
+  if ((rc = make_tmap(&a.tk, k, B, S, Hkv, kcols, BK))) return rc;
   if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, BK))) return rc;
+  if (k_rope && (rc = make_tmap(&a.tkr, k_rope, B, S, 1, 64, BK))) return rc;
   a.units = u_q->units.ptr;
   a.cta_off = u_q->off.ptr;
   a.n_units = (int)u_q->units.n;
@@ -654,6 +673,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     e = launch_attn_bwd_dq(a, u_q->ncta, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
+  if (k_rope) {
+    ProfScope ps("bwd_dq_round", stream);
+    e = launch_bwd_dq_round(ds->rope_acc.ptr, dk_rope, (long long)nrope, 1.0f, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope-key gradient rounding launch");
+  }
   return CPATTN_OK;
 }
 }  // namespace
@@ -684,6 +708,25 @@ int cp_attn_bwd_shard(const void* q, const void* k, const void* v, const void* o
   std::lock_guard<std::mutex> lk(g_mu);
   return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, Dqk, Dv, cp, load_balance, shard, dk_part,
                   dv_part, stream);
+}
+
+int cp_attn_fwd_mla(const void* q, const void* k_nope, const void* k_rope, const void* v, void* out, float* lse,
+                    int B, int H, int S, int cp, int load_balance, cudaStream_t stream) {
+  if (!k_rope) return fail(CPATTN_ERR_INVALID_ARG, "null pointer");
+  AttnShape sh{B, H, H, S, 192, 128, cp, load_balance};
+  return fwd_impl(q, k_nope, v, out, lse, sh, -1, stream, k_rope);
+}
+
+int cp_attn_bwd_mla(const void* q, const void* k_nope, const void* k_rope, const void* v, const void* out,
+                    const float* lse, const void* dout, void* dq, void* dk_nope, void* dk_rope, void* dv, int B, int H,
+                    int S, int cp, int load_balance, cudaStream_t stream) {
+  AttnShape sh{B, H, H, S, 192, 128, cp, load_balance};
+  int rc = check_attn(sh);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k_nope, k_rope, v, out, lse, dout, dq, dk_nope, dk_rope, dv}))) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return bwd_impl(q, k_nope, v, out, lse, dout, dq, dk_nope, dv, B, H, H, S, 192, 128, cp, load_balance, -1, nullptr,
+                  nullptr, stream, k_rope, dk_rope);
 }
 
 int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out, int B, int Hq,
@@ -870,6 +913,7 @@ int cp_attn_release(void) {
   for (auto& kv : s.bwd_units) { cudaFree(kv.second.units.ptr); cudaFree(kv.second.off.ptr); }
   cudaFree(s.bwd_stats.ptr);
   cudaFree(s.dq_acc.ptr);
+  cudaFree(s.rope_acc.ptr);
   cudaFree(s.dec_o.ptr);
   cudaFree(s.dec_ml.ptr);
   cudaFree(s.err);

@@ -30,6 +30,12 @@
 #include "internal.h"
 
 namespace cpattn {
+
+// fire-and-forget fp32 add of four consecutive floats (16-byte aligned) in global memory
+__device__ __forceinline__ void red_add_v4(float* p, float x, float y, float z, float w) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x), "f"(y), "f"(z), "f"(w) : "memory");
+}
+
 namespace {
 
 constexpr int kThreads = 320;
@@ -150,7 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     fence_mbar_init();
   }
   if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
-  if (warp == 8 && lane == 0) { prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tdo); }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tdo);
+    if (a.rope_shared) prefetch_tmap(&a.tkr);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -169,8 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         ok = mbar_wait(&bar.kv_empty, kvph ^ 1, ab);
         if (ok) {
           mbar_expect_tx(&bar.kv_full, C::K_BYTES + C::V_BYTES);
-          for (int bx = 0; bx < DQK / 64; ++bx)
-            tma_load_4d(smem + C::OFF_K + bx * TK * 128, &a.tk, &bar.kv_full, bx * 64, u.h, pm.row(u.t * TK), u.b);
+          for (int bx = 0; bx < DQK / 64; ++bx) {
+            if (DQK == 192 && bx == 2 && a.rope_shared)  // the shared rope keys
+              tma_load_4d(smem + C::OFF_K + bx * TK * 128, &a.tkr, &bar.kv_full, 0, 0, pm.row(u.t * TK), u.b);
+            else
+              tma_load_4d(smem + C::OFF_K + bx * TK * 128, &a.tk, &bar.kv_full, bx * 64, u.h, pm.row(u.t * TK), u.b);
+          }
           for (int bx = 0; bx < DV / 64; ++bx)
             tma_load_4d(smem + C::OFF_V + bx * TK * 128, &a.tv, &bar.kv_full, bx * 64, u.h, pm.row(u.t * TK), u.b);
         }
@@ -385,7 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       acc_ph ^= 1;
       tc_fence_after();
       __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) + (((size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0)) * a.sh.Hkv + u.h) * DV;
-      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) + (((size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0)) * a.sh.Hkv + u.h) * DQK;
+      // shared rope keys: dk holds the 128 nope columns per head, and the rope
+      // columns are summed over heads into dk_rope_acc
+      const bool rope = DQK == 192 && a.rope_shared;
+      const size_t krow = (size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0);
+      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) + (krow * a.sh.Hkv + u.h) * (rope ? 128 : DQK);
 #pragma unroll 1
       for (int c0 = g * (DV / 2); c0 < (g + 1) * (DV / 2); c0 += 32) {
         uint32_t o[32];
@@ -407,7 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + C::T_DK + c0, o);
         tmem_ld_wait();
-        if (kvalid) {
+        if (kvalid && rope && c0 >= 128) {
+          float* acc = a.dk_rope_acc + krow * 64 + (c0 - 128);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            red_add_v4(acc + 4 * v4, sc * __uint_as_float(o[4 * v4 + 0]), sc * __uint_as_float(o[4 * v4 + 1]),
+                       sc * __uint_as_float(o[4 * v4 + 2]), sc * __uint_as_float(o[4 * v4 + 3]));
+        } else if (kvalid) {
           uint4* dst = reinterpret_cast<uint4*>(dkp + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -493,7 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     fence_mbar_init();
   }
   if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
-  if (warp == 8 && lane == 0) { prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tdo); }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tdo);
+    if (a.rope_shared) prefetch_tmap(&a.tkr);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -540,8 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         __syncwarp();
         if (lane == 0) {
           mbar_expect_tx(&bar.kv_full[ks], C::K_BYTES + C::V_BYTES);
-          for (int bx = 0; bx < DQK / 64; ++bx)
-            tma_load_4d(st + C::ST_K + bx * BK * 128, &a.tk, &bar.kv_full[ks], bx * 64, hkv, pm.row(kt * BK), u.b);
+          for (int bx = 0; bx < DQK / 64; ++bx) {
+            if (DQK == 192 && bx == 2 && a.rope_shared)  // the shared rope keys
+              tma_load_4d(st + C::ST_K + bx * BK * 128, &a.tkr, &bar.kv_full[ks], 0, 0, pm.row(kt * BK), u.b);
+            else
+              tma_load_4d(st + C::ST_K + bx * BK * 128, &a.tk, &bar.kv_full[ks], bx * 64, hkv, pm.row(kt * BK), u.b);
+          }
           for (int bx = 0; bx < DV / 64; ++bx)
             tma_load_4d(st + C::ST_V + bx * BK * 128, &a.tv, &bar.kv_full[ks], bx * 64, hkv, pm.row(kt * BK), u.b);
         }

@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     prefetch_tmap(&a.tq);
     prefetch_tmap(&a.tk);
     prefetch_tmap(&a.tv);
+    if (a.rope_shared) prefetch_tmap(&a.tkr);
   }
   tc_fence_before();
   __syncthreads();
@@ -152,9 +153,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       auto load_k = [&](int kt, const FwdUnit& u) {
         const int i = ng % C::NK;
-        for (int bx = 0; bx < DQK / 64; ++bx)
-          tma_load_4d(smem + C::OFF_K + i * C::K_BYTES + bx * BN * 128, &a.tk, &bar.kv_full[i], bx * 64, u.hkv,
-                      pm.row(kt * BN), u.b);
+        for (int bx = 0; bx < DQK / 64; ++bx) {
+          unsigned char* dst = smem + C::OFF_K + i * C::K_BYTES + bx * BN * 128;
+          if (DQK == 192 && bx == 2 && a.rope_shared)  // the shared rope keys
+            tma_load_4d(dst, &a.tkr, &bar.kv_full[i], 0, 0, pm.row(kt * BN), u.b);
+          else
+            tma_load_4d(dst, &a.tk, &bar.kv_full[i], bx * 64, u.hkv, pm.row(kt * BN), u.b);
+        }
       };
       auto load_v = [&](int kt, const FwdUnit& u) {
         const int i = ng % C::NK, vi = ng % C::NV;
@@ -173,7 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int bx = 0; bx < DQK / 64; ++bx) {
           tma_prefetch_l2_4d(&a.tq, bx * 64, u2.h0, pm.row(u2.t0 * BM), u2.b);
           if (u2.h1 >= 0) tma_prefetch_l2_4d(&a.tq, bx * 64, u2.h1, pm.row(u2.t1 * BM), u2.b);
-          if (kt0 >= 0) tma_prefetch_l2_4d(&a.tk, bx * 64, u2.hkv, pm.row(kt0 * BN), u2.b);
+          if (kt0 >= 0) {
+            if (DQK == 192 && bx == 2 && a.rope_shared)
+              tma_prefetch_l2_4d(&a.tkr, 0, 0, pm.row(kt0 * BN), u2.b);
+            else
+              tma_prefetch_l2_4d(&a.tk, bx * 64, u2.hkv, pm.row(kt0 * BN), u2.b);
+          }
         }
         for (int bx = 0; kt0 >= 0 && bx < DV / 64; ++bx) tma_prefetch_l2_4d(&a.tv, bx * 64, u2.hkv, pm.row(kt0 * BN), u2.b);
       };

@@ -61,6 +61,11 @@ struct FwdUnit {
 
 struct FwdArgs {
   CUtensorMap tq, tk, tv;
+  // MLA with one rope key per token shared by all heads (Dqk = 192): tk maps
+  // the per-head 128-column nope keys, tkr the [B, S, 1, 64] rope keys, which
+  // fill K's third 64-column box
+  CUtensorMap tkr;
+  int rope_shared;
   void* out;
   float* lse;
   const FwdUnit* units;
@@ -78,6 +83,9 @@ struct BwdUnit {  // dk/dv unit: one key tile of one KV head; dq unit: one query
 };
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;  // dq kernel uses 128-row boxes; dkdv uses BQ-row boxes for q/do
+  CUtensorMap tkr;              // MLA shared rope keys [B, S, 1, 64] (rope_shared; tk: nope keys)
+  int rope_shared;
+  float* dk_rope_acc;           // rope_shared: [B, S, 64] fp32, dK's rope columns summed over heads
   CUtensorMap tdq;              // fused kernel: fp32 dQ accumulator, 32-column x 128-row boxes
   float* dq_acc;                // fused kernel: [B, S, Hq, Dqk] fp32, zeroed by the preprocess
   int q_lo, q_hi;               // fused kernel: query slots that take part ([0, S) except per shard)

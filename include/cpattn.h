@@ -145,6 +145,39 @@ int cp_attn_bwd_shard(const void* q, const void* k, const void* v, const void* o
                       float* dv_part, cudaStream_t stream);
 
 /*
+ * MLA with the rope key shared by all heads ("Add support for EP to context
+ * parallelism in self-attention", Main code changes: MLA attention under
+ * context parallelism; the shared rope key is the DeepSeek-V3 form of it):
+ * each head's key is its own 128-column "nope" part followed by one 64-column
+ * rope key per token that every head uses, so K is never materialised per
+ * head.  The attention is exactly cp_attn_fwd / cp_attn_bwd with
+ * Hq = Hkv = H, Dqk = 192, Dv = 128 and k[b, s, h] = concat(k_nope[b, s, h],
+ * k_rope[b, s]); scale = 1/sqrt(192).
+ *   q        bf16 [B, S, H, 192], device (nope columns, then rope columns)
+ *   k_nope   bf16 [B, S, H, 128], device
+ *   k_rope   bf16 [B, S, 64], device (one rope key per token)
+ *   v        bf16 [B, S, H, 128], device
+ *   out, lse as cp_attn_fwd (out [B, S, H, 128], lse fp32 [B, H, S]).
+ * Order and load_balance as cp_attn_fwd; all token-indexed tensors in the
+ * same order.
+ */
+int cp_attn_fwd_mla(const void* q, const void* k_nope, const void* k_rope, const void* v, void* out,
+                    float* lse, int B, int H, int S, int cp, int load_balance, cudaStream_t stream);
+
+/*
+ * Backward of cp_attn_fwd_mla: dq [B, S, H, 192], dk_nope [B, S, H, 128],
+ * dv [B, S, H, 128] as cp_attn_bwd, and dk_rope bf16 [B, S, 64] = the rope
+ * columns of every head's dk summed over the heads (the gradient of the
+ * shared rope key).  All outputs are device buffers, overwritten.  The rope
+ * sum goes through an fp32 scratch buffer of B*S*64 floats (library-owned,
+ * grown on demand) by atomic adds whose order varies, so dk_rope may differ
+ * in its last bits between calls.
+ */
+int cp_attn_bwd_mla(const void* q, const void* k_nope, const void* k_rope, const void* v, const void* out,
+                    const float* lse, const void* dout, void* dq, void* dk_nope, void* dk_rope, void* dv,
+                    int B, int H, int S, int cp, int load_balance, cudaStream_t stream);
+
+/*
  * Grouped-query decode attention ("Add Pallas GPU decode attention in
  * Maxtext inference", Description: decode attention through a GQA kernel):
  * one query token per sequence against a KV cache.

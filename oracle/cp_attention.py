@@ -35,6 +35,14 @@ Maxtext inference" (#1066)):
   the "dot_product without sharding" that the unit test of "Add support for
   EP to context parallelism", Description ("Verify attention output logit
   against dot product") compares the sharded kernel with.
+* ``mla_key`` / ``cp_attention_mla_fwd`` / ``cp_attention_mla_bwd`` -- MLA
+  attention under context parallelism ("Add support for EP to context
+  parallelism in self-attention", Main code changes) with the key's rope
+  part shared by every head: each head's key is its own "nope" columns
+  followed by the token's single rope key.  The key is materialised per head
+  here and the plain context-parallel attention above is applied; the rope
+  key's gradient is the sum over heads of the rope columns of the per-head
+  key gradients (the chain rule through the broadcast).
 * ``gqa_decode`` -- one query token per sequence against a KV cache,
   grouped-query heads ("Add Pallas GPU decode attention", Description:
   ``pallas_decode_attention.gqa`` replaces dot-product decode attention).
@@ -63,6 +71,7 @@ __all__ = [
     "causal_attention_fwd", "causal_attention_bwd",
     "cp_attention_fwd", "cp_attention_bwd",
     "shard_pair_counts", "gqa_decode", "gqa_decode_int8",
+    "mla_key", "cp_attention_mla_fwd", "cp_attention_mla_bwd",
 ]
 
 _ROW_BLOCK = 512
@@ -257,6 +266,31 @@ def cp_attention_bwd(q, k, v, out, lse, dout, cp, load_balance=True, scale=None)
         dk += dks
         dv += dvs
     return dq, dk, dv
+
+
+
+def mla_key(k_nope, k_rope):
+    """Per-head key of MLA with a shared rope part: k_nope [B,S,H,Dn] (one per
+    head) and k_rope [B,S,Dr] (one per token, used by every head) give
+    [B,S,H,Dn+Dr], each head's nope columns followed by the rope key."""
+    B, S, H, _ = k_nope.shape
+    rope = np.broadcast_to(k_rope[:, :, None, :], (B, S, H, k_rope.shape[-1]))
+    return np.concatenate([k_nope, rope], axis=-1)
+
+
+def cp_attention_mla_fwd(q, k_nope, k_rope, v, cp, load_balance=True, scale=None):
+    """``cp_attention_fwd`` with the key built by ``mla_key`` (scale defaults
+    to 1/sqrt(Dn+Dr), the full key width)."""
+    return cp_attention_fwd(q, mla_key(k_nope, k_rope), v, cp, load_balance, scale)
+
+
+def cp_attention_mla_bwd(q, k_nope, k_rope, v, out, lse, dout, cp, load_balance=True, scale=None):
+    """Gradients of ``cp_attention_mla_fwd``: dq, dk_nope [B,S,H,Dn], dk_rope
+    [B,S,Dr] (the rope columns of the per-head key gradient summed over the
+    heads, since every head reads the same rope key) and dv."""
+    dq, dk, dv = cp_attention_bwd(q, mla_key(k_nope, k_rope), v, out, lse, dout, cp, load_balance, scale)
+    Dn = k_nope.shape[-1]
+    return dq, dk[..., :Dn], dk[..., Dn:].sum(axis=2), dv
 
 
 def shard_pair_counts(S, cp, load_balance=True):

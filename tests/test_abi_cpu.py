@@ -84,6 +84,13 @@ def test_bad_arguments_are_rejected_on_host():
     assert lib.cp_attn_bwd(*([P] * 9), 1, 4, 4, 768, 128, 128, 2, 2, None) == -2
     # per-shard backward: shard out of range
     assert lib.cp_attn_bwd_shard(*([P] * 9), 1, 4, 4, 256, 128, 128, 2, 1, 2, P, P, None) == -1
+    # MLA with shared rope keys: null rope keys, S not a multiple of 2cp, misaligned pointer
+    assert lib.cp_attn_fwd_mla(P, P, None, P, P, P, 1, 4, 256, 2, 1, None) == -1
+    assert lib.cp_attn_fwd_mla(P, P, P, P, P, P, 1, 4, 250, 2, 1, None) == -1
+    assert lib.cp_attn_bwd_mla(*([P] * 11), 1, 4, 250, 2, 1, None) == -1
+    assert lib.cp_attn_bwd_mla(P, P, None, *([P] * 8), 1, 4, 256, 2, 1, None) == -1
+    assert lib.cp_attn_bwd_mla(P, ctypes.c_void_p(0x1008), *([P] * 9), 1, 4, 256, 2, 1, None) == -1
+    assert "aligned" in _err()
     # decode: group too large, bad head dim, null lens
     assert lib.gqa_decode(P, P, P, P, P, 1, 64, 2, 128, 128, None) == -2
     assert lib.gqa_decode(P, P, P, P, P, 1, 8, 2, 128, 96, None) == -2

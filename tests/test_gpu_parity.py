@@ -345,3 +345,58 @@ def test_decode_int8_edge_lengths():
                             vs.numpy().astype(np.float64), lens.numpy())
     assert torch.all(out[0] == 0)
     assert_close_out(_f64(out), ref, "int8 decode edge lengths")
+
+
+# ---------------------------------------------------------------------------
+# MLA with the rope key shared by the heads
+# ---------------------------------------------------------------------------
+
+def _mla_inputs(B, S, H, seed):
+    q, kfull, v, dout = synth.attention_inputs(B, S, H, H, 192, 128, seed=seed)
+    kn = kfull[..., :128].contiguous()
+    kr = kfull[:, :, 0, 128:].contiguous()  # one 64-column rope key per token
+    return q, kn, kr, v, dout
+
+
+@pytest.mark.parametrize("cfg", [(1, 384, 2, 2, True), (2, 256, 3, 2, True), (1, 512, 4, 4, False)])
+def test_mla_shared_rope_parity(cfg):
+    B, S, H, cp, lb = cfg
+    q, kn, kr, v, dout = _mla_inputs(B, S, H, seed=19)
+    dev = [x.cuda() for x in (q, kn, kr, v, dout)]
+    if lb:
+        dev = [cp_.lb_permute(x, cp) for x in dev]
+    qd, knd, krd, vd, dd = dev
+    out, lse = cp_.attn_fwd_mla(qd, knd, krd, vd, cp, lb)
+    dq, dkn, dkr, dv = cp_.attn_bwd_mla(qd, knd, krd, vd, out, lse, dd, cp, lb)
+    torch.cuda.synchronize()
+    cp_.check_device()
+    pos = O.lb_positions(S, cp, lb)
+    qs, kns, krs, vs, ds = (O.permute(_f64(x), pos) for x in (q, kn, kr, v, dout))
+    o_ref, l_ref = O.cp_attention_mla_fwd(qs, kns, krs, vs, cp, lb)
+    assert_close_out(_f64(out), o_ref, "mla out %s" % (cfg,))
+    err = float(np.max(np.abs(lse.cpu().numpy().astype(np.float64) - l_ref)))
+    assert err <= 1e-2, "mla lse max-abs %.3e" % err
+    g_ref = O.cp_attention_mla_bwd(qs, kns, krs, vs, o_ref, l_ref, ds, cp, lb)
+    for got, want, name in zip((dq, dkn, dkr, dv), g_ref, ("dq", "dk_nope", "dk_rope", "dv")):
+        assert_close_grad(_f64(got), want, "mla %s %s" % (name, cfg))
+
+
+def test_mla_shared_rope_matches_materialised_key():
+    """The shared rope key gives what the per-head key concat(k_nope, k_rope)
+    gives through the plain MLA path: out, lse, dq, dv bit for bit (the same
+    tiles), dk_nope equal to that path's nope columns, dk_rope to the sum over
+    heads of its rope columns."""
+    B, S, H, cp = 1, 512, 4, 2
+    q, kn, kr, v, dout = (cp_.lb_permute(x.cuda(), cp) for x in _mla_inputs(B, S, H, seed=23))
+    kfull = torch.cat([kn, kr[:, :, None, :].expand(B, S, H, 64)], dim=-1).contiguous()
+    out1, lse1 = cp_.attn_fwd_mla(q, kn, kr, v, cp, True)
+    out2, lse2 = cp_.attn_fwd(q, kfull, v, cp, True)
+    dq1, dkn1, dkr1, dv1 = cp_.attn_bwd_mla(q, kn, kr, v, out1, lse1, dout, cp, True)
+    dq2, dk2, dv2 = cp_.attn_bwd(q, kfull, v, out2, lse2, dout, cp, True)
+    torch.cuda.synchronize()
+    cp_.check_device()
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    assert torch.equal(dq1, dq2) and torch.equal(dv1, dv2)
+    assert torch.equal(dkn1, dk2[..., :128])
+    want = dk2[..., 128:].double().sum(dim=2)
+    assert_close_grad(_f64(dkr1), want.cpu().numpy(), "dk_rope vs summed rope columns")

@@ -322,6 +322,50 @@ def test_bwd_finite_differences(lb):
     np.testing.assert_allclose(dv, _fd_grad(f, v), rtol=1e-6, atol=1e-8)
 
 
+
+def _mla_brute_key(k_nope, k_rope):
+    """Per-head key written out entry by entry: head h of token s is its
+    nope columns, then the token's rope key."""
+    B, S, H, Dn = k_nope.shape
+    Dr = k_rope.shape[-1]
+    k = np.zeros((B, S, H, Dn + Dr))
+    for b in range(B):
+        for s_ in range(S):
+            for h in range(H):
+                for d in range(Dn):
+                    k[b, s_, h, d] = k_nope[b, s_, h, d]
+                for d in range(Dr):
+                    k[b, s_, h, Dn + d] = k_rope[b, s_, d]
+    return k
+
+
+@pytest.mark.parametrize("lb", [False, True])
+def test_mla_shared_rope_key(lb):
+    """MLA with one rope key per token shared by the heads: the forward equals
+    brute-force attention with that key written out per head, and the
+    gradients (above all the rope key's, which collects every head's
+    contribution) match finite differences of sum(out * dout)."""
+    rng = np.random.default_rng(21)
+    B, S, H, Dn, Dr, Dv, cp = 1, 8, 3, 3, 2, 2, 2
+    q = _rand((B, S, H, Dn + Dr), rng)
+    kn = _rand((B, S, H, Dn), rng)
+    kr = _rand((B, S, Dr), rng)
+    v = _rand((B, S, H, Dv), rng)
+    dout = _rand((B, S, H, Dv), rng)
+    pos = O.lb_positions(S, cp, lb)
+    o, l = O.cp_attention_mla_fwd(q, kn, kr, v, cp, lb)
+    ob, lbr = _brute_fwd(q, _mla_brute_key(kn, kr), v, pos, pos)
+    np.testing.assert_allclose(o, ob, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l, lbr, rtol=1e-12, atol=1e-12)
+    dq, dkn, dkr, dv = O.cp_attention_mla_bwd(q, kn, kr, v, o, l, dout, cp, lb)
+    assert dkr.shape == (B, S, Dr) and dkn.shape == (B, S, H, Dn)
+    f = lambda: float(np.sum(_brute_fwd(q, _mla_brute_key(kn, kr), v, pos, pos)[0] * dout))  # noqa: E731
+    np.testing.assert_allclose(dkr, _fd_grad(f, kr), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dkn, _fd_grad(f, kn), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dq, _fd_grad(f, q), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dv, _fd_grad(f, v), rtol=1e-6, atol=1e-8)
+
+
 def test_bwd_shift_invariants():
     """Adding one vector to every key shifts each row of scores by a
     constant, so sum_j dk_j = 0; adding one vector c to every value adds c
