@@ -38,6 +38,9 @@ WORKLOADS = {
                                    q_scale=1.0),
     "deepseek_v3_mla_s32768_cp4": dict(B=1, S=32768, Hq=128, Hkv=128, Dqk=192, Dv=128, cp=4, lb=True,
                                        q_scale=1.0),
+    # the same with one 64-column rope key per token shared by the heads (k_nope per head)
+    "deepseek_v3_mla_rope_s32768_cp4": dict(B=1, S=32768, Hq=128, Hkv=128, Dqk=192, Dv=128, cp=4, lb=True,
+                                            q_scale=1.0, rope=True),
     "tiny_s256_cp2": dict(B=1, S=256, Hq=2, Hkv=2, Dqk=64, Dv=64, cp=2, lb=True, q_scale=1.0),
 }
 DECODE = dict(B=24, Hq=32, Hkv=8, D=128, Smax=2048, lo=1024, hi=2048)
@@ -320,6 +323,11 @@ def run_ours(args, w, wname):
     B, S, Hq, Hkv, Dqk, Dv, cp, lb = (w[k] for k in ("B", "S", "Hq", "Hkv", "Dqk", "Dv", "cp", "lb"))
     q, k, v, dout = synth.attention_inputs_device(B, S, Hq, Hkv, Dqk, Dv, seed=args.seed + 1000 * rank,
                                                   q_scale=w["q_scale"], device=dev)
+    rope = bool(w.get("rope"))
+    kr = None
+    if rope:  # per-head nope keys and one rope key per token (the other extras assume one key tensor)
+        k, kr = k[..., :128].contiguous(), k[:, :, 0, 128:].contiguous()
+        args.no_extras = True
     D = DECODE
     dq_, dkc, dvc, dlens = synth.decode_inputs(D["B"], D["Hq"], D["Hkv"], D["D"], D["Smax"], D["lo"], D["hi"],
                                                seed=args.seed + 4)
@@ -333,6 +341,8 @@ def run_ours(args, w, wname):
     dq_p, dk_p, dv_p = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     out_n, dq_n, dk_n, dv_n = (torch.empty_like(x) for x in (out_p, q, k, v))
     dec_out = torch.empty_like(dq_)
+    if rope:
+        krp, dkr_p, dkr_n = (torch.empty_like(kr) for _ in range(3))
 
     def step(qi=q, ki=k, vi=v, di=dout, dqi=dq_, dkci=dkc, dvci=dvc, dli=dlens):
         if lb:
@@ -343,13 +353,23 @@ def run_ours(args, w, wname):
             a, bk, c, d = qp, kp, vp, dop
         else:
             a, bk, c, d = qi, ki, vi, di
-        cpattn.attn_fwd(a, bk, c, cp, lb, out_p, lse)
-        cpattn.attn_bwd(a, bk, c, out_p, lse, d, cp, lb, dq_p, dk_p, dv_p)
+        if rope:
+            kri = kr
+            if lb:
+                cpattn.lb_permute(kr, cp, krp)
+                kri = krp
+            cpattn.attn_fwd_mla(a, bk, kri, c, cp, lb, out_p, lse)
+            cpattn.attn_bwd_mla(a, bk, kri, c, out_p, lse, d, cp, lb, dq_p, dk_p, dkr_p, dv_p)
+        else:
+            cpattn.attn_fwd(a, bk, c, cp, lb, out_p, lse)
+            cpattn.attn_bwd(a, bk, c, out_p, lse, d, cp, lb, dq_p, dk_p, dv_p)
         if lb:
             cpattn.lb_unpermute(out_p, cp, out_n)
             cpattn.lb_unpermute(dq_p, cp, dq_n)
             cpattn.lb_unpermute(dk_p, cp, dk_n)
             cpattn.lb_unpermute(dv_p, cp, dv_n)
+            if rope:
+                cpattn.lb_unpermute(dkr_p, cp, dkr_n)
         cpattn.gqa_decode(dqi, dkci, dvci, dli, dec_out)
 
     for _ in range(args.warmup):
@@ -421,7 +441,9 @@ def run_ours(args, w, wname):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wname, "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "Dqk": Dqk, "Dv": Dv, "cp": cp,
-                   "load_balance": lb, "decode": "B=24 Hq=32 Hkv=8 D=128 Smax=2048 lens~U[1024,2048]",
+                   "load_balance": lb, **({"k_rope": "one 64-column rope key per token, shared by the heads"}
+                                          if rope else {}),
+                   "decode": "B=24 Hq=32 Hkv=8 D=128 Smax=2048 lens~U[1024,2048]",
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2 (q,k,v,dout %.0f MB + decode KV %.0f MB per step)" % (
                        4 * q.numel() * 2 / 1e6, 2 * dkc.numel() * 2 / 1e6)},

@@ -234,15 +234,18 @@ def attn_fwd_mla(q, k_nope, k_rope, v, cp, load_balance=True, out=None, lse=None
     return out, lse
 
 
-def attn_bwd_mla(q, k_nope, k_rope, v, out, lse, dout, cp, load_balance=True):
+def attn_bwd_mla(q, k_nope, k_rope, v, out, lse, dout, cp, load_balance=True, dq=None, dk_nope=None, dk_rope=None,
+                 dv=None):
     """dq, dk_nope, dk_rope (summed over heads), dv of sum(out * dout) for
     ``attn_fwd_mla``."""
     B, S, H = _mla_shapes(q, k_nope, k_rope, v)
     _need(out, torch.bfloat16, "out", 4)
     _need(dout, torch.bfloat16, "dout", 4)
     _need(lse, torch.float32, "lse", 3)
-    dq, dk_nope, dk_rope, dv = (torch.empty_like(q), torch.empty_like(k_nope), torch.empty_like(k_rope),
-                                torch.empty_like(v))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk_nope = torch.empty_like(k_nope) if dk_nope is None else dk_nope
+    dk_rope = torch.empty_like(k_rope) if dk_rope is None else dk_rope
+    dv = torch.empty_like(v) if dv is None else dv
     _check(load().cp_attn_bwd_mla(_ptr(q), _ptr(k_nope), _ptr(k_rope), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
                                   _ptr(dq), _ptr(dk_nope), _ptr(dk_rope), _ptr(dv), B, H, S, cp, _lb(load_balance),
                                   _stream(q)))
