@@ -495,9 +495,10 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     regs_inc<kRegsEw>();
     // ------------------------------------------------------------ element-wise warps
     // Group g (warps 4g..4g+3) owns query columns [64g, 64g+64) of S^T/dP^T
-    // (thread = key row = TMEM lane) and dQ columns [gD/2, (g+1)D/2) (thread =
-    // query row).  A failed wait (abort or timeout) runs on with whatever is in
-    // TMEM, so every role walks all of its steps and every wait stays bounded.
+    // (thread = key row = TMEM lane) and, at the end of a unit, dV/dK columns
+    // [gD/2, (g+1)D/2).  A failed wait (abort or timeout) runs on with whatever
+    // is in TMEM, so every role walks all of its steps and every wait stays
+    // bounded.
     const int g = warp >> 2;
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
