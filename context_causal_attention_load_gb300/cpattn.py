@@ -67,6 +67,7 @@ def load(path=None):
         "gqa_decode_int8": [_P] * 7 + [_I] * 5 + [_P],
         "cp_lb_positions": [_I, _I, _I, ctypes.POINTER(ctypes.c_int)],
         "cp_attn_tile_counts": [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)],
+        "cp_attn_fwd_schedule": [_I] * 7 + [ctypes.POINTER(ctypes.c_longlong)],
         "cp_attn_check_device": [_P],
         "cp_attn_release": [],
         "cp_attn_profile_start": [],
@@ -272,6 +273,14 @@ def lb_positions(S, cp, load_balance=True):
     _check(load().cp_lb_positions(S, cp, _lb(load_balance), arr))
     return list(arr)
 
+
+
+def fwd_schedule(B, Hq, Hkv, S, cp, load_balance, num_ctas):
+    """Modelled load of each of num_ctas CTAs under the forward's work plan
+    (host only: no device work)."""
+    arr = (ctypes.c_longlong * num_ctas)()
+    _check(load().cp_attn_fwd_schedule(B, Hq, Hkv, S, cp, _lb(load_balance), num_ctas, arr))
+    return list(arr)
 
 def tile_counts(S, cp, load_balance=True):
     arr = (ctypes.c_longlong * cp)()

@@ -258,7 +258,8 @@ int upload(DevBuf<T>& b, const std::vector<T>& v) {
 // more than the model says (a full Llama2-shaped forward ran 6% slower under
 // it for a modelled 1% gain).
 template <typename U>
-int upload_plan(std::vector<std::pair<long long, U>> w, int num_sms, UnitPlan<U>& plan) {
+void plan_units(std::vector<std::pair<long long, U>> w, int num_sms, std::vector<U>& units,
+                std::vector<int>& off, std::vector<long long>* cta_cost = nullptr) {
   std::stable_sort(w.begin(), w.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
   const int ncta = (int)std::min<size_t>(w.size(), (size_t)std::max(1, num_sms));
   const size_t n = w.size();
@@ -307,16 +308,27 @@ int upload_plan(std::vector<std::pair<long long, U>> w, int num_sms, UnitPlan<U>
   }
   std::vector<std::vector<U>> lists(ncta);
   for (size_t i = 0; i < n; ++i) lists[bin[i]].push_back(w[i].second);
-  std::vector<U> units;
-  std::vector<int> off(ncta + 1, 0);
+  units.clear();
+  off.assign(ncta + 1, 0);
   for (int c = 0; c < ncta; ++c) {
     off[c] = (int)units.size();
     units.insert(units.end(), lists[c].begin(), lists[c].end());
   }
   off[ncta] = (int)units.size();
+  if (cta_cost) {
+    cta_cost->assign(ncta, 0);
+    for (size_t i = 0; i < n; ++i) (*cta_cost)[bin[i]] += w[i].first;
+  }
+}
+
+template <typename U>
+int upload_plan(std::vector<std::pair<long long, U>> w, int num_sms, UnitPlan<U>& plan) {
+  std::vector<U> units;
+  std::vector<int> off;
+  plan_units(std::move(w), num_sms, units, off);
   int rc = upload(plan.units, units);
   if (!rc) rc = upload(plan.off, off);
-  plan.ncta = ncta;
+  plan.ncta = (int)off.size() - 1;
   return rc;
 }
 
@@ -836,6 +848,21 @@ int cp_attn_tile_counts(int S, int cp, int load_balance, long long* per_shard_ho
     const int s = std::min(cp - 1, (qt * kTile) / per);
     per_shard_host[s] += count_kv_tiles(pm, tile_max_pos(pm, qt, kTile));
   }
+  return CPATTN_OK;
+}
+
+int cp_attn_fwd_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance, int num_ctas,
+                         long long* cta_cost_host) {
+  if (!cta_cost_host) return fail(CPATTN_ERR_INVALID_ARG, "null cta_cost_host");
+  if (num_ctas < 1) return fail(CPATTN_ERR_INVALID_ARG, "num_ctas must be >= 1");
+  AttnShape sh{B, Hq, Hkv, S, 128, 128, cp, load_balance};
+  int rc = check_attn(sh);
+  if (rc) return rc;
+  std::vector<FwdUnit> units;
+  std::vector<int> off;
+  std::vector<long long> cost;
+  plan_units(build_fwd_units(sh, -1), num_ctas, units, off, &cost);
+  for (int c = 0; c < num_ctas; ++c) cta_cost_host[c] = c < (int)cost.size() ? cost[c] : 0;
   return CPATTN_OK;
 }
 

@@ -247,6 +247,18 @@ int cp_lb_positions(int S, int cp, int load_balance, int* pos_host);
 int cp_attn_tile_counts(int S, int cp, int load_balance, long long* per_shard_host);
 
 /*
+ * Host helper: the plan the forward uses on a GPU with num_ctas SMs.  The
+ * forward's work units (pairs of 128-row query tiles sharing a KV head) are
+ * dealt to min(units, num_ctas) CTAs so that the most-loaded CTA carries as
+ * little as possible; cta_cost_host[c] (host, num_ctas entries) receives the
+ * modelled load of CTA c, a unit costing (its key steps + 4) per query tile it
+ * holds; CTAs without units get 0.  Shapes as cp_attn_fwd (head dims do not
+ * enter the plan).  No device work; returns CPATTN_OK or an argument error.
+ */
+int cp_attn_fwd_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance, int num_ctas,
+                         long long* cta_cost_host);
+
+/*
  * Kernel timing for profiling and benchmarks.  Between profile_start and
  * profile_stop every kernel the library launches is bracketed by two CUDA
  * events recorded on its own stream.  profile_stop waits for those events

@@ -98,3 +98,39 @@ def test_bad_arguments_are_rejected_on_host():
     # int8 decode: head dim, null scales
     assert lib.gqa_decode_int8(P, P, P, P, P, P, P, 1, 8, 2, 128, 64, None) == -2
     assert lib.gqa_decode_int8(P, P, P, None, P, P, P, 1, 8, 2, 128, 128, None) == -1
+
+
+def _schedule(B, Hq, Hkv, S, cp, lb, n):
+    arr = (ctypes.c_longlong * n)()
+    assert lib.cp_attn_fwd_schedule(B, Hq, Hkv, S, cp, lb, n, arr) == 0, _err()
+    return list(arr)
+
+
+def test_fwd_schedule_by_hand():
+    """S = 256 with one head: the two 128-row query tiles form one unit that
+    walks both key tiles, cost (2 steps + 4) x 2 tiles, on the first CTA."""
+    assert _schedule(1, 1, 1, 256, 2, 0, 4) == [12, 0, 0, 0]
+    assert _schedule(1, 1, 1, 256, 2, 1, 4) == [12, 0, 0, 0]
+    # one more query tile (S = 384, natural order): units (tiles 0,1) and (tile 2)
+    assert sorted(_schedule(1, 1, 1, 384, 1, 0, 2)) == [7, 12]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,cp", [(1, 32, 32, 8192, 4), (4, 32, 32, 8192, 4), (1, 64, 8, 16384, 8)])
+def test_fwd_schedule_balance(B, Hq, Hkv, S, cp):
+    """Every CTA gets work, the total does not depend on how many CTAs share
+    it, the plan is deterministic, and with several units per CTA the most
+    loaded CTA is within 3% of the mean."""
+    c152 = _schedule(B, Hq, Hkv, S, cp, 1, 152)
+    assert min(c152) > 0
+    total = sum(c152)
+    assert sum(_schedule(B, Hq, Hkv, S, cp, 1, 100)) == total
+    assert _schedule(B, Hq, Hkv, S, cp, 1, 1) == [total]
+    assert _schedule(B, Hq, Hkv, S, cp, 1, 152) == c152
+    assert max(c152) <= 1.03 * total / 152
+
+
+def test_fwd_schedule_rejects_bad_arguments():
+    arr = (ctypes.c_longlong * 4)()
+    assert lib.cp_attn_fwd_schedule(1, 1, 1, 256, 2, 1, 0, arr) == -1
+    assert lib.cp_attn_fwd_schedule(1, 1, 1, 250, 2, 1, 4, arr) == -1
+    assert lib.cp_attn_fwd_schedule(1, 1, 1, 256, 2, 1, 4, None) == -1
