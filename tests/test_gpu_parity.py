@@ -400,3 +400,28 @@ def test_mla_shared_rope_matches_materialised_key():
     assert torch.equal(dkn1, dk2[..., :128])
     want = dk2[..., 128:].double().sum(dim=2)
     assert_close_grad(_f64(dkr1), want.cpu().numpy(), "dk_rope vs summed rope columns")
+
+
+def test_mla_shared_rope_zero_copy():
+    """load_balance=2 with the shared rope key: natural-order tensors give
+    permute -> attend -> unpermute's results (out, lse, dq, dk_nope, dv bit for
+    bit; dk_rope to its summation order)."""
+    B, S, H, cp = 1, 512, 2, 2
+    nat = [x.cuda() for x in _mla_inputs(B, S, H, seed=29)]
+    out2, lse2 = cp_.attn_fwd_mla(*nat[:4], cp, 2)
+    g2 = cp_.attn_bwd_mla(*nat[:4], out2, lse2, nat[4], cp, 2)
+    perm = [cp_.lb_permute(x, cp) for x in nat]
+    out1, lse1 = cp_.attn_fwd_mla(*perm[:4], cp, 1)
+    g1 = cp_.attn_bwd_mla(*perm[:4], out1, lse1, perm[4], cp, 1)
+    torch.cuda.synchronize()
+    cp_.check_device()
+    pos = torch.from_numpy(O.lb_positions(S, cp, True)).long()
+    lse1_nat = torch.empty_like(lse1)
+    lse1_nat[:, :, pos.cuda()] = lse1
+    assert torch.equal(out2, cp_.lb_unpermute(out1, cp)) and torch.equal(lse2, lse1_nat)
+    for a2, a1, name in zip(g2, g1, ("dq", "dk_nope", "dk_rope", "dv")):
+        a1n = cp_.lb_unpermute(a1, cp)
+        if name == "dk_rope":
+            assert_close_grad(_f64(a2), _f64(a1n), "zero-copy dk_rope")
+        else:
+            assert torch.equal(a2, a1n), name
