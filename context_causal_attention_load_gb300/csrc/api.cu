@@ -724,7 +724,8 @@ int cp_attn_bwd_shard(const void* q, const void* k, const void* v, const void* o
 
 int cp_attn_fwd_mla(const void* q, const void* k_nope, const void* k_rope, const void* v, void* out, float* lse,
                     int B, int H, int S, int cp, int load_balance, cudaStream_t stream) {
-  if (!k_rope) return fail(CPATTN_ERR_INVALID_ARG, "null pointer");
+  int rc = check_ptrs({k_rope});
+  if (rc) return rc;
   AttnShape sh{B, H, H, S, 192, 128, cp, load_balance};
   return fwd_impl(q, k_nope, v, out, lse, sh, -1, stream, k_rope);
 }

@@ -86,6 +86,8 @@ def test_bad_arguments_are_rejected_on_host():
     assert lib.cp_attn_bwd_shard(*([P] * 9), 1, 4, 4, 256, 128, 128, 2, 1, 2, P, P, None) == -1
     # MLA with shared rope keys: null rope keys, S not a multiple of 2cp, misaligned pointer
     assert lib.cp_attn_fwd_mla(P, P, None, P, P, P, 1, 4, 256, 2, 1, None) == -1
+    assert lib.cp_attn_fwd_mla(P, P, ctypes.c_void_p(0x1008), P, P, P, 1, 4, 256, 2, 1, None) == -1
+    assert "aligned" in _err()
     assert lib.cp_attn_fwd_mla(P, P, P, P, P, P, 1, 4, 250, 2, 1, None) == -1
     assert lib.cp_attn_bwd_mla(*([P] * 11), 1, 4, 250, 2, 1, None) == -1
     assert lib.cp_attn_bwd_mla(P, P, None, *([P] * 8), 1, 4, 256, 2, 1, None) == -1
