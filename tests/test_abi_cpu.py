@@ -136,3 +136,22 @@ def test_fwd_schedule_rejects_bad_arguments():
     assert lib.cp_attn_fwd_schedule(1, 1, 1, 256, 2, 1, 0, arr) == -1
     assert lib.cp_attn_fwd_schedule(1, 1, 1, 250, 2, 1, 4, arr) == -1
     assert lib.cp_attn_fwd_schedule(1, 1, 1, 256, 2, 1, 4, None) == -1
+
+
+def test_binding_checks_tensors_before_the_library():
+    """The Python binding refuses host tensors, wrong dtypes and wrong MLA
+    shapes itself (no device is needed to see it)."""
+    import torch
+
+    from context_causal_attention_load_gb300 import cpattn
+    q = torch.zeros(1, 256, 2, 192, dtype=torch.bfloat16)
+    kn = torch.zeros(1, 256, 2, 128, dtype=torch.bfloat16)
+    kr = torch.zeros(1, 256, 64, dtype=torch.bfloat16)
+    v = torch.zeros(1, 256, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        cpattn.attn_fwd_mla(q, kn, kr, v, 2)
+    with pytest.raises(ValueError, match="CUDA"):
+        cpattn.attn_fwd(q, kn, v, 2)
+    with pytest.raises(ValueError):
+        cpattn.fwd_schedule(1, 1, 1, 256, 2, 3, 4)  # load_balance must be 0, 1 or 2
+    assert cpattn.fwd_schedule(1, 1, 1, 256, 2, True, 2) == [12, 0]
