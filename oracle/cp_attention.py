@@ -46,6 +46,16 @@ Maxtext inference" (#1066)):
 * ``gqa_decode`` -- one query token per sequence against a KV cache,
   grouped-query heads ("Add Pallas GPU decode attention", Description:
   ``pallas_decode_attention.gqa`` replaces dot-product decode attention).
+* ``mla_decode`` -- decode against an MLA latent cache in the absorbed form
+  (MLA under context parallelism: "Add support for EP to context parallelism
+  in self-attention", Main code changes; one query token per sequence:
+  "Add Pallas GPU decode attention", Description): every head's key at
+  position t is the token's cached latent vector (its compressed KV followed
+  by its rope key) and its value is the compressed-KV part of the same
+  vector, so all query heads share one cached row per token.  The query of a
+  head is its nope query taken into the latent space, followed by its rope
+  query.  Per (b, h): softmax over t < lens[b] of scale * q . ckv_t, times
+  ckv_t[:Dv].
 * ``gqa_decode_int8`` -- the same against an int8-quantised KV cache (the
   inference setup of "rename context to context_autoregressive", Tests, runs
   with ``quantize_kvcache=True``): each cached vector is stored as int8
@@ -71,7 +81,7 @@ __all__ = [
     "causal_attention_fwd", "causal_attention_bwd",
     "cp_attention_fwd", "cp_attention_bwd",
     "shard_pair_counts", "gqa_decode", "gqa_decode_int8",
-    "mla_key", "cp_attention_mla_fwd", "cp_attention_mla_bwd",
+    "mla_key", "cp_attention_mla_fwd", "cp_attention_mla_bwd", "mla_decode",
 ]
 
 _ROW_BLOCK = 512
@@ -337,3 +347,30 @@ def gqa_decode_int8(q, kq, vq, kscale, vscale, lens, scale=None):
     k = np.asarray(kq, np.float64) * np.asarray(kscale, np.float64)[..., None]
     v = np.asarray(vq, np.float64) * np.asarray(vscale, np.float64)[..., None]
     return gqa_decode(q, k, v, lens, scale)
+
+
+def mla_decode(q, ckv, lens, dv=512, scale=None):
+    """Absorbed-MLA decode: q [B,H,Dk] (each head's latent query, then its rope
+    query), ckv [B,Smax,Dk] (each token's latent row: compressed KV, then rope
+    key), lens [B] -> out [B,H,dv] in the latent space:
+        out[b,h] = sum_{t<lens[b]} softmax_t(scale * q[b,h] . ckv[b,t]) ckv[b,t,:dv].
+    scale defaults to 1/sqrt(192), the softmax scale of the attention the
+    absorption comes from (a 128-column nope plus 64-column rope head)."""
+    q = np.asarray(q, np.float64)
+    ckv = np.asarray(ckv, np.float64)
+    B, H, Dk = q.shape
+    if ckv.shape[0] != B or ckv.shape[2] != Dk:
+        raise ValueError("q and ckv shapes do not match")
+    if scale is None:
+        scale = 1.0 / math.sqrt(192.0)
+    out = np.zeros((B, H, dv))
+    for b in range(B):
+        n = int(lens[b])
+        if n <= 0:
+            continue
+        rows = ckv[b, :n, :]
+        s = scale * (q[b] @ rows.T)  # [H, n]
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        out[b] = (p @ rows[:, :dv]) / p.sum(axis=1, keepdims=True)
+    return out

@@ -526,3 +526,70 @@ def test_decode_int8_key_scale_acts_like_query_scale():
     a = O.gqa_decode_int8(q, kq, vq, 2.5 * ks, vs, lens)
     b = O.gqa_decode_int8(2.5 * q, kq, vq, ks, vs, lens)
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# absorbed-MLA decode
+# --------------------------------------------------------------------------
+
+def test_mla_decode_brute_force():
+    """Element-by-element loops on a tiny latent cache."""
+    rng = np.random.default_rng(41)
+    B, H, Dk, Dv, Smax = 2, 3, 8, 6, 5
+    q = _rand((B, H, Dk), rng)
+    ckv = _rand((B, Smax, Dk), rng)
+    lens = [5, 3]
+    sc = 0.37
+    got = O.mla_decode(q, ckv, lens, dv=Dv, scale=sc)
+    for b in range(B):
+        for h in range(H):
+            sc_t = [sc * sum(q[b, h, i] * ckv[b, t, i] for i in range(Dk)) for t in range(lens[b])]
+            mx = max(sc_t)
+            w = [math.exp(x - mx) for x in sc_t]
+            for d in range(Dv):
+                want = sum(w[t] * ckv[b, t, d] for t in range(lens[b])) / sum(w)
+                assert abs(got[b, h, d] - want) < 1e-12
+
+
+def test_mla_decode_equals_unabsorbed_mla():
+    """The absorbed form against MLA written out per head: key of head h at
+    position t = (its nope key W_uk[h] c_t, the token's rope key r_t), value =
+    W_uv[h] c_t, query = (q_nope[h], q_rope[h]).  Decoding that per-head cache
+    with the plain GQA decode and projecting the latent output with W_uv
+    must agree: q_nope . (W_uk c) = (W_uk^T q_nope) . c by associativity."""
+    rng = np.random.default_rng(42)
+    B, H, Dc, Dr, Dn, Smax = 2, 4, 16, 4, 6, 9
+    lens = np.array([9, 4])
+    c = _rand((B, Smax, Dc), rng)
+    r = _rand((B, Smax, Dr), rng)
+    w_uk = _rand((H, Dn, Dc), rng)
+    w_uv = _rand((H, Dn, Dc), rng)
+    q_nope = _rand((B, H, Dn), rng)
+    q_rope = _rand((B, H, Dr), rng)
+    sc = 1.0 / math.sqrt(Dn + Dr)
+    # written out per head
+    k_full = np.concatenate([np.einsum("hnc,bsc->bhsn", w_uk, c), np.broadcast_to(r[:, None], (B, H, Smax, Dr))],
+                            axis=-1)
+    v_full = np.einsum("hnc,bsc->bhsn", w_uv, c)
+    q_full = np.concatenate([q_nope, q_rope], axis=-1)
+    want = O.gqa_decode(q_full, k_full, v_full, lens, scale=sc)
+    # absorbed
+    q_abs = np.concatenate([np.einsum("hnc,bhn->bhc", w_uk, q_nope), q_rope], axis=-1)
+    ckv = np.concatenate([c, r], axis=-1)
+    lat = O.mla_decode(q_abs, ckv, lens, dv=Dc, scale=sc)
+    got = np.einsum("hnc,bhc->bhn", w_uv, lat)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_mla_decode_special_lengths():
+    """lens = 0 gives zeros; lens = 1 gives the first token's value exactly;
+    the default scale is 1/sqrt(192)."""
+    rng = np.random.default_rng(43)
+    q = _rand((2, 3, 10), rng)
+    ckv = _rand((2, 4, 10), rng)
+    out = O.mla_decode(q, ckv, [0, 1], dv=7)
+    assert np.all(out[0] == 0)
+    assert np.array_equal(out[1], np.broadcast_to(ckv[1, 0, :7], (3, 7)))
+    a = O.mla_decode(q, ckv, [4, 4], dv=7)
+    b = O.mla_decode(q, ckv, [4, 4], dv=7, scale=1.0 / math.sqrt(192.0))
+    assert np.array_equal(a, b)
