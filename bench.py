@@ -4,9 +4,14 @@
 One step = the whole hot path over one batch of seeded synthetic input:
   load-balance permute of q, k, v, dout -> forward (all cp shards) ->
   backward -> unpermute of out, dq, dk, dv -> one GQA decode batch.
-Default workload: the Llama2-7B-shaped attention layer (B=1, Hq=Hkv=32,
-S=8192, head dim 128, cp=4 load-balanced) plus the decode batch (B=24,
-Hq=32, Hkv=8, D=128, cache 2048, lengths U[1024, 2048]).
+Default workload: the Llama3.1-70B-shaped long-context GQA layer (B=1,
+Hq=64, Hkv=8, S=131072, head dim 128, cp=8 load-balanced) plus the decode
+batch (B=24, Hq=32, Hkv=8, D=128, cache 2048, lengths U[1024, 2048]).  The
+line also carries: the same layer with load balancing off (whole step and
+per-shard forward/backward times), the zero-copy step, decode alone (bf16
+and int8 caches), the end-to-end step through the Python API with host
+copies, the Llama2-7B-shaped and DeepSeek-V3-shaped MLA layers' steps, and
+the float64 oracle timed on a bounded sample on the host cores.
 
 Prints ONE JSON line (rank 0).  `value` is fwd+bwd TFLOP/s (unmasked pairs
 only, S(S+1)/2 per head; fwd 2(Dqk+Dv), bwd 2(3Dqk+2Dv) FLOPs per pair)
@@ -42,7 +47,15 @@ WORKLOADS = {
     "deepseek_v3_mla_rope_s32768_cp4": dict(B=1, S=32768, Hq=128, Hkv=128, Dqk=192, Dv=128, cp=4, lb=True,
                                             q_scale=1.0, rope=True),
     "tiny_s256_cp2": dict(B=1, S=256, Hq=2, Hkv=2, Dqk=64, Dv=64, cp=2, lb=True, q_scale=1.0),
+    # the Llama3.1-70B head layout at shorter sequences: cases small enough for a full ncu capture
+    # (traffic scaled to the 131072-token launch by the tile pairs processed)
+    "llama3_70b_gqa_s16384_cp8": dict(B=1, S=16384, Hq=64, Hkv=8, Dqk=128, Dv=128, cp=8, lb=True, q_scale=1.0),
+    "llama3_70b_gqa_s32768_cp8": dict(B=1, S=32768, Hq=64, Hkv=8, Dqk=128, Dv=128, cp=8, lb=True, q_scale=1.0),
 }
+# the largest single-GPU configuration (Llama3.1-70B-shaped GQA at 131072
+# tokens, load-balanced) is the headline; the others ride along in the line
+HEADLINE = "llama3_70b_s131072_cp8"
+EXTRA_WORKLOADS = ("llama2_7b_s8192_cp4", "deepseek_v3_mla_s32768_cp4", "deepseek_v3_mla_rope_s32768_cp4")
 DECODE = dict(B=24, Hq=32, Hkv=8, D=128, Smax=2048, lo=1024, hi=2048)
 METRIC = "causal CP-attention fwd+bwd TFLOP/s and % of BF16 peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -50,7 +63,7 @@ KERNEL_SOURCES = {
     "attn_fwd": "attn_fwd.cu", "attn_fwd_shard": "attn_fwd.cu", "attn_bwd_dkdv": "attn_bwd.cu",
     "attn_bwd_dq": "attn_bwd.cu", "bwd_preprocess": "attn_bwd.cu", "gqa_decode": "decode.cu",
     "attn_bwd_fused": "attn_bwd_fused.cu", "bwd_dq_round": "attn_bwd_fused.cu",
-    "lb_permute": "permute.cu", "lb_unpermute": "permute.cu",
+    "lb_permute": "permute.cu", "lb_unpermute": "permute.cu", "mla_decode": "mla_decode.cu",
 }
 
 
@@ -301,6 +314,108 @@ def run_reference(args, w, wname):
 # GPU path
 # ---------------------------------------------------------------------------
 
+def peak_for(peaks, timed_s):
+    """Dense bf16 peak that applies to a kernel timed inside a region of
+    timed_s seconds: the burst figure for a short region, the sustained one
+    (the rate under the power cap) for a region of a second or more."""
+    if timed_s >= 1.0:
+        return peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")), "bf16_tflops_sustained"
+    return peaks.get("bf16_tflops"), "bf16_tflops"
+
+
+class AttnStep:
+    """One training step of the attention path for workload w: load-balance
+    permute of q, k, v, dout -> forward (all cp shards) -> backward ->
+    unpermute of out, dq, dk, dv (permute and unpermute only with load
+    balance).  Buffers are allocated once."""
+
+    def __init__(self, w, q, k, v, dout, cpattn, kr=None):
+        import torch
+        self.w, self.cpattn = w, cpattn
+        self.q, self.k, self.v, self.dout, self.kr = q, k, v, dout, kr
+        B, S, Hq, Dv = w["B"], w["S"], w["Hq"], w["Dv"]
+        dev = q.device
+        self.lb = w["lb"]
+        self.qp, self.kp, self.vp, self.dop = (torch.empty_like(x) for x in (q, k, v, dout))
+        self.out_p = torch.empty(B, S, Hq, Dv, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+        self.dq_p, self.dk_p, self.dv_p = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        self.out_n, self.dq_n, self.dk_n, self.dv_n = (torch.empty_like(x) for x in (self.out_p, q, k, v))
+        if kr is not None:
+            self.krp, self.dkr_p, self.dkr_n = (torch.empty_like(kr) for _ in range(3))
+
+    def __call__(self, qi=None, ki=None, vi=None, di=None):
+        c = self.cpattn
+        cp, lb = self.w["cp"], self.lb
+        qi = self.q if qi is None else qi
+        ki = self.k if ki is None else ki
+        vi = self.v if vi is None else vi
+        di = self.dout if di is None else di
+        if lb:
+            c.lb_permute(qi, cp, self.qp)
+            c.lb_permute(ki, cp, self.kp)
+            c.lb_permute(vi, cp, self.vp)
+            c.lb_permute(di, cp, self.dop)
+            a, bk, cv, d = self.qp, self.kp, self.vp, self.dop
+        else:
+            a, bk, cv, d = qi, ki, vi, di
+        if self.kr is not None:
+            kri = self.kr
+            if lb:
+                c.lb_permute(self.kr, cp, self.krp)
+                kri = self.krp
+            c.attn_fwd_mla(a, bk, kri, cv, cp, lb, self.out_p, self.lse)
+            c.attn_bwd_mla(a, bk, kri, cv, self.out_p, self.lse, d, cp, lb, self.dq_p, self.dk_p, self.dkr_p,
+                           self.dv_p)
+        else:
+            c.attn_fwd(a, bk, cv, cp, lb, self.out_p, self.lse)
+            c.attn_bwd(a, bk, cv, self.out_p, self.lse, d, cp, lb, self.dq_p, self.dk_p, self.dv_p)
+        if lb:
+            c.lb_unpermute(self.out_p, cp, self.out_n)
+            c.lb_unpermute(self.dq_p, cp, self.dq_n)
+            c.lb_unpermute(self.dk_p, cp, self.dk_n)
+            c.lb_unpermute(self.dv_p, cp, self.dv_n)
+            if self.kr is not None:
+                c.lb_unpermute(self.dkr_p, cp, self.dkr_n)
+
+    def results(self):
+        if self.lb:
+            return self.out_n, self.dq_n, self.dk_n, self.dv_n
+        return self.out_p, self.dq_p, self.dk_p, self.dv_p
+
+
+def time_steps(fn, n):
+    """Device milliseconds per call of fn over n calls (CUDA events on the
+    current stream, synchronised on both sides)."""
+    import torch
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def kernel_table(prof, w, peaks, timed_s, lens_host=None):
+    peak, peak_name = peak_for(peaks, timed_s)
+    total = sum(t for _, t in prof.values()) or 1.0
+    kernels = {}
+    for name, (n, tot) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        e = {"launches": n, "ms_per_launch": tot / n, "share": tot / total}
+        kf = kernel_flops(name, w)
+        if kf is not None:
+            e["tflops"] = kf / (tot / n / 1e3) / 1e12
+            e["frac_of_bf16"] = e["tflops"] / peak
+            e["peak"] = peak_name
+        if name == "gqa_decode" and lens_host is not None:
+            e["gbs"] = kernel_bytes(name, w, lens_host) / (tot / n / 1e3) / 1e9
+            e["frac_of_hbm"] = e["gbs"] / peaks["hbm_gbs"]
+        kernels[name] = e
+    return kernels
+
+
 def run_ours(args, w, wname):
     import torch
     import torch.distributed as dist
@@ -333,43 +448,11 @@ def run_ours(args, w, wname):
                                                seed=args.seed + 4)
     dq_, dkc, dvc, dlens = dq_.to(dev), dkc.to(dev), dvc.to(dev), dlens.to(dev)
     lens_host = dlens.cpu().tolist()
-
-    # persistent buffers: permuted inputs, outputs, gradients (natural order)
-    qp, kp, vp, dop = (torch.empty_like(x) for x in (q, k, v, dout))
-    out_p = torch.empty(B, S, Hq, Dv, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
-    dq_p, dk_p, dv_p = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    out_n, dq_n, dk_n, dv_n = (torch.empty_like(x) for x in (out_p, q, k, v))
     dec_out = torch.empty_like(dq_)
-    if rope:
-        krp, dkr_p, dkr_n = (torch.empty_like(kr) for _ in range(3))
+    attn = AttnStep(w, q, k, v, dout, cpattn, kr)
 
     def step(qi=q, ki=k, vi=v, di=dout, dqi=dq_, dkci=dkc, dvci=dvc, dli=dlens):
-        if lb:
-            cpattn.lb_permute(qi, cp, qp)
-            cpattn.lb_permute(ki, cp, kp)
-            cpattn.lb_permute(vi, cp, vp)
-            cpattn.lb_permute(di, cp, dop)
-            a, bk, c, d = qp, kp, vp, dop
-        else:
-            a, bk, c, d = qi, ki, vi, di
-        if rope:
-            kri = kr
-            if lb:
-                cpattn.lb_permute(kr, cp, krp)
-                kri = krp
-            cpattn.attn_fwd_mla(a, bk, kri, c, cp, lb, out_p, lse)
-            cpattn.attn_bwd_mla(a, bk, kri, c, out_p, lse, d, cp, lb, dq_p, dk_p, dkr_p, dv_p)
-        else:
-            cpattn.attn_fwd(a, bk, c, cp, lb, out_p, lse)
-            cpattn.attn_bwd(a, bk, c, out_p, lse, d, cp, lb, dq_p, dk_p, dv_p)
-        if lb:
-            cpattn.lb_unpermute(out_p, cp, out_n)
-            cpattn.lb_unpermute(dq_p, cp, dq_n)
-            cpattn.lb_unpermute(dk_p, cp, dk_n)
-            cpattn.lb_unpermute(dv_p, cp, dv_n)
-            if rope:
-                cpattn.lb_unpermute(dkr_p, cp, dkr_n)
+        attn(qi, ki, vi, di)
         cpattn.gqa_decode(dqi, dkci, dvci, dli, dec_out)
 
     for _ in range(args.warmup):
@@ -378,6 +461,9 @@ def run_ours(args, w, wname):
     cpattn.check_device()
 
     # ---- timed region ---------------------------------------------------
+    # every library launch is bracketed by two CUDA events on its own stream
+    # (per-kernel times for the roofline); two event records per launch are
+    # negligible against launches of milliseconds
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -396,21 +482,22 @@ def run_ours(args, w, wname):
     cpattn.check_device()
     ms = ev0.elapsed_time(ev1) / args.steps
     ms_max = max_over_ranks(ms, dev)
+    timed_s = ms_max * args.steps / 1e3
     f_step = flops_fwd(w) + flops_bwd(w)
     value = aggregate_throughput(f_step, ms_max / 1e3, world) / 1e12
     launches = sum(n for n, _ in prof.values())
 
     peaks, peak_src = load_peaks()
+    peak_t, peak_name = peak_for(peaks, timed_s)
     # dominant kernel of the step
-    dom = max(prof.items(), key=lambda kv: kv[1][1])
-    dname, (dn, dms) = dom
+    dname, (dn, dms) = max(prof.items(), key=lambda kv: kv[1][1])
     davg = dms / dn
     fl = kernel_flops(dname, w)
     if fl is not None:
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
         achieved = fl / (davg / 1e3) / 1e12
-        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": "%s bf16_tflops_sustained" % peak_src,
+        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": achieved / peak_t,
+                "peak_source": "%s %s (timed region %.1f s)" % (peak_src, peak_name, timed_s),
                 "traffic": stored_traffic(dname, wname), "ms_per_launch": davg,
                 "algorithmic_flops_per_launch": fl}
     else:
@@ -421,21 +508,6 @@ def run_ours(args, w, wname):
                 "frac": achieved / peak if achieved else None, "peak_source": "%s hbm_gbs" % peak_src,
                 "traffic": stored_traffic(dname, wname), "ms_per_launch": davg}
 
-    kernels = {}
-    for name, (n, tot) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
-        e = {"launches": n, "ms_per_launch": tot / n, "share": tot / sum(t for _, t in prof.values())}
-        kf = kernel_flops(name, w)
-        if kf is not None:
-            e["tflops"] = kf / (tot / n / 1e3) / 1e12
-            e["frac_of_bf16_sustained"] = e["tflops"] / peaks.get("bf16_tflops_sustained", 1700.0)
-        if name == "gqa_decode":
-            e["gbs"] = kernel_bytes(name, w, lens_host) / (tot / n / 1e3) / 1e9
-            e["frac_of_hbm"] = e["gbs"] / peaks["hbm_gbs"]
-        if name in ("lb_permute", "lb_unpermute"):
-            per_launch = (2 * (q.numel() + k.numel() + v.numel() + dout.numel()) * 2) / 4
-            e["gbs_avg_tensor"] = per_launch / (tot / n / 1e3) / 1e9
-        kernels[name] = e
-
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -443,35 +515,35 @@ def run_ours(args, w, wname):
         "config": {"workload": wname, "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "Dqk": Dqk, "Dv": Dv, "cp": cp,
                    "load_balance": lb, **({"k_rope": "one 64-column rope key per token, shared by the heads"}
                                           if rope else {}),
+                   "step": "lb_permute q,k,v,dout -> fwd (all cp shards) -> bwd -> lb_unpermute out,dq,dk,dv"
+                           " -> one GQA decode batch",
                    "decode": "B=24 Hq=32 Hkv=8 D=128 Smax=2048 lens~U[1024,2048]",
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2 (q,k,v,dout %.0f MB + decode KV %.0f MB per step)" % (
-                       4 * q.numel() * 2 / 1e6, 2 * dkc.numel() * 2 / 1e6)},
+                       (q.numel() + k.numel() + v.numel() + dout.numel()) * 2 / 1e6, 2 * dkc.numel() * 2 / 1e6)},
         "roofline": roof,
         "gpu_launches": launches,
-        "kernels": kernels,
+        "kernels": kernel_table(prof, w, peaks, timed_s, lens_host),
         "clocks": clocks,
     }
 
     if not args.no_extras:
         line["e2e"] = measure_e2e(args, w, step, (q, k, v, dout, dq_, dkc, dvc, dlens),
-                                  (out_n if lb else out_p, dq_n if lb else dq_p, dk_n if lb else dk_p,
-                                   dv_n if lb else dv_p, dec_out), f_step, world, dev)
-        line["decode"] = measure_decode(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
-        line["decode_int8"] = measure_decode_int8(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
-        line["shards"] = measure_shards(w, qp if lb else q, kp if lb else k, vp if lb else v, cpattn)
-        # the same shards with four sequences: at one sequence a shard is 256 two-tile units for 152
-        # SMs, so its time is set by how the units pack (the slowest shard has to run two units on
-        # most SMs); with four, the per-shard times show the balance of the work itself
-        w4 = dict(w, B=4 * w["B"])
-        g4 = torch.Generator(device=dev).manual_seed(args.seed + 99)
-        q4, k4, v4 = [torch.randn(w4["B"], w["S"], h, d, device=dev, generator=g4).to(torch.bfloat16)
-                      for h, d in ((w["Hq"], w["Dqk"]), (w["Hkv"], w["Dqk"]), (w["Hkv"], w["Dv"]))]
-        line["shards_4seq"] = measure_shards(w4, q4, k4, v4, cpattn)
-        del q4, k4, v4
-        if lb and (w["S"] // (2 * w["cp"])) % 128 == 0:
+                                  tuple(attn.results()) + (dec_out,), f_step, ms_max, world, dev)
+        if lb:
+            line["lb_off_step"] = measure_lb_off(w, q, k, v, dout, f_step, peaks, cpattn)
+        line["shards"] = measure_shards(w, attn, cpattn)
+        if lb and (S // (2 * cp)) % 128 == 0:
             line["zero_copy"] = measure_zero_copy(args, w, (q, k, v, dout), (dq_, dkc, dvc, dlens), dec_out, f_step,
                                                   ms_max, world, dev, cpattn)
+        line["decode"] = measure_decode(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
+        line["decode_int8"] = measure_decode_int8(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn)
+        line["mla_decode"] = measure_mla_decode(lens_host, peaks, cpattn, dev, args.seed)
+        del attn, q, k, v, dout
+        torch.cuda.empty_cache()
+        line["other_workloads"] = {
+            name: measure_workload(name, peaks, cpattn, dev, args.seed)
+            for name in EXTRA_WORKLOADS if name != wname}
         if rank == 0 and world == 1:
             line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -480,7 +552,7 @@ def run_ours(args, w, wname):
         dist.destroy_process_group()
 
 
-def measure_e2e(args, w, step, inputs, outputs, f_step, world, dev):
+def measure_e2e(args, w, step, inputs, outputs, f_step, ms_step, world, dev):
     """Same metric through the public API with the step's inputs copied from
     pinned host memory and its results copied back, inside the timed region."""
     import torch
@@ -489,7 +561,7 @@ def measure_e2e(args, w, step, inputs, outputs, f_step, world, dev):
     host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outputs]
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = sum(x.numel() * x.element_size() for x in host_out)
-    n = max(3, min(args.steps, 20))
+    n = max(3, min(args.steps, int(6000.0 / max(ms_step, 1e-3))))
 
     def e2e_step():
         for h, d in zip(host_in, dev_in):
@@ -501,15 +573,32 @@ def measure_e2e(args, w, step, inputs, outputs, f_step, world, dev):
     e2e_step()
     torch.cuda.synchronize()
     barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for _ in range(n):
-        e2e_step()
-    ev1.record()
-    torch.cuda.synchronize()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / n, dev)
+    ms = max_over_ranks(time_steps(e2e_step, n), dev)
     return {"value": aggregate_throughput(f_step, ms / 1e3, world) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n}
+
+
+def measure_lb_off(w, q, k, v, dout, f_step, peaks, cpattn, n=3):
+    """fwd + bwd of all shards with load_balance = 0 (natural order, no
+    permutes).  On one GPU the persistent grid spreads every shard's units
+    over all SMs, so the whole step costs about the same either way; the
+    per-shard times (``shards``) show the imbalance the reorder removes."""
+    import torch
+    cp = w["cp"]
+    out = torch.empty(w["B"], w["S"], w["Hq"], w["Dv"], dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty(w["B"], w["Hq"], w["S"], dtype=torch.float32, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def s():
+        cpattn.attn_fwd(q, k, v, cp, 0, out, lse)
+        cpattn.attn_bwd(q, k, v, out, lse, dout, cp, 0, dq, dk, dv)
+
+    s()
+    cpattn.check_device()
+    ms = time_steps(s, n)
+    del out, lse, dq, dk, dv
+    return {"ms_per_step": ms, "tflops": f_step / (ms / 1e3) / 1e12, "steps": n,
+            "what": "fwd + bwd, load_balance = 0, natural order, no permutes, no decode"}
 
 
 def measure_decode(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
@@ -562,18 +651,16 @@ def measure_zero_copy(args, w, inputs, dec_inputs, dec_out, f_step, ms_step, wor
         zstep()
     torch.cuda.synchronize()
     cpattn.check_device()
-    n = max(3, min(args.steps, 50))
+    n = max(3, min(args.steps, int(6000.0 / max(ms_step, 1e-3))))
     barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for _ in range(n):
-        zstep()
-    ev1.record()
-    torch.cuda.synchronize()
+    cpattn.profile_start()
+    ms = max_over_ranks(time_steps(zstep, n), dev)
+    prof = cpattn.profile_stop()
     barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / n, dev)
+    peaks, _ = load_peaks()
     return {"ms_per_step": ms, "value": aggregate_throughput(f_step, ms / 1e3, world) / 1e12, "unit": "TFLOP/s",
             "steps": n, "saved_ms_vs_permuted_step": ms_step - ms,
+            "kernels": kernel_table(prof, w, peaks, ms * n / 1e3),
             "what": "fwd + bwd with load_balance=2 (natural-order tensors, balanced schedule) + decode"}
 
 
@@ -613,38 +700,132 @@ def measure_decode_int8(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
             "l2": "flushed before each launch (512 MB write + 512 MB read)"}
 
 
-def measure_shards(w, q, k, v, cpattn, iters=5):
-    """Per-shard forward time (each shard alone on the whole GPU) and tile
-    counts, load balance on vs off."""
+def measure_mla_decode(lens_host, peaks, cpattn, dev, seed, iters=30):
+    """Absorbed-MLA decode (DeepSeek-V3-shaped: 128 heads, 576-column latent
+    rows of which the first 512 are the value) on the decode workload's
+    batch and lengths, L2 flushed before each launch like ``measure_decode``.
+    Bytes: the valid latent rows, q and out; FLOPs: both products over the
+    valid positions."""
+    import torch
+    from context_causal_attention_load_gb300 import synth
+    B, H, Smax = DECODE["B"], 128, DECODE["Smax"]
+    q, ckv, _ = synth.mla_decode_inputs(B, H, Smax, 1, Smax, seed=seed + 6)
+    lens = torch.tensor(lens_host, dtype=torch.int32)
+    q, ckv, lens = q.to(dev), ckv.to(dev), lens.to(dev)
+    out = torch.empty(B, H, 512, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        cpattn.mla_decode(q, ckv, lens, out=out)
+    cpattn.check_device()
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        torch.sum(flush_rd, dim=0, out=sink)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        cpattn.mla_decode(q, ckv, lens, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    med = ts[len(ts) // 2]
+    n = int(sum(int(x) for x in lens_host))
+    by = n * 576 * 2 + q.numel() * 2 + out.numel() * 2
+    fl = 2.0 * n * H * (576 + 512)
+    gbs = by / (med / 1e3) / 1e9
+    return {"us": med * 1e3, "bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "tflops": fl / (med / 1e3) / 1e12, "frac_of_bf16": fl / (med / 1e3) / 1e12 / peaks["bf16_tflops"],
+            "config": "B=%d H=%d latent 576 (value 512) Smax=%d, lengths of the decode workload" % (B, H, Smax),
+            "l2": "flushed before each launch (512 MB write + 512 MB read)"}
+
+
+def measure_shards(w, attn, cpattn, iters=3):
+    """Per-shard forward and backward times, each shard's launch alone on the
+    whole GPU, with load balancing on (slot-order tensors) and off (natural
+    order), plus the tile-pair counts per head.  The backward of one shard
+    writes its dq rows and its fp32 dk/dv contributions."""
     import torch
     res = {}
     cp = w["cp"]
+    q, k, v, dout = attn.q, attn.k, attn.v, attn.dout
     out = torch.empty(w["B"], w["S"], w["Hq"], w["Dv"], dtype=torch.bfloat16, device=q.device)
     lse = torch.empty(w["B"], w["Hq"], w["S"], dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q)
+    dkp = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dvp = torch.empty(v.shape, dtype=torch.float32, device=q.device)
     for lb in (True, False):
-        times = []
+        if lb:  # slot order, as the step leaves the permuted tensors
+            qq, kk, vv, dd = attn.qp, attn.kp, attn.vp, attn.dop
+        else:
+            qq, kk, vv, dd = q, k, v, dout
+        cpattn.attn_fwd(qq, kk, vv, cp, lb, out, lse)
+        fwd, bwd = [], []
         for s in range(cp):
-            cpattn.attn_fwd_shard(q, k, v, cp, s, lb, out, lse)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(iters):
-                cpattn.attn_fwd_shard(q, k, v, cp, s, lb, out, lse)
-            e1.record()
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1) / iters)
-        res["lb_on" if lb else "lb_off"] = {
-            "tile_pairs_per_head": cpattn.tile_counts(w["S"], cp, lb), "fwd_ms": times,
-            "max_over_min": max(times) / min(times)}
+            f = lambda: cpattn.attn_fwd_shard(qq, kk, vv, cp, s, lb, out, lse)  # noqa: E731
+            f()
+            fwd.append(time_steps(f, iters))
+        cpattn.attn_fwd(qq, kk, vv, cp, lb, out, lse)  # full out/lse for the backward
+        for s in range(cp):
+            f = lambda: cpattn.attn_bwd_shard(qq, kk, vv, out, lse, dd, cp, s, lb, dq, dkp, dvp)  # noqa: E731
+            f()
+            bwd.append(time_steps(f, iters))
+        e = {"tile_pairs_per_head": cpattn.tile_counts(w["S"], cp, lb), "fwd_ms": fwd,
+             "fwd_max_over_min": max(fwd) / min(fwd)}
+        if bwd:
+            e["bwd_ms"] = bwd
+            e["bwd_max_over_min"] = max(bwd) / min(bwd)
+        res["lb_on" if lb else "lb_off"] = e
+    cpattn.check_device()
+    del out, lse, dq, dkp, dvp
+    return res
+
+
+def measure_workload(name, peaks, cpattn, dev, seed, steps=None, warmup=3):
+    """The attention step (no decode) of another workload, for the same line:
+    step time, fwd+bwd TFLOP/s, per-kernel rates; for the Llama2-shaped and
+    the MLA layer also their per-shard times at one sequence."""
+    import torch
+    from context_causal_attention_load_gb300 import synth
+    w = WORKLOADS[name]
+    B, S, Hq, Hkv, Dqk, Dv = (w[k] for k in ("B", "S", "Hq", "Hkv", "Dqk", "Dv"))
+    q, k, v, dout = synth.attention_inputs_device(B, S, Hq, Hkv, Dqk, Dv, seed=seed, q_scale=w["q_scale"],
+                                                  device=dev)
+    kr = None
+    if w.get("rope"):
+        k, kr = k[..., :128].contiguous(), k[:, :, 0, 128:].contiguous()
+    attn = AttnStep(w, q, k, v, dout, cpattn, kr)
+    for _ in range(warmup):
+        attn()
+    torch.cuda.synchronize()
+    cpattn.check_device()
+    est = time_steps(attn, 1)
+    n = steps or max(3, min(100, int(3000.0 / max(est, 1e-3))))
+    cpattn.profile_start()
+    ms = time_steps(attn, n)
+    prof = cpattn.profile_stop()
+    timed_s = ms * n / 1e3
+    f_step = flops_fwd(w) + flops_bwd(w)
+    peak, peak_name = peak_for(peaks, timed_s)
+    res = {"ms_per_step": ms, "tflops": f_step / (ms / 1e3) / 1e12, "steps": n,
+           "frac": f_step / (ms / 1e3) / 1e12 / peak, "peak": peak_name,
+           "config": {k: w[k] for k in ("B", "S", "Hq", "Hkv", "Dqk", "Dv", "cp", "lb")},
+           "kernels": kernel_table(prof, w, peaks, timed_s)}
+    if name in ("llama2_7b_s8192_cp4", "deepseek_v3_mla_s32768_cp4"):
+        res["shards"] = measure_shards(w, attn, cpattn, iters=10 if name.startswith("llama2") else 3)
+    del attn, q, k, v, dout
+    torch.cuda.empty_cache()
     return res
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama2_7b_s8192_cp4")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip e2e/decode/shard/cpu measurements")
     args = ap.parse_args()

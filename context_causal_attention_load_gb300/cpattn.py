@@ -65,10 +65,12 @@ def load(path=None):
         "cp_attn_bwd_mla": [_P] * 11 + [_I] * 5 + [_P],
         "gqa_decode": [_P] * 5 + [_I] * 5 + [_P],
         "gqa_decode_int8": [_P] * 7 + [_I] * 5 + [_P],
+        "mla_decode": [_P] * 4 + [_I] * 3 + [ctypes.c_float, _P],
         "cp_lb_positions": [_I, _I, _I, ctypes.POINTER(ctypes.c_int)],
         "cp_attn_tile_counts": [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)],
         "cp_attn_fwd_schedule": [_I] * 7 + [ctypes.POINTER(ctypes.c_longlong)],
         "cp_attn_check_device": [_P],
+        "cp_attn_test_stall_forward": [_I, _L],
         "cp_attn_release": [],
         "cp_attn_profile_start": [],
         "cp_attn_profile_stop": [ctypes.POINTER(KernelStat), ctypes.c_int, ctypes.POINTER(ctypes.c_int)],
@@ -268,6 +270,23 @@ def gqa_decode(q, kcache, vcache, lens, out=None):
     return out
 
 
+def mla_decode(q, ckv, lens, scale=None, out=None):
+    """Absorbed-MLA decode: q [B,H,576] bf16, ckv [B,Smax,576] bf16 (latent
+    rows: 512 compressed-KV columns, then 64 rope columns), lens [B] int32 ->
+    out [B,H,512] bf16; scale defaults to 1/sqrt(192)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(ckv, torch.bfloat16, "ckv", 3)
+    _need(lens, torch.int32, "lens", 1)
+    B, H, Dk = q.shape
+    if Dk != 576 or ckv.shape[0] != B or ckv.shape[2] != 576 or lens.shape[0] != B:
+        raise ValueError("MLA decode shapes: q [B,H,576], ckv [B,Smax,576], lens [B]")
+    out = torch.empty(B, H, 512, dtype=torch.bfloat16, device=q.device) if out is None else out
+    _need(out, torch.bfloat16, "out", 3)
+    sc = (1.0 / 192.0 ** 0.5) if scale is None else float(scale)
+    _check(load().mla_decode(_ptr(q), _ptr(ckv), _ptr(lens), _ptr(out), B, H, ckv.shape[1], sc, _stream(q)))
+    return out
+
+
 def lb_positions(S, cp, load_balance=True):
     arr = (ctypes.c_int * S)()
     _check(load().cp_lb_positions(S, cp, _lb(load_balance), arr))
@@ -291,6 +310,13 @@ def tile_counts(S, cp, load_balance=True):
 def check_device(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     _check(load().cp_attn_check_device(ctypes.c_void_p(s)))
+
+
+def test_stall_forward(stage, wait_limit_cycles=2_000_000):
+    """Test hook: the next forward launch leaves out ring stage `stage`'s
+    loads and its pipeline waits give up after wait_limit_cycles (the
+    bounded-wait timeout path; see include/cpattn.h).  stage < 0 clears it."""
+    _check(load().cp_attn_test_stall_forward(int(stage), int(wait_limit_cycles)))
 
 
 def release():

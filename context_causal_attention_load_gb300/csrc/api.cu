@@ -143,6 +143,7 @@ struct DevState {
   DevBuf<float> dq_acc;     // fused backward's fp32 dQ accumulator
   DevBuf<float> rope_acc;   // MLA with shared rope keys: dK's rope columns summed over heads
   DevBuf<float> dec_o, dec_ml;
+  DevBuf<float> mla_o, mla_ml;  // absorbed-MLA decode chunk partials
 };
 
 std::mutex g_mu;
@@ -334,6 +335,7 @@ int upload_plan(std::vector<std::pair<long long, U>> w, int num_sms, UnitPlan<U>
 
 // ---- argument checks ------------------------------------------------------
 constexpr int kTile = 128;  // rows per attention tile
+constexpr int kMaxCache = 1 << 30;  // decode cache positions (lengths plus a slice stay in int range)
 
 int check_attn(const AttnShape& sh) {
   if (sh.B < 1 || sh.S < 1 || sh.Hq < 1 || sh.Hkv < 1 || sh.cp < 1)
@@ -442,11 +444,13 @@ int fwd_units_cached(DevState& ds, const AttnShape& sh, int shard, UnitPlan<FwdU
 }
 
 // backward units.  kind 0: dk/dv, one 128-row key tile of a KV head, cost =
-// query tiles (of BQ rows, all heads of the group) that see it.  kind 1: dq,
-// one 128-row query tile of a query head, cost = key tiles it sees.  Both
-// plus 3 steps of per-unit overhead.
-int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, UnitPlan<BwdUnit>** out) {
-  std::vector<int> key{kind, sh.B, sh.Hq, sh.Hkv, sh.S, sh.cp, sh.lb, sh.Dqk};
+// query tiles (of BQ rows, all heads of the group) that see it; for one
+// shard (shard >= 0) only the query tiles that hold a slot of the shard
+// count, and key tiles none of them sees are left out, so the shard's launch
+// is dealt by its own work.  kind 1: dq, one 128-row query tile of a query
+// head, cost = key tiles it sees.  Both plus 3 steps of per-unit overhead.
+int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, UnitPlan<BwdUnit>** out, int shard = -1) {
+  std::vector<int> key{kind, sh.B, sh.Hq, sh.Hkv, sh.S, sh.cp, sh.lb, sh.Dqk, shard};
   auto it = ds.bwd_units.find(key);
   if (it == ds.bwd_units.end()) {
     const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
@@ -454,16 +458,21 @@ int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, UnitPlan<BwdUn
     std::vector<std::pair<long long, BwdUnit>> w;
     if (kind == 0) {
       const int BQ = bwd_dkdv_q_tile(sh.Dqk);
+      const int lo = shard < 0 ? 0 : shard * (sh.S / sh.cp), hi = shard < 0 ? sh.S : (shard + 1) * (sh.S / sh.cp);
       for (int kt = 0; kt < nt; ++kt) {
         const int bound = tile_min_pos(pm, kt, kTile);
         long long n = 0;
-        for (int qt = next_q_tile(pm, BQ, -1, bound); qt >= 0; qt = next_q_tile(pm, BQ, qt, bound)) ++n;
+        for (int qt = next_q_tile(pm, BQ, -1, bound); qt >= 0; qt = next_q_tile(pm, BQ, qt, bound))
+          if (qt * BQ < hi && qt * BQ + BQ > lo) ++n;
+        if (n == 0 && shard >= 0) continue;
         for (int b = 0; b < sh.B; ++b)
           for (int g = 0; g < sh.Hkv; ++g) w.push_back({n + 3, BwdUnit{b, g, kt, 0}});
       }
     } else {
       const int BK = bwd_dq_kv_tile(sh.Dqk);
+      const int lo = shard < 0 ? 0 : shard * (sh.S / sh.cp), hi = shard < 0 ? sh.S : (shard + 1) * (sh.S / sh.cp);
       for (int qt = 0; qt < nt; ++qt) {
+        if (qt * kTile >= hi || qt * kTile + kTile <= lo) continue;  // no slot of the shard
         const int bound = tile_max_pos(pm, qt, kTile);
         long long n = 0;
         for (int kt = next_kv_tile(pm, BK, -1, bound); kt >= 0; kt = next_kv_tile(pm, BK, kt, bound)) ++n;
@@ -503,6 +512,13 @@ int permute_impl(const void* src, void* dst, int B, int S, long long row_bytes, 
   return CPATTN_OK;
 }
 
+// test hook of the bounded waits: consumed by the next forward launch
+struct FwdStall {
+  int stage = -1;
+  long long limit = 0;
+};
+FwdStall g_fwd_stall;
+
 // k_rope non-null: MLA with one rope key per token shared by the heads (k holds
 // the per-head 128-column nope keys)
 int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, const AttnShape& sh, int shard,
@@ -532,6 +548,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
   a.sh = sh;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.Dqk));
   a.err = ds->err;
+  a.wait_limit = kWaitLimitCycles;
+  a.fault_skip_stage = -1;
+  if (g_fwd_stall.stage >= 0) {
+    a.fault_skip_stage = g_fwd_stall.stage;
+    a.wait_limit = g_fwd_stall.limit;
+    g_fwd_stall = FwdStall{};
+  }
   const int grid = plan->ncta;
   cudaError_t e;
   {
@@ -585,13 +608,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   const size_t nstat = (size_t)B * Hq * Spad;
   if ((rc = ensure(ds->bwd_stats, 2 * nstat, stream, false))) return rc;
   const bool fused = bwd_fused_supported(Dqk, Dv);
-  if (shard >= 0 && !fused) return fail(CPATTN_ERR_UNSUPPORTED, "per-shard backward needs Dqk == Dv (64 or 128)");
   const size_t nacc = (size_t)B * S * Hq * Dqk;
   if (fused && (rc = ensure(ds->dq_acc, nacc, stream, false))) return rc;
   UnitPlan<BwdUnit>* u_kv;
   UnitPlan<BwdUnit>* u_q = nullptr;
-  if ((rc = bwd_units_cached(*ds, sh, 0, &u_kv))) return rc;
-  if (!fused && (rc = bwd_units_cached(*ds, sh, 1, &u_q))) return rc;
+  if ((rc = bwd_units_cached(*ds, sh, 0, &u_kv, shard))) return rc;
+  if (!fused && (rc = bwd_units_cached(*ds, sh, 1, &u_q, shard))) return rc;
   BwdArgs a{};
   a.lse_l2 = ds->bwd_stats.ptr;
   a.delta = ds->bwd_stats.ptr + nstat;
@@ -615,6 +637,16 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
                               sh, Spad, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
+  if (shard >= 0) {  // key tiles (and query rows) the shard does not touch stay zero
+    const size_t nk = (size_t)B * S * Hkv;
+    cudaError_t ez = cudaSuccess;
+    if (dk_part) ez = cudaMemsetAsync(dk_part, 0, nk * Dqk * sizeof(float), stream);
+    if (ez == cudaSuccess && dv_part) ez = cudaMemsetAsync(dv_part, 0, nk * Dv * sizeof(float), stream);
+    if (ez == cudaSuccess && dk) ez = cudaMemsetAsync(dk, 0, nk * Dqk * 2, stream);
+    if (ez == cudaSuccess && dv) ez = cudaMemsetAsync(dv, 0, nk * Dv * 2, stream);
+    if (ez == cudaSuccess && !fused) ez = cudaMemsetAsync(dq, 0, nacc * 2, stream);
+    if (ez != cudaSuccess) return cuda_fail(ez, "clearing the shard partials");
+  }
   if (fused) {
     // one kernel: 128-row key tiles, 128-row query steps; dQ through the fp32 accumulator
     if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, 128))) return rc;
@@ -625,23 +657,15 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     a.units = u_kv->units.ptr;
     a.cta_off = u_kv->off.ptr;
     a.n_units = (int)u_kv->units.n;
-    if (shard >= 0) {  // key tiles no query of the shard sees are skipped: their partials are zero
-      const size_t nk = (size_t)B * S * Hkv;
-      cudaError_t ez = cudaSuccess;
-      if (dk_part) ez = cudaMemsetAsync(dk_part, 0, nk * Dqk * sizeof(float), stream);
-      if (ez == cudaSuccess && dv_part) ez = cudaMemsetAsync(dv_part, 0, nk * Dv * sizeof(float), stream);
-      if (ez == cudaSuccess && dk) ez = cudaMemsetAsync(dk, 0, nk * Dqk * 2, stream);
-      if (ez == cudaSuccess && dv) ez = cudaMemsetAsync(dv, 0, nk * Dv * 2, stream);
-      if (ez != cudaSuccess) return cuda_fail(ez, "clearing the shard partials");
-    }
-    {
+    if (u_kv->ncta > 0) {
       ProfScope ps("attn_bwd_fused", stream);
       e = launch_attn_bwd_fused(a, u_kv->ncta, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "fused bwd launch");
     {
       ProfScope ps("bwd_dq_round", stream);
-      e = launch_bwd_dq_round(a.dq_acc, dq, (long long)nacc, a.scale, stream);
+      e = PosMap::make(S, cp, load_balance).lb == 2 ? launch_bwd_dq_round_nat(a.dq_acc, dq, sh, a.scale, stream)
+                                                     : launch_bwd_dq_round(a.dq_acc, dq, (long long)nacc, a.scale, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "dq rounding launch");
     return CPATTN_OK;
@@ -665,8 +689,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   a.units = u_kv->units.ptr;
   a.cta_off = u_kv->off.ptr;
   a.n_units = (int)u_kv->units.n;
-  {
-    ProfScope ps("attn_bwd_dkdv", stream);
+  if (u_kv->ncta > 0) {
+    ProfScope ps(shard < 0 ? "attn_bwd_dkdv" : "attn_bwd_dkdv_shard", stream);
     e = launch_attn_bwd_dkdv(a, u_kv->ncta, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dk/dv launch");
@@ -680,8 +704,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   a.units = u_q->units.ptr;
   a.cta_off = u_q->off.ptr;
   a.n_units = (int)u_q->units.n;
-  {
-    ProfScope ps("attn_bwd_dq", stream);
+  if (u_q->ncta > 0) {
+    ProfScope ps(shard < 0 ? "attn_bwd_dq" : "attn_bwd_dq_shard", stream);
     e = launch_attn_bwd_dq(a, u_q->ncta, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
@@ -745,6 +769,9 @@ int cp_attn_bwd_mla(const void* q, const void* k_nope, const void* k_rope, const
 int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out, int B, int Hq,
                int Hkv, int Smax, int D, cudaStream_t stream) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Smax < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, Hq, Hkv, Smax must be >= 1");
+  if (Smax > kMaxCache) return fail(CPATTN_ERR_INVALID_ARG, "Smax (%d) above the supported %d", Smax, kMaxCache);
+  if ((long long)B * Hkv * decode_max_split(Smax) > 0x7fffffffLL)
+    return fail(CPATTN_ERR_INVALID_ARG, "B*Hkv*ceil(Smax/%d) exceeds 2^31 decode items", kDecodeSplit);
   if (Hq % Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   if (Hq / Hkv > 16) return fail(CPATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16", Hq / Hkv);
   if (D != 64 && D != 128) return fail(CPATTN_ERR_UNSUPPORTED, "decode head dim %d not in {64, 128}", D);
@@ -774,6 +801,9 @@ int gqa_decode_int8(const void* q, const void* kcache, const void* vcache, const
                     const float* vscale, const int* lens, void* out, int B, int Hq, int Hkv, int Smax, int D,
                     cudaStream_t stream) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Smax < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, Hq, Hkv, Smax must be >= 1");
+  if (Smax > kMaxCache) return fail(CPATTN_ERR_INVALID_ARG, "Smax (%d) above the supported %d", Smax, kMaxCache);
+  if ((long long)B * Hkv * decode_max_split(Smax) > 0x7fffffffLL)
+    return fail(CPATTN_ERR_INVALID_ARG, "B*Hkv*ceil(Smax/%d) exceeds 2^31 decode items", kDecodeSplit);
   if (Hq % Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   if (Hq / Hkv > 16) return fail(CPATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16", Hq / Hkv);
   if (D != 128) return fail(CPATTN_ERR_UNSUPPORTED, "int8 decode head dim %d is not 128", D);
@@ -801,9 +831,44 @@ int gqa_decode_int8(const void* q, const void* kcache, const void* vcache, const
   return CPATTN_OK;
 }
 
+int mla_decode(const void* q, const void* ckv, const int* lens, void* out, int B, int H, int Smax, float scale,
+               cudaStream_t stream) {
+  if (B < 1 || H < 1 || Smax < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, H, Smax must be >= 1");
+  if (H > 128) return fail(CPATTN_ERR_UNSUPPORTED, "mla_decode: H = %d > 128 heads", H);
+  if (B > mla_decode_max_batch()) return fail(CPATTN_ERR_UNSUPPORTED, "mla_decode: batch %d > %d", B, mla_decode_max_batch());
+  if (Smax > kMaxCache) return fail(CPATTN_ERR_INVALID_ARG, "Smax (%d) above the supported %d", Smax, kMaxCache);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CPATTN_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (!lens) return fail(CPATTN_ERR_INVALID_ARG, "null lens");
+  int rc = check_ptrs({q, ckv, out});
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState* ds;
+  if ((rc = get_state(&ds))) return rc;
+  if ((rc = need_sm103(*ds))) return rc;
+  const int nch = mla_decode_chunks(Smax);
+  const size_t rows = (size_t)B * nch * H;
+  if ((rc = ensure(ds->mla_o, rows * 512, stream, false))) return rc;
+  if ((rc = ensure(ds->mla_ml, rows * 2, stream, false))) return rc;
+  MlaDecodeArgs a{};
+  a.q = q; a.ckv = ckv; a.lens = lens; a.out = out;
+  a.part_o = ds->mla_o.ptr; a.part_ml = ds->mla_ml.ptr; a.err = ds->err;
+  a.B = B; a.H = H; a.Smax = Smax; a.nch = nch;
+  a.scale_log2 = (float)(1.4426950408889634 * (double)scale);
+  cudaError_t e;
+  {
+    ProfScope ps("mla_decode", stream);
+    e = launch_mla_decode(a, ds->num_sms, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
+  return CPATTN_OK;
+}
+
 int gqa_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* lens, void* out, int B,
                        int Hq, int Hkv, int Smax, int D, cudaStream_t stream) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Smax < 1) return fail(CPATTN_ERR_INVALID_ARG, "B, Hq, Hkv, Smax must be >= 1");
+  if (Smax > kMaxCache) return fail(CPATTN_ERR_INVALID_ARG, "Smax (%d) above the supported %d", Smax, kMaxCache);
+  if ((long long)B * Hkv * decode_max_split(Smax) > 0x7fffffffLL)
+    return fail(CPATTN_ERR_INVALID_ARG, "B*Hkv*ceil(Smax/%d) exceeds 2^31 decode items", kDecodeSplit);
   if (Hq % Hkv) return fail(CPATTN_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   if (Hq / Hkv > 16) return fail(CPATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16", Hq / Hkv);
   if (D != 64 && D != 128) return fail(CPATTN_ERR_UNSUPPORTED, "decode head dim %d not in {64, 128}", D);
@@ -867,18 +932,41 @@ int cp_attn_fwd_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance
   return CPATTN_OK;
 }
 
+int cp_attn_test_stall_forward(int stage, long long wait_limit_cycles) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (stage < 0) {
+    g_fwd_stall = FwdStall{};
+    return CPATTN_OK;
+  }
+  if (wait_limit_cycles < 100000 || wait_limit_cycles > kWaitLimitCycles)
+    return fail(CPATTN_ERR_INVALID_ARG, "wait_limit_cycles must be in [1e5, %lld]", kWaitLimitCycles);
+  g_fwd_stall.stage = stage;
+  g_fwd_stall.limit = wait_limit_cycles;
+  return CPATTN_OK;
+}
+
 int cp_attn_check_device(cudaStream_t stream) {
   std::lock_guard<std::mutex> lk(g_mu);
-  DevState* ds;
-  int rc = get_state(&ds);
-  if (rc) return rc;
-  cudaError_t e = cudaStreamSynchronize(stream);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  // the library's error word exists once a call that keeps scratch ran on this
+  // device; looking for it creates nothing (so a caller of the allocation-free
+  // decode alone may call this too)
   int word = 0;
-  e = cudaMemcpy(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+  auto it = g_dev.find(dev);
+  if (it != g_dev.end() && it->second.err) {
+    e = cudaMemcpy(&word, it->second.err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+    if (word != DEV_OK) cudaMemset(it->second.err, 0, sizeof(int));
+  }
+  int word_na = 0;  // the allocation-free decode keeps its own word in its static array
+  e = noalloc_take_error(&word_na);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the allocation-free decode's error word");
+  if (word == DEV_OK) word = word_na;
   if (word == DEV_OK) return CPATTN_OK;
-  cudaMemset(ds->err, 0, sizeof(int));
   if (word == DEV_TIMEOUT) return fail(CPATTN_ERR_DEVICE_TIMEOUT, "a kernel pipeline wait timed out");
   if (word == DEV_LENS_CLAMPED) return fail(CPATTN_ERR_DEVICE_BOUNDS, "decode lens outside [0, Smax] were clamped");
   if (word == DEV_SMEM_ALIGN) return fail(CPATTN_ERR_CUDA, "a kernel's shared memory was not 1024-byte aligned");
@@ -944,6 +1032,8 @@ int cp_attn_release(void) {
   cudaFree(s.rope_acc.ptr);
   cudaFree(s.dec_o.ptr);
   cudaFree(s.dec_ml.ptr);
+  cudaFree(s.mla_o.ptr);
+  cudaFree(s.mla_ml.ptr);
   cudaFree(s.err);
   g_dev.erase(it);
   return CPATTN_OK;

@@ -41,6 +41,18 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int TK = 128;  // key rows per dk/dv unit; query rows per dq unit
 
+// next query tile of T slots (> cur) that sees keys at position bound and
+// holds a slot in [lo, hi) (the query slots taking part: all of them, or one
+// shard's); tiles come in increasing slot order
+__device__ __forceinline__ int next_q_tile_in(const PosMap& pm, int T, int cur, int bound, int lo, int hi) {
+  if (cur < 0) cur = lo / T - 1;  // no tile before the first one holding lo can qualify
+  for (int qt = next_q_tile(pm, T, cur, bound); qt >= 0; qt = next_q_tile(pm, T, qt, bound)) {
+    if (qt * T >= hi) return -1;
+    if (qt * T + T > lo) return qt;
+  }
+  return -1;
+}
+
 
 // ============================================================================
 // preprocess: -lse*log2(e) (-inf past S) and -rowsum(dO*O) (0 past S), stored
@@ -193,14 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       int kmin, kmax;
       pm.range(u.t * TK, u.t * TK + TK, kmin, kmax);
       for (int hq = u.h * G; hq < u.h * G + G && ok; ++hq) {
-        for (int qt = next_q_tile(pm, BQ, -1, kmin); qt >= 0; qt = next_q_tile(pm, BQ, qt, kmin)) {
+        for (int qt = next_q_tile_in(pm, BQ, -1, kmin, a.q_lo, a.q_hi); qt >= 0;
+             qt = next_q_tile_in(pm, BQ, qt, kmin, a.q_lo, a.q_hi)) {
           if (lane == 0) ok = mbar_wait(&bar.q_empty[qs], qph ^ 1, ab);
           if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
           unsigned char* st = smem + C::OFF_ST + qs * C::STAGE;
           int* qp = reinterpret_cast<int*>(st + C::ST_POS);
-          for (int i = lane; i < BQ; i += 32) {
+          for (int i = lane; i < BQ; i += 32) {  // rows outside the slots taking part see no key
             const int s = qt * BQ + i;
-            qp[i] = s < pm.S ? pm.pos(s) : -1;
+            qp[i] = (s < pm.S && s >= a.q_lo && s < a.q_hi) ? pm.pos(s) : -1;
           }
           __syncwarp();
           if (lane == 0) {
@@ -270,10 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         int kmin, kmax;
         pm.range(u.t * TK, u.t * TK + TK, kmin, kmax);
         // flatten (head, query tile) steps; step i uses buffer i % NBUF and ring stage
-        int hq = u.h * G, qt = next_q_tile(pm, BQ, -1, kmin);
+        int hq = u.h * G, qt = next_q_tile_in(pm, BQ, -1, kmin, a.q_lo, a.q_hi);
         auto advance = [&](int& h_, int& t_) {
-          t_ = next_q_tile(pm, BQ, t_, kmin);
-          if (t_ < 0 && ++h_ < u.h * G + G) t_ = next_q_tile(pm, BQ, -1, kmin);
+          t_ = next_q_tile_in(pm, BQ, t_, kmin, a.q_lo, a.q_hi);
+          if (t_ < 0 && ++h_ < u.h * G + G) t_ = next_q_tile_in(pm, BQ, -1, kmin, a.q_lo, a.q_hi);
         };
         int cur_stage = qs;
         if (!(ok = mbar_wait(&bar.q_full[qs], qph, ab))) break;
@@ -315,8 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         mma_commit(&bar.acc_full);
         mma_commit(&bar.kv_empty);
       }
-      mma_commit(&bar.done);
-      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+      mma_drain(&bar.done, a.err);
     }
   } else {
     // ------------------------------------------------------------ element-wise groups
@@ -340,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       const bool k_inside = u.t * TK + TK <= pm.S;
       int i = 0;
       for (int hq = u.h * G; hq < u.h * G + G && ok; ++hq) {
-        for (int qt = next_q_tile(pm, BQ, -1, kmin); qt >= 0; qt = next_q_tile(pm, BQ, qt, kmin), ++i) {
+        for (int qt = next_q_tile_in(pm, BQ, -1, kmin, a.q_lo, a.q_hi); qt >= 0;
+             qt = next_q_tile_in(pm, BQ, qt, kmin, a.q_lo, a.q_hi), ++i) {
           const int buf = NBUF == 2 ? (i & 1) : 0;
           ok = mbar_wait(&bar.q_full[qs], qph, ab);
           if (ok) ok = mbar_wait(&bar.sd_full[buf], sdph[buf], ab);
@@ -350,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
           const unsigned char* st = smem + C::OFF_ST + qs * C::STAGE;
           int qmin, qmax;
           pm.range(qt * BQ, qt * BQ + BQ, qmin, qmax);
-          const bool full = (kmax <= qmin) && k_inside;
+          const bool full = (kmax <= qmin) && k_inside && qt * BQ >= a.q_lo && qt * BQ + BQ <= a.q_hi;
           const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll 1
           for (int c0 = g * HC; c0 < (g + 1) * HC; c0 += 32) {
@@ -397,18 +410,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       acc_ph ^= 1;
       tc_fence_after();
-      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) + (((size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0)) * a.sh.Hkv + u.h) * DV;
+      const size_t krow = (size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0);
+      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(a.dv) + (krow * a.sh.Hkv + u.h) * DV;
       // shared rope keys: dk holds the 128 nope columns per head, and the rope
       // columns are summed over heads into dk_rope_acc
       const bool rope = DQK == 192 && a.rope_shared;
-      const size_t krow = (size_t)u.b * pm.S + (kvalid ? pm.row(kslot) : 0);
       __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(a.dk) + (krow * a.sh.Hkv + u.h) * (rope ? 128 : DQK);
 #pragma unroll 1
       for (int c0 = g * (DV / 2); c0 < (g + 1) * (DV / 2); c0 += 32) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + C::T_DV + c0, o);
         tmem_ld_wait();
-        if (kvalid) {
+        if (kvalid && a.dv_part) {  // one shard's contribution, unrounded
+          float4* dst = reinterpret_cast<float4*>(a.dv_part + (krow * a.sh.Hkv + u.h) * DV + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]), __uint_as_float(o[4 * v4 + 1]),
+                                  __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
+        }
+        if (kvalid && a.dv) {
           uint4* dst = reinterpret_cast<uint4*>(dvp + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -424,13 +444,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + C::T_DK + c0, o);
         tmem_ld_wait();
+        if (kvalid && a.dk_part) {  // one shard's contribution, unrounded (no shared rope key here)
+          float4* dst = reinterpret_cast<float4*>(a.dk_part + (krow * a.sh.Hkv + u.h) * DQK + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = make_float4(sc * __uint_as_float(o[4 * v4 + 0]), sc * __uint_as_float(o[4 * v4 + 1]),
+                                  sc * __uint_as_float(o[4 * v4 + 2]), sc * __uint_as_float(o[4 * v4 + 3]));
+        }
         if (kvalid && rope && c0 >= 128) {
           float* acc = a.dk_rope_acc + krow * 64 + (c0 - 128);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)
             red_add_v4(acc + 4 * v4, sc * __uint_as_float(o[4 * v4 + 0]), sc * __uint_as_float(o[4 * v4 + 1]),
                        sc * __uint_as_float(o[4 * v4 + 2]), sc * __uint_as_float(o[4 * v4 + 3]));
-        } else if (kvalid) {
+        } else if (kvalid && a.dk) {
           uint4* dst = reinterpret_cast<uint4*>(dkp + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -659,8 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         if (!ok) break;
         mma_commit(&bar.acc_full);
       }
-      mma_commit(&bar.done);
-      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+      mma_drain(&bar.done, a.err);
     }
   } else {
     // ------------------------------------------------------------ element-wise groups
@@ -743,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + C::T_DQ + c0, o);
         tmem_ld_wait();
-        if (qvalid) {
+        if (qvalid && qslot >= a.q_lo && qslot < a.q_hi) {  // one shard's rows only, for a shard
           uint4* dst = reinterpret_cast<uint4*>(dqp + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)

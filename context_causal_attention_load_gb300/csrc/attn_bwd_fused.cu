@@ -152,12 +152,28 @@ __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* l
 }
 
 // (query head, query tile) steps of a key-tile unit: the query tiles that
-// see the key tile (and, per shard, hold a slot in [lo, hi))
-template <bool SHARD>
+// see the key tile (and, per shard, hold a slot in [lo, hi)).
+// Where every tile of slots is one tile of positions (no reorder, or chunks
+// that are whole tiles, which natural-order tensors always have), the tiles
+// are walked by DESCENDING position: from the last tile of the sequence down
+// to the one holding the key tile's first position.  Every key tile of a head
+// sees the top of the sequence, so the CTAs working on key tiles of the same
+// head start on the same query tile and move through the same Q/dO tiles (and
+// the same dQ accumulator rows) at about the same time: those tiles come from
+// DRAM once and from L2 for the others.  Natural-order tensors then also load
+// consecutive rows of memory, and permuted and natural-order tensors go
+// through the same steps in the same order.  Otherwise (chunks that are not
+// whole tiles, or one shard's steps) the tiles are walked in slot order.
+template <bool SHARD, bool NAT>
 struct StepWalk {
   int h_end, kmin, lo, hi;
   __device__ __forceinline__ int next_tile(const PosMap& pm, int qt) const {
+    if (!SHARD && (NAT || pm.lb == 0 || pm.c % kRows == 0)) {
+      const int pt = qt < 0 ? (pm.S + kRows - 1) / kRows - 1 : pm.pos(qt * kRows) / kRows - 1;
+      return pt >= kmin / kRows ? pm.slot(pt * kRows) / kRows : -1;
+    }
     if (!SHARD) return next_q_tile(pm, kRows, qt, kmin);
+    if (qt < 0) qt = lo / kRows - 1;  // no tile before the shard's first can qualify
     for (qt = next_q_tile(pm, kRows, qt, kmin); qt >= 0; qt = next_q_tile(pm, kRows, qt, kmin)) {
       if (qt * kRows >= hi) return -1;  // tiles come in increasing slot order
       if (qt * kRows + kRows > lo) return qt;
@@ -263,7 +279,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       const BwdUnit u = a.units[ui];
       int kmin, kmax;
       pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-      const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
+      const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
       int hq = u.h * G, qt = -1;
       if (!w.next(pm, hq, qt)) continue;
       do {
@@ -309,7 +325,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
+        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;  // every role skips a unit no query sees
         if (!(ok = mbar_wait(&bar.kv_empty, (uc & 1) ^ 1, ab))) break;
@@ -404,7 +420,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
+        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;
         if (!(ok = mbar_wait(&bar.kv_full, uc & 1, ab))) break;
@@ -449,13 +465,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         mma_commit(&bar.kv_empty);  // K (last read by dQ) and V are done
         ++uc;
       }
-      mma_commit(&bar.done);
-      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+      mma_drain(&bar.done, a.err);
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ dQ reducer
     // adds each staged dQ tile into the fp32 accumulator; the boxes in the dS
-    // space go first, in their own bulk group, because the next dS waits on them
+    // space go first, in their own bulk group, because the next dS waits on them.
+    // The accumulator is in slot order for natural-order tensors too (the
+    // rounding pass writes each slot's row to its natural row): measured on
+    // the Llama3.1-70B-shaped layer, reduce-adds into the natural rows cost
+    // the natural-order backward about a fifth of its time, into the slot
+    // rows nothing measurable, for the same tiles in the same order.
     if (lane == 0) {
       int gs = 0;
       for (int r = 0;; ++r) {
@@ -464,7 +484,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
+        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;
         do {
@@ -473,7 +493,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           for (int box = 0; box < C::NBOX; ++box) {
             const unsigned char* bb = box < 2 ? smem + C::OFF_DS + box * (kRows * 128)
                                               : smem + C::OFF_DO + (gs & 1) * C::TILE + (box - 2) * (kRows * 128);
-            tma_reduce_add_4d(bb, &a.tdq, box * 32, hq, mem_row<NAT>(pm, qt * kRows), u.b);
+            tma_reduce_add_4d(bb, &a.tdq, box * 32, hq, qt * kRows, u.b);  // slot order (see above)
             if (box == 1) bulk_commit_group();
           }
           if (C::NBOX > 2) {
@@ -516,7 +536,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
       const bool k_inside = u.t * kRows + kRows <= pm.S;
       {
-        const StepWalk<SHARD> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
+        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
         int hq = u.h * G, qt = -1;
         if (!w.next(pm, hq, qt)) continue;
       }
@@ -636,6 +656,23 @@ __global__ void __launch_bounds__(256) bwd_dq_round_kernel(const float* __restri
   }
 }
 
+// natural-order dq: row b*S + pos(s) of dq = scale * row b*S + s of the
+// slot-order accumulator; one row (Hq*D elements) per CTA iteration
+__global__ void __launch_bounds__(256) bwd_dq_round_nat_kernel(const float* __restrict__ acc, __nv_bfloat16* dq,
+                                                               int B, PosMap pm, int row8, float scale) {
+  for (long long r = blockIdx.x; r < (long long)B * pm.S; r += gridDim.x) {
+    const int b = int(r / pm.S), s = int(r - (long long)b * pm.S);
+    const float4* src = reinterpret_cast<const float4*>(acc) + 2 * r * row8;
+    uint4* dst = reinterpret_cast<uint4*>(dq) + ((long long)b * pm.S + pm.pos(s)) * row8;
+    for (int i = threadIdx.x; i < row8; i += blockDim.x) {
+      const float4 x = __ldcs(src + 2 * i);
+      const float4 y = __ldcs(src + 2 * i + 1);
+      dst[i] = make_uint4(pack_bf16(scale * x.x, scale * x.y), pack_bf16(scale * x.z, scale * x.w),
+                          pack_bf16(scale * y.x, scale * y.y), pack_bf16(scale * y.z, scale * y.w));
+    }
+  }
+}
+
 template <int D, bool SHARD, bool NAT>
 cudaError_t launch_fused(const BwdArgs& a, int grid, cudaStream_t st) {
   auto kern = attn_bwd_fused_kernel<D, SHARD, NAT>;
@@ -674,6 +711,15 @@ cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st) {
   }
   if (shard) return launch_fused<128, true, false>(a, grid, st);
   return nat ? launch_fused<128, false, true>(a, grid, st) : launch_fused<128, false, false>(a, grid, st);
+}
+
+cudaError_t launch_bwd_dq_round_nat(const float* acc, void* dq, const AttnShape& sh, float scale, cudaStream_t st) {
+  const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
+  long long blocks = (long long)sh.B * sh.S;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  bwd_dq_round_nat_kernel<<<(int)blocks, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(dq), sh.B, pm,
+                                                       sh.Hq * sh.Dqk / 8, scale);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, float scale, cudaStream_t st) {

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const PosMap pm = PosMap::make(a.sh.S, a.sh.cp, a.sh.lb);
-  const Abort ab{abort_flag, a.err};
+  const Abort ab{abort_flag, a.err, a.wait_limit};
 
   if (tid == 0) {
     mbar_init(&bar.q_full, 1);
@@ -139,6 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       int qph = 0;
       int ng = 0, nq = 0;  // ring stages and Q loads issued
       bool ok = true;
+      // test hook (fault_skip_stage): one stage's loads are left out, so its
+      // full barrier never completes and the MMA thread's bounded wait on it
+      // runs out; everything after that is the ordinary abort path
+      auto skipped = [&]() { return ng == a.fault_skip_stage; };
       // claim ring stage ng for `bytes` of loads (its K slot, and its V slot
       // when it carries V, must have been released)
       auto claim = [&](bool with_v, uint32_t bytes) {
@@ -148,10 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int pg = ng - 1;  // the stage before holds the one V slot
           if (!(ok = mbar_wait(&bar.kv_empty[pg % C::NK], (pg / C::NK) & 1, ab))) return false;
         }
-        mbar_expect_tx(&bar.kv_full[i], bytes);
+        if (!skipped()) mbar_expect_tx(&bar.kv_full[i], bytes);
         return true;
       };
       auto load_k = [&](int kt, const FwdUnit& u) {
+        if (skipped()) return;
         const int i = ng % C::NK;
         for (int bx = 0; bx < DQK / 64; ++bx) {
           unsigned char* dst = smem + C::OFF_K + i * C::K_BYTES + bx * BN * 128;
@@ -162,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       };
       auto load_v = [&](int kt, const FwdUnit& u) {
+        if (skipped()) return;
         const int i = ng % C::NK, vi = ng % C::NV;
         for (int bx = 0; bx < DV / 64; ++bx)
           tma_load_4d(smem + C::OFF_V + vi * C::V_BYTES + bx * BN * 128, &a.tv, &bar.kv_full[i], bx * 64, u.hkv,
@@ -222,12 +228,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       if (!ok) {
-        // let the copies already issued land (bounded) before the CTA exits
-        volatile int own = 0;
-        const Abort quiet{&own, a.err};
+        // let the copies already issued land before the CTA exits: each wait
+        // bounded on its own (a stage that never completes does not cut the
+        // others' waits short)
+        auto drain = [&](uint64_t* b, uint32_t parity) {
+          volatile int own = 0;
+          mbar_wait(b, parity, Abort{&own, a.err, a.wait_limit});
+        };
         // stage g's loads complete phase g / NK of its barrier
-        for (int g = ng - 1; g >= 0 && g >= ng - C::NK; --g) mbar_wait(&bar.kv_full[g % C::NK], (g / C::NK) & 1, quiet);
-        if (nq > 0) mbar_wait(&bar.q_full, (nq - 1) & 1, quiet);
+        for (int g = ng - 1; g >= 0 && g >= ng - C::NK; --g) drain(&bar.kv_full[g % C::NK], (g / C::NK) & 1);
+        if (nq > 0) drain(&bar.q_full, (nq - 1) & 1);
       }
     }
   } else if (warp == 9) {
@@ -308,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       // wait for every issued MMA before TMEM is released
-      mma_commit(&bar.done);
-      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+      mma_drain(&bar.done, a.err, a.wait_limit);
     }
   }
   } else {

@@ -181,16 +181,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+constexpr long long kWaitLimitCycles = 4000000000LL;  // about two seconds
+
 // Abort state shared by all roles of a CTA.  A wait that runs out of time
-// records DEV_TIMEOUT in the global error word and raises the CTA's abort
-// flag; every other wait then gives up promptly, the roles leave their
-// loops and the CTA frees its TMEM and exits.
+// (limit SM clock cycles) records DEV_TIMEOUT in the global error word and
+// raises the CTA's abort flag; every other wait then gives up promptly, the
+// roles leave their loops and the CTA frees its TMEM and exits.
 struct Abort {
   volatile int* flag;  // shared memory
   int* err;            // global error word
+  long long limit = kWaitLimitCycles;
 };
-
-constexpr long long kWaitLimitCycles = 4000000000LL;  // about two seconds
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab) {
   const uint32_t a = smem_u32(bar);
@@ -200,7 +201,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_try(a, parity)) return true;
     if ((it & 63) == 0) {
       if (*ab.flag) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > ab.limit) {
         *ab.flag = 1;
         atomicExch(ab.err, DEV_TIMEOUT);
         __threadfence_block();
@@ -292,6 +293,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// Commit, then wait until every tcgen05 operation this thread issued has
+// completed, before the CTA releases its TMEM.  Bounded, but it does not give
+// up on the CTA's abort flag: after an abort the MMAs already issued still
+// complete (they wait on nothing), and TMEM must not be freed under them.
+__device__ __forceinline__ void mma_drain(uint64_t* done, int* err, long long limit = kWaitLimitCycles) {
+  mma_commit(done);
+  volatile int own = 0;
+  mbar_wait(done, 0, Abort{&own, err, limit});
 }
 
 // instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation

@@ -597,8 +597,7 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
           issue_s(k + 2);
         }
       }
-      mma_commit(&bar.done);
-      mbar_wait(&bar.done, 0, Abort{abort_flag, a.err});
+      mma_drain(&bar.done, a.err);
     }
   } else {
     // ---------------------------------------------------------- softmax + epilogue
@@ -726,13 +725,15 @@ __global__ void __launch_bounds__(kCombineThreads) gqa_decode_combine_kernel(Dec
   const int bg = blockIdx.x;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int G = a.Hq / a.Hkv;
+  // launched early (programmatic dependent launch): the partials are
+  // complete and visible once the attention grid has finished, and so is
+  // every input written before it (the attention grid itself waits for its
+  // predecessors), so lens is read only after the wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int len = a.lens[b];
   len = len < 0 ? 0 : (len > a.Smax ? a.Smax : len);
   const int nsplit = (len + kDecodeSplit - 1) / kDecodeSplit;
   if (nsplit <= 1) return;
-  // launched early (programmatic dependent launch): the partials are
-  // complete and visible once the attention grid has finished
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* ml0 = a.part_ml + (size_t)bg * max_split * GMAX * 2;
   const float* po = a.part_o + (size_t)bg * max_split * GMAX * D;
   __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.Hq + (size_t)g * G) * D;
@@ -856,7 +857,7 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-int decode_max_split(int Smax) { return (Smax + kDecodeSplit - 1) / kDecodeSplit; }
+int decode_max_split(int Smax) { return (int)(((long long)Smax + kDecodeSplit - 1) / kDecodeSplit); }
 
 static int gmax_of(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16; }
 
@@ -918,6 +919,28 @@ cudaError_t noalloc_scratch(int dev, unsigned char** out) {
   }
   *out = g_noalloc_ptr[dev];
   return cudaSuccess;
+}
+
+// Read the array's error word (and clear it) on the current device, with
+// plain symbol copies that allocate nothing; 0 if the array was never used
+// there.  The caller has synchronised the stream the calls ran on.
+cudaError_t noalloc_take_error(int* word) {
+  *word = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) return cudaSuccess;
+  }
+  if ((e = cudaMemcpyFromSymbol(word, cpattn_noalloc_scratch, sizeof(int), 0, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return e;
+  if (*word != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(cpattn_noalloc_scratch, &zero, sizeof(int), 0, cudaMemcpyHostToDevice);
+  }
+  return e;
 }
 
 cudaError_t launch_gqa_decode_noalloc(const void* q, const void* kc, const void* vc, const int* lens, void* out,

@@ -43,6 +43,27 @@ size_t noalloc_decode_bytes(int B, int Hq, int Hkv, int Smax, int D);
 size_t noalloc_decode_limit();
 cudaError_t launch_gqa_decode_noalloc(const void* q, const void* kc, const void* vc, const int* lens, void* out,
                                       int B, int Hq, int Hkv, int Smax, int D, cudaStream_t st);
+// read and clear the allocation-free decode's error word on the current device
+// (symbol copies only; 0 if that decode never ran there)
+cudaError_t noalloc_take_error(int* word);
+
+// absorbed-MLA decode: latent rows of 576 columns (512 compressed KV, then 64
+// rope) shared by every head; value = the first 512 columns
+struct MlaDecodeArgs {
+  CUtensorMap tq, tk;
+  const void* q;     // [B, H, 576] bf16
+  const void* ckv;   // [B, Smax, 576] bf16
+  const int* lens;   // [B]
+  void* out;         // [B, H, 512] bf16
+  float* part_o;     // [B][nch][H][512] fp32 chunk partials
+  float* part_ml;    // [B][nch][H][2] (row max in the log2 domain, row sum)
+  int* err;
+  int B, H, Smax, nch;
+  float scale_log2;
+};
+int mla_decode_chunks(int Smax);  // 256-position chunks of a cache of Smax
+int mla_decode_max_batch();
+cudaError_t launch_mla_decode(const MlaDecodeArgs& a, int num_sms, cudaStream_t st);
 
 // ---- attention ------------------------------------------------------------
 struct AttnShape {
@@ -74,6 +95,8 @@ struct FwdArgs {
   AttnShape sh;
   float scale_log2;
   int* err;
+  long long wait_limit;  // SM clock cycles a pipeline wait may take before it gives up
+  int fault_skip_stage;  // test hook: the producer skips this ring stage's loads (-1: none)
 };
 cudaError_t launch_attn_fwd(const FwdArgs& a, int grid, cudaStream_t st);
 int attn_fwd_smem_bytes(int Dqk, int Dv);
@@ -112,6 +135,8 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
 bool bwd_fused_supported(int Dqk, int Dv);
 cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, float scale, cudaStream_t st);
+// natural-order tensors (zero-copy load balance): the accumulator is in slot order
+cudaError_t launch_bwd_dq_round_nat(const float* acc, void* dq, const AttnShape& sh, float scale, cudaStream_t st);
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, int grid, cudaStream_t st);
 int bwd_dkdv_q_tile(int Dqk);  // query rows per step of the dk/dv kernel

@@ -1,0 +1,388 @@
+// Absorbed-MLA decode on tcgen05 tensor cores.
+//
+// MLA attention under context parallelism ("Add support for EP to context
+// parallelism in self-attention", Main code changes) at decode time: one new
+// query token per sequence against the cache ("Add Pallas GPU decode
+// attention in Maxtext inference", Description).  In the absorbed form every
+// query head reads the same cached latent row per token, 576 columns: the
+// 512-column compressed KV followed by the 64-column rope key.  The row is
+// the key of every head, and its first 512 columns are the value:
+//   out[b, h] = sum_{t < lens[b]} softmax_t(scale q[b, h] . ckv[b, t]) ckv[b, t, :512].
+//
+// Work item = (sequence b, chunk of 256 positions, value half v): with the
+// heads as the MMA rows,
+//   S = Q K^T   M = 128 heads, N = 256 positions, K = 576 (nine 64-column boxes)
+//   O = P V_v   M = 128 heads, N = 4 x 64 value columns, K = 256 positions
+// TMEM: S in columns [0, 256), the item's half of O in [256, 512).  Both
+// halves of a chunk compute the same S (the scores are cheap next to the
+// cache read), so each CTA holds 256 value columns; the two halves are
+// neighbouring items, run by neighbouring CTAs at the same time, so the
+// second read of the chunk's rows comes from L2.  Each item writes its
+// partial (o, row max, row sum); a second kernel merges the chunks of each
+// (b, h).  Persistent grid, one CTA per SM, items numbered densely over the
+// sequences' valid chunks and dealt round-robin.
+//
+// Roles (192 threads): warps 0-3 softmax and epilogue (thread = head row =
+// TMEM lane), warp 4 TMA producer, warp 5 MMA issuer.  One ring of three
+// 48 KB stages carries, per item, nine (Q box, K box) pairs for S and then
+// the four value boxes of the item's half.  Positions of the last chunk at or
+// past lens[b] get zero weight; their value rows are zeroed in shared memory
+// before O reads them, so whatever the cache holds there cannot reach the
+// output.
+#include "common.cuh"
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int kMdThreads = 192;
+constexpr int kMdDk = 576, kMdDv = 512;
+constexpr int kMdRows = 128;               // heads per MMA (rows past H are zero)
+constexpr int kMdT = 256;                  // positions per chunk
+constexpr int kMdKBoxes = kMdDk / 64;      // 9
+constexpr int kMdVBoxes = kMdDv / 2 / 64;  // 4 per half
+constexpr int kMdStagesPerItem = kMdKBoxes + kMdVBoxes;
+constexpr int kMdNS = 3;
+constexpr int kMdQBox = kMdRows * 128;   // 16 KB
+constexpr int kMdKBox = kMdT * 128;      // 32 KB
+constexpr int kMdStage = kMdQBox + kMdKBox;
+constexpr int kMdOffP = kMdNS * kMdStage;          // P: 4 boxes of 64 positions x 128 rows
+constexpr int kMdPBytes = 4 * kMdRows * 128;       // 64 KB
+constexpr int kMdOffBar = kMdOffP + kMdPBytes;
+constexpr int kMdOffMisc = kMdOffBar + 256;
+constexpr int kMdMaxB = 1024;
+constexpr int kMdOffLens = kMdOffMisc + 64;
+constexpr int kMdOffPre = kMdOffLens + kMdMaxB * 4;
+constexpr int kMdSmem = kMdOffPre + (kMdMaxB + 1) * 4 + 1024;
+static_assert(kMdSmem <= 232448, "shared memory budget");
+static_assert(kMdStage % 1024 == 0 && kMdOffP % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+struct MdBars {
+  uint64_t full[kMdNS], empty[kMdNS];
+  uint64_t s_full, s_free, p_full, o_full, o_free;
+  uint64_t vfix[kMdVBoxes];
+  uint64_t done;
+};
+static_assert(sizeof(MdBars) <= 256, "barrier area");
+
+struct MdItem {
+  int b, chunk, half, len;
+};
+// dense item j -> (b, chunk, half): pre[b] = items of the sequences before b
+// (two per valid chunk), pre[B] = the total
+__device__ __forceinline__ MdItem md_item(int j, const int* pre, const int* lens, int B) {
+  int lo = 0, hi = B - 1;  // largest b with pre[b] <= j
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= j) lo = mid;
+    else hi = mid - 1;
+  }
+  const int r = j - pre[lo];
+  return MdItem{lo, r >> 1, r & 1, lens[lo]};
+}
+
+__global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_constant__ MlaDecodeArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  MdBars& bar = *reinterpret_cast<MdBars*>(smem + kMdOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMdOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMdOffMisc + 16);
+  int* lens_s = reinterpret_cast<int*>(smem + kMdOffLens);
+  int* pre = reinterpret_cast<int*>(smem + kMdOffPre);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ncta = gridDim.x, cta = blockIdx.x;
+  const Abort ab{abort_flag, a.err};
+  // the merge grid (a programmatic dependent) may be scheduled now; it waits
+  // for this grid before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  if (tid == 0) {
+    for (int i = 0; i < kMdNS; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.s_free, 128);
+    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.o_full, 1);
+    mbar_init(&bar.o_free, 128);
+    for (int i = 0; i < kMdVBoxes; ++i) mbar_init(&bar.vfix[i], 128);
+    mbar_init(&bar.done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (warp == 4 && lane == 0) { prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); }
+  // stage (and validate) the lengths, then number the items
+  for (int bb = tid; bb < a.B; bb += kMdThreads) {
+    const int l = a.lens[bb];
+    if ((l < 0 || l > a.Smax) && cta == 0) atomicExch(a.err, DEV_LENS_CLAMPED);
+    lens_s[bb] = l < 0 ? 0 : (l > a.Smax ? a.Smax : l);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix of items per sequence: each lane scans a run of sequences
+    const int per = (a.B + 31) / 32, b0 = lane * per, b1 = min(a.B, b0 + per);
+    int run = 0;
+    for (int bb = b0; bb < b1; ++bb) run += 2 * ((lens_s[bb] + kMdT - 1) / kMdT);
+    int inc = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    int acc = inc - run;
+    for (int bb = b0; bb < b1; ++bb) {
+      pre[bb] = acc;
+      acc += 2 * ((lens_s[bb] + kMdT - 1) / kMdT);
+    }
+    if (lane == 31) pre[a.B] = inc;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = pre[a.B];
+  const int n_items = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // items j = cta + k * ncta
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int g = 0;  // ring stage counter
+      bool ok = true;
+      for (int k = 0; k < n_items && ok; ++k) {
+        const MdItem it = md_item(cta + k * ncta, pre, lens_s, a.B);
+        for (int s = 0; s < kMdStagesPerItem; ++s, ++g) {
+          const int st = g % kMdNS;
+          if (!(ok = mbar_wait(&bar.empty[st], ((g / kMdNS) & 1) ^ 1, ab))) break;
+          unsigned char* sb = smem + st * kMdStage;
+          if (s < kMdKBoxes) {  // query box and key box s
+            mbar_expect_tx(&bar.full[st], kMdStage);
+            tma_load_3d(sb, &a.tq, &bar.full[st], s * 64, 0, it.b);
+            tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], s * 64, it.chunk * kMdT, it.b);
+          } else {  // value box of this half, in the key slot
+            const int vb = it.half * kMdVBoxes + (s - kMdKBoxes);
+            mbar_expect_tx(&bar.full[st], kMdKBox);
+            tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], vb * 64, it.chunk * kMdT, it.b);
+          }
+        }
+      }
+      if (!ok) {  // let the copies already issued land (each wait bounded on its own)
+        for (int h = g - 1; h >= 0 && h >= g - kMdNS; --h) {
+          volatile int own = 0;
+          mbar_wait(&bar.full[h % kMdNS], (h / kMdNS) & 1, Abort{&own, a.err});
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(kMdRows, kMdT, 0, 0);  // Q (K-major) x K (K-major)
+      constexpr uint32_t IDESC_O = idesc_bf16(kMdRows, 64, 0, 1);    // P (K-major) x V (MN-major)
+      const uint32_t s0 = smem_u32(smem);
+      const uint64_t pdesc = sdesc_sw128(s0 + kMdOffP, 16, 1024);
+      int g = 0, nfix = 0;
+      bool ok = true;
+      for (int k = 0; k < n_items && ok; ++k) {
+        const MdItem it = md_item(cta + k * ncta, pre, lens_s, a.B);
+        const bool partial = it.len - it.chunk * kMdT < kMdT;
+        if (k > 0 && !(ok = mbar_wait(&bar.s_free, (k - 1) & 1, ab))) break;  // S columns read out
+        for (int c = 0; c < kMdKBoxes; ++c, ++g) {
+          const int st = g % kMdNS;
+          if (!(ok = mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab))) break;
+          tc_fence_after();
+          const uint64_t qd = sdesc_sw128(s0 + st * kMdStage, 16, 1024);
+          const uint64_t kd = sdesc_sw128(s0 + st * kMdStage + kMdQBox, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar.empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bar.s_full);
+        if (!(ok = mbar_wait(&bar.p_full, k & 1, ab))) break;
+        if (k > 0 && !(ok = mbar_wait(&bar.o_free, (k - 1) & 1, ab))) break;  // O columns read out
+        tc_fence_after();
+        for (int i = 0; i < kMdVBoxes; ++i, ++g) {
+          const int st = g % kMdNS;
+          if (!(ok = mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab))) break;
+          if (partial && !(ok = mbar_wait(&bar.vfix[i], nfix & 1, ab))) break;  // rows past the length zeroed
+          tc_fence_after();
+          const uint64_t vd = sdesc_sw128(s0 + st * kMdStage + kMdQBox, kMdKBox, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kMdT / 16; ++kk)
+            mma_ss(tmem + 256 + 64 * i, pdesc + ((((kk >> 2) * (kMdRows * 128)) + (kk & 3) * 32) >> 4),
+                   vd + ((kk * 16 * 128) >> 4), IDESC_O, kk > 0 ? 1u : 0u);
+          mma_commit(&bar.empty[st]);
+        }
+        if (!ok) break;
+        if (partial) ++nfix;
+        mma_commit(&bar.o_full);
+      }
+      mma_drain(&bar.done, a.err);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax and epilogue
+    // thread r = head row = TMEM lane; a failed wait runs on (every wait is
+    // bounded and the barrier counts still complete)
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const float sl2 = a.scale_log2;
+    int nfix = 0;
+    for (int k = 0; k < n_items; ++k) {
+      const MdItem it = md_item(cta + k * ncta, pre, lens_s, a.B);
+      const int nvalid = min(kMdT, it.len - it.chunk * kMdT);  // positions of the chunk inside the cache
+      mbar_wait(&bar.s_full, k & 1, ab);
+      tc_fence_after();
+      float m = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < kMdT / 32; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base + 32 * c, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 * c + j < nvalid) m = fmaxf(m, __uint_as_float(sv[j]));
+      }
+      const float m2 = m * sl2;  // finite: every item holds at least one position
+      float l = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < kMdT / 32; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base + 32 * c, sv);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = 32 * c + j < nvalid ? fast_exp2(__uint_as_float(sv[j]) * sl2 - m2) : 0.f;
+          const float p1 = 32 * c + j + 1 < nvalid ? fast_exp2(__uint_as_float(sv[j + 1]) * sl2 - m2) : 0.f;
+          l += p0 + p1;
+          pk[j >> 1] = pack_bf16(p0, p1);
+        }
+        // P row r, positions [32c, 32c+32): box c/2, 16-byte chunks 4(c&1)..+3, 128-byte swizzle
+        unsigned char* rowp = smem + kMdOffP + (c >> 1) * (kMdRows * 128) + r * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ch = 4 * (c & 1) + q;
+          *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.s_free);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar.p_full);
+      if (nvalid < kMdT) {
+        // zero the value rows past the length (stage of value box i of item k)
+        for (int i = 0; i < kMdVBoxes; ++i) {
+          const int g = k * kMdStagesPerItem + kMdKBoxes + i;
+          const int st = g % kMdNS;
+          mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab);
+          unsigned char* vb = smem + st * kMdStage + kMdQBox;
+          for (int row = r; row < kMdT; row += 128)
+            if (row >= nvalid)
+#pragma unroll
+              for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vb + row * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+          mbar_arrive(&bar.vfix[i]);
+        }
+        ++nfix;
+      }
+      // epilogue: this item's partial (o half, row max, row sum)
+      mbar_wait(&bar.o_full, k & 1, ab);
+      tc_fence_after();
+      const size_t prow = ((size_t)it.b * a.nch + it.chunk) * a.H + r;
+#pragma unroll 1
+      for (int c = 0; c < 256 / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + lane_base + 256 + 32 * c, ov);
+        tmem_ld_wait();
+        if (r < a.H) {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kMdDv + it.half * 256 + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
+                                  __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+        }
+      }
+      if (r < a.H && it.half == 0) {
+        a.part_ml[2 * prow] = m2;
+        a.part_ml[2 * prow + 1] = l;
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.o_free);
+    }
+    (void)nfix;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// merge of the chunks of each (b, h): 128 threads, four value columns each;
+// launched as a programmatic dependent, so lens and the partials are read
+// only after the attention grid has completed
+__global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_constant__ MlaDecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x / a.H, h = blockIdx.x - b * a.H;
+  int len = a.lens[b];
+  len = len < 0 ? 0 : (len > a.Smax ? a.Smax : len);
+  const int nch = (len + kMdT - 1) / kMdT;
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.H + h) * kMdDv + 4 * threadIdx.x;
+  if (nch == 0) {  // empty cache: zeros
+    *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+    return;
+  }
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, a.part_ml[2 * (((size_t)b * a.nch + c) * a.H + h)]);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < nch; ++c) {
+    const size_t prow = ((size_t)b * a.nch + c) * a.H + h;
+    const float w = fast_exp2(a.part_ml[2 * prow] - M);
+    L = fmaf(a.part_ml[2 * prow + 1], w, L);
+    const float4 x = reinterpret_cast<const float4*>(a.part_o + prow * kMdDv)[threadIdx.x];
+    acc.x = fmaf(x.x, w, acc.x);
+    acc.y = fmaf(x.y, w, acc.y);
+    acc.z = fmaf(x.z, w, acc.z);
+    acc.w = fmaf(x.w, w, acc.w);
+  }
+  const float il = 1.f / L;
+  *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16(acc.x * il, acc.y * il), pack_bf16(acc.z * il, acc.w * il));
+}
+
+}  // namespace
+
+int mla_decode_chunks(int Smax) { return (int)(((long long)Smax + kMdT - 1) / kMdT); }
+int mla_decode_max_batch() { return kMdMaxB; }
+
+cudaError_t launch_mla_decode(const MlaDecodeArgs& a0, int num_sms, cudaStream_t st) {
+  MlaDecodeArgs a = a0;
+  const unsigned long long Dk = kMdDk;
+  unsigned long long qd[3] = {Dk, (unsigned long long)a.H, (unsigned long long)a.B};
+  unsigned long long qs[2] = {Dk * 2, (unsigned long long)a.H * Dk * 2};
+  unsigned qb[3] = {64, (unsigned)kMdRows, 1};
+  unsigned long long kd[3] = {Dk, (unsigned long long)a.Smax, (unsigned long long)a.B};
+  unsigned long long ks[2] = {Dk * 2, (unsigned long long)a.Smax * Dk * 2};
+  unsigned kb[3] = {64, (unsigned)kMdT, 1};
+  if (encode_tmap(&a.tq, a.q, 3, qd, qs, qb, 2) || encode_tmap(&a.tk, a.ckv, 3, kd, ks, kb, 2))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMdSmem);
+  if (e != cudaSuccess) return e;
+  mla_decode_kernel<<<num_sms, kMdThreads, kMdSmem, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.H);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel, a);
+}
+
+}  // namespace cpattn

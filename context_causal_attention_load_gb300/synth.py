@@ -9,7 +9,8 @@ very same bf16 values.
 
 import torch
 
-__all__ = ["attention_inputs", "attention_inputs_device", "decode_inputs", "to_f64"]
+__all__ = ["attention_inputs", "attention_inputs_device", "decode_inputs", "decode_inputs_int8",
+           "mla_decode_inputs", "to_f64"]
 
 
 def _normal(shape, seed, scale=1.0):
@@ -73,6 +74,16 @@ def decode_inputs_int8(B, Hq, Hkv, D, Smax, len_lo, len_hi, seed=0):
     gl = torch.Generator(device="cpu").manual_seed(int(seed) + 4)
     lens = torch.randint(int(len_lo), int(len_hi) + 1, (B,), generator=gl, dtype=torch.int32)
     return q, kq, vq, ks, vs, lens
+
+
+def mla_decode_inputs(B, H, Smax, len_lo, len_hi, seed=0, Dk=576):
+    """q [B,H,Dk] and latent cache ckv [B,Smax,Dk] (bf16, N(0,1)), lens [B]
+    int32 uniform in [len_lo, len_hi]."""
+    q = _normal((B, H, Dk), seed)
+    ckv = _normal((B, Smax, Dk), seed + 1)
+    g = torch.Generator(device="cpu").manual_seed(int(seed) + 4)
+    lens = torch.randint(int(len_lo), int(len_hi) + 1, (B,), generator=g, dtype=torch.int32)
+    return q, ckv, lens
 
 
 def to_f64(t):

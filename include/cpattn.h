@@ -134,10 +134,11 @@ int cp_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
  *            contribution (summing them over all shards gives dk, dv; keys
  *            no query of the shard sees get zero);
  *   dk, dv   bf16, device, may be NULL: the same partial sums rounded.
- * Requires Dqk == Dv (64 or 128) and load_balance 0 or 1; otherwise
- * CPATTN_ERR_UNSUPPORTED.  Rows of
- * a 128-row query tile that straddles a shard boundary outside the shard are
- * masked out, so the partials are exact per shard for any S.
+ * Head dims as cp_attn_bwd (the MLA dims run the two-kernel backward
+ * restricted to the shard); load_balance 0 or 1 (slot-order tensors),
+ * otherwise CPATTN_ERR_UNSUPPORTED.  Rows of a query tile that straddles a
+ * shard boundary outside the shard are masked out, so the partials are
+ * exact per shard for any S.
  */
 int cp_attn_bwd_shard(const void* q, const void* k, const void* v, const void* out, const float* lse,
                       const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
@@ -186,10 +187,32 @@ int cp_attn_bwd_mla(const void* q, const void* k_nope, const void* k_rope, const
  * q [B, Hq, D] bf16, kcache/vcache [B, Hkv, Smax, D] bf16, lens [B] int32,
  * out [B, Hq, D] bf16; all device.  lens[b] == 0 gives out = 0; lens[b]
  * outside [0, Smax] is clamped and latched as CPATTN_ERR_DEVICE_BOUNDS.
- * Requires D in {64, 128}, Hq % Hkv == 0, Hq/Hkv <= 16.
+ * Requires D in {64, 128}, Hq % Hkv == 0, Hq/Hkv <= 16, Smax <= 2^30.
  */
 int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out,
                int B, int Hq, int Hkv, int Smax, int D, cudaStream_t stream);
+
+/*
+ * Absorbed-MLA decode (MLA attention under context parallelism, "Add
+ * support for EP to context parallelism in self-attention", Main code
+ * changes, at decode time, "Add Pallas GPU decode attention in Maxtext
+ * inference", Description): one query token per sequence; every head uses
+ * the same cached latent row per token, 576 columns (the 512-column
+ * compressed KV, then the 64-column rope key), as its key and the first
+ * 512 columns of it as its value:
+ *   out[b, h] = sum_{t < lens[b]} softmax_t(scale q[b,h] . ckv[b,t]) ckv[b,t,:512].
+ * q [B, H, 576] bf16 (each head's query taken into the latent space, then
+ * its rope query), ckv [B, Smax, 576] bf16, lens [B] int32, out [B, H, 512]
+ * bf16 (the latent output, before the value up-projection); all device.
+ * scale is the softmax scale of the attention the absorption comes from
+ * (1/sqrt(192) for 128 nope + 64 rope columns).  lens[b] == 0 gives zeros;
+ * lens outside [0, Smax] is clamped and latched as CPATTN_ERR_DEVICE_BOUNDS.
+ * Cache rows at or past lens[b] are read but never reach the output.
+ * Requires 1 <= H <= 128, B <= 1024, Smax <= 2^30.  Scratch: fp32 chunk
+ * partials of B*ceil(Smax/256)*H*514 floats (library-owned, grown on demand).
+ */
+int mla_decode(const void* q, const void* ckv, const int* lens, void* out, int B, int H, int Smax, float scale,
+               cudaStream_t stream);
 
 /*
  * gqa_decode against an int8-quantised KV cache (the inference setup of
@@ -226,9 +249,11 @@ int gqa_decode_int8(const void* q, const void* kcache, const void* vcache, const
  * call shares the one array (each call writes every entry it later reads,
  * so nothing an earlier call left behind is used), and calls whose
  * executions overlap on the GPU (different streams, or several host
- * threads) race on it: serialise them.  lens outside [0, Smax] are clamped
- * as in gqa_decode; the flag goes to the array's own error word and is not
- * reported by cp_attn_check_device.
+ * threads) race on it: serialise them.  Device-side faults (lens outside
+ * [0, Smax], clamped as in gqa_decode; a pipeline wait that timed out) are
+ * latched in an error word inside the same array; cp_attn_check_device
+ * reads and clears it with symbol copies, so checking allocates nothing
+ * either.
  */
 int gqa_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* lens,
                        void* out, int B, int Hq, int Hkv, int Smax, int D, cudaStream_t stream);
@@ -275,7 +300,29 @@ typedef struct {
 int cp_attn_profile_start(void);
 int cp_attn_profile_stop(cpattn_kernel_stat* stats, int max_stats, int* n_stats);
 
-/* Synchronise `stream`, then read and clear the device error word. */
+/*
+ * Test hook for the bounded pipeline waits (no counterpart on the pages; it
+ * exists so that the timeout path can be exercised without hanging a GPU).
+ * The NEXT forward launch (cp_attn_fwd, cp_attn_fwd_shard or
+ * cp_attn_fwd_mla on any thread) leaves out the loads of ring stage `stage`
+ * in every CTA whose producer reaches that stage, and every pipeline wait
+ * of that launch gives up after wait_limit_cycles SM clock cycles instead
+ * of about two seconds.  The wait on the missing stage runs out, latches
+ * CPATTN_ERR_DEVICE_TIMEOUT in the device error word (read it with
+ * cp_attn_check_device), and every role of the CTA leaves its loop; the
+ * launch ends with out/lse undefined and the device stays usable.
+ * stage < 0 clears a pending hook.  Requires 1e5 <= wait_limit_cycles <= 4e9
+ * when stage >= 0.
+ */
+int cp_attn_test_stall_forward(int stage, long long wait_limit_cycles);
+
+/*
+ * Synchronise `stream`, then read and clear the device error words of the
+ * current device: the library's own (it exists once a call that keeps
+ * scratch has run on the device; this call never creates it) and the
+ * allocation-free decode's.  Returns CPATTN_OK, CPATTN_ERR_DEVICE_TIMEOUT or
+ * CPATTN_ERR_DEVICE_BOUNDS; allocates no device memory.
+ */
 int cp_attn_check_device(cudaStream_t stream);
 
 /* Thread-local message of the last failed call ("" if none). */

@@ -155,3 +155,13 @@ def test_binding_checks_tensors_before_the_library():
     with pytest.raises(ValueError):
         cpattn.fwd_schedule(1, 1, 1, 256, 2, 3, 4)  # load_balance must be 0, 1 or 2
     assert cpattn.fwd_schedule(1, 1, 1, 256, 2, True, 2) == [12, 0]
+
+
+def test_stall_hook_checks_its_limit():
+    """The timeout test hook takes a wait limit of 1e5..4e9 cycles; clearing
+    it is always accepted (host state only, no device work)."""
+    from context_causal_attention_load_gb300 import cpattn
+    assert lib.cp_attn_test_stall_forward(0, 10) == -1
+    assert lib.cp_attn_test_stall_forward(0, 10 ** 10) == -1
+    assert lib.cp_attn_test_stall_forward(-1, 0) == 0
+    cpattn.test_stall_forward(-1)

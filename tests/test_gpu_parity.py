@@ -175,6 +175,8 @@ def test_bwd_parity(cfg):
     (1, 320, 4, 2, 128, 128, 2, True),    # shards of 160 rows: tiles straddle the boundary
     (2, 256, 2, 2, 64, 64, 2, True),
     (1, 384, 2, 1, 128, 128, 3, False),   # natural order
+    (1, 512, 2, 2, 192, 128, 2, True),    # MLA head dims (the two-kernel backward)
+    (1, 480, 2, 2, 192, 128, 3, True),    # MLA, shards of 160 rows: 64-row steps straddle the boundary
 ])
 def test_bwd_shard_partials(cfg):
     """Per-shard backward against the oracle on that shard's rows; the shards'
@@ -209,15 +211,14 @@ def test_bwd_shard_partials(cfg):
     assert_close_grad(dv_sum.numpy(), _f64(dv_full), "sum of dv parts %s" % (cfg,))
 
 
-def test_bwd_shard_mla_unsupported():
+def test_bwd_shard_rejects_natural_order():
+    """The per-shard backward takes tensors in slot order only."""
     B, S, H, cp = 1, 256, 1, 2
-    q = torch.zeros(B, S, H, 192, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(B, S, H, 192, dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros(B, S, H, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(B, S, H, 128, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(B, S, H, 128, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(B, H, S, dtype=torch.float32, device="cuda")
     with pytest.raises(cp_.CpAttnError) as e:
-        cp_.attn_bwd_shard(q, k, v, out, lse, out, cp, 0)
+        cp_.attn_bwd_shard(q, q, q, out, lse, out, cp, 0, 2)
     assert e.value.code == -2
 
 
@@ -230,7 +231,8 @@ def test_bwd_shard_mla_unsupported():
 def test_zero_copy_matches_permuted_path(cfg):
     """load_balance=2: natural-order tensors, load-balanced schedule.  out,
     lse, dk and dv are bit-identical to permute -> attend -> unpermute (the
-    same tiles in the same order); dq agrees to its reduction order; all of
+    same tiles in the same order: the backward walks a key tile's query tiles
+    by position in both layouts); dq agrees to its reduction order; all of
     them against the oracle on the natural-order inputs."""
     B, S, Hq, Hkv, Dqk, Dv, cp = cfg
     q, k, v, dout = synth.attention_inputs(B, S, Hq, Hkv, Dqk, Dv, seed=17)
@@ -425,3 +427,53 @@ def test_mla_shared_rope_zero_copy():
             assert_close_grad(_f64(a2), _f64(a1n), "zero-copy dk_rope")
         else:
             assert torch.equal(a2, a1n), name
+
+
+# ---------------------------------------------------------------------------
+# absorbed-MLA decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [
+    # B, H, Smax, lo, hi
+    (24, 128, 2048, 1024, 2048),   # DeepSeek-V3-shaped: 128 heads, batch and lengths of the decode workload
+    (3, 128, 700, 1, 700),         # ragged chunks, lengths from 1
+    (2, 16, 512, 256, 257),        # 16 heads, around a chunk boundary
+    (1, 128, 256, 256, 256),       # one whole chunk
+    (5, 64, 1300, 0, 1300),        # may include an empty cache
+])
+def test_mla_decode_parity(cfg):
+    B, H, Smax, lo, hi = cfg
+    q, ckv, lens = synth.mla_decode_inputs(B, H, Smax, lo, hi, seed=51)
+    out = cp_.mla_decode(q.cuda(), ckv.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref = O.mla_decode(_f64(q), _f64(ckv), lens.numpy())
+    assert_close_out(_f64(out), ref, "mla decode %s" % (cfg,))
+
+
+def test_mla_decode_ignores_rows_past_the_length():
+    """Cache rows at or past lens[b] hold NaN: they get zero weight and their
+    value rows are cleared before the output product, so nothing leaks."""
+    B, H, Smax = 3, 128, 600
+    q, ckv, lens = synth.mla_decode_inputs(B, H, Smax, 1, 600, seed=52)
+    lens = torch.tensor([300, 1, 513], dtype=torch.int32)
+    dirty = ckv.clone()
+    for b in range(B):
+        dirty[b, int(lens[b]):] = float("nan")
+    out = cp_.mla_decode(q.cuda(), dirty.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref = O.mla_decode(_f64(q), _f64(ckv), lens.numpy())
+    assert bool(torch.isfinite(out.float()).all())
+    assert_close_out(_f64(out), ref, "mla decode with NaN past the lengths")
+
+
+def test_mla_decode_flags_bad_lengths():
+    q, ckv, lens = synth.mla_decode_inputs(2, 8, 300, 10, 300, seed=53)
+    bad = torch.tensor([-3, 10_000], dtype=torch.int32)
+    out = cp_.mla_decode(q.cuda(), ckv.cuda(), bad.cuda())
+    with pytest.raises(cp_.CpAttnError) as e:
+        cp_.check_device()
+    assert e.value.code == -6
+    ref = O.mla_decode(_f64(q), _f64(ckv), np.array([0, 300]))
+    assert_close_out(_f64(out), ref, "mla decode, clamped lengths")
