@@ -9,26 +9,25 @@
 // the key of every head, and its first 512 columns are the value:
 //   out[b, h] = sum_{t < lens[b]} softmax_t(scale q[b, h] . ckv[b, t]) ckv[b, t, :512].
 //
-// Work item = (sequence b, chunk of 256 positions, value half v): with the
-// heads as the MMA rows,
+// Work item = (sequence b, chunk of 256 positions), with the heads as the
+// MMA rows:
 //   S = Q K^T   M = 128 heads, N = 256 positions, K = 576 (nine 64-column boxes)
-//   O = P V_v   M = 128 heads, N = 4 x 64 value columns, K = 256 positions
-// TMEM: S in columns [0, 256), the item's half of O in [256, 512).  Both
-// halves of a chunk compute the same S (the scores are cheap next to the
-// cache read), so each CTA holds 256 value columns; the two halves are
-// neighbouring items, run by neighbouring CTAs at the same time, so the
-// second read of the chunk's rows comes from L2.  Each item writes its
-// partial (o, row max, row sum); a second kernel merges the chunks of each
-// (b, h).  Persistent grid, one CTA per SM, items numbered densely over the
-// sequences' valid chunks and dealt round-robin.
+//   O = P V     M = 128 heads, N = 8 x 64 value columns, K = 256 positions
+// TMEM: S in columns [0, 256); after the softmax has read it, O's value
+// columns 256-511 go there and columns 0-255 go to [256, 512).  Each item
+// writes its partial (o, row max, row sum); a second kernel merges the chunks
+// of each (b, h).  Persistent grid, one CTA per SM: the whole chunks of all
+// sequences are numbered first and the partial last chunks after them, and
+// items are dealt round-robin, so with about one item per SM the short
+// chunks are the ones that share an SM.
 //
 // Roles (192 threads): warps 0-3 softmax and epilogue (thread = head row =
 // TMEM lane), warp 4 TMA producer, warp 5 MMA issuer.  One ring of three
 // 48 KB stages carries, per item, nine (Q box, K box) pairs for S and then
-// the four value boxes of the item's half.  Positions of the last chunk at or
-// past lens[b] get zero weight; their value rows are zeroed in shared memory
-// before O reads them, so whatever the cache holds there cannot reach the
-// output.
+// the eight value boxes (the first 512 columns of the same rows, now from
+// L2).  Positions of a last chunk at or past lens[b] get zero weight; their
+// value rows are zeroed in shared memory before O reads them, so whatever
+// the cache holds there cannot reach the output.
 #include "common.cuh"
 #include "internal.h"
 
@@ -40,7 +39,7 @@ constexpr int kMdDk = 576, kMdDv = 512;
 constexpr int kMdRows = 128;               // heads per MMA (rows past H are zero)
 constexpr int kMdT = 256;                  // positions per chunk
 constexpr int kMdKBoxes = kMdDk / 64;      // 9
-constexpr int kMdVBoxes = kMdDv / 2 / 64;  // 4 per half
+constexpr int kMdVBoxes = kMdDv / 64;      // 8
 constexpr int kMdStagesPerItem = kMdKBoxes + kMdVBoxes;
 constexpr int kMdNS = 3;
 constexpr int kMdQBox = kMdRows * 128;   // 16 KB
@@ -52,33 +51,65 @@ constexpr int kMdOffBar = kMdOffP + kMdPBytes;
 constexpr int kMdOffMisc = kMdOffBar + 256;
 constexpr int kMdMaxB = 1024;
 constexpr int kMdOffLens = kMdOffMisc + 64;
-constexpr int kMdOffPre = kMdOffLens + kMdMaxB * 4;
-constexpr int kMdSmem = kMdOffPre + (kMdMaxB + 1) * 4 + 1024;
+constexpr int kMdOffPre = kMdOffLens + kMdMaxB * 4;            // whole chunks before each sequence
+constexpr int kMdOffPre2 = kMdOffPre + (kMdMaxB + 1) * 4;       // partial chunks before each sequence
+constexpr int kMdSmem = kMdOffPre2 + (kMdMaxB + 1) * 4 + 1024;
 static_assert(kMdSmem <= 232448, "shared memory budget");
 static_assert(kMdStage % 1024 == 0 && kMdOffP % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 struct MdBars {
   uint64_t full[kMdNS], empty[kMdNS];
-  uint64_t s_full, s_free, p_full, o_full, o_free;
+  uint64_t s_full, p_full, o_full, o_free;
   uint64_t vfix[kMdVBoxes];
   uint64_t done;
 };
 static_assert(sizeof(MdBars) <= 256, "barrier area");
 
 struct MdItem {
-  int b, chunk, half, len;
+  int b, chunk, len;
 };
-// dense item j -> (b, chunk, half): pre[b] = items of the sequences before b
-// (two per valid chunk), pre[B] = the total
-__device__ __forceinline__ MdItem md_item(int j, const int* pre, const int* lens, int B) {
-  int lo = 0, hi = B - 1;  // largest b with pre[b] <= j
+// largest b in [0, B) with pre[b] <= j
+__device__ __forceinline__ int md_search(int j, const int* pre, int B) {
+  int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (pre[mid] <= j) lo = mid;
     else hi = mid - 1;
   }
-  const int r = j - pre[lo];
-  return MdItem{lo, r >> 1, r & 1, lens[lo]};
+  return lo;
+}
+// dense item j -> (b, chunk): whole chunks first (pre_full[b] = whole chunks
+// of the sequences before b, pre_full[B] their total), then the partial last
+// chunks (pre_part[b] = sequences before b that end inside a chunk)
+__device__ __forceinline__ MdItem md_item(int j, const int* pre_full, const int* pre_part, const int* lens, int B) {
+  const int nfull = pre_full[B];
+  if (j < nfull) {
+    const int b = md_search(j, pre_full, B);
+    return MdItem{b, j - pre_full[b], lens[b]};
+  }
+  const int b = md_search(j - nfull, pre_part, B);
+  return MdItem{b, lens[b] / kMdT, lens[b]};
+}
+
+// exclusive prefix over the sequences of f(b) by one warp (each lane scans a
+// run of sequences); out[B] receives the total
+template <typename F>
+__device__ __forceinline__ void md_prefix(int B, int lane, int* out, F f) {
+  const int per = (B + 31) / 32, b0 = lane * per, b1 = min(B, b0 + per);
+  int run = 0;
+  for (int bb = b0; bb < b1; ++bb) run += f(bb);
+  int inc = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  int acc = inc - run;
+  for (int bb = b0; bb < b1; ++bb) {
+    out[bb] = acc;
+    acc += f(bb);
+  }
+  if (lane == 31) out[B] = inc;
 }
 
 __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_constant__ MlaDecodeArgs a) {
@@ -89,6 +120,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMdOffMisc + 16);
   int* lens_s = reinterpret_cast<int*>(smem + kMdOffLens);
   int* pre = reinterpret_cast<int*>(smem + kMdOffPre);
+  int* pre2 = reinterpret_cast<int*>(smem + kMdOffPre2);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ncta = gridDim.x, cta = blockIdx.x;
   const Abort ab{abort_flag, a.err};
@@ -99,7 +131,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
   if (tid == 0) {
     for (int i = 0; i < kMdNS; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
     mbar_init(&bar.s_full, 1);
-    mbar_init(&bar.s_free, 128);
     mbar_init(&bar.p_full, 128);
     mbar_init(&bar.o_full, 1);
     mbar_init(&bar.o_free, 128);
@@ -117,28 +148,13 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
     lens_s[bb] = l < 0 ? 0 : (l > a.Smax ? a.Smax : l);
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive prefix of items per sequence: each lane scans a run of sequences
-    const int per = (a.B + 31) / 32, b0 = lane * per, b1 = min(a.B, b0 + per);
-    int run = 0;
-    for (int bb = b0; bb < b1; ++bb) run += 2 * ((lens_s[bb] + kMdT - 1) / kMdT);
-    int inc = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += t;
-    }
-    int acc = inc - run;
-    for (int bb = b0; bb < b1; ++bb) {
-      pre[bb] = acc;
-      acc += 2 * ((lens_s[bb] + kMdT - 1) / kMdT);
-    }
-    if (lane == 31) pre[a.B] = inc;
-  }
+  if (warp == 0) md_prefix(a.B, lane, pre, [&](int bb) { return lens_s[bb] / kMdT; });
+  if (warp == 1) md_prefix(a.B, lane, pre2, [&](int bb) { return lens_s[bb] % kMdT ? 1 : 0; });
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = pre[a.B];
+  const int total = pre[a.B] + pre2[a.B];
   const int n_items = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // items j = cta + k * ncta
 
   if (warp == 4) {
@@ -147,7 +163,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
       int g = 0;  // ring stage counter
       bool ok = true;
       for (int k = 0; k < n_items && ok; ++k) {
-        const MdItem it = md_item(cta + k * ncta, pre, lens_s, a.B);
+        const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
         for (int s = 0; s < kMdStagesPerItem; ++s, ++g) {
           const int st = g % kMdNS;
           if (!(ok = mbar_wait(&bar.empty[st], ((g / kMdNS) & 1) ^ 1, ab))) break;
@@ -156,8 +172,8 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
             mbar_expect_tx(&bar.full[st], kMdStage);
             tma_load_3d(sb, &a.tq, &bar.full[st], s * 64, 0, it.b);
             tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], s * 64, it.chunk * kMdT, it.b);
-          } else {  // value box of this half, in the key slot
-            const int vb = it.half * kMdVBoxes + (s - kMdKBoxes);
+          } else {  // value box, in the key slot
+            const int vb = s - kMdKBoxes;
             mbar_expect_tx(&bar.full[st], kMdKBox);
             tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], vb * 64, it.chunk * kMdT, it.b);
           }
@@ -180,9 +196,9 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
       int g = 0, nfix = 0;
       bool ok = true;
       for (int k = 0; k < n_items && ok; ++k) {
-        const MdItem it = md_item(cta + k * ncta, pre, lens_s, a.B);
+        const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
         const bool partial = it.len - it.chunk * kMdT < kMdT;
-        if (k > 0 && !(ok = mbar_wait(&bar.s_free, (k - 1) & 1, ab))) break;  // S columns read out
+        if (k > 0 && !(ok = mbar_wait(&bar.o_free, (k - 1) & 1, ab))) break;  // the last O read out
         for (int c = 0; c < kMdKBoxes; ++c, ++g) {
           const int st = g % kMdNS;
           if (!(ok = mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab))) break;
@@ -196,8 +212,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
         }
         if (!ok) break;
         mma_commit(&bar.s_full);
-        if (!(ok = mbar_wait(&bar.p_full, k & 1, ab))) break;
-        if (k > 0 && !(ok = mbar_wait(&bar.o_free, (k - 1) & 1, ab))) break;  // O columns read out
+        if (!(ok = mbar_wait(&bar.p_full, k & 1, ab))) break;  // P written, S read: its columns take O
         tc_fence_after();
         for (int i = 0; i < kMdVBoxes; ++i, ++g) {
           const int st = g % kMdNS;
@@ -207,7 +222,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
           const uint64_t vd = sdesc_sw128(s0 + st * kMdStage + kMdQBox, kMdKBox, 1024);
 #pragma unroll
           for (int kk = 0; kk < kMdT / 16; ++kk)
-            mma_ss(tmem + 256 + 64 * i, pdesc + ((((kk >> 2) * (kMdRows * 128)) + (kk & 3) * 32) >> 4),
+            mma_ss(tmem + (i < 4 ? 256 + 64 * i : 64 * (i - 4)), pdesc + ((((kk >> 2) * (kMdRows * 128)) + (kk & 3) * 32) >> 4),
                    vd + ((kk * 16 * 128) >> 4), IDESC_O, kk > 0 ? 1u : 0u);
           mma_commit(&bar.empty[st]);
         }
@@ -226,7 +241,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
     const float sl2 = a.scale_log2;
     int nfix = 0;
     for (int k = 0; k < n_items; ++k) {
-      const MdItem it = md_item(cta + k * ncta, pre, lens_s, a.B);
+      const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
       const int nvalid = min(kMdT, it.len - it.chunk * kMdT);  // positions of the chunk inside the cache
       mbar_wait(&bar.s_full, k & 1, ab);
       tc_fence_after();
@@ -265,7 +280,6 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
         }
       }
       tc_fence_before();
-      mbar_arrive(&bar.s_free);
       fence_proxy_async_smem();
       mbar_arrive(&bar.p_full);
       if (nvalid < kMdT) {
@@ -284,24 +298,25 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
         }
         ++nfix;
       }
-      // epilogue: this item's partial (o half, row max, row sum)
+      // epilogue: this item's partial (o, row max, row sum); value columns
+      // 0-255 are in TMEM [256, 512), 256-511 in [0, 256)
       mbar_wait(&bar.o_full, k & 1, ab);
       tc_fence_after();
       const size_t prow = ((size_t)it.b * a.nch + it.chunk) * a.H + r;
 #pragma unroll 1
-      for (int c = 0; c < 256 / 32; ++c) {
+      for (int c = 0; c < kMdDv / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + 256 + 32 * c, ov);
+        tmem_ld32(tmem + lane_base + (c < 8 ? 256 + 32 * c : 32 * (c - 8)), ov);
         tmem_ld_wait();
         if (r < a.H) {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kMdDv + it.half * 256 + 32 * c);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kMdDv + 32 * c);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)
             dst[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
                                   __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
         }
       }
-      if (r < a.H && it.half == 0) {
+      if (r < a.H) {
         a.part_ml[2 * prow] = m2;
         a.part_ml[2 * prow + 1] = l;
       }
