@@ -819,6 +819,29 @@ def measure_workload(name, peaks, cpattn, dev, seed, steps=None, warmup=3):
     return res
 
 
+def run_only(args):
+    """One decode measurement alone (for profiling it): prints its JSON."""
+    import torch
+    from context_causal_attention_load_gb300 import build as cbuild
+    from context_causal_attention_load_gb300 import synth
+    cbuild.build()
+    from context_causal_attention_load_gb300 import cpattn
+    cpattn.load()
+    dev = torch.device("cuda", 0)
+    D = DECODE
+    dq_, dkc, dvc, dlens = (x.to(dev) for x in synth.decode_inputs(D["B"], D["Hq"], D["Hkv"], D["D"], D["Smax"],
+                                                                   D["lo"], D["hi"], seed=args.seed + 4))
+    lens_host = dlens.cpu().tolist()
+    peaks, _ = load_peaks()
+    if args.only == "decode":
+        r = measure_decode(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn, iters=args.steps)
+    elif args.only == "decode_int8":
+        r = measure_decode_int8(dq_, dkc, dvc, dlens, lens_host, peaks, cpattn, iters=args.steps)
+    else:
+        r = measure_mla_decode(lens_host, peaks, cpattn, dev, args.seed, iters=args.steps)
+    print(json.dumps({args.only: r}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -828,11 +851,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip e2e/decode/shard/cpu measurements")
+    ap.add_argument("--only", choices=["decode", "decode_int8", "mla_decode"],
+                    help="time one decode measurement alone (--steps launches) and print it")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     w = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.only:
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args, w, args.workload)
     else:
         run_ours(args, w, args.workload)

@@ -160,33 +160,90 @@ __device__ __forceinline__ void ew_p(uint32_t t_s, uint32_t t_pk, const float* l
 // sees the top of the sequence, so the CTAs working on key tiles of the same
 // head start on the same query tile and move through the same Q/dO tiles (and
 // the same dQ accumulator rows) at about the same time: those tiles come from
-// DRAM once and from L2 for the others.  Natural-order tensors then also load
-// consecutive rows of memory, and permuted and natural-order tensors go
-// through the same steps in the same order.  Otherwise (chunks that are not
-// whole tiles, or one shard's steps) the tiles are walked in slot order.
+// DRAM once and from L2 for the others.  Permuted and natural-order tensors
+// go through the same steps in the same order.  The walk keeps the chunk and
+// the offset in it of the current position tile, so a step costs no integer
+// division (the producer computes it on the path that feeds the MMAs).
+// Otherwise (chunks that are not whole tiles, or one shard's steps) the tiles
+// are walked in slot order.
 template <bool SHARD, bool NAT>
-struct StepWalk {
+struct StepIter {
   int h_end, kmin, lo, hi;
-  __device__ __forceinline__ int next_tile(const PosMap& pm, int qt) const {
-    if (!SHARD && (NAT || pm.lb == 0 || pm.c % kRows == 0)) {
-      const int pt = qt < 0 ? (pm.S + kRows - 1) / kRows - 1 : pm.pos(qt * kRows) / kRows - 1;
-      return pt >= kmin / kRows ? pm.slot(pt * kRows) / kRows : -1;
+  bool posw;              // walk by descending position
+  int tpc, first, top;    // tiles per chunk; position tiles holding kmin and the sequence's end
+  int hq, qt, pt, ch, off;  // current step: query head, slot tile, position tile, its chunk and offset
+
+  __device__ __forceinline__ void init(const PosMap& pm, int h0, int h_end_, int kmin_, int lo_, int hi_) {
+    h_end = h_end_;
+    kmin = kmin_;
+    lo = lo_;
+    hi = hi_;
+    hq = h0;
+    posw = !SHARD && (NAT || pm.lb == 0 || pm.c % kRows == 0);
+    tpc = pm.lb ? pm.c / kRows : 1;
+    first = kmin / kRows;
+    top = (pm.S + kRows - 1) / kRows - 1;
+  }
+  __device__ __forceinline__ void to_top(const PosMap& pm) {
+    pt = top;
+    if (pm.lb) {
+      ch = 2 * pm.cp - 1;
+      off = tpc - 1;
+      qt = pm.mem_chunk_of(ch) * tpc + off;
+    } else {
+      qt = pt;
     }
-    if (!SHARD) return next_q_tile(pm, kRows, qt, kmin);
-    if (qt < 0) qt = lo / kRows - 1;  // no tile before the shard's first can qualify
-    for (qt = next_q_tile(pm, kRows, qt, kmin); qt >= 0; qt = next_q_tile(pm, kRows, qt, kmin)) {
-      if (qt * kRows >= hi) return -1;  // tiles come in increasing slot order
-      if (qt * kRows + kRows > lo) return qt;
+  }
+  __device__ __forceinline__ int slot_order_tile(const PosMap& pm, int cur) const {
+    if (!SHARD) return next_q_tile(pm, kRows, cur, kmin);
+    if (cur < 0) cur = lo / kRows - 1;  // no tile before the shard's first can qualify
+    for (cur = next_q_tile(pm, kRows, cur, kmin); cur >= 0; cur = next_q_tile(pm, kRows, cur, kmin)) {
+      if (cur * kRows >= hi) return -1;  // tiles come in increasing slot order
+      if (cur * kRows + kRows > lo) return cur;
     }
     return -1;
   }
-  __device__ __forceinline__ bool next(const PosMap& pm, int& hq, int& qt) const {
-    qt = next_tile(pm, qt);
+  // first step of the unit; false if no query tile sees the key tile
+  __device__ __forceinline__ bool begin(const PosMap& pm) {
+    if (posw) {  // the top tile sees every key
+      to_top(pm);
+      return true;
+    }
+    for (;; ) {
+      qt = slot_order_tile(pm, -1);
+      if (qt >= 0) return true;
+      if (++hq >= h_end) return false;
+    }
+  }
+  // advance to the next step; false after the unit's last one
+  __device__ __forceinline__ bool next(const PosMap& pm) {
+    if (posw) {
+      if (pt > first) {
+        --pt;
+        if (pm.lb) {
+          if (--off < 0) {
+            --ch;
+            off = tpc - 1;
+          }
+          qt = pm.mem_chunk_of(ch) * tpc + off;
+        } else {
+          qt = pt;
+        }
+        return true;
+      }
+      if (++hq >= h_end) return false;
+      to_top(pm);
+      return true;
+    }
+    qt = slot_order_tile(pm, qt);
     if (qt >= 0) return true;
     if (++hq >= h_end) return false;
-    qt = next_tile(pm, -1);
+    qt = slot_order_tile(pm, -1);
     return qt >= 0;
   }
+  // memory row of the current query tile: natural-order tensors keep a
+  // position tile at its position, the others a slot tile at its slot
+  __device__ __forceinline__ int mem_row() const { return NAT ? pt * kRows : qt * kRows; }
 };
 
 // memory row of slot `slot`: natural-order tensors (NAT, load_balance 2) keep
@@ -279,9 +336,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       const BwdUnit u = a.units[ui];
       int kmin, kmax;
       pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-      const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
-      int hq = u.h * G, qt = -1;
-      if (!w.next(pm, hq, qt)) continue;
+      StepIter<SHARD, NAT> it;
+      it.init(pm, u.h * G, u.h * G + G, kmin, a.q_lo, a.q_hi);
+      if (!it.begin(pm)) continue;
       do {
         mbar_wait(&bar.dq_full, gs & 1, ab);  // runs on after an abort: the staging is garbage, the waits bounded
         tc_fence_after();
@@ -303,7 +360,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         fence_proxy_async_smem();
         mbar_arrive(&bar.staged);
         ++gs;
-      } while (w.next(pm, hq, qt));
+      } while (it.next(pm));
     }
   };
 
@@ -325,41 +382,47 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
-        int hq = u.h * G, qt = -1;
-        if (!w.next(pm, hq, qt)) continue;  // every role skips a unit no query sees
+        StepIter<SHARD, NAT> it;
+        it.init(pm, u.h * G, u.h * G + G, kmin, a.q_lo, a.q_hi);
+        if (!it.begin(pm)) continue;  // every role skips a unit no query sees
+        // everything a load needs is computed before the wait that releases
+        // its stage: the dO stage is freed late (it stages dQ), and any work
+        // between that release and the load lands on the MMA chain
+        const int krow = mem_row<NAT>(pm, u.t * kRows);
+        asm volatile("" ::"r"(krow));
         if (!(ok = mbar_wait(&bar.kv_empty, (uc & 1) ^ 1, ab))) break;
         mbar_expect_tx(&bar.kv_full, 2 * C::TILE);
         for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_4d(smem + C::OFF_K + bx * kRows * 128, &a.tk, &bar.kv_full, bx * 64, u.h, mem_row<NAT>(pm, u.t * kRows), u.b);
-          tma_load_4d(smem + C::OFF_V + bx * kRows * 128, &a.tv, &bar.kv_full, bx * 64, u.h, mem_row<NAT>(pm, u.t * kRows), u.b);
+          tma_load_4d(smem + C::OFF_K + bx * kRows * 128, &a.tk, &bar.kv_full, bx * 64, u.h, krow, u.b);
+          tma_load_4d(smem + C::OFF_V + bx * kRows * 128, &a.tv, &bar.kv_full, bx * 64, u.h, krow, u.b);
         }
         bool more;
         do {
-          int nhq = hq, nqt = qt;
-          more = w.next(pm, nhq, nqt);
+          const int hq = it.hq, qt = it.qt, qrow = it.mem_row();
+          more = it.next(pm);  // (the step after this one)
           const int st = gs & 1;
           const uint32_t ph = ((gs >> 1) & 1) ^ 1;
+          const size_t vo = ((size_t)u.b * a.sh.Hq + hq) * a.Spad + (size_t)qt * kRows;
+          unsigned char* vec = smem + C::OFF_VEC + st * C::VEC_BYTES;
+          // (an empty asm that reads the values keeps the compiler from sinking
+          // their computation below the waits)
+          asm volatile("" ::"r"(qrow), "l"(vo), "r"(it.qt), "r"(it.hq), "r"((int)more));
           if (!(ok = mbar_wait(&bar.q_empty[st], ph, ab))) break;
           info[st].hq = hq;
           info[st].qt = qt;
           info[st].last = more ? 0 : 1;
           mbar_expect_tx(&bar.q_full[st], C::TILE + C::VEC_BYTES);  // (release: the info is visible to q_full's waiters)
           for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_4d(smem + C::OFF_Q + st * C::TILE + bx * kRows * 128, &a.tq, &bar.q_full[st], bx * 64, hq,
-                        mem_row<NAT>(pm, qt * kRows), u.b);
-          const size_t vo = ((size_t)u.b * a.sh.Hq + hq) * a.Spad + (size_t)qt * kRows;
-          unsigned char* vec = smem + C::OFF_VEC + st * C::VEC_BYTES;
+            tma_load_4d(smem + C::OFF_Q + st * C::TILE + bx * kRows * 128, &a.tq, &bar.q_full[st], bx * 64, hq, qrow,
+                        u.b);
           bulk_load(vec, a.lse_l2 + vo, kRows * 4, &bar.q_full[st]);
           bulk_load(vec + kRows * 4, a.delta + vo, kRows * 4, &bar.q_full[st]);
           if (!(ok = mbar_wait(&bar.do_empty[st], ph, ab))) break;
           mbar_expect_tx(&bar.do_full[st], C::TILE);
           for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_4d(smem + C::OFF_DO + st * C::TILE + bx * kRows * 128, &a.tdo, &bar.do_full[st], bx * 64, hq,
-                        mem_row<NAT>(pm, qt * kRows), u.b);
+            tma_load_4d(smem + C::OFF_DO + st * C::TILE + bx * kRows * 128, &a.tdo, &bar.do_full[st], bx * 64, hq, qrow,
+                        u.b);
           ++gs;
-          hq = nhq;
-          qt = nqt;
         } while (more);
         ++uc;
       }
@@ -420,9 +483,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
-        int hq = u.h * G, qt = -1;
-        if (!w.next(pm, hq, qt)) continue;
+        StepIter<SHARD, NAT> it;
+        it.init(pm, u.h * G, u.h * G + G, kmin, a.q_lo, a.q_hi);
+        if (!it.begin(pm)) continue;
         if (!(ok = mbar_wait(&bar.kv_full, uc & 1, ab))) break;
         tc_fence_after();
         // prologue: S and dP of the unit's first step
@@ -484,10 +547,11 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         const BwdUnit u = a.units[ui];
         int kmin, kmax;
         pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
-        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
-        int hq = u.h * G, qt = -1;
-        if (!w.next(pm, hq, qt)) continue;
+        StepIter<SHARD, NAT> it;
+        it.init(pm, u.h * G, u.h * G + G, kmin, a.q_lo, a.q_hi);
+        if (!it.begin(pm)) continue;
         do {
+          const int hq = it.hq, qt = it.qt;
           mbar_wait(&bar.staged, gs & 1, ab);  // runs on after an abort: the staging is garbage, the waits bounded
 #pragma unroll
           for (int box = 0; box < C::NBOX; ++box) {
@@ -506,7 +570,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           bulk_wait_read<0>();
           mbar_arrive(&bar.do_empty[gs & 1]);  // the dO stage (staging space) may be reloaded
           ++gs;
-        } while (w.next(pm, hq, qt));
+        } while (it.next(pm));
       }
       bulk_wait_all();  // every dQ reduce has landed before the CTA retires
     }
@@ -536,9 +600,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       pm.range(u.t * kRows, u.t * kRows + kRows, kmin, kmax);
       const bool k_inside = u.t * kRows + kRows <= pm.S;
       {
-        const StepWalk<SHARD, NAT> w{u.h * G + G, kmin, a.q_lo, a.q_hi};
-        int hq = u.h * G, qt = -1;
-        if (!w.next(pm, hq, qt)) continue;
+        StepIter<SHARD, NAT> it;
+        it.init(pm, u.h * G, u.h * G + G, kmin, a.q_lo, a.q_hi);
+        if (!it.begin(pm)) continue;
       }
       bool last;
       do {
