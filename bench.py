@@ -601,10 +601,14 @@ def measure_lb_off(w, q, k, v, dout, f_step, peaks, cpattn, n=3):
             "what": "fwd + bwd, load_balance = 0, natural order, no permutes, no decode"}
 
 
-def measure_decode(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
-    """Decode alone, L2 flushed before every timed launch: a 512 MB write,
-    then a 512 MB read of another buffer so that the written lines are
-    already back in HBM (no write-back traffic inside the timed launch)."""
+def measure_decode(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30, layers=32):
+    """Decode alone, two ways.  Cold: one call per timed region with L2
+    flushed before it (a 512 MB write, then a 512 MB read of another buffer
+    so that the written lines are already back in HBM); the event pair's
+    ticks are about 2 us apart here, so the mean over the calls is reported
+    next to the median.  Steady: the calls of one decode step over `layers`
+    layers, each with its own cache of the same shape (so every call streams
+    its cache from HBM), back to back in one timed region, per layer."""
     import torch
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=q.device)
     flush_rd = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=q.device)
@@ -622,12 +626,42 @@ def measure_decode(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
+    del flush, flush_rd
     ts.sort()
     med = ts[len(ts) // 2]
+    mean = sum(ts) / len(ts)
     by = decode_bytes(lens_host)
-    gbs = by / (med / 1e3) / 1e9
-    return {"us": med * 1e3, "kv_bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
-            "l2": "flushed before each launch (512 MB write + 512 MB read)"}
+    gbs = by / (mean / 1e3) / 1e9
+    res = {"us": mean * 1e3, "us_median": med * 1e3, "kv_bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+           "l2": "flushed before each launch (512 MB write + 512 MB read)"}
+    # steady state over the layers of one decode step
+    g = torch.Generator(device=q.device).manual_seed(99)
+    caches = [(torch.randn(q.shape, device=q.device, generator=g).to(q.dtype),
+               torch.randn(kc.shape, device=q.device, generator=g).to(kc.dtype),
+               torch.randn(vc.shape, device=q.device, generator=g).to(vc.dtype)) for _ in range(layers)]
+    outs = [torch.empty_like(q) for _ in range(layers)]
+    for _ in range(2):
+        for (qi, ki, vi), oi in zip(caches, outs):
+            cpattn.gqa_decode(qi, ki, vi, lens, oi)
+    torch.cuda.synchronize()
+    tl = []
+    for _ in range(7):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for (qi, ki, vi), oi in zip(caches, outs):
+            cpattn.gqa_decode(qi, ki, vi, lens, oi)
+        e1.record()
+        torch.cuda.synchronize()
+        tl.append(e0.elapsed_time(e1) / layers)
+    cpattn.check_device()
+    tl.sort()
+    per = tl[len(tl) // 2]
+    sgbs = by / (per / 1e3) / 1e9
+    res["steady"] = {"per_layer_us": per * 1e3, "layers": layers, "gbs": sgbs, "frac_of_hbm": sgbs / peaks["hbm_gbs"],
+                     "note": "one decode step: %d calls on %d distinct caches of the decode shape, back to back "
+                             "(%.1f GB of caches, far above L2)" % (layers, layers,
+                                                                   layers * 2 * kc.numel() * kc.element_size() / 1e9)}
+    return res
 
 
 def measure_zero_copy(args, w, inputs, dec_inputs, dec_out, f_step, ms_step, world, dev, cpattn):
@@ -692,11 +726,12 @@ def measure_decode_int8(q, kc, vc, lens, lens_host, peaks, cpattn, iters=30):
         ts.append(e0.elapsed_time(e1))
     ts.sort()
     med = ts[len(ts) // 2]
+    mean = sum(ts) / len(ts)  # event ticks are about 2 us apart: the mean resolves finer than the median
     n = int(sum(int(x) for x in lens_host))
     by = n * DECODE["Hkv"] * DECODE["D"] * 2 + n * DECODE["Hkv"] * 4 * 2
-    gbs = by / (med / 1e3) / 1e9
-    return {"us": med * 1e3, "kv_bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
-            "bf16_equivalent_gbs": decode_bytes(lens_host) / (med / 1e3) / 1e9,
+    gbs = by / (mean / 1e3) / 1e9
+    return {"us": mean * 1e3, "us_median": med * 1e3, "kv_bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "bf16_equivalent_gbs": decode_bytes(lens_host) / (mean / 1e3) / 1e9,
             "l2": "flushed before each launch (512 MB write + 512 MB read)"}
 
 
@@ -731,12 +766,13 @@ def measure_mla_decode(lens_host, peaks, cpattn, dev, seed, iters=30):
         ts.append(e0.elapsed_time(e1))
     ts.sort()
     med = ts[len(ts) // 2]
+    mean = sum(ts) / len(ts)  # event ticks are about 2 us apart: the mean resolves finer than the median
     n = int(sum(int(x) for x in lens_host))
     by = n * 576 * 2 + q.numel() * 2 + out.numel() * 2
     fl = 2.0 * n * H * (576 + 512)
-    gbs = by / (med / 1e3) / 1e9
-    return {"us": med * 1e3, "bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
-            "tflops": fl / (med / 1e3) / 1e12, "frac_of_bf16": fl / (med / 1e3) / 1e12 / peaks["bf16_tflops"],
+    gbs = by / (mean / 1e3) / 1e9
+    return {"us": mean * 1e3, "us_median": med * 1e3, "bytes": by, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "tflops": fl / (mean / 1e3) / 1e12, "frac_of_bf16": fl / (mean / 1e3) / 1e12 / peaks["bf16_tflops"],
             "config": "B=%d H=%d latent 576 (value 512) Smax=%d, lengths of the decode workload" % (B, H, Smax),
             "l2": "flushed before each launch (512 MB write + 512 MB read)"}
 

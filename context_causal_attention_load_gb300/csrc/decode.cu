@@ -261,9 +261,11 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
 //   O^T = V^T P^T: M = 128 dims,      N = 16 head columns, K = 128 positions
 // so an item is 16 tcgen05 MMAs instead of thousands of FMAs.  The group's
 // G <= 16 heads are the N columns (columns past G are computed and ignored;
-// their P rows stay zero).  Persistent: one CTA per SM; only slices that hold
-// positions are items, numbered densely and dealt round-robin so every CTA
-// gets the same count to within one.  Warp 0 streams K and q with TMA through
+// their P rows stay zero).  Persistent: one CTA per SM; the items are dealt
+// round-robin, every whole 128-position slice first and the partial last
+// slices of the rows after them, so the CTAs end with the short items and
+// stream nearly the same number of bytes.  An item loads only the 32-row TMA
+// boxes that hold its positions.  Warp 0 streams K and q with TMA through
 // one 3-stage ring and warp 10 streams V through another (K is freed as soon
 // as the scores are formed, so more of the next items' bytes are in flight
 // while the softmax runs), warp 1 issues the MMAs, and two softmax groups
@@ -293,6 +295,8 @@ struct TcCfg {
   static constexpr int KSTAGE = K_BYTES + Q_BYTES;
   static constexpr int S8_BYTES = ROWS * D;     // one int8 tile: 128 rows x 128 bytes
   static constexpr int KS_STAGE = S8_BYTES + Q_BYTES;  // int8 K tile + the item's bf16 q rows
+  static constexpr int BOX = 32;                // cache rows per TMA box: an item loads ceil(n / 32) boxes
+  static constexpr int BOX_BYTES = BOX * 128;   // a box of 128-byte rows (64 bf16 columns or 128 int8 values)
   static constexpr int P_BYTES = NH * ROWS * 2;  // P^T as [head][position], two boxes of 64 positions
   static constexpr int OFF_V = NK * KSTAGE;
   static constexpr int OFF_KS = OFF_V + NV * V_BYTES;              // int8 K staging
@@ -310,6 +314,7 @@ struct TcCfg {
                     OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(ROWS == 128, "one position per softmax / converter thread");
+  static_assert(BOX_BYTES % 1024 == 0, "boxes keep the 128-byte swizzle phase");
 };
 template <int NK, int NV>
 struct TcBars {
@@ -357,25 +362,40 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, i
          (uint32_t(M >> 4) << 24);
 }
 
-// dense item j -> (b, g, slice): pre[b] = items of rows before b (Hkv slices
-// per 128 positions), pre[B] = the total
+// Item slot j of the deal: the whole 128-position slices of every row come
+// first (pre[b] = whole slices of the rows before b, over all KV heads;
+// pre[B] = their count), then one slot per row (b, g) for its partial last
+// slice, empty (n == 0) when lens[b] is a multiple of 128.  Dealing the
+// whole slices first and the short ones last evens out the bytes per CTA.
 struct Item {
-  int b, g, sp, len, nsplit;
+  int b, g, sp, len, nsplit, n;  // n: positions of the slice in the cache
 };
 __device__ __forceinline__ Item loaded_item(int j, const int* pre, const int* lens, int B, int Hkv) {
-  int lo = 0, hi = B - 1;  // largest b with pre[b] <= j (never a row without items)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pre[mid] <= j) lo = mid;
-    else hi = mid - 1;
-  }
   Item it;
-  it.b = lo;
-  it.len = lens[lo];
+  const int nfull = pre[B];
+  if (j < nfull) {
+    int lo = 0, hi = B - 1;  // largest b with pre[b] <= j: a row with whole slices
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= j) lo = mid;
+      else hi = mid - 1;
+    }
+    it.b = lo;
+    it.len = lens[lo];
+    const int nf = it.len / kDecodeSplit;
+    const int r = j - pre[lo];
+    it.g = r / nf;
+    it.sp = r - it.g * nf;
+    it.n = kDecodeSplit;
+  } else {
+    const int r = j - nfull;
+    it.b = r / Hkv;
+    it.g = r - it.b * Hkv;
+    it.len = lens[it.b];
+    it.sp = it.len / kDecodeSplit;
+    it.n = it.len - it.sp * kDecodeSplit;
+  }
   it.nsplit = (it.len + kDecodeSplit - 1) / kDecodeSplit;
-  const int r = j - pre[lo];
-  it.g = r / it.nsplit;
-  it.sp = r - it.g * it.nsplit;
   return it;
 }
 
@@ -417,7 +437,9 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
     fence_mbar_init();
   }
   if (warp == 1) { tmem_alloc(tmem_slot, 64); tmem_relinquish(); }
-  if (warp == 0 && lane == 0) { prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tq); }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tq); prefetch_tmap(&a.tk2); prefetch_tmap(&a.tv2);
+  }
   // P rows of heads past G are never written again: zero both P buffers once
   for (int i = tid; i < 2 * P_BYTES / 16; i += kThreadsTc)
     reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
@@ -430,10 +452,10 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
   }
   fence_proxy_async_smem();
   __syncthreads();
-  if (warp == 0) {  // exclusive prefix of items per row: each lane scans a run of rows
+  if (warp == 0) {  // exclusive prefix of whole slices per row: each lane scans a run of rows
     const int per = (a.B + 31) / 32, b0 = lane * per, b1 = min(a.B, b0 + per);
     int run = 0;
-    for (int bb = b0; bb < b1; ++bb) run += (lens_s[bb] + kDecodeSplit - 1) / kDecodeSplit * a.Hkv;
+    for (int bb = b0; bb < b1; ++bb) run += lens_s[bb] / kDecodeSplit * a.Hkv;
     int inc = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -443,7 +465,7 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
     int acc = inc - run;
     for (int bb = b0; bb < b1; ++bb) {
       pre[bb] = acc;
-      acc += (lens_s[bb] + kDecodeSplit - 1) / kDecodeSplit * a.Hkv;
+      acc += lens_s[bb] / kDecodeSplit * a.Hkv;
     }
     if (lane == 31) pre[a.B] = inc;
   } else {
@@ -456,52 +478,59 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S_b at cols 16b, O_b at 32 + 16b
-  const int total = pre[a.B];
-  const int n_items = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // this CTA's items k: j = cta + k*ncta
+  const int total = pre[a.B] + a.B * a.Hkv;  // item slots
+  const int n_slots = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // this CTA's slots i: j = cta + i*ncta
+  // every role walks the same slots and skips the same empty ones, so the
+  // item counter k (ring stages, buffers, phases) agrees between them
+  auto count_items = [&]() {
+    int n = 0;
+    for (int i = 0; i < n_slots; ++i) n += loaded_item(cta + i * ncta, pre, lens_s, a.B, a.Hkv).n > 0;
+    return n;
+  };
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer: K and q (int8: K staging)
+  if (warp == 0 || warp == 10) {
+    // ---------------------------------------------------------- TMA producers: K and q (warp 0), V (warp 10)
+    // (int8: into the staging tiles).  An item loads only the 32-row boxes
+    // that hold its positions.
     if (lane == 0) {
-      for (int k = 0; k < n_items; ++k) {
-        const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
+      const bool is_v = warp == 10;
+      int k = 0;
+      for (int i = 0; i < n_slots; ++i) {
+        const Item it = loaded_item(cta + i * ncta, pre, lens_s, a.B, a.Hkv);
+        if (it.n == 0) continue;
+        // a whole slice in one 128-row box per 64 columns, a short one in the
+        // 32-row boxes that hold its positions
+        const bool whole = it.n == ROWS;
+        const int nb = whole ? 1 : (it.n + C::BOX - 1) / C::BOX, t0 = it.sp * ROWS;
+        const int bbytes = whole ? ROWS * 128 : C::BOX_BYTES, brows = whole ? ROWS : C::BOX;
+        const CUtensorMap* mk = whole ? &a.tk : &a.tk2;
+        const CUtensorMap* mv = whole ? &a.tv : &a.tv2;
         if (INT8) {
           const int st = k % C::NS;
-          if (!mbar_wait(&bar.ksempty[st], ((k / C::NS) & 1) ^ 1, ab)) break;
-          unsigned char* sb = smem + C::OFF_KS + st * C::KS_STAGE;
-          mbar_expect_tx(&bar.ksfull[st], C::KS_STAGE);
-          tma_load_4d(sb, &a.tk, &bar.ksfull[st], 0, it.sp * ROWS, it.g, it.b);
-          for (int bx = 0; bx < 2; ++bx)
-            tma_load_3d(sb + C::S8_BYTES + bx * (NH * 128), &a.tq, &bar.ksfull[st], bx * 64, it.g * G, it.b);
-          continue;
+          uint64_t* fb = is_v ? &bar.vsfull[st] : &bar.ksfull[st];
+          if (!mbar_wait(is_v ? &bar.vsempty[st] : &bar.ksempty[st], ((k / C::NS) & 1) ^ 1, ab)) break;
+          unsigned char* sb = smem + (is_v ? C::OFF_VS + st * C::S8_BYTES : C::OFF_KS + st * C::KS_STAGE);
+          mbar_expect_tx(fb, nb * bbytes + (is_v ? 0 : C::Q_BYTES));
+          for (int jb = 0; jb < nb; ++jb)
+            tma_load_4d(sb + jb * bbytes, is_v ? mv : mk, fb, 0, t0 + jb * brows, it.g, it.b);
+          if (!is_v)
+            for (int bx = 0; bx < 2; ++bx)
+              tma_load_3d(sb + C::S8_BYTES + bx * (NH * 128), &a.tq, fb, bx * 64, it.g * G, it.b);
+        } else {
+          const int ns = is_v ? NV : NK;
+          const int st = k % ns;
+          uint64_t* fb = is_v ? &bar.vfull[st] : &bar.kfull[st];
+          if (!mbar_wait(is_v ? &bar.vempty[st] : &bar.kempty[st], ((k / ns) & 1) ^ 1, ab)) break;
+          unsigned char* sb = smem + (is_v ? OFF_V + st * V_BYTES : st * KSTAGE);
+          mbar_expect_tx(fb, 2 * nb * bbytes + (is_v ? 0 : C::Q_BYTES));
+          for (int bx = 0; bx < 2; ++bx) {
+            for (int jb = 0; jb < nb; ++jb)
+              tma_load_4d(sb + bx * (ROWS * 128) + jb * bbytes, is_v ? mv : mk, fb, bx * 64, t0 + jb * brows, it.g,
+                          it.b);
+            if (!is_v) tma_load_3d(sb + K_BYTES + bx * (NH * 128), &a.tq, fb, bx * 64, it.g * G, it.b);
+          }
         }
-        const int st = k % NK;
-        if (!mbar_wait(&bar.kempty[st], ((k / NK) & 1) ^ 1, ab)) break;
-        unsigned char* sb = smem + st * KSTAGE;
-        mbar_expect_tx(&bar.kfull[st], KSTAGE);
-        for (int bx = 0; bx < 2; ++bx) {
-          tma_load_4d(sb + bx * (ROWS * 128), &a.tk, &bar.kfull[st], bx * 64, it.sp * ROWS, it.g, it.b);
-          tma_load_3d(sb + K_BYTES + bx * (NH * 128), &a.tq, &bar.kfull[st], bx * 64, it.g * G, it.b);
-        }
-      }
-    }
-  } else if (warp == 10) {
-    // ---------------------------------------------------------- TMA producer: V (int8: V staging)
-    if (lane == 0) {
-      for (int k = 0; k < n_items; ++k) {
-        const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
-        if (INT8) {
-          const int st = k % C::NS;
-          if (!mbar_wait(&bar.vsempty[st], ((k / C::NS) & 1) ^ 1, ab)) break;
-          mbar_expect_tx(&bar.vsfull[st], C::S8_BYTES);
-          tma_load_4d(smem + C::OFF_VS + st * C::S8_BYTES, &a.tv, &bar.vsfull[st], 0, it.sp * ROWS, it.g, it.b);
-          continue;
-        }
-        const int st = k % NV;
-        if (!mbar_wait(&bar.vempty[st], ((k / NV) & 1) ^ 1, ab)) break;
-        unsigned char* sb = smem + OFF_V + st * V_BYTES;
-        mbar_expect_tx(&bar.vfull[st], V_BYTES);
-        for (int bx = 0; bx < 2; ++bx)
-          tma_load_4d(sb + bx * (ROWS * 128), &a.tv, &bar.vfull[st], bx * 64, it.sp * ROWS, it.g, it.b);
+        ++k;
       }
     }
   } else if (INT8 && warp >= 11) {
@@ -511,6 +540,7 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
     // then garbage and the error word is set)
     const bool is_v = warp >= 15;
     const int r = tid - (is_v ? 480 : 352);
+    const int n_items = count_items();
     for (int k = 0; k < n_items; ++k) {
       const int ss = k % C::NS;
       const uint32_t sph = (k / C::NS) & 1;
@@ -578,6 +608,7 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
         mma_commit(&bar.o_full[k & 1]);
         mma_commit(&bar.vempty[k % NV]);
       };
+      const int n_items = count_items();
       bool ok = true;
       // scores of the first two items, then: O(k) once group k&1 has written
       // P(k); S(k+2) into the buffer that group has finished reading
@@ -613,18 +644,20 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
     float* rmax = reinterpret_cast<float*>(smem + OFF_RED) + gi * 2 * 4 * NH;
     float* rsum = rmax + 4 * NH;
     __nv_bfloat16* ogb = static_cast<__nv_bfloat16*>(a.out);
-    for (int k = gi; k < n_items; k += 2) {
-      const Item it = loaded_item(cta + k * ncta, pre, lens_s, a.B, a.Hkv);
+    int k = -1;  // item counter over the non-empty slots
+    for (int i = 0; i < n_slots; ++i) {
+      const Item it = loaded_item(cta + i * ncta, pre, lens_s, a.B, a.Hkv);
+      if (it.n == 0) continue;
+      if ((++k & 1) != gi) continue;
       __nv_bfloat16* og = ogb + ((size_t)it.b * a.Hq + (size_t)it.g * G) * D;
       const int buf = k & 1;
       const uint32_t par = (k >> 1) & 1;
-      const int n = min(ROWS, it.len - it.sp * ROWS);
+      const int n = it.n;
       float ksc = 1.f, vsc = 1.f;  // int8 cache: this position's scales, fetched while the scores form
-      if (INT8) {
-        const int t = it.sp * ROWS + r;
-        const size_t so = ((size_t)it.b * a.Hkv + it.g) * a.Smax + t;
-        ksc = t < a.Smax ? a.kscale[so] : 0.f;
-        vsc = t < a.Smax ? a.vscale[so] : 0.f;
+      if (INT8 && r < n) {  // positions past the length are never read (p is 0 there)
+        const size_t so = ((size_t)it.b * a.Hkv + it.g) * a.Smax + it.sp * ROWS + r;
+        ksc = a.kscale[so];
+        vsc = a.vscale[so];
       }
       // a failed wait (abort or timeout) runs on: the named barriers need every thread
       mbar_wait(&bar.s_full[buf], par, ab);
@@ -650,6 +683,20 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
       for (int h = 0; h < GMAX; ++h) {
         M[h] = fmaxf(fmaxf(rmax[h], rmax[NH + h]), fmaxf(rmax[2 * NH + h], rmax[3 * NH + h]));
         p[h] = (h < G && r < n) ? fast_exp2(sv[h] - M[h]) : 0.f;
+      }
+      // value rows at or past the length: loaded from a cache that may hold
+      // anything there, or not loaded and left by an earlier item (or never
+      // written); they get zero weight, and are zeroed before O reads them
+      if (!INT8 && n < ROWS) {
+        mbar_wait(&bar.vfull[k % NV], (k / NV) & 1, ab);
+        if (r >= n) {
+          unsigned char* vb = smem + OFF_V + (k % NV) * V_BYTES;
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vb + bx * (ROWS * 128) + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+        }
       }
       // P^T[head][position] in the K-major 128-byte-swizzled layout of the MMA's B operand
       {
@@ -714,59 +761,57 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
   }
 }
 
-// merge the slices of every (b, g) that has more than one: one CTA of
-// kCombineThreads per (b, g); each thread owns output elements and loads the
-// (max, sum, partial) of sixteen slices at a time, all in flight together,
-// merging chunks of slices online (a chain of dependent global loads here
-// would cost more than the attention itself)
-constexpr int kCombineThreads = 512;
+// merge the slices of every row (b, g) that has more than one: one CTA of D
+// threads per (b, g, head h), thread = dim; each thread loads the (max, sum,
+// partial) of sixteen slices at a time, all in flight together, merging
+// chunks of slices online (a chain of dependent global loads here would cost
+// more than the attention itself).  The CTAs are small, so they can be
+// resident beside the attention grid's and start as soon as it completes.
 template <int D, int GMAX>
-__global__ void __launch_bounds__(kCombineThreads) gqa_decode_combine_kernel(DecodeArgs a, int max_split) {
-  const int bg = blockIdx.x;
-  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+__global__ void __launch_bounds__(D) gqa_decode_combine_kernel(DecodeArgs a, int max_split) {
   const int G = a.Hq / a.Hkv;
+  const int bg = blockIdx.x / G, h = blockIdx.x - bg * G;
+  const int b = bg / a.Hkv, g = bg - b * a.Hkv, d = threadIdx.x;
   // launched early (programmatic dependent launch): the partials are
   // complete and visible once the attention grid has finished, and so is
   // every input written before it (the attention grid itself waits for its
-  // predecessors), so lens is read only after the wait
+  // predecessors), so lens is read only after the wait; the next kernel in
+  // the stream may then start its own set-up
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   int len = a.lens[b];
   len = len < 0 ? 0 : (len > a.Smax ? a.Smax : len);
   const int nsplit = (len + kDecodeSplit - 1) / kDecodeSplit;
   if (nsplit <= 1) return;
-  const float* ml0 = a.part_ml + (size_t)bg * max_split * GMAX * 2;
-  const float* po = a.part_o + (size_t)bg * max_split * GMAX * D;
-  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.Hq + (size_t)g * G) * D;
-  for (int x = threadIdx.x; x < G * D; x += kCombineThreads) {
-    const int h = x / D, d = x - h * D;
-    float M = -INFINITY, L = 0.f, acc = 0.f;
-    for (int s0 = 0; s0 < nsplit; s0 += 16) {
-      float o[16], m[16], l[16];
+  const float* ml0 = a.part_ml + ((size_t)bg * max_split * GMAX + h) * 2;
+  const float* po = a.part_o + ((size_t)bg * max_split * GMAX + h) * D + d;
+  float M = -INFINITY, L = 0.f, acc = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += 16) {
+    float o[16], m[16], l[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const bool in = s0 + j < nsplit;
-        const float* ml = ml0 + ((size_t)(s0 + j) * GMAX + h) * 2;
-        o[j] = in ? po[((size_t)(s0 + j) * GMAX + h) * D + d] : 0.f;
-        m[j] = in ? ml[0] : -INFINITY;
-        l[j] = in ? ml[1] : 0.f;
-      }
-      float mc = m[0];
-#pragma unroll
-      for (int j = 1; j < 16; ++j) mc = fmaxf(mc, m[j]);
-      const float mn = fmaxf(M, mc);  // finite: every chunk holds at least one slice
-      const float f = fast_exp2(M - mn);
-      acc *= f;
-      L *= f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float w = fast_exp2(m[j] - mn);  // 0 for slices past nsplit
-        acc = fmaf(o[j], w, acc);
-        L = fmaf(l[j], w, L);
-      }
-      M = mn;
+    for (int j = 0; j < 16; ++j) {
+      const bool in = s0 + j < nsplit;
+      const float* ml = ml0 + (size_t)(s0 + j) * GMAX * 2;
+      o[j] = in ? po[(size_t)(s0 + j) * GMAX * D] : 0.f;
+      m[j] = in ? ml[0] : -INFINITY;
+      l[j] = in ? ml[1] : 0.f;
     }
-    og[x] = __float2bfloat16(acc / L);
+    float mc = m[0];
+#pragma unroll
+    for (int j = 1; j < 16; ++j) mc = fmaxf(mc, m[j]);
+    const float mn = fmaxf(M, mc);  // finite: every chunk holds at least one slice
+    const float f = fast_exp2(M - mn);
+    acc *= f;
+    L *= f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float w = fast_exp2(m[j] - mn);  // 0 for slices past nsplit
+      acc = fmaf(o[j], w, acc);
+      L = fmaf(l[j], w, L);
+    }
+    M = mn;
   }
+  static_cast<__nv_bfloat16*>(a.out)[((size_t)b * a.Hq + (size_t)g * G + h) * D + d] = __float2bfloat16(acc / L);
 }
 
 // the merge grid may be scheduled while the attention grid still runs (its
@@ -774,8 +819,8 @@ __global__ void __launch_bounds__(kCombineThreads) gqa_decode_combine_kernel(Dec
 template <int D, int GMAX>
 cudaError_t launch_combine(const DecodeArgs& a, int max_split, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B * a.Hkv);
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.gridDim = dim3(a.B * a.Hkv * (a.Hq / a.Hkv));
+  cfg.blockDim = dim3(D);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -807,10 +852,12 @@ cudaError_t launch_tc(const DecodeArgs& a0, cudaStream_t st) {
   unsigned long long kd[4] = {D, (unsigned long long)a.Smax, (unsigned long long)a.Hkv, (unsigned long long)a.B};
   unsigned long long ks[3] = {D * eb, (unsigned long long)a.Smax * D * eb, (unsigned long long)a.Hkv * a.Smax * D * eb};
   unsigned kb[4] = {INT8 ? 128u : 64u, (unsigned)C::ROWS, 1, 1};  // 128-byte rows either way
+  unsigned kb2[4] = {INT8 ? 128u : 64u, (unsigned)C::BOX, 1, 1};  // short slices
   unsigned long long qd[3] = {D, (unsigned long long)a.Hq, (unsigned long long)a.B};
   unsigned long long qs[2] = {D * 2, (unsigned long long)a.Hq * D * 2};
   unsigned qb[3] = {64, (unsigned)C::NH, 1};
   if (encode_tmap(&a.tk, a.kc, 4, kd, ks, kb, (int)eb) || encode_tmap(&a.tv, a.vc, 4, kd, ks, kb, (int)eb) ||
+      encode_tmap(&a.tk2, a.kc, 4, kd, ks, kb2, (int)eb) || encode_tmap(&a.tv2, a.vc, 4, kd, ks, kb2, (int)eb) ||
       encode_tmap(&a.tq, a.q, 3, qd, qs, qb, 2))
     return cudaErrorInvalidValue;
   auto kern = gqa_decode_tc_kernel<GMAX, INT8>;

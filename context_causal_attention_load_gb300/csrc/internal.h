@@ -21,6 +21,7 @@ int encode_bf16_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned l
 
 struct DecodeArgs {
   CUtensorMap tk, tv, tq;  // used by the tensor-core path (D = 128)
+  CUtensorMap tk2, tv2;    // the same caches in 32-row boxes (short slices)
   const void* q;
   const void* kc;
   const void* vc;

@@ -187,6 +187,7 @@ int cp_attn_bwd_mla(const void* q, const void* k_nope, const void* k_rope, const
  * q [B, Hq, D] bf16, kcache/vcache [B, Hkv, Smax, D] bf16, lens [B] int32,
  * out [B, Hq, D] bf16; all device.  lens[b] == 0 gives out = 0; lens[b]
  * outside [0, Smax] is clamped and latched as CPATTN_ERR_DEVICE_BOUNDS.
+ * Cache rows at or past lens[b] may be read but never reach the output.
  * Requires D in {64, 128}, Hq % Hkv == 0, Hq/Hkv <= 16, Smax <= 2^30.
  */
 int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* out,

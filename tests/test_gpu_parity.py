@@ -272,7 +272,10 @@ def test_zero_copy_matches_permuted_path(cfg):
     (2, 6, 2, 128, 512, 255, 257),        # G = 3, around a split boundary
     (2, 16, 1, 128, 640, 300, 640),       # G = 16, D = 128 (two-stage ring)
     (1, 2, 1, 128, 128, 128, 128),        # one slice: no merge pass
-    (2, 8, 2, 128, 4500, 2100, 4500),     # 17-36 slices: the merge runs in chunks of 16
+    (2, 8, 2, 128, 4500, 2100, 4500),     # rows over several CTA ranges
+    (1, 4, 1, 128, 65536, 65536, 65536),  # one row cut into every CTA's range
+    (1, 2, 1, 128, 64, 5, 5),             # fewer positions than CTAs: one-position ranges
+    (3, 32, 8, 128, 1000, 1, 1000),       # lengths from 1 up: rows of one item next to long ones
 ])
 def test_decode_parity(cfg):
     B, Hq, Hkv, D, Smax, lo, hi = cfg
@@ -297,6 +300,34 @@ def test_decode_edge_lengths():
     ref = O.gqa_decode(_f64(q), _f64(kc), _f64(vc), lens.numpy())
     assert torch.all(out[0] == 0)
     assert_close_out(_f64(out), ref, "decode edge lengths")
+
+
+def test_decode_ignores_rows_past_the_length():
+    """Cache rows at or past lens[b] hold NaN: they get zero weight and their
+    values are never used (bf16 cache; int8 cache with NaN scales there)."""
+    B, Hq, Hkv, D, Smax = 4, 16, 4, 128, 700
+    q, kc, vc, _ = synth.decode_inputs(B, Hq, Hkv, D, Smax, 1, 1, seed=24)
+    lens = torch.tensor([1, 129, 300, 700], dtype=torch.int32)
+    kd, vd = kc.clone(), vc.clone()
+    for b in range(B):
+        kd[b, :, int(lens[b]):] = float("nan")
+        vd[b, :, int(lens[b]):] = float("nan")
+    out = cp_.gqa_decode(q.cuda(), kd.cuda(), vd.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref = O.gqa_decode(_f64(q), _f64(kc), _f64(vc), lens.numpy())
+    assert_close_out(_f64(out), ref, "decode with NaN past the lengths")
+    q8, kq, vq, ks, vs, _ = synth.decode_inputs_int8(B, Hq, Hkv, D, Smax, 1, 1, seed=25)
+    ksd, vsd = ks.clone(), vs.clone()
+    for b in range(B):
+        ksd[b, :, int(lens[b]):] = float("nan")
+        vsd[b, :, int(lens[b]):] = float("nan")
+    out8 = cp_.gqa_decode_int8(q8.cuda(), kq.cuda(), vq.cuda(), ksd.cuda(), vsd.cuda(), lens.cuda())
+    torch.cuda.synchronize()
+    cp_.check_device()
+    ref8 = O.gqa_decode_int8(_f64(q8), kq.numpy(), vq.numpy(), ks.numpy().astype(np.float64),
+                             vs.numpy().astype(np.float64), lens.numpy())
+    assert_close_out(_f64(out8), ref8, "int8 decode with NaN scales past the lengths")
 
 
 def test_decode_bad_lengths_are_flagged():
