@@ -51,6 +51,8 @@ WORKLOADS = {
     # (traffic scaled to the 131072-token launch by the tile pairs processed)
     "llama3_70b_gqa_s16384_cp8": dict(B=1, S=16384, Hq=64, Hkv=8, Dqk=128, Dv=128, cp=8, lb=True, q_scale=1.0),
     "llama3_70b_gqa_s32768_cp8": dict(B=1, S=32768, Hq=64, Hkv=8, Dqk=128, Dv=128, cp=8, lb=True, q_scale=1.0),
+    # the DeepSeek-V3 MLA head layout at a shorter sequence, for the same purpose
+    "deepseek_v3_mla_s4096_cp4": dict(B=1, S=4096, Hq=128, Hkv=128, Dqk=192, Dv=128, cp=4, lb=True, q_scale=1.0),
 }
 # the largest single-GPU configuration (Llama3.1-70B-shaped GQA at 131072
 # tokens, load-balanced) is the headline; the others ride along in the line
@@ -64,6 +66,7 @@ KERNEL_SOURCES = {
     "attn_bwd_dq": "attn_bwd.cu", "bwd_preprocess": "attn_bwd.cu", "gqa_decode": "decode.cu",
     "attn_bwd_fused": "attn_bwd_fused.cu", "bwd_dq_round": "attn_bwd_fused.cu",
     "lb_permute": "permute.cu", "lb_unpermute": "permute.cu", "mla_decode": "mla_decode.cu",
+    "attn_bwd_mla": "attn_bwd_mla.cu",
 }
 
 
@@ -93,6 +96,7 @@ def kernel_flops(name, w):
     return {
         "attn_fwd": 2.0 * p * (w["Dqk"] + w["Dv"]),
         "attn_bwd_fused": 2.0 * p * (3 * w["Dqk"] + 2 * w["Dv"]),
+        "attn_bwd_mla": 2.0 * p * (3 * w["Dqk"] + 2 * w["Dv"]),
         "attn_bwd_dkdv": 2.0 * p * (2 * w["Dqk"] + 2 * w["Dv"]),
         "attn_bwd_dq": 2.0 * p * w["Dqk"],
     }.get(name)

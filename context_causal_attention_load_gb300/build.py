@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 BUILD = os.path.join(ROOT, "_build", "cpattn")
-SOURCES = ["api.cu", "permute.cu", "decode.cu", "mla_decode.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_fused.cu"]
+SOURCES = ["api.cu", "permute.cu", "decode.cu", "mla_decode.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_fused.cu", "attn_bwd_mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -607,7 +607,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   const int Spad = (S + kTile - 1) / kTile * kTile;
   const size_t nstat = (size_t)B * Hq * Spad;
   if ((rc = ensure(ds->bwd_stats, 2 * nstat, stream, false))) return rc;
-  const bool fused = bwd_fused_supported(Dqk, Dv);
+  // MLA head dims take their own fused kernel (per-shard calls keep the two-kernel path)
+  const bool mla_fused = Dqk == 192 && Dv == 128 && shard < 0;
+  const bool fused = bwd_fused_supported(Dqk, Dv) || mla_fused;
   const size_t nacc = (size_t)B * S * Hq * Dqk;
   if (fused && (rc = ensure(ds->dq_acc, nacc, stream, false))) return rc;
   UnitPlan<BwdUnit>* u_kv;
@@ -647,31 +649,6 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     if (ez == cudaSuccess && !fused) ez = cudaMemsetAsync(dq, 0, nacc * 2, stream);
     if (ez != cudaSuccess) return cuda_fail(ez, "clearing the shard partials");
   }
-  if (fused) {
-    // one kernel: 128-row key tiles, 128-row query steps; dQ through the fp32 accumulator
-    if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, 128))) return rc;
-    if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, 128))) return rc;
-    if ((rc = make_tmap(&a.tk, k, B, S, Hkv, Dqk, 128))) return rc;
-    if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
-    if ((rc = make_tmap_f32(&a.tdq, a.dq_acc, B, S, Hq, Dqk, 128))) return rc;
-    a.units = u_kv->units.ptr;
-    a.cta_off = u_kv->off.ptr;
-    a.n_units = (int)u_kv->units.n;
-    if (u_kv->ncta > 0) {
-      ProfScope ps("attn_bwd_fused", stream);
-      e = launch_attn_bwd_fused(a, u_kv->ncta, stream);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "fused bwd launch");
-    {
-      ProfScope ps("bwd_dq_round", stream);
-      e = PosMap::make(S, cp, load_balance).lb == 2 ? launch_bwd_dq_round_nat(a.dq_acc, dq, sh, a.scale, stream)
-                                                     : launch_bwd_dq_round(a.dq_acc, dq, (long long)nacc, a.scale, stream);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "dq rounding launch");
-    return CPATTN_OK;
-  }
-  // dk/dv: key tiles of 128 rows, query/dout boxes of BQ rows
-  const int BQ = bwd_dkdv_q_tile(Dqk);
   const size_t nrope = (size_t)B * S * 64;
   if (k_rope) {
     if ((rc = ensure(ds->rope_acc, nrope, stream, false))) return rc;
@@ -681,6 +658,39 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     a.dk_rope_acc = ds->rope_acc.ptr;
   }
   const int kcols = k_rope ? 128 : Dqk;
+  if (fused) {
+    // one kernel: 128-row key tiles, 128-row query steps (MLA: 64-row half-steps);
+    // dQ through the fp32 accumulator
+    const int qrows = mla_fused ? 64 : 128;
+    if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, qrows))) return rc;
+    if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, qrows))) return rc;
+    if ((rc = make_tmap(&a.tk, k, B, S, Hkv, kcols, 128))) return rc;
+    if ((rc = make_tmap(&a.tv, v, B, S, Hkv, Dv, 128))) return rc;
+    if (k_rope && (rc = make_tmap(&a.tkr, k_rope, B, S, 1, 64, 128))) return rc;
+    if ((rc = make_tmap_f32(&a.tdq, a.dq_acc, B, S, Hq, Dqk, qrows))) return rc;
+    a.units = u_kv->units.ptr;
+    a.cta_off = u_kv->off.ptr;
+    a.n_units = (int)u_kv->units.n;
+    if (u_kv->ncta > 0) {
+      ProfScope ps(mla_fused ? "attn_bwd_mla" : "attn_bwd_fused", stream);
+      e = mla_fused ? launch_attn_bwd_mla(a, u_kv->ncta, stream) : launch_attn_bwd_fused(a, u_kv->ncta, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "fused bwd launch");
+    {
+      ProfScope ps("bwd_dq_round", stream);
+      e = PosMap::make(S, cp, load_balance).lb == 2 ? launch_bwd_dq_round_nat(a.dq_acc, dq, sh, a.scale, stream)
+                                                     : launch_bwd_dq_round(a.dq_acc, dq, (long long)nacc, a.scale, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "dq rounding launch");
+    if (k_rope) {
+      ProfScope ps("bwd_dq_round", stream);
+      e = launch_bwd_dq_round(ds->rope_acc.ptr, dk_rope, (long long)nrope, 1.0f, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "rope-key gradient rounding launch");
+    }
+    return CPATTN_OK;
+  }
+  // dk/dv: key tiles of 128 rows, query/dout boxes of BQ rows
+  const int BQ = bwd_dkdv_q_tile(Dqk);
   if ((rc = make_tmap(&a.tq, q, B, S, Hq, Dqk, BQ))) return rc;
   if ((rc = make_tmap(&a.tdo, dout, B, S, Hq, Dv, BQ))) return rc;
   if ((rc = make_tmap(&a.tk, k, B, S, Hkv, kcols, 128))) return rc;

@@ -138,6 +138,9 @@ cudaError_t launch_attn_bwd_fused(const BwdArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_bwd_dq_round(const float* acc, void* dq, long long n, float scale, cudaStream_t st);
 // natural-order tensors (zero-copy load balance): the accumulator is in slot order
 cudaError_t launch_bwd_dq_round_nat(const float* acc, void* dq, const AttnShape& sh, float scale, cudaStream_t st);
+// fused backward for MLA head dims (Dqk = 192, Dv = 128): 64-row query
+// half-steps, dQ through the fp32 accumulator (q/do/tdq maps of 64-row boxes)
+cudaError_t launch_attn_bwd_mla(const BwdArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, int grid, cudaStream_t st);
 int bwd_dkdv_q_tile(int Dqk);  // query rows per step of the dk/dv kernel

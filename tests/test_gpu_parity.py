@@ -150,8 +150,10 @@ def test_fwd_deterministic():
     (1, 1024, 8, 2, 128, 128, 4, True),
     (1, 320, 4, 2, 128, 128, 2, True),
     (2, 200, 2, 1, 128, 128, 1, True),
-    (1, 384, 2, 2, 192, 128, 2, True),
+    (1, 384, 2, 2, 192, 128, 2, True),    # MLA head dims: the fused MLA kernel
     (1, 512, 4, 4, 128, 128, 4, False),
+    (1, 640, 4, 2, 192, 128, 2, True),    # MLA dims, two query heads per KV head, chunks of 160
+    (2, 200, 2, 2, 192, 128, 1, False),   # MLA dims, S not a multiple of 64: the last half-tile partial
 ])
 def test_bwd_parity(cfg):
     B, S, Hq, Hkv, Dqk, Dv, cp, lb = cfg
@@ -175,7 +177,7 @@ def test_bwd_parity(cfg):
     (1, 320, 4, 2, 128, 128, 2, True),    # shards of 160 rows: tiles straddle the boundary
     (2, 256, 2, 2, 64, 64, 2, True),
     (1, 384, 2, 1, 128, 128, 3, False),   # natural order
-    (1, 512, 2, 2, 192, 128, 2, True),    # MLA head dims (the two-kernel backward)
+    (1, 512, 2, 2, 192, 128, 2, True),    # MLA head dims (per shard: the two-kernel backward)
     (1, 480, 2, 2, 192, 128, 3, True),    # MLA, shards of 160 rows: 64-row steps straddle the boundary
 ])
 def test_bwd_shard_partials(cfg):
@@ -429,7 +431,10 @@ def test_mla_shared_rope_matches_materialised_key():
     torch.cuda.synchronize()
     cp_.check_device()
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
-    assert torch.equal(dq1, dq2) and torch.equal(dv1, dv2)
+    assert torch.equal(dv1, dv2)
+    # dq goes through an fp32 accumulator that several CTAs add into, in an
+    # order that varies: equal to rounding
+    assert_close_grad(_f64(dq1), _f64(dq2), "dq of the shared and the materialised rope key", rel=1e-3)
     assert torch.equal(dkn1, dk2[..., :128])
     want = dk2[..., 128:].double().sum(dim=2)
     assert_close_grad(_f64(dkr1), want.cpu().numpy(), "dk_rope vs summed rope columns")
@@ -454,8 +459,8 @@ def test_mla_shared_rope_zero_copy():
     assert torch.equal(out2, cp_.lb_unpermute(out1, cp)) and torch.equal(lse2, lse1_nat)
     for a2, a1, name in zip(g2, g1, ("dq", "dk_nope", "dk_rope", "dv")):
         a1n = cp_.lb_unpermute(a1, cp)
-        if name == "dk_rope":
-            assert_close_grad(_f64(a2), _f64(a1n), "zero-copy dk_rope")
+        if name in ("dk_rope", "dq"):  # fp32 accumulators added into in a varying order
+            assert_close_grad(_f64(a2), _f64(a1n), "zero-copy %s" % name, rel=1e-3)
         else:
             assert torch.equal(a2, a1n), name
 
