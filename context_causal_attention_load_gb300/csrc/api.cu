@@ -322,11 +322,50 @@ void plan_units(std::vector<std::pair<long long, U>> w, int num_sms, std::vector
   }
 }
 
+// The same deal by groups of units (grp[i]: group of unit i; equal ids come in
+// runs, in order): the groups are dealt one after the other, each group's
+// units by decreasing cost to the least-loaded CTA, and every CTA runs its
+// units group by group, heaviest first within a group.  With a KV head per
+// group, the units of one head are in flight on most CTAs at the same time,
+// so the query tiles they walk (and the dQ rows they add into) are shared
+// through L2 instead of coming from DRAM once per CTA.  The last group's
+// small units still go last, so the balance stays close to plain LPT's.
 template <typename U>
-int upload_plan(std::vector<std::pair<long long, U>> w, int num_sms, UnitPlan<U>& plan) {
+void plan_units_grouped(std::vector<std::pair<long long, U>> w, const std::vector<int>& grp, int num_sms,
+                        std::vector<U>& units, std::vector<int>& off) {
+  const int ncta = (int)std::min<size_t>(w.size(), (size_t)std::max(1, num_sms));
+  using Load = std::pair<long long, int>;  // (cost so far, CTA): ties go to the lower CTA
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> pq;
+  for (int c = 0; c < ncta; ++c) pq.push({0, c});
+  std::vector<std::vector<U>> lists(ncta);
+  for (size_t i0 = 0; i0 < w.size();) {
+    size_t i1 = i0;
+    while (i1 < w.size() && grp[i1] == grp[i0]) ++i1;
+    std::stable_sort(w.begin() + i0, w.begin() + i1, [](const auto& x, const auto& y) { return x.first > y.first; });
+    for (size_t i = i0; i < i1; ++i) {
+      const Load top = pq.top();
+      pq.pop();
+      lists[top.second].push_back(w[i].second);
+      pq.push({top.first + w[i].first, top.second});
+    }
+    i0 = i1;
+  }
+  units.clear();
+  off.assign(ncta + 1, 0);
+  for (int c = 0; c < ncta; ++c) {
+    off[c] = (int)units.size();
+    units.insert(units.end(), lists[c].begin(), lists[c].end());
+  }
+  off[ncta] = (int)units.size();
+}
+
+template <typename U>
+int upload_plan(std::vector<std::pair<long long, U>> w, int num_sms, UnitPlan<U>& plan,
+                const std::vector<int>* grp = nullptr) {
   std::vector<U> units;
   std::vector<int> off;
-  plan_units(std::move(w), num_sms, units, off);
+  if (grp) plan_units_grouped(std::move(w), *grp, num_sms, units, off);
+  else plan_units(std::move(w), num_sms, units, off);
   int rc = upload(plan.units, units);
   if (!rc) rc = upload(plan.off, off);
   plan.ncta = (int)off.size() - 1;
@@ -384,9 +423,21 @@ int tile_min_pos(const PosMap& pm, int t, int T) {
   return mn;
 }
 
+// The grouped deal (by KV head) where the plain one would leave each head on
+// fewer than about four CTAs at a time: the plain deal runs units of equal
+// cost together, i.e. the same tile index of every head, so B*Hkv heads share
+// the SMs.  Measured: the DeepSeek-V3-shaped MLA layer (128 KV heads)
+// gains a third of its backward from it; the Llama3.1-70B-shaped layer (8 KV
+// heads, 19 CTAs per head under the plain deal) loses 5%.  Only with many
+// units per CTA (with few, the plain deal's MULTIFIT packing matters more).
+bool use_grouped_deal(const AttnShape& sh, size_t n_units, int num_sms) {
+  return (long long)sh.B * sh.Hkv >= 64 && n_units > (size_t)std::max(1, num_sms) * 8;
+}
+
 // forward units: pairs of 128-row query tiles sharing a KV head, with their
 // cost (query tiles x (key steps + 4 steps of per-unit overhead))
-std::vector<std::pair<long long, FwdUnit>> build_fwd_units(const AttnShape& sh, int shard) {
+std::vector<std::pair<long long, FwdUnit>> build_fwd_units(const AttnShape& sh, int shard,
+                                                           std::vector<int>* grp = nullptr) {
   const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
   const int nqt = (sh.S + kTile - 1) / kTile;
   const int G = sh.Hq / sh.Hkv;
@@ -402,6 +453,7 @@ std::vector<std::pair<long long, FwdUnit>> build_fwd_units(const AttnShape& sh, 
     FwdUnit u{b, h0, h1, t0, t1, hkv, nkv, 0};
     const long long cost = (long long)(nkv + 4) * (h1 >= 0 ? 2 : 1);
     w.push_back({cost, u});
+    if (grp) grp->push_back(b * sh.Hkv + hkv);
   };
   // tiles of one head paired with their neighbour in the same memory chunk
   auto pair_rows = [&](int b, int hkv, int h) {
@@ -435,7 +487,10 @@ int fwd_units_cached(DevState& ds, const AttnShape& sh, int shard, UnitPlan<FwdU
   auto it = ds.fwd_units.find(key);
   if (it == ds.fwd_units.end()) {
     UnitPlan<FwdUnit> plan;
-    int rc = upload_plan(build_fwd_units(sh, shard), ds.num_sms, plan);
+    std::vector<int> grp;
+    auto w = build_fwd_units(sh, shard, &grp);
+    const bool grouped = use_grouped_deal(sh, w.size(), ds.num_sms);
+    int rc = upload_plan(std::move(w), ds.num_sms, plan, grouped ? &grp : nullptr);
     if (rc) return rc;
     it = ds.fwd_units.emplace(key, plan).first;
   }
@@ -456,18 +511,26 @@ int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, UnitPlan<BwdUn
     const PosMap pm = PosMap::make(sh.S, sh.cp, sh.lb);
     const int nt = (sh.S + kTile - 1) / kTile;
     std::vector<std::pair<long long, BwdUnit>> w;
+    std::vector<int> grp;  // kind 0: the KV head of each unit, for the grouped deal
     if (kind == 0) {
       const int BQ = bwd_dkdv_q_tile(sh.Dqk);
       const int lo = shard < 0 ? 0 : shard * (sh.S / sh.cp), hi = shard < 0 ? sh.S : (shard + 1) * (sh.S / sh.cp);
+      std::vector<long long> cost(nt, -1);
       for (int kt = 0; kt < nt; ++kt) {
         const int bound = tile_min_pos(pm, kt, kTile);
         long long n = 0;
         for (int qt = next_q_tile(pm, BQ, -1, bound); qt >= 0; qt = next_q_tile(pm, BQ, qt, bound))
           if (qt * BQ < hi && qt * BQ + BQ > lo) ++n;
         if (n == 0 && shard >= 0) continue;
-        for (int b = 0; b < sh.B; ++b)
-          for (int g = 0; g < sh.Hkv; ++g) w.push_back({n + 3, BwdUnit{b, g, kt, 0}});
+        cost[kt] = n + 3;
       }
+      for (int b = 0; b < sh.B; ++b)
+        for (int g = 0; g < sh.Hkv; ++g)
+          for (int kt = 0; kt < nt; ++kt)
+            if (cost[kt] >= 0) {
+              w.push_back({cost[kt], BwdUnit{b, g, kt, 0}});
+              grp.push_back(b * sh.Hkv + g);
+            }
     } else {
       const int BK = bwd_dq_kv_tile(sh.Dqk);
       const int lo = shard < 0 ? 0 : shard * (sh.S / sh.cp), hi = shard < 0 ? sh.S : (shard + 1) * (sh.S / sh.cp);
@@ -480,8 +543,9 @@ int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, UnitPlan<BwdUn
           for (int h = 0; h < sh.Hq; ++h) w.push_back({n + 3, BwdUnit{b, h, qt, 0}});
       }
     }
+    const bool grouped = kind == 0 && use_grouped_deal(sh, w.size(), ds.num_sms);
     UnitPlan<BwdUnit> plan;
-    int rc = upload_plan(std::move(w), ds.num_sms, plan);
+    int rc = upload_plan(std::move(w), ds.num_sms, plan, grouped ? &grp : nullptr);
     if (rc) return rc;
     it = ds.bwd_units.emplace(key, plan).first;
   }
