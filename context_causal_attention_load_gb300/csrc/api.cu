@@ -441,15 +441,18 @@ int tile_min_pos(const PosMap& pm, int t, int T) {
   return mn;
 }
 
-// The grouped deal (by KV head) where the plain one would leave each head on
-// fewer than about four CTAs at a time: the plain deal runs units of equal
-// cost together, i.e. the same tile index of every head, so B*Hkv heads share
-// the SMs.  Measured: the DeepSeek-V3-shaped MLA layer (128 KV heads)
-// gains a third of its backward from it; the Llama3.1-70B-shaped layer (8 KV
-// heads, 19 CTAs per head under the plain deal) loses 5%.  Only with many
-// units per CTA (with few, the plain deal's MULTIFIT packing matters more).
-bool use_grouped_deal(const AttnShape& sh, size_t n_units, int num_sms) {
-  return (long long)sh.B * sh.Hkv >= 64 && n_units > (size_t)std::max(1, num_sms) * 8;
+// The grouped deal (by KV head), only with many units per CTA (with few, the
+// plain deal's MULTIFIT packing matters more).  The plain deal runs units of
+// equal cost together, i.e. the same tile index of every head, so B*Hkv heads
+// share the SMs.  Forward: always (measured: the DeepSeek-V3-shaped MLA layer,
+// 128 KV heads, 47 -> 37 ms; the Llama3.1-70B-shaped layer, 8 KV heads,
+// 205 -> 198 ms).  Backward: only where the plain deal leaves each head on
+// fewer than about four CTAs (B*Hkv >= 64): the MLA backward gains a third
+// from it, but the 70B-shaped backward loses 6% (152 CTAs then add into the
+// same head's dQ rows at once, where the plain deal spreads them over 8).
+bool use_grouped_deal(const AttnShape& sh, size_t n_units, int num_sms, bool backward) {
+  if (n_units <= (size_t)std::max(1, num_sms) * 8) return false;
+  return !backward || (long long)sh.B * sh.Hkv >= 64;
 }
 
 // forward units: pairs of 128-row query tiles sharing a KV head, with their
@@ -507,7 +510,7 @@ int fwd_units_cached(DevState& ds, const AttnShape& sh, int shard, UnitPlan<FwdU
     UnitPlan<FwdUnit> plan;
     std::vector<int> grp;
     auto w = build_fwd_units(sh, shard, &grp);
-    const bool grouped = use_grouped_deal(sh, w.size(), ds.num_sms);
+    const bool grouped = use_grouped_deal(sh, w.size(), ds.num_sms, false);
     int rc = upload_plan(std::move(w), ds.num_sms, plan, grouped ? &grp : nullptr);
     if (rc) return rc;
     it = ds.fwd_units.emplace(key, plan).first;
@@ -561,7 +564,7 @@ int bwd_units_cached(DevState& ds, const AttnShape& sh, int kind, UnitPlan<BwdUn
           for (int h = 0; h < sh.Hq; ++h) w.push_back({n + 3, BwdUnit{b, h, qt, 0}});
       }
     }
-    const bool grouped = kind == 0 && use_grouped_deal(sh, w.size(), ds.num_sms);
+    const bool grouped = kind == 0 && use_grouped_deal(sh, w.size(), ds.num_sms, true);
     UnitPlan<BwdUnit> plan;
     int rc = upload_plan(std::move(w), ds.num_sms, plan, grouped ? &grp : nullptr);
     if (rc) return rc;
@@ -1021,7 +1024,7 @@ int cp_attn_fwd_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance
   std::vector<long long> cost;
   std::vector<int> grp;
   auto w = build_fwd_units(sh, -1, &grp);
-  if (use_grouped_deal(sh, w.size(), num_ctas)) plan_units_grouped(std::move(w), grp, num_ctas, units, off, &cost);
+  if (use_grouped_deal(sh, w.size(), num_ctas, false)) plan_units_grouped(std::move(w), grp, num_ctas, units, off, &cost);
   else plan_units(std::move(w), num_ctas, units, off, &cost);
   for (int c = 0; c < num_ctas; ++c) cta_cost_host[c] = c < (int)cost.size() ? cost[c] : 0;
   return CPATTN_OK;

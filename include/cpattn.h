@@ -276,9 +276,9 @@ int cp_attn_tile_counts(int S, int cp, int load_balance, long long* per_shard_ho
  * Host helper: the plan the forward uses on a GPU with num_ctas SMs.  The
  * forward's work units (pairs of 128-row query tiles sharing a KV head) are
  * dealt to min(units, num_ctas) CTAs so that the most-loaded CTA carries as
- * little as possible (with B*Hkv >= 64 and many units per CTA, one KV head
- * after the other, so that a head's units run on most SMs at the same time
- * and share its K/V tiles through L2); cta_cost_host[c] (host, num_ctas entries) receives the
+ * little as possible (with many units per CTA, one KV head after the other,
+ * so that a head's units run on most SMs at the same time and share its K/V
+ * tiles through L2); cta_cost_host[c] (host, num_ctas entries) receives the
  * modelled load of CTA c, a unit costing (its key steps + 4) per query tile it
  * holds; CTAs without units get 0.  Shapes as cp_attn_fwd (head dims do not
  * enter the plan).  No device work; returns CPATTN_OK or an argument error.
