@@ -69,6 +69,7 @@ def load(path=None):
         "cp_lb_positions": [_I, _I, _I, ctypes.POINTER(ctypes.c_int)],
         "cp_attn_tile_counts": [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)],
         "cp_attn_fwd_schedule": [_I] * 7 + [ctypes.POINTER(ctypes.c_longlong)],
+        "cp_attn_fwd_shard_schedule": [_I] * 8 + [ctypes.POINTER(ctypes.c_longlong)],
         "cp_attn_check_device": [_P],
         "cp_attn_test_stall_forward": [_I, _L],
         "cp_attn_release": [],
@@ -300,6 +301,13 @@ def fwd_schedule(B, Hq, Hkv, S, cp, load_balance, num_ctas):
     arr = (ctypes.c_longlong * num_ctas)()
     _check(load().cp_attn_fwd_schedule(B, Hq, Hkv, S, cp, _lb(load_balance), num_ctas, arr))
     return list(arr)
+
+def fwd_shard_schedule(B, Hq, Hkv, S, cp, load_balance, shard, num_ctas):
+    """The same for one shard's forward plan (shard -1: the whole forward)."""
+    arr = (ctypes.c_longlong * num_ctas)()
+    _check(load().cp_attn_fwd_shard_schedule(B, Hq, Hkv, S, cp, _lb(load_balance), shard, num_ctas, arr))
+    return list(arr)
+
 
 def tile_counts(S, cp, load_balance=True):
     arr = (ctypes.c_longlong * cp)()

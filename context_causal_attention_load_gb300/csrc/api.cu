@@ -340,27 +340,45 @@ void plan_units_grouped(std::vector<std::pair<long long, U>> w, const std::vecto
   std::priority_queue<Load, std::vector<Load>, std::greater<Load>> pq;
   for (int c = 0; c < ncta; ++c) pq.push({0, c});
   std::vector<std::vector<U>> lists(ncta);
-  // the last groups, holding at least two units per CTA, are dealt as one:
-  // their small units even out what the earlier groups left
-  size_t tail = w.size();
-  while (tail > 0 && w.size() - tail < (size_t)ncta * 2) {
-    const int gl = grp[tail - 1];
-    while (tail > 0 && grp[tail - 1] == gl) --tail;
+  // The smallest units, whose costs add up to at least one largest unit per
+  // CTA, are held back and dealt last, all groups together, heaviest first:
+  // they even out what the grouped phase leaves (even where a group's costs
+  // are far apart, e.g. one shard's units of a sequence's first and last
+  // chunks), at the price of head order for a small share of the work.
+  long long cut = -1;
+  {
+    std::vector<long long> c(w.size());
+    long long mx = 0;
+    for (size_t i = 0; i < w.size(); ++i) {
+      c[i] = w[i].first;
+      mx = std::max(mx, c[i]);
+    }
+    std::sort(c.begin(), c.end());
+    long long acc = 0;
+    for (size_t i = 0; i < c.size() && acc < mx * ncta; ++i) {
+      acc += c[i];
+      cut = c[i];
+    }
   }
-  for (size_t i0 = 0; i0 < w.size();) {
-    size_t i1 = i0;
-    if (i0 >= tail) i1 = w.size();
-    else
-      while (i1 < tail && grp[i1] == grp[i0]) ++i1;
-    std::stable_sort(w.begin() + i0, w.begin() + i1, [](const auto& x, const auto& y) { return x.first > y.first; });
-    for (size_t i = i0; i < i1; ++i) {
+  auto deal = [&](std::vector<std::pair<long long, U>>& seg) {
+    std::stable_sort(seg.begin(), seg.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+    for (const auto& cu : seg) {
       const Load top = pq.top();
       pq.pop();
-      lists[top.second].push_back(w[i].second);
-      pq.push({top.first + w[i].first, top.second});
+      lists[top.second].push_back(cu.second);
+      pq.push({top.first + cu.first, top.second});
     }
+  };
+  std::vector<std::pair<long long, U>> seg, tail;
+  for (size_t i0 = 0; i0 < w.size();) {
+    size_t i1 = i0;
+    while (i1 < w.size() && grp[i1] == grp[i0]) ++i1;
+    seg.clear();
+    for (size_t i = i0; i < i1; ++i) (w[i].first <= cut ? tail : seg).push_back(w[i]);
+    deal(seg);
     i0 = i1;
   }
+  deal(tail);
   if (cta_cost) {
     cta_cost->assign(ncta, 0);
     while (!pq.empty()) {
@@ -1014,16 +1032,22 @@ int cp_attn_tile_counts(int S, int cp, int load_balance, long long* per_shard_ho
 
 int cp_attn_fwd_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance, int num_ctas,
                          long long* cta_cost_host) {
+  return cp_attn_fwd_shard_schedule(B, Hq, Hkv, S, cp, load_balance, -1, num_ctas, cta_cost_host);
+}
+
+int cp_attn_fwd_shard_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance, int shard, int num_ctas,
+                               long long* cta_cost_host) {
   if (!cta_cost_host) return fail(CPATTN_ERR_INVALID_ARG, "null cta_cost_host");
   if (num_ctas < 1) return fail(CPATTN_ERR_INVALID_ARG, "num_ctas must be >= 1");
   AttnShape sh{B, Hq, Hkv, S, 128, 128, cp, load_balance};
   int rc = check_attn(sh);
   if (rc) return rc;
+  if (shard < -1 || shard >= cp) return fail(CPATTN_ERR_INVALID_ARG, "shard %d outside [-1, %d)", shard, cp);
   std::vector<FwdUnit> units;
   std::vector<int> off;
   std::vector<long long> cost;
   std::vector<int> grp;
-  auto w = build_fwd_units(sh, -1, &grp);
+  auto w = build_fwd_units(sh, shard, &grp);
   if (use_grouped_deal(sh, w.size(), num_ctas, false)) plan_units_grouped(std::move(w), grp, num_ctas, units, off, &cost);
   else plan_units(std::move(w), num_ctas, units, off, &cost);
   for (int c = 0; c < num_ctas; ++c) cta_cost_host[c] = c < (int)cost.size() ? cost[c] : 0;

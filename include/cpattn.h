@@ -287,6 +287,14 @@ int cp_attn_fwd_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance
                          long long* cta_cost_host);
 
 /*
+ * The same for the plan of one shard's forward (cp_attn_fwd_shard with that
+ * shard); shard = -1 is the whole forward, as cp_attn_fwd_schedule.  Returns
+ * CPATTN_OK or an argument error (shard outside [-1, cp)).
+ */
+int cp_attn_fwd_shard_schedule(int B, int Hq, int Hkv, int S, int cp, int load_balance, int shard, int num_ctas,
+                               long long* cta_cost_host);
+
+/*
  * Kernel timing for profiling and benchmarks.  Between profile_start and
  * profile_stop every kernel the library launches is bracketed by two CUDA
  * events recorded on its own stream.  profile_stop waits for those events

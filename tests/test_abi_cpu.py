@@ -143,6 +143,24 @@ def test_fwd_schedule_by_head_for_many_heads():
     assert max(c152) <= 1.03 * total / 152
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,S,cp", [(1, 128, 128, 32768, 4), (1, 64, 8, 131072, 8)])
+def test_fwd_shard_schedules_balance(B, Hq, Hkv, S, cp):
+    """Every shard's plan on its own: the shards' totals agree (balanced
+    reorder) and each plan's most loaded CTA is within 3% of its mean (one
+    shard's units mix a first and a last chunk, so their costs are far
+    apart: the small ones must still even out the deal)."""
+    totals = []
+    for shard in range(cp):
+        arr = (ctypes.c_longlong * 152)()
+        assert lib.cp_attn_fwd_shard_schedule(B, Hq, Hkv, S, cp, 1, shard, 152, arr) == 0, _err()
+        c = list(arr)
+        totals.append(sum(c))
+        assert max(c) <= 1.03 * sum(c) / 152, "shard %d: %d vs mean %.1f" % (shard, max(c), sum(c) / 152)
+    assert max(totals) <= 1.01 * min(totals)
+    arr = (ctypes.c_longlong * 152)()
+    assert lib.cp_attn_fwd_shard_schedule(B, Hq, Hkv, S, cp, 1, cp, 152, arr) == -1
+
+
 def test_fwd_schedule_rejects_bad_arguments():
     arr = (ctypes.c_longlong * 4)()
     assert lib.cp_attn_fwd_schedule(1, 1, 1, 256, 2, 1, 0, arr) == -1
