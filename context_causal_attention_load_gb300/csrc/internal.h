@@ -13,7 +13,7 @@ cudaError_t launch_lb_permute(const void* src, void* dst, int B, int S, long lon
 // second kernel merges the slices of each (batch, kv head).
 // bf16 tiled tensor map, 128-byte swizzle (returns 0 on success)
 int decode_int8_max_batch();
-// tensor map with 128-byte swizzle and zero fill; elem_bytes 2 (bf16) or 1 (int8 as bytes)
+// tensor map with 128-byte swizzle and zero fill; elem_bytes 2 (bf16), 1 (int8 as bytes) or 4 (fp32)
 int encode_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
                 const unsigned long long* strides, const unsigned* box, int elem_bytes);
 int encode_bf16_tmap(CUtensorMap* m, const void* ptr, int rank, const unsigned long long* dims,
@@ -52,6 +52,7 @@ cudaError_t noalloc_take_error(int* word);
 // rope) shared by every head; value = the first 512 columns
 struct MlaDecodeArgs {
   CUtensorMap tq, tk;
+  CUtensorMap tpo;   // part_o as fp32 {512, H, nch, B}, boxes of 32 columns x min(H, 128) rows
   const void* q;     // [B, H, 576] bf16
   const void* ckv;   // [B, Smax, 576] bf16
   const int* lens;   // [B]

@@ -112,6 +112,20 @@ __device__ __forceinline__ void md_prefix(int B, int lane, int* out, F f) {
   if (lane == 31) out[B] = inc;
 }
 
+// TMA store of a tile from shared memory into global memory, tracked by the
+// issuing thread's bulk async-group
+__device__ __forceinline__ void md_tma_store_4d(const void* src, const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+// this thread's bulk async-groups, all but the newest N, have read their sources
+template <int N>
+__device__ __forceinline__ void md_bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_constant__ MlaDecodeArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -299,30 +313,45 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
         ++nfix;
       }
       // epilogue: this item's partial (o, row max, row sum); value columns
-      // 0-255 are in TMEM [256, 512), 256-511 in [0, 256)
+      // 0-255 are in TMEM [256, 512), 256-511 in [0, 256).  o goes out as
+      // sixteen fp32 boxes of 32 columns x 128 head rows, staged four at a
+      // time in the P buffer (dead once O is complete; 128-byte swizzle) and
+      // written by TMA stores, so the 256 KiB leave in whole lines
       mbar_wait(&bar.o_full, k & 1, ab);
       tc_fence_after();
-      const size_t prow = ((size_t)it.b * a.nch + it.chunk) * a.H + r;
 #pragma unroll 1
       for (int c = 0; c < kMdDv / 32; ++c) {
         uint32_t ov[32];
         tmem_ld32(tmem + lane_base + (c < 8 ? 256 + 32 * c : 32 * (c - 8)), ov);
         tmem_ld_wait();
-        if (r < a.H) {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kMdDv + 32 * c);
+        unsigned char* buf = smem + kMdOffP + (c & 3) * (kMdRows * 128);
+        if (c >= 4) {  // the store that last used this buffer has read it
+          if (r == 0) md_bulk_wait_read<3>();
+          named_bar(1, 128);
+        }
+        unsigned char* rp = buf + r * 128;
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            dst[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
-                                  __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(rp + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(ov[4 * ch], ov[4 * ch + 1], ov[4 * ch + 2], ov[4 * ch + 3]);
+        fence_proxy_async_smem();
+        named_bar(1, 128);
+        if (r == 0) {
+          md_tma_store_4d(buf, &a.tpo, 32 * c, 0, it.chunk, it.b);
+          bulk_commit_group();
         }
       }
+      const size_t prow = ((size_t)it.b * a.nch + it.chunk) * a.H + r;
       if (r < a.H) {
         a.part_ml[2 * prow] = m2;
         a.part_ml[2 * prow + 1] = l;
       }
       tc_fence_before();
       mbar_arrive(&bar.o_free);
+      if (r == 0) md_bulk_wait_read<0>();  // the next item may write P
+      named_bar(1, 128);
     }
+    if (r == 0) bulk_wait_all();  // the partials have landed before the CTA retires
     (void)nfix;
   }
 
@@ -335,9 +364,10 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
   }
 }
 
-// merge of the chunks of each (b, h): 128 threads, four value columns each;
-// launched as a programmatic dependent, so lens and the partials are read
-// only after the attention grid has completed
+// merge of the chunks of each (b, h): one CTA of 128 threads per (b, h),
+// four value columns per thread; four chunks' loads in flight at a time,
+// merged online.  Launched as a programmatic dependent, so lens and the
+// partials are read only after the attention grid has completed.
 __global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_constant__ MlaDecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x / a.H, h = blockIdx.x - b * a.H;
@@ -349,19 +379,37 @@ __global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_cons
     *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
     return;
   }
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, a.part_ml[2 * (((size_t)b * a.nch + c) * a.H + h)]);
-  float L = 0.f;
+  float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = 0; c < nch; ++c) {
-    const size_t prow = ((size_t)b * a.nch + c) * a.H + h;
-    const float w = fast_exp2(a.part_ml[2 * prow] - M);
-    L = fmaf(a.part_ml[2 * prow + 1], w, L);
-    const float4 x = reinterpret_cast<const float4*>(a.part_o + prow * kMdDv)[threadIdx.x];
-    acc.x = fmaf(x.x, w, acc.x);
-    acc.y = fmaf(x.y, w, acc.y);
-    acc.z = fmaf(x.z, w, acc.z);
-    acc.w = fmaf(x.w, w, acc.w);
+  for (int c0 = 0; c0 < nch; c0 += 4) {
+    float m[4], l[4];
+    float4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool in = c0 + j < nch;
+      const size_t prow = ((size_t)b * a.nch + c0 + j) * a.H + h;
+      m[j] = in ? __ldcg(a.part_ml + 2 * prow) : -INFINITY;
+      l[j] = in ? __ldcg(a.part_ml + 2 * prow + 1) : 0.f;
+      x[j] = in ? __ldcg(reinterpret_cast<const float4*>(a.part_o + prow * kMdDv) + threadIdx.x)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float mn = fmaxf(M, fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])));  // finite: chunk 0 is in
+    const float f = fast_exp2(M - mn);
+    L *= f;
+    acc.x *= f;
+    acc.y *= f;
+    acc.z *= f;
+    acc.w *= f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float w = fast_exp2(m[j] - mn);  // 0 past the last chunk
+      L = fmaf(l[j], w, L);
+      acc.x = fmaf(x[j].x, w, acc.x);
+      acc.y = fmaf(x[j].y, w, acc.y);
+      acc.z = fmaf(x[j].z, w, acc.z);
+      acc.w = fmaf(x[j].w, w, acc.w);
+    }
+    M = mn;
   }
   const float il = 1.f / L;
   *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16(acc.x * il, acc.y * il), pack_bf16(acc.z * il, acc.w * il));
@@ -381,7 +429,12 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a0, int num_sms, cudaStream_t
   unsigned long long kd[3] = {Dk, (unsigned long long)a.Smax, (unsigned long long)a.B};
   unsigned long long ks[2] = {Dk * 2, (unsigned long long)a.Smax * Dk * 2};
   unsigned kb[3] = {64, (unsigned)kMdT, 1};
-  if (encode_tmap(&a.tq, a.q, 3, qd, qs, qb, 2) || encode_tmap(&a.tk, a.ckv, 3, kd, ks, kb, 2))
+  unsigned long long pd[4] = {(unsigned long long)kMdDv, (unsigned long long)a.H, (unsigned long long)a.nch,
+                              (unsigned long long)a.B};
+  unsigned long long ps[3] = {kMdDv * 4ull, (unsigned long long)a.H * kMdDv * 4, (unsigned long long)a.nch * a.H * kMdDv * 4};
+  unsigned pb[4] = {32, (unsigned)(a.H < kMdRows ? a.H : kMdRows), 1, 1};
+  if (encode_tmap(&a.tq, a.q, 3, qd, qs, qb, 2) || encode_tmap(&a.tk, a.ckv, 3, kd, ks, kb, 2) ||
+      encode_tmap(&a.tpo, a.part_o, 4, pd, ps, pb, 4))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMdSmem);
   if (e != cudaSuccess) return e;
