@@ -905,6 +905,31 @@ def measure_workload(name, peaks, cpattn, dev, seed, steps=None, warmup=3):
            "kernels": kernel_table(prof, w, peaks, timed_s)}
     if name in ("llama2_7b_s8192_cp4", "deepseek_v3_mla_s32768_cp4"):
         res["shards"] = measure_shards(w, attn, cpattn, iters=10 if name.startswith("llama2") else 3)
+    if w["lb"] and (S // (2 * w["cp"])) % 128 == 0:
+        # the same step with load_balance = 2: natural-order tensors, no permutes
+        cp = w["cp"]
+        out = torch.empty(B, S, Hq, Dv, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        if kr is not None:
+            dkr = torch.empty_like(kr)
+
+            def zstep():
+                cpattn.attn_fwd_mla(q, k, kr, v, cp, 2, out, lse)
+                cpattn.attn_bwd_mla(q, k, kr, v, out, lse, dout, cp, 2, dq, dk, dkr, dv)
+        else:
+            def zstep():
+                cpattn.attn_fwd(q, k, v, cp, 2, out, lse)
+                cpattn.attn_bwd(q, k, v, out, lse, dout, cp, 2, dq, dk, dv)
+        for _ in range(warmup):
+            zstep()
+        torch.cuda.synchronize()
+        cpattn.check_device()
+        zms = time_steps(zstep, n)
+        res["zero_copy"] = {"ms_per_step": zms, "tflops": f_step / (zms / 1e3) / 1e12,
+                            "frac": f_step / (zms / 1e3) / 1e12 / peak, "steps": n,
+                            "what": "fwd + bwd with load_balance=2 (natural-order tensors, balanced schedule)"}
+        del out, lse, dq, dk, dv
     del attn, q, k, v, dout
     torch.cuda.empty_cache()
     return res
