@@ -430,6 +430,20 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d(smem + C::OFF_DO + st * C::TILE + bx * kRows * 128, &a.tdo, &bar.do_full[st], bx * 64, hq, qrow,
                         u.b);
+          // with the unit's last step queued, the next unit's K and V go to
+          // L2: their loads wait for this unit's last MMA, and would otherwise
+          // meet the full HBM latency at every unit boundary
+          if (!more) {
+            const int ui2 = unit_index(a.cta_off, r + 1, cta);
+            if (ui2 >= 0) {
+              const BwdUnit u2 = a.units[ui2];
+              const int krow2 = mem_row<NAT>(pm, u2.t * kRows);
+              for (int bx = 0; bx < D / 64; ++bx) {
+                tma_prefetch_l2_4d(&a.tk, bx * 64, u2.h, krow2, u2.b);
+                tma_prefetch_l2_4d(&a.tv, bx * 64, u2.h, krow2, u2.b);
+              }
+            }
+          }
           ++gs;
         } while (more);
         ++uc;
