@@ -276,20 +276,25 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(DecodeArgs a, floa
 // ---------------------------------------------------------------------------
 // INT8: the cache holds int8 vectors with one fp32 scale per (b, g,
 // position).  TMA stages each item's int8 K (with the bf16 q rows) and int8
-// V; eight converter warps turn them into fp16 tiles (int8 is exact in fp16,
-// so the conversion is exact and needs no multiply) and the MMAs run as fp16
-// x fp16 -> fp32.  The scales are folded in by the softmax threads, one
-// position each: the key scale into the scores, the value scale into P.  The
-// staging costs shared memory: two stages per ring instead of three.
+// V; eight converter warps turn them into fp16 (int8 is exact in fp16, so the
+// conversion is exact and needs no multiply) and the MMAs run as fp16 x fp16
+// -> fp32.  K goes straight into TMEM as the A operand of the scores (thread
+// = position = TMEM lane, 64 columns of fp16 pairs per item), so only V and
+// q take fp16 tiles in shared memory, and what that saves buys deeper int8
+// staging (three K and three V stages): the staged bytes are what is in flight
+// from HBM.  The scales are folded in by the softmax threads, one position
+// each: the key scale into the scores, the value scale into P; each thread
+// fetches its position's scales one item ahead with cp.async into a small
+// ring of its own.
 template <bool INT8>
 struct TcCfg {
   static constexpr int D = 128;
   static constexpr int NH = 16;                 // head columns of the MMAs
   static constexpr int ROWS = kDecodeSplit;     // positions per item
-  static constexpr int NK = INT8 ? 2 : 3;       // K (+q) ring stages: freed once the scores are formed
-  static constexpr int NV = INT8 ? 2 : 3;       // V ring stages: freed once the output is formed
-  static constexpr int NS = 2;                  // int8 staging stages per tensor
-  static constexpr int K_BYTES = ROWS * D * 2;  // two 64-column boxes
+  static constexpr int NK = 3;                  // K (+q) stages: freed once the scores are formed (int8: K in TMEM)
+  static constexpr int NV = INT8 ? 2 : 3;       // V stages: freed once the output is formed
+  static constexpr int NSK = 3, NSV = 3;        // int8 staging stages of K (+ bf16 q) and of V
+  static constexpr int K_BYTES = INT8 ? 0 : ROWS * D * 2;  // two 64-column boxes (int8: none, K is in TMEM)
   static constexpr int V_BYTES = ROWS * D * 2;
   static constexpr int Q_BYTES = NH * D * 2;    // two boxes of 16 rows
   static constexpr int KSTAGE = K_BYTES + Q_BYTES;
@@ -299,17 +304,23 @@ struct TcCfg {
   static constexpr int BOX_BYTES = BOX * 128;   // a box of 128-byte rows (64 bf16 columns or 128 int8 values)
   static constexpr int P_BYTES = NH * ROWS * 2;  // P^T as [head][position], two boxes of 64 positions
   static constexpr int OFF_V = NK * KSTAGE;
-  static constexpr int OFF_KS = OFF_V + NV * V_BYTES;              // int8 K staging
-  static constexpr int OFF_VS = OFF_KS + (INT8 ? NS * KS_STAGE : 0);  // int8 V staging
-  static constexpr int OFF_P = OFF_VS + (INT8 ? NS * S8_BYTES : 0);
+  static constexpr int OFF_KS = OFF_V + NV * V_BYTES;                 // int8 K staging
+  static constexpr int OFF_VS = OFF_KS + (INT8 ? NSK * KS_STAGE : 0);  // int8 V staging
+  static constexpr int OFF_P = OFF_VS + (INT8 ? NSV * S8_BYTES : 0);
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_RED = OFF_BAR + 256;  // per group: float rmax[4][NH], rsum[4][NH]
-  static constexpr int OFF_MISC = OFF_RED + 2 * 2 * 4 * NH * 4;
+  static constexpr int OFF_RED = OFF_BAR + 512;  // per group: float rmax[4][NH], rsum[2][4][NH]
+  static constexpr int OFF_SC = OFF_RED + 2 * 3 * 4 * NH * 4;  // int8: per group float [2][key|value][ROWS]
+  static constexpr int OFF_MISC = OFF_SC + (INT8 ? 2 * 2 * 2 * ROWS * 4 : 0);
   static constexpr int OFF_LENS = OFF_MISC + 64;
   static constexpr int MAX_B = 1024;             // batch rows staged in shared memory
   static constexpr int OFF_PRE = OFF_LENS + MAX_B * 4;
   static constexpr int SMEM = OFF_PRE + (MAX_B + 1) * 4 + 1024;
-  static constexpr int kThreads = INT8 ? 608 : 352;  // + warps 11-14 converting K, 15-18 converting V
+  static constexpr int kThreads = INT8 ? 640 : 384;  // + warps 12-15 converting K, 16-19 converting V
+  // TMEM: S_b at 16b (b = item parity), O_b at 32 + 16b (b = item mod 4); int8: K stage i at 128 + 64i
+  static constexpr int T_O = 32;
+  static constexpr int T_K = 128;
+  static constexpr int TMEM_COLS = INT8 ? 512 : 128;
+  static_assert(!INT8 || T_K + NK * 64 <= TMEM_COLS, "TMEM budget");
   static_assert(KSTAGE % 1024 == 0 && OFF_V % 1024 == 0 && OFF_KS % 1024 == 0 && OFF_VS % 1024 == 0 &&
                     OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -319,41 +330,57 @@ struct TcCfg {
 template <int NK, int NV>
 struct TcBars {
   uint64_t kfull[NK], kempty[NK], vfull[NV], vempty[NV];
-  uint64_t ksfull[2], ksempty[2], vsfull[2], vsempty[2];  // int8 staging
-  uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t done;
+  uint64_t ksfull[4], ksempty[4], vsfull[3], vsempty[3];  // int8 staging
+  uint64_t s_full[2], p_full[2], o_full[4];
+  uint64_t done, done2;
 };
 namespace tcd {
 constexpr int MAX_B = TcCfg<false>::MAX_B;
 }  // namespace tcd
 
-// one cached int8 row (128 values, staged with a 128-byte swizzle) to fp16
-// row r of a K-major, 128-byte-swizzled tile of two 64-column boxes, exactly:
+// 16 cached int8 values (one 16-byte chunk) to 8 words of fp16 pairs
+// (values 2i, 2i + 1 in word i, the lower index in the low half), exactly:
 // the biased byte b = x + 128 in the mantissa of fp16 1024 is 1024 + b, and
 // subtracting 1152 leaves x
-__device__ __forceinline__ void int8_row_to_f16(const unsigned char* stg, unsigned char* tile, int r) {
+__device__ __forceinline__ void int8_chunk_to_f16(const uint4 w, uint32_t (&o)[8]) {
   const uint32_t nmagic = 0xE480E480u;  // fp16x2 (-1152, -1152)
+  const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // fp16 pairs (1024 + b0, 1024 + b1) and (1024 + b2, 1024 + b3)
+    const uint32_t lo = __byte_perm(wv[i], 0x64646464u, 0x5140);
+    const uint32_t hi = __byte_perm(wv[i], 0x64646464u, 0x7362);
+    uint32_t x;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(lo), "r"(nmagic));
+    o[2 * i] = x;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(hi), "r"(nmagic));
+    o[2 * i + 1] = x;
+  }
+}
+
+// one cached int8 row (128 values, staged with a 128-byte swizzle) to fp16
+// row r of a K-major, 128-byte-swizzled tile of two 64-column boxes
+__device__ __forceinline__ void int8_row_to_f16(const unsigned char* stg, unsigned char* tile, int r) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {  // 16 values per 16-byte chunk
     const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
-    const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
     uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      // fp16 pairs (1024 + b0, 1024 + b1) and (1024 + b2, 1024 + b3)
-      const uint32_t lo = __byte_perm(wv[i], 0x64646464u, 0x5140);
-      const uint32_t hi = __byte_perm(wv[i], 0x64646464u, 0x7362);
-      uint32_t x;
-      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(lo), "r"(nmagic));
-      o[2 * i] = x;
-      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(x) : "r"(hi), "r"(nmagic));
-      o[2 * i + 1] = x;
-    }
+    int8_chunk_to_f16(w, o);
     unsigned char* box = tile + (c >> 2) * (128 * 128) + r * 128;
     const int cc = 2 * (c & 3);
     *reinterpret_cast<uint4*>(box + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
     *reinterpret_cast<uint4*>(box + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
+}
+
+// 4-byte asynchronous copy global -> shared (cp.async, completion per thread by group)
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // instruction descriptor, kind::f16 with fp16 A/B and fp32 accumulation
@@ -370,34 +397,34 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, i
 struct Item {
   int b, g, sp, len, nsplit, n;  // n: positions of the slice in the cache
 };
-__device__ __forceinline__ Item loaded_item(int j, const int* pre, const int* lens, int B, int Hkv) {
-  Item it;
-  const int nfull = pre[B];
-  if (j < nfull) {
-    int lo = 0, hi = B - 1;  // largest b with pre[b] <= j: a row with whole slices
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= j) lo = mid;
-      else hi = mid - 1;
+// Every role visits its slots in increasing j, so the row of a whole slice
+// is found by walking on from the previous one (no search per item).
+struct ItemWalk {
+  int b = 0;
+  __device__ __forceinline__ Item at(int j, const int* pre, const int* lens, int B, int Hkv) {
+    Item it;
+    const int nfull = pre[B];
+    if (j < nfull) {
+      while (pre[b + 1] <= j) ++b;  // the last row with pre[b] <= j (pre[B] > j ends the walk)
+      it.b = b;
+      it.len = lens[b];
+      const int nf = it.len / kDecodeSplit;
+      const int r = j - pre[b];
+      it.g = r / nf;
+      it.sp = r - it.g * nf;
+      it.n = kDecodeSplit;
+    } else {
+      const int r = j - nfull;
+      it.b = r / Hkv;
+      it.g = r - it.b * Hkv;
+      it.len = lens[it.b];
+      it.sp = it.len / kDecodeSplit;
+      it.n = it.len - it.sp * kDecodeSplit;
     }
-    it.b = lo;
-    it.len = lens[lo];
-    const int nf = it.len / kDecodeSplit;
-    const int r = j - pre[lo];
-    it.g = r / nf;
-    it.sp = r - it.g * nf;
-    it.n = kDecodeSplit;
-  } else {
-    const int r = j - nfull;
-    it.b = r / Hkv;
-    it.g = r - it.b * Hkv;
-    it.len = lens[it.b];
-    it.sp = it.len / kDecodeSplit;
-    it.n = it.len - it.sp * kDecodeSplit;
+    it.nsplit = (it.len + kDecodeSplit - 1) / kDecodeSplit;
+    return it;
   }
-  it.nsplit = (it.len + kDecodeSplit - 1) / kDecodeSplit;
-  return it;
-}
+};
 
 template <int GMAX, bool INT8>
 __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel(const __grid_constant__ DecodeArgs a,
@@ -408,6 +435,7 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
   constexpr int OFF_BAR = C::OFF_BAR, OFF_RED = C::OFF_RED, OFF_MISC = C::OFF_MISC, OFF_LENS = C::OFF_LENS;
   constexpr int OFF_PRE = C::OFF_PRE, kThreadsTc = C::kThreads;
   using Bars = TcBars<NK, NV>;
+  static_assert(sizeof(Bars) <= 512, "barrier space");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bar = *reinterpret_cast<Bars*>(smem + OFF_BAR);
@@ -427,16 +455,16 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
     // int8: a K or V stage completes when its 128 converter threads have written it
     for (int i = 0; i < NK; ++i) { mbar_init(&bar.kfull[i], INT8 ? 128 : 1); mbar_init(&bar.kempty[i], 1); }
     for (int i = 0; i < NV; ++i) { mbar_init(&bar.vfull[i], INT8 ? 128 : 1); mbar_init(&bar.vempty[i], 1); }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar.ksfull[i], 1); mbar_init(&bar.ksempty[i], 128);
-      mbar_init(&bar.vsfull[i], 1); mbar_init(&bar.vsempty[i], 128);
-    }
-    for (int i = 0; i < 2; ++i) { mbar_init(&bar.s_full[i], 1); mbar_init(&bar.p_full[i], 128); mbar_init(&bar.o_full[i], 1); }
+    for (int i = 0; i < C::NSK; ++i) { mbar_init(&bar.ksfull[i], 1); mbar_init(&bar.ksempty[i], 128); }
+    for (int i = 0; i < C::NSV; ++i) { mbar_init(&bar.vsfull[i], 1); mbar_init(&bar.vsempty[i], 128); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.s_full[i], 1); mbar_init(&bar.p_full[i], 128); }
+    for (int i = 0; i < 4; ++i) mbar_init(&bar.o_full[i], 1);
     mbar_init(&bar.done, 1);
+    mbar_init(&bar.done2, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) { tmem_alloc(tmem_slot, 64); tmem_relinquish(); }
+  if (warp == 1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&a.tk); prefetch_tmap(&a.tv); prefetch_tmap(&a.tq); prefetch_tmap(&a.tk2); prefetch_tmap(&a.tv2);
   }
@@ -477,14 +505,15 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S_b at cols 16b, O_b at 32 + 16b
+  const uint32_t tmem = *tmem_slot;
   const int total = pre[a.B] + a.B * a.Hkv;  // item slots
   const int n_slots = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // this CTA's slots i: j = cta + i*ncta
   // every role walks the same slots and skips the same empty ones, so the
   // item counter k (ring stages, buffers, phases) agrees between them
   auto count_items = [&]() {
     int n = 0;
-    for (int i = 0; i < n_slots; ++i) n += loaded_item(cta + i * ncta, pre, lens_s, a.B, a.Hkv).n > 0;
+    ItemWalk w;
+    for (int i = 0; i < n_slots; ++i) n += w.at(cta + i * ncta, pre, lens_s, a.B, a.Hkv).n > 0;
     return n;
   };
 
@@ -495,8 +524,9 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
     if (lane == 0) {
       const bool is_v = warp == 10;
       int k = 0;
+      ItemWalk walk;
       for (int i = 0; i < n_slots; ++i) {
-        const Item it = loaded_item(cta + i * ncta, pre, lens_s, a.B, a.Hkv);
+        const Item it = walk.at(cta + i * ncta, pre, lens_s, a.B, a.Hkv);
         if (it.n == 0) continue;
         // a whole slice in one 128-row box per 64 columns, a short one in the
         // 32-row boxes that hold its positions
@@ -506,9 +536,10 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
         const CUtensorMap* mk = whole ? &a.tk : &a.tk2;
         const CUtensorMap* mv = whole ? &a.tv : &a.tv2;
         if (INT8) {
-          const int st = k % C::NS;
+          const int ns = is_v ? C::NSV : C::NSK;
+          const int st = k % ns;
           uint64_t* fb = is_v ? &bar.vsfull[st] : &bar.ksfull[st];
-          if (!mbar_wait(is_v ? &bar.vsempty[st] : &bar.ksempty[st], ((k / C::NS) & 1) ^ 1, ab)) break;
+          if (!mbar_wait(is_v ? &bar.vsempty[st] : &bar.ksempty[st], ((k / ns) & 1) ^ 1, ab)) break;
           unsigned char* sb = smem + (is_v ? C::OFF_VS + st * C::S8_BYTES : C::OFF_KS + st * C::KS_STAGE);
           mbar_expect_tx(fb, nb * bbytes + (is_v ? 0 : C::Q_BYTES));
           for (int jb = 0; jb < nb; ++jb)
@@ -533,24 +564,37 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
         ++k;
       }
     }
-  } else if (INT8 && warp >= 11) {
+  } else if (INT8 && warp >= 12) {
     // ---------------------------------------------------------- int8 -> fp16 converters
-    // warps 11-14 convert K (and the item's q rows, bf16 -> fp16), warps 15-18
-    // convert V; thread r owns row r.  A failed wait runs on (the tiles are
-    // then garbage and the error word is set)
-    const bool is_v = warp >= 15;
-    const int r = tid - (is_v ? 480 : 352);
+    // warps 12-15 convert K into TMEM (thread = position = TMEM lane of its
+    // warp's quarter) and the item's q rows (bf16 -> fp16) into shared
+    // memory; warps 16-19 convert V, thread r owning row r.  A failed wait
+    // runs on (the tiles are then garbage and the error word is set)
+    const bool is_v = warp >= 16;
+    const int r = is_v ? tid - 512 : (warp & 3) * 32 + lane;
     const int n_items = count_items();
     for (int k = 0; k < n_items; ++k) {
-      const int ss = k % C::NS;
-      const uint32_t sph = (k / C::NS) & 1;
       if (!is_v) {
-        const int kst = k % NK;
+        const int kst = k % NK, ss = k % C::NSK;
         mbar_wait(&bar.kempty[kst], ((k / NK) & 1) ^ 1, ab);
-        mbar_wait(&bar.ksfull[ss], sph, ab);
+        mbar_wait(&bar.ksfull[ss], (k / C::NSK) & 1, ab);
+        tc_fence_after();
         const unsigned char* sb = smem + C::OFF_KS + ss * C::KS_STAGE;
-        unsigned char* kb = smem + kst * KSTAGE;
-        int8_row_to_f16(sb, kb, r);
+        unsigned char* kb = smem + kst * KSTAGE;  // the q stage (K itself is in TMEM)
+        const uint32_t tk = tmem + (uint32_t((warp & 3) * 32) << 16) + C::T_K + kst * 64;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {  // dims 64hh .. 64hh + 63: TMEM columns 32hh .. 32hh + 31
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cg = 4 * hh + c;
+            uint32_t w8[8];
+            int8_chunk_to_f16(*reinterpret_cast<const uint4*>(sb + r * 128 + ((cg ^ (r & 7)) << 4)), w8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[8 * c + i] = w8[i];
+          }
+          tmem_st32(tk + hh * 32, o);
+        }
         // q: 16 rows x 128 bf16 in two swizzled boxes; thread r converts 16 values in place order
         {
           const uint4 u0 = reinterpret_cast<const uint4*>(sb + C::S8_BYTES)[2 * r];
@@ -568,22 +612,31 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
           reinterpret_cast<uint4*>(kb + K_BYTES)[2 * r + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
         fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(&bar.ksempty[ss]);
         mbar_arrive(&bar.kfull[kst]);
       } else {
-        const int vst = k % NV;
+        const int vst = k % NV, ss = k % C::NSV;
         mbar_wait(&bar.vempty[vst], ((k / NV) & 1) ^ 1, ab);
-        mbar_wait(&bar.vsfull[ss], sph, ab);
+        mbar_wait(&bar.vsfull[ss], (k / C::NSV) & 1, ab);
         int8_row_to_f16(smem + C::OFF_VS + ss * C::S8_BYTES, smem + OFF_V + vst * V_BYTES, r);
         fence_proxy_async_smem();
         mbar_arrive(&bar.vsempty[ss]);
         mbar_arrive(&bar.vfull[vst]);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      // K (K-major) x q (K-major); V^T (MN-major) x P^T (K-major); fp16 operands for the int8 cache
+  } else if (warp == 1 || warp == 11) {
+    // ---------------------------------------------------------- MMA issuers
+    // warp 1 issues the scores, warp 11 the outputs: one thread issues a
+    // tcgen05.mma about every 60 cycles whatever its size, and an item's
+    // sixteen small MMAs with their commits and waits took one thread longer
+    // than the item's bytes take to stream.  The two sequences share no TMEM
+    // columns and no shared-memory operand; a group writes P(k+2) only after
+    // O(k) has completed, which keeps two P buffers and barriers enough.
+    {
+      // K (K-major; int8 cache: fp16 in TMEM) x q (K-major); V^T (MN-major) x P^T (K-major); fp16
+      // operands for the int8 cache
       constexpr uint32_t IDESC_S = INT8 ? idesc_f16(128, NH, 0, 0) : idesc_bf16(128, NH, 0, 0);
       constexpr uint32_t IDESC_O = INT8 ? idesc_f16(128, NH, 1, 0) : idesc_bf16(128, NH, 1, 0);
       const uint32_t s0 = smem_u32(smem);
@@ -591,9 +644,14 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
         const uint32_t sb = s0 + (k % NK) * KSTAGE;
         const uint64_t ak = sdesc_sw128(sb, 16, 1024), bq = sdesc_sw128(sb + K_BYTES, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + (k & 1) * 16, ak + (((kk >> 2) * (ROWS * 128) + (kk & 3) * 32) >> 4),
-                 bq + (((kk >> 2) * (NH * 128) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t bk = bq + (((kk >> 2) * (NH * 128) + (kk & 3) * 32) >> 4);
+          if (INT8)  // K from TMEM: fp16 pairs, 8 columns per 16 dims
+            mma_ts(tmem + (k & 1) * 16, tmem + C::T_K + (k % NK) * 64 + kk * 8, bk, IDESC_S, kk > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + (k & 1) * 16, ak + (((kk >> 2) * (ROWS * 128) + (kk & 3) * 32) >> 4), bk, IDESC_S,
+                   kk > 0 ? 1u : 0u);
+        }
         mma_commit(&bar.s_full[k & 1]);
         mma_commit(&bar.kempty[k % NK]);
       };
@@ -603,61 +661,152 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
         const uint64_t bp = sdesc_sw128(s0 + OFF_P + (k & 1) * P_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < ROWS / 16; ++kk)
-          mma_ss(tmem + 32 + (k & 1) * 16, av + ((kk * 16 * 128) >> 4),
+          mma_ss(tmem + C::T_O + (k & 3) * 16, av + ((kk * 16 * 128) >> 4),
                  bp + (((kk >> 2) * (NH * 128) + (kk & 3) * 32) >> 4), IDESC_O, kk > 0 ? 1u : 0u);
-        mma_commit(&bar.o_full[k & 1]);
+        mma_commit(&bar.o_full[k & 3]);
         mma_commit(&bar.vempty[k % NV]);
       };
-      const int n_items = count_items();
       bool ok = true;
-      // scores of the first two items, then: O(k) once group k&1 has written
-      // P(k); S(k+2) into the buffer that group has finished reading
-      for (int k = 0; k < 2 && k < n_items && ok; ++k) {
-        if (!(ok = mbar_wait(&bar.kfull[k % NK], (k / NK) & 1, ab))) break;
-        tc_fence_after();
-        issue_s(k);
-      }
-      for (int k = 0; ok && k < n_items; ++k) {
-        if (!(ok = mbar_wait(&bar.p_full[k & 1], (k >> 1) & 1, ab))) break;
-        if (!(ok = mbar_wait(&bar.vfull[k % NV], (k / NV) & 1, ab))) break;
-        tc_fence_after();
-        issue_o(k);
-        if (k + 2 < n_items) {
-          if (!(ok = mbar_wait(&bar.kfull[(k + 2) % NK], ((k + 2) / NK) & 1, ab))) break;
-          tc_fence_after();
-          issue_s(k + 2);
+      if (warp == 1) {
+        if (lane == 0) {
+          const int n_items = count_items();
+          for (int k = 0; ok && k < n_items; ++k) {
+            // S(k) overwrites S(k-2), which its group has read once it has written P(k-2)
+            if (k >= 2 && !(ok = mbar_wait(&bar.p_full[k & 1], ((k - 2) >> 1) & 1, ab))) break;
+            if (!(ok = mbar_wait(&bar.kfull[k % NK], (k / NK) & 1, ab))) break;
+            tc_fence_after();
+            issue_s(k);
+          }
+          mma_drain(&bar.done, a.err);
         }
+      } else {
+        // the whole warp waits for each V tile in turn (never more than one
+        // phase behind its barrier: the next tile of a stage lands only after
+        // this warp's O of the current one) and, for a partial slice, zeroes
+        // the value rows at or past the length before O reads them: they were
+        // loaded from a cache that may hold anything there, or not loaded and
+        // left by an earlier item (or never written), and get zero weight
+        ItemWalk walk;
+        int k = 0;
+        for (int i = 0; ok && i < n_slots; ++i) {
+          const Item it = walk.at(cta + i * ncta, pre, lens_s, a.B, a.Hkv);
+          if (it.n == 0) continue;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar.vfull[k % NV], (k / NV) & 1, ab));
+          if (!ok) break;
+          if (!INT8 && it.n < ROWS) {
+            unsigned char* vb = smem + OFF_V + (k % NV) * V_BYTES;
+            for (int x = lane; x < (ROWS - it.n) * 16; x += 32) {  // 16-byte chunks: 8 per row in each of two boxes
+              const int row = it.n + (x >> 4), c = x & 15;
+              *reinterpret_cast<uint4*>(vb + (c >> 3) * (ROWS * 128) + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            ok = mbar_wait(&bar.p_full[k & 1], (k >> 1) & 1, ab);
+            if (ok) {
+              tc_fence_after();
+              issue_o(k);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ++k;
+        }
+        if (lane == 0) mma_drain(&bar.done2, a.err);
       }
-      mma_drain(&bar.done, a.err);
     }
   } else {
     // ---------------------------------------------------------- softmax + epilogue
     // group gi takes items k = gi, gi + 2, ...; thread = TMEM lane = position
     // (scores) and = dim (output); control flow is uniform over the group's
-    // 128 threads, so its named barrier completes.  rmax is rewritten only
-    // after the group's next first barrier, rsum after its second, and every
-    // thread reaches those after reading both for this item.
+    // 128 threads, so its named barrier completes.  An item's output is read
+    // after the group has written the next item's P (which waits for that
+    // output, as it reuses its P buffer), so the tensor core forms O while the
+    // group already works on the next scores (O in TMEM and its barriers by
+    // k & 3).  rmax is rewritten only once the group's next scores
+    // exist, which needs every thread's P of this item; an item's rsum (by
+    // item parity within the group) is read after the next item's barrier and
+    // rewritten only after the barrier of the item after that.
     const int gi = (warp - 2) >> 2;
     const int wq = warp & 3;            // TMEM lane quarter of this warp
     const int r = wq * 32 + lane;       // position / dim handled by this thread
     const uint32_t lane_base = uint32_t(wq * 32) << 16;
-    float* rmax = reinterpret_cast<float*>(smem + OFF_RED) + gi * 2 * 4 * NH;
-    float* rsum = rmax + 4 * NH;
+    float* rmax = reinterpret_cast<float*>(smem + OFF_RED) + gi * 3 * 4 * NH;
+    float* rsum0 = rmax + 4 * NH;
     __nv_bfloat16* ogb = static_cast<__nv_bfloat16*>(a.out);
-    int k = -1;  // item counter over the non-empty slots
-    for (int i = 0; i < n_slots; ++i) {
-      const Item it = loaded_item(cta + i * ncta, pre, lens_s, a.B, a.Hkv);
-      if (it.n == 0) continue;
-      if ((++k & 1) != gi) continue;
-      __nv_bfloat16* og = ogb + ((size_t)it.b * a.Hq + (size_t)it.g * G) * D;
+    // this group's items in order (k counts the CTA's non-empty slots)
+    ItemWalk walk;
+    int ni = 0, nk = -1;
+    auto next_mine = [&](Item& nit, int& kk) {
+      for (; ni < n_slots; ++ni) {
+        nit = walk.at(cta + ni * ncta, pre, lens_s, a.B, a.Hkv);
+        if (nit.n == 0) continue;
+        if ((++nk & 1) != gi) continue;
+        kk = nk;
+        ++ni;
+        return true;
+      }
+      return false;
+    };
+    // int8 cache: position r's key and value scales, fetched one item ahead
+    // into this thread's slots of a two-item ring (a cold load, or a register
+    // carried over from a load issued one item earlier, would otherwise sit on
+    // every item's path).  One copy group per item, empty where the item has
+    // no position r or there is no next item, so that waiting for all but the
+    // newest group always covers the current item.
+    float* scr = reinterpret_cast<float*>(smem + C::OFF_SC) + gi * 2 * 2 * ROWS + r;
+    auto fetch_scales = [&](const Item& sit, int kk, bool any) {
+      if (!INT8) return;
+      if (any && r < sit.n) {  // positions past the length are never read (p is 0 there)
+        const size_t so = ((size_t)sit.b * a.Hkv + sit.g) * a.Smax + sit.sp * ROWS + r;
+        float* d = scr + ((kk >> 1) & 1) * 2 * ROWS;
+        cp_async4(d, a.kscale + so);
+        cp_async4(d + ROWS, a.vscale + so);
+      }
+      cp_async_commit();
+    };
+    // the output of item (pit, pk): thread r owns dim r of every head
+    auto wait_o = [&](int pk) {
+      mbar_wait(&bar.o_full[pk & 3], (pk >> 2) & 1, ab);
+      tc_fence_after();
+    };
+    auto epilogue = [&](const Item& pit, int pk) {
+      const float* rs = rsum0 + ((pk >> 1) & 1) * 4 * NH;
+      uint32_t orr[16];
+      tmem_ld16(tmem + lane_base + C::T_O + (pk & 3) * 16, orr);
+      tmem_ld_wait();
+      __nv_bfloat16* og = ogb + ((size_t)pit.b * a.Hq + (size_t)pit.g * G) * D;
+      const int bg = pit.b * a.Hkv + pit.g;
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (h >= G) continue;
+        const float L = (rs[h] + rs[NH + h]) + (rs[2 * NH + h] + rs[3 * NH + h]);
+        const float o = __uint_as_float(orr[h]);
+        if (pit.nsplit == 1) {
+          og[h * D + r] = __float2bfloat16(o / L);
+        } else {
+          a.part_o[(((size_t)bg * max_split + pit.sp) * GMAX + h) * D + r] = o;
+          if (r == 0) a.part_ml[(((size_t)bg * max_split + pit.sp) * GMAX + h) * 2 + 1] = L;
+        }
+      }
+    };
+    Item it, pit;
+    int k = 0, pk = 0;
+    bool have = next_mine(it, k), have_prev = false;
+    fetch_scales(it, k, have);
+    while (have) {
+      Item itn;
+      int kn = 0;
+      const bool have_n = next_mine(itn, kn);
+      fetch_scales(itn, kn, have_n);
       const int buf = k & 1;
       const uint32_t par = (k >> 1) & 1;
       const int n = it.n;
-      float ksc = 1.f, vsc = 1.f;  // int8 cache: this position's scales, fetched while the scores form
-      if (INT8 && r < n) {  // positions past the length are never read (p is 0 there)
-        const size_t so = ((size_t)it.b * a.Hkv + it.g) * a.Smax + it.sp * ROWS + r;
-        ksc = a.kscale[so];
-        vsc = a.vscale[so];
+      float ksc = 1.f, vsc = 1.f;
+      if (INT8 && r < n) {
+        cp_async_wait<1>();  // this item's copies (the newest group is the next item's)
+        ksc = scr[par * 2 * ROWS];
+        vsc = scr[par * 2 * ROWS + ROWS];
       }
       // a failed wait (abort or timeout) runs on: the named barriers need every thread
       mbar_wait(&bar.s_full[buf], par, ab);
@@ -678,27 +827,17 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
         if (lane == 0) rmax[wq * NH + h] = m;
       }
       named_bar(1 + gi, 128);
-      float M[GMAX], p[GMAX];
+      float p[GMAX];
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
-        M[h] = fmaxf(fmaxf(rmax[h], rmax[NH + h]), fmaxf(rmax[2 * NH + h], rmax[3 * NH + h]));
-        p[h] = (h < G && r < n) ? fast_exp2(sv[h] - M[h]) : 0.f;
+        const float M = fmaxf(fmaxf(rmax[h], rmax[NH + h]), fmaxf(rmax[2 * NH + h], rmax[3 * NH + h]));
+        p[h] = (h < G && r < n) ? fast_exp2(sv[h] - M) : 0.f;
+        if (h < G && r == 0 && it.nsplit > 1)
+          a.part_ml[(((size_t)(it.b * a.Hkv + it.g) * max_split + it.sp) * GMAX + h) * 2] = M;
       }
-      // value rows at or past the length: loaded from a cache that may hold
-      // anything there, or not loaded and left by an earlier item (or never
-      // written); they get zero weight, and are zeroed before O reads them
-      if (!INT8 && n < ROWS) {
-        mbar_wait(&bar.vfull[k % NV], (k / NV) & 1, ab);
-        if (r >= n) {
-          unsigned char* vb = smem + OFF_V + (k % NV) * V_BYTES;
-#pragma unroll
-          for (int bx = 0; bx < 2; ++bx)
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(vb + bx * (ROWS * 128) + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // P^T[head][position] in the K-major 128-byte-swizzled layout of the MMA's B operand
+      // P^T[head][position] in the K-major 128-byte-swizzled layout of the MMA's B operand,
+      // once O of the group's previous item has read the buffer
+      if (have_prev) wait_o(pk);
       {
         unsigned char* pb = smem + OFF_P + buf * P_BYTES + (r >> 6) * (NH * 128);
         const int chunk = (r & 63) >> 3;
@@ -716,39 +855,27 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
       tc_fence_before();
       mbar_arrive(&bar.p_full[buf]);
       // the denominators while the tensor core forms O
+      float* rs = rsum0 + par * 4 * NH;
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
         float l = p[h];
 #pragma unroll
         for (int off = 16; off; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        if (lane == 0) rsum[wq * NH + h] = l;
+        if (lane == 0) rs[wq * NH + h] = l;
       }
-      named_bar(1 + gi, 128);
-      float L[GMAX];
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h) L[h] = (rsum[h] + rsum[NH + h]) + (rsum[2 * NH + h] + rsum[3 * NH + h]);
-      // output: thread r owns dim r of every head
-      mbar_wait(&bar.o_full[buf], par, ab);
-      tc_fence_after();
-      uint32_t orr[16];
-      tmem_ld16(tmem + lane_base + 32 + buf * 16, orr);
-      tmem_ld_wait();
-      const int bg = it.b * a.Hkv + it.g;
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h) {
-        if (h >= G) continue;
-        const float o = __uint_as_float(orr[h]);
-        if (it.nsplit == 1) {
-          og[h * D + r] = __float2bfloat16(o / L[h]);
-        } else {
-          a.part_o[(((size_t)bg * max_split + it.sp) * GMAX + h) * D + r] = o;
-          if (r == 0) {
-            float* ml = a.part_ml + (((size_t)bg * max_split + it.sp) * GMAX + h) * 2;
-            ml[0] = M[h];
-            ml[1] = L[h];
-          }
-        }
-      }
+      // the previous item's output (its sums were complete at this item's barrier)
+      if (have_prev) epilogue(pit, pk);
+      pit = it;
+      pk = k;
+      have_prev = true;
+      it = itn;
+      k = kn;
+      have = have_n;
+    }
+    if (have_prev) {
+      named_bar(1 + gi, 128);  // every warp's sums of the last item
+      wait_o(pk);
+      epilogue(pit, pk);
     }
   }
 
@@ -757,7 +884,7 @@ __global__ void __launch_bounds__(TcCfg<INT8>::kThreads, 1) gqa_decode_tc_kernel
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 

@@ -382,6 +382,28 @@ def test_decode_int8_edge_lengths():
     assert_close_out(_f64(out), ref, "int8 decode edge lengths")
 
 
+def test_decode_repeatable_over_many_calls():
+    """The decode is bitwise repeatable (no atomics; every partial and its
+    merge in a fixed order), so repeated calls on the same inputs must agree
+    bit for bit.  Many short and partial slices (lengths from 1) stress the
+    hand-off between the roles: a wait that confuses one pipeline phase with
+    another shows here as an occasional differing call long before it fails
+    a tolerance."""
+    B, Hq, Hkv, D, Smax = 24, 32, 8, 128, 2048
+    q, kc, vc, lens = (x.cuda() for x in synth.decode_inputs(B, Hq, Hkv, D, Smax, 1, Smax, seed=9))
+    q8, kq, vq, ks, vs, _ = synth.decode_inputs_int8(B, Hq, Hkv, D, Smax, 1, 1, seed=10)
+    q8, kq, vq, ks, vs = (x.cuda() for x in (q8, kq, vq, ks, vs))
+    ref = cp_.gqa_decode(q, kc, vc, lens).clone()
+    ref8 = cp_.gqa_decode_int8(q8, kq, vq, ks, vs, lens).clone()
+    cp_.check_device()
+    bad = bad8 = 0
+    for _ in range(200):
+        bad += not torch.equal(cp_.gqa_decode(q, kc, vc, lens), ref)
+        bad8 += not torch.equal(cp_.gqa_decode_int8(q8, kq, vq, ks, vs, lens), ref8)
+    cp_.check_device()
+    assert bad == 0 and bad8 == 0, (bad, bad8)
+
+
 # ---------------------------------------------------------------------------
 # MLA with the rope key shared by the heads
 # ---------------------------------------------------------------------------
