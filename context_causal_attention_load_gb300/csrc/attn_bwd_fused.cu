@@ -50,6 +50,14 @@ constexpr int kRegsEw = 152;
 constexpr int kRegsWg2 = 112;
 constexpr int kRegsWg3 = 96;
 static_assert(256 * kRegsEw + 128 * kRegsWg2 + 128 * kRegsWg3 <= kThreadsF * kRegsLaunchF, "register split");
+// a warpgroup's share is set with setmaxnreg.inc when it grows from the launch
+// count and .dec when it shrinks (either one in the other direction is invalid)
+template <int N>
+__device__ __forceinline__ void regs_to() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  if constexpr (N > kRegsLaunchF) regs_inc<N>();
+  else if constexpr (N < kRegsLaunchF) regs_dec<N>();
+}
 constexpr int kRows = 128;      // key rows per unit, query rows per step
 
 template <int D>
@@ -375,10 +383,10 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
   // each role's code sits under its own setmaxnreg, so the compiler
   // allocates it against that role's register budget
   if (warp >= 12) {
-  regs_dec<kRegsWg3>();
+  regs_to<kRegsWg3>();
   dq_readout();
   } else if (warp >= 8) {
-  regs_dec<kRegsWg2>();
+  regs_to<kRegsWg2>();
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -600,7 +608,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     }
   }
   } else {
-    regs_inc<kRegsEw>();
+    regs_to<kRegsEw>();
     // ------------------------------------------------------------ element-wise warps
     // Group g (warps 4g..4g+3) owns query columns [64g, 64g+64) of S^T/dP^T
     // (thread = key row = TMEM lane) and, at the end of a unit, dV/dK columns
