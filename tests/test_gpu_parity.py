@@ -509,6 +509,19 @@ def test_mla_decode_parity(cfg):
     assert_close_out(_f64(out), ref, "mla decode %s" % (cfg,))
 
 
+def test_mla_decode_repeatable_over_many_calls():
+    """The absorbed-MLA decode writes its partials and merges them in a fixed
+    order, so repeated calls agree bit for bit (lengths from 1: whole and
+    partial chunks, rows fixed up past the length)."""
+    q, ckv, lens = synth.mla_decode_inputs(24, 128, 2048, 1, 2048, seed=53)
+    q, ckv, lens = q.cuda(), ckv.cuda(), lens.cuda()
+    ref = cp_.mla_decode(q, ckv, lens).clone()
+    cp_.check_device()
+    bad = sum(not torch.equal(cp_.mla_decode(q, ckv, lens), ref) for _ in range(100))
+    cp_.check_device()
+    assert bad == 0, bad
+
+
 def test_mla_decode_ignores_rows_past_the_length():
     """Cache rows at or past lens[b] hold NaN: they get zero weight and their
     value rows are cleared before the output product, so nothing leaks."""
