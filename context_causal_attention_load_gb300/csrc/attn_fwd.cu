@@ -210,15 +210,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int bx = 0; bx < DQK / 64; ++bx)
             tma_load_4d(smem + C::OFF_Q + C::Q_BYTES + bx * BM * 128, &a.tq, &bar.q_full, bx * 64, u.h1,
                         pm.row(u.t1 * BM), u.b);
-        const int bound = kv_bound(pm, u);
-        int kt = next_kv_tile(pm, BN, -1, bound);
+        KvWalk kw;
+        kw.start(pm, BN, kv_bound(pm, u));
+        int kt = kw.t;
         // prologue stage: the first K tile
         if (!claim(false, C::K_BYTES)) break;
         load_k(kt, u);
         ++ng;
         // step j: V_j and, unless it is the last, K_{j+1}
         while (kt >= 0) {
-          const int nkt = next_kv_tile(pm, BN, kt, bound);
+          kw.next(pm);
+          const int nkt = kw.t;
           if (!claim(true, C::V_BYTES + (nkt >= 0 ? C::K_BYTES : 0))) break;
           load_v(kt, u);
           if (nkt >= 0) load_k(nkt, u);
@@ -350,9 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
       float m = -INFINITY, l = 0.f;
       int j = 0;
-      for (int kt = next_kv_tile(pm, BN, -1, bound); kt >= 0; kt = next_kv_tile(pm, BN, kt, bound), ++j) {
-        int kmin, kmax;
-        pm.range(kt * BN, kt * BN + BN, kmin, kmax);
+      // the key tiles and their positions walked incrementally: this
+      // bookkeeping runs on the softmax thread between two steps, sharing
+      // its issue slots with the other tile's softmax (a division per step
+      // here cost about a third of a step)
+      KvWalk kw;
+      kw.start(pm, BN, bound);
+      for (; kw.t >= 0; kw.next(pm), ++j) {
+        const int kt = kw.t, kmin = kw.kmin, kmax = kw.kmax;
         const bool inside = kt * BN + BN <= pm.S;
         const int cls = (kmin > qmax) ? 0 : ((kmax <= qmin && inside) ? 2 : 1);  // 0 none, 1 partial, 2 all
         const int* kp = kpos_s + t * BN;

@@ -120,6 +120,71 @@ CPATTN_HD int next_kv_tile(const PosMap& m, int T, int cur, int bound) {
   return -1;
 }
 
+// The key tiles of next_kv_tile, walked with their position range [kmin,
+// kmax] and without an integer division per tile where every chunk is a
+// whole number of tiles (or there is no reorder): the walk keeps the tile's
+// chunk, its offset in the chunk and its first position.  Otherwise each
+// step falls back to next_kv_tile and PosMap::range.
+struct KvWalk {
+  int t, kmin, kmax;        // current tile (-1 after the last) and its positions
+  int nt, T, bound, tpc, k, off;
+  bool inc;
+
+  CPATTN_HD void start(const PosMap& m, int T_, int bound_) {
+    T = T_;
+    bound = bound_;
+    nt = (m.S + T - 1) / T;
+    inc = !m.lb || m.c % T == 0;
+    if (!inc) {
+      t = next_kv_tile(m, T, -1, bound);
+      fill(m);
+      return;
+    }
+    tpc = m.lb ? m.c / T : nt;
+    t = 0;
+    k = 0;
+    off = 0;
+    kmin = 0;  // chunk_of(0) = 0
+    settle(m);
+  }
+  CPATTN_HD void next(const PosMap& m) {
+    if (!inc) {
+      t = next_kv_tile(m, T, t, bound);
+      fill(m);
+      return;
+    }
+    ++t;
+    kmin += T;
+    if (++off == tpc) {
+      ++k;
+      off = 0;
+      if (m.lb) kmin = m.chunk_of(k) * m.c;
+    }
+    settle(m);
+  }
+
+ private:
+  // skip the rest of every chunk whose next tile starts past the bound
+  CPATTN_HD void settle(const PosMap& m) {
+    if (!m.lb) {
+      if (t >= nt || kmin > bound) { t = -1; return; }
+      kmax = kmin + T - 1 < m.S - 1 ? kmin + T - 1 : m.S - 1;
+      return;
+    }
+    while (t < nt && kmin > bound) {
+      ++k;
+      off = 0;
+      t = k * tpc;
+      kmin = m.chunk_of(k) * m.c;
+    }
+    if (t >= nt) { t = -1; return; }
+    kmax = kmin + T - 1;
+  }
+  CPATTN_HD void fill(const PosMap& m) {
+    if (t >= 0) m.range(t * T, t * T + T, kmin, kmax);
+  }
+};
+
 CPATTN_HD int next_q_tile(const PosMap& m, int T, int cur, int bound) {
   const int nt = (m.S + T - 1) / T;
   int t = cur + 1;
