@@ -89,7 +89,7 @@ struct FCfg {
 // tile, and whether it is the last step of its unit (walking the steps costs
 // a chain of integer divisions; only the producer, which runs ahead, pays it)
 struct StepInfo {
-  int hq, qt, last, pad;
+  int hq, qt, last, qmin;  // qmin: first position of the query tile (decides the masked path)
 };
 
 struct FBars {
@@ -251,6 +251,14 @@ struct StepIter {
     if (++hq >= h_end) return false;
     qt = slot_order_tile(pm, -1);
     return qt >= 0;
+  }
+  // first position of the current query tile (a position tile's own when
+  // walking by position; otherwise from the slot range)
+  __device__ __forceinline__ int qmin(const PosMap& pm) const {
+    if (posw) return pt * kRows;
+    int mn, mx;
+    pm.range(qt * kRows, qt * kRows + kRows, mn, mx);
+    return mn;
   }
   // memory row of the current query tile: natural-order tensors keep a
   // position tile at its position, the others a slot tile at its slot
@@ -414,7 +422,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         }
         bool more;
         do {
-          const int hq = it.hq, qt = it.qt, qrow = it.mem_row();
+          const int hq = it.hq, qt = it.qt, qrow = it.mem_row(), qmin = it.qmin(pm);
           more = it.next(pm);  // (the step after this one)
           const int st = gs & 1;
           const uint32_t ph = ((gs >> 1) & 1) ^ 1;
@@ -422,11 +430,12 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
           unsigned char* vec = smem + C::OFF_VEC + st * C::VEC_BYTES;
           // (an empty asm that reads the values keeps the compiler from sinking
           // their computation below the waits)
-          asm volatile("" ::"r"(qrow), "l"(vo), "r"(it.qt), "r"(it.hq), "r"((int)more));
+          asm volatile("" ::"r"(qrow), "l"(vo), "r"(it.qt), "r"(it.hq), "r"((int)more), "r"(qmin));
           if (!(ok = mbar_wait(&bar.q_empty[st], ph, ab))) break;
           info[st].hq = hq;
           info[st].qt = qt;
           info[st].last = more ? 0 : 1;
+          info[st].qmin = qmin;
           mbar_expect_tx(&bar.q_full[st], C::TILE + C::VEC_BYTES);  // (release: the info is visible to q_full's waiters)
           for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d(smem + C::OFF_Q + st * C::TILE + bx * kRows * 128, &a.tq, &bar.q_full[st], bx * 64, hq, qrow,
@@ -645,8 +654,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         tc_fence_after();
         const int qt = info[st].qt;
         last = info[st].last != 0;
-        int qmin, qmax;
-        pm.range(qt * kRows, qt * kRows + kRows, qmin, qmax);
+        const int qmin = info[st].qmin;  // (from the producer: no division on this path)
         const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * C::VEC_BYTES) + g * 64;
         const float* del_s = lse_s + kRows;
         float p[64];

@@ -65,7 +65,7 @@ struct MCfg {
   static constexpr int VEC_BYTES = 2 * kHalf * 4;
   static constexpr int OFF_BAR = OFF_VEC + 2 * VEC_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + 256;  // TMEM address, abort flag, MStepInfo[2] at +32
-  static constexpr int SMEM = OFF_MISC + 64;
+  static constexpr int SMEM = OFF_MISC + 80;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DS % 1024 == 0 &&
                     OFF_STG % 1024 == 0 && Q_BYTES % 1024 == 0 && DO_BYTES % 1024 == 0,
@@ -81,7 +81,7 @@ struct MCfg {
 
 // what the producer publishes with each Q stage
 struct MStepInfo {
-  int hq, qt, half, last;
+  int hq, qt, half, last, qmin;  // qmin: first position of the half-step's rows (decides the masked path)
 };
 
 struct MBars {
@@ -159,6 +159,13 @@ struct MStepIter {
   }
   // memory row of the current query tile
   __device__ __forceinline__ int mem_row() const { return NAT ? pt * kKeys : qt * kKeys; }
+  // first position of the current tile's rows [half * kHalf, +kHalf)
+  __device__ __forceinline__ int qmin(const PosMap& pm, int half) const {
+    if (posw) return pt * kKeys + half * kHalf;
+    int mn, mx;
+    pm.range(qt * kKeys + half * kHalf, qt * kKeys + half * kHalf + kHalf, mn, mx);
+    return mn;
+  }
 };
 
 template <bool NAT>
@@ -313,6 +320,7 @@ __global__ void __launch_bounds__(kThreadsM, 1) attn_bwd_mla_kernel(const __grid
         bool more;
         do {
           const int hq = it.hq, qt = it.qt, qrow = it.mem_row();
+          const int qmin0 = it.qmin(pm, 0), qmin1 = it.qmin(pm, 1);
           more = it.next(pm);
           for (int half = 0; half < 2 && ok; ++half) {
             const int st = gs & 1;
@@ -325,6 +333,7 @@ __global__ void __launch_bounds__(kThreadsM, 1) attn_bwd_mla_kernel(const __grid
             info[st].qt = qt;
             info[st].half = half;
             info[st].last = (!more && half == 1) ? 1 : 0;
+            info[st].qmin = half ? qmin1 : qmin0;
             mbar_expect_tx(&bar.q_full[st], C::Q_BYTES + C::VEC_BYTES);  // (release: the info is visible to q_full's waiters)
             for (int bx = 0; bx < 3; ++bx)
               tma_load_4d(smem + C::OFF_Q + st * C::Q_BYTES + bx * C::QBOX, &a.tq, &bar.q_full[st], bx * 64, hq,
@@ -581,8 +590,7 @@ __global__ void __launch_bounds__(kThreadsM, 1) attn_bwd_mla_kernel(const __grid
         const int qt = info[st].qt, half = info[st].half;
         last = info[st].last != 0;
         const int slot0 = qt * kKeys + half * kHalf;
-        int qmin, qmax;
-        pm.range(slot0, slot0 + kHalf, qmin, qmax);
+        const int qmin = info[st].qmin;  // (from the producer: no division on this path)
         const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * C::VEC_BYTES) + g * 32;
         const float* del_s = lse_s + kHalf;
         float p[32];
