@@ -961,14 +961,13 @@ int mla_decode(const void* q, const void* ckv, const int* lens, void* out, int B
   DevState* ds;
   if ((rc = get_state(&ds))) return rc;
   if ((rc = need_sm103(*ds))) return rc;
-  const int nch = mla_decode_chunks(Smax);
-  const size_t rows = (size_t)B * nch * H;
-  if ((rc = ensure(ds->mla_o, rows * 512, stream, false))) return rc;
-  if ((rc = ensure(ds->mla_ml, rows * 2, stream, false))) return rc;
+  const int nch = mla_decode_chunks(Smax), nchp = (nch + 1) & ~1;
+  if ((rc = ensure(ds->mla_o, (size_t)B * H * nch * 512, stream, false))) return rc;
+  if ((rc = ensure(ds->mla_ml, (size_t)B * H * nchp * 2, stream, false))) return rc;
   MlaDecodeArgs a{};
   a.q = q; a.ckv = ckv; a.lens = lens; a.out = out;
   a.part_o = ds->mla_o.ptr; a.part_ml = ds->mla_ml.ptr; a.err = ds->err;
-  a.B = B; a.H = H; a.Smax = Smax; a.nch = nch;
+  a.B = B; a.H = H; a.Smax = Smax; a.nch = nch; a.nchp = nchp;
   a.scale_log2 = (float)(1.4426950408889634 * (double)scale);
   cudaError_t e;
   {

@@ -52,15 +52,14 @@ cudaError_t noalloc_take_error(int* word);
 // rope) shared by every head; value = the first 512 columns
 struct MlaDecodeArgs {
   CUtensorMap tq, tk;
-  CUtensorMap tpo;   // part_o as fp32 {512, H, nch, B}, boxes of 32 columns x min(H, 128) rows
   const void* q;     // [B, H, 576] bf16
   const void* ckv;   // [B, Smax, 576] bf16
   const int* lens;   // [B]
   void* out;         // [B, H, 512] bf16
-  float* part_o;     // [B][nch][H][512] fp32 chunk partials
-  float* part_ml;    // [B][nch][H][2] (row max in the log2 domain, row sum)
+  float* part_o;     // [B][H][nch][512] fp32 chunk partials
+  float* part_ml;    // [B][H][nchp][2] (row max in the log2 domain, row sum); nchp = nch rounded up to even
   int* err;
-  int B, H, Smax, nch;
+  int B, H, Smax, nch, nchp;
   float scale_log2;
 };
 int mla_decode_chunks(int Smax);  // 256-position chunks of a cache of Smax

@@ -15,33 +15,49 @@
 //   O = P V     M = 128 heads, N = 8 x 64 value columns, K = 256 positions
 // TMEM: S in columns [0, 256); after the softmax has read it, O's value
 // columns 256-511 go there and columns 0-255 go to [256, 512).  Each item
-// writes its partial (o, row max, row sum); a second kernel merges the chunks
-// of each (b, h).  Persistent grid, one CTA per SM: the whole chunks of all
+// writes its partial (o, row max, row sum), laid out so that the chunks of a
+// (b, h) row are contiguous; a second kernel merges them.  Persistent grid, one CTA per SM: the whole chunks of all
 // sequences are numbered first and the partial last chunks after them, and
 // items are dealt round-robin, so with about one item per SM the short
 // chunks are the ones that share an SM.
 //
-// Roles (192 threads): warps 0-3 softmax and epilogue (thread = head row =
-// TMEM lane), warp 4 TMA producer, warp 5 MMA issuer.  One ring of three
-// 48 KB stages carries, per item, nine (Q box, K box) pairs for S and then
-// the eight value boxes (the first 512 columns of the same rows, now from
-// L2).  Positions of a last chunk at or past lens[b] get zero weight; their
-// value rows are zeroed in shared memory before O reads them, so whatever
-// the cache holds there cannot reach the output.
+// Roles (320 threads): warps 0-7 softmax, two threads per head row (TMEM
+// lane), warps 0-3 on the chunk's first 128 positions and warps 4-7 on the
+// rest; warp 8 TMA producer, warp 9 MMA issuer.  One ring of three 48 KB
+// stages carries, per item, nine (Q box, K box) pairs for S and then the
+// eight value boxes (the first 512 columns of the same rows, now from L2).
+// Positions of a last chunk at or past lens[b] get zero weight, O's
+// 16-position steps past the length are not issued, and the MMA warp zeroes
+// the value rows past the length in the last step it issues, so whatever
+// the cache holds there cannot reach the output.  The partial output is
+// 256 KiB per item, which takes an SM about as long to write as the O
+// products take to form, so warps 0-3 write it box by box as O completes,
+// staged in the three query slots (idle once S is done).
 #include "common.cuh"
 #include "internal.h"
 
 namespace cpattn {
 namespace {
 
-constexpr int kMdThreads = 192;
+constexpr int kMdThreads = 320;
+constexpr int kMdSoftmax = 256;            // softmax and epilogue threads (warps 0-7)
 constexpr int kMdDk = 576, kMdDv = 512;
 constexpr int kMdRows = 128;               // heads per MMA (rows past H are zero)
 constexpr int kMdT = 256;                  // positions per chunk
 constexpr int kMdKBoxes = kMdDk / 64;      // 9
 constexpr int kMdVBoxes = kMdDv / 64;      // 8
-constexpr int kMdStagesPerItem = kMdKBoxes + kMdVBoxes;
-constexpr int kMdNS = 3;
+constexpr int kMdNS = 3;                   // ring stages
+// S takes the key boxes rope first (8, 0, 1, ..., 7), so its last three
+// stages hold value boxes 5-7: O reads those in place and only value boxes
+// 0-4 are fetched again
+constexpr int kMdVKept = kMdNS;
+constexpr int kMdStagesPerItem = kMdKBoxes + kMdVBoxes - kMdVKept;
+__host__ __device__ constexpr int md_sbox(int c) { return (c + kMdKBoxes - 1) % kMdKBoxes; }  // key box of S step c
+__host__ __device__ constexpr int md_vbox(int i) {  // value box of O step i: the kept ones first
+  return i < kMdVKept ? kMdVBoxes - kMdVKept + i : i - kMdVKept;
+}
+static_assert(md_sbox(kMdKBoxes - kMdVKept) == kMdVBoxes - kMdVKept && md_sbox(kMdKBoxes - 1) == kMdVBoxes - 1,
+              "the last S stages hold the kept value boxes");
 constexpr int kMdQBox = kMdRows * 128;   // 16 KB
 constexpr int kMdKBox = kMdT * 128;      // 32 KB
 constexpr int kMdStage = kMdQBox + kMdKBox;
@@ -49,8 +65,9 @@ constexpr int kMdOffP = kMdNS * kMdStage;          // P: 4 boxes of 64 positions
 constexpr int kMdPBytes = 4 * kMdRows * 128;       // 64 KB
 constexpr int kMdOffBar = kMdOffP + kMdPBytes;
 constexpr int kMdOffMisc = kMdOffBar + 256;
+constexpr int kMdOffRed = kMdOffMisc + 64;                      // row max and row sum of each half: [2][2][128] fp32
 constexpr int kMdMaxB = 1024;
-constexpr int kMdOffLens = kMdOffMisc + 64;
+constexpr int kMdOffLens = kMdOffRed + 4 * kMdRows * 4;
 constexpr int kMdOffPre = kMdOffLens + kMdMaxB * 4;            // whole chunks before each sequence
 constexpr int kMdOffPre2 = kMdOffPre + (kMdMaxB + 1) * 4;       // partial chunks before each sequence
 constexpr int kMdSmem = kMdOffPre2 + (kMdMaxB + 1) * 4 + 1024;
@@ -59,11 +76,12 @@ static_assert(kMdStage % 1024 == 0 && kMdOffP % 1024 == 0, "swizzled tiles need 
 
 struct MdBars {
   uint64_t full[kMdNS], empty[kMdNS];
-  uint64_t s_full, p_full, o_full, o_free;
-  uint64_t vfix[kMdVBoxes];
+  uint64_t s_full, p_full, o_free, qs_free;
+  uint64_t o_box[kMdVBoxes];  // O's value box i complete
   uint64_t done;
 };
 static_assert(sizeof(MdBars) <= 256, "barrier area");
+static_assert(kMdKBoxes >= kMdNS && kMdQBox == kMdRows * 128, "query slots: first stages of an item; epilogue staging");
 
 struct MdItem {
   int b, chunk, len;
@@ -112,20 +130,6 @@ __device__ __forceinline__ void md_prefix(int B, int lane, int* out, F f) {
   if (lane == 31) out[B] = inc;
 }
 
-// TMA store of a tile from shared memory into global memory, tracked by the
-// issuing thread's bulk async-group
-__device__ __forceinline__ void md_tma_store_4d(const void* src, const CUtensorMap* map, int c0, int c1, int c2, int c3) {
-  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
-// this thread's bulk async-groups, all but the newest N, have read their sources
-template <int N>
-__device__ __forceinline__ void md_bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
 __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_constant__ MlaDecodeArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -145,16 +149,16 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
   if (tid == 0) {
     for (int i = 0; i < kMdNS; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
     mbar_init(&bar.s_full, 1);
-    mbar_init(&bar.p_full, 128);
-    mbar_init(&bar.o_full, 1);
-    mbar_init(&bar.o_free, 128);
-    for (int i = 0; i < kMdVBoxes; ++i) mbar_init(&bar.vfix[i], 128);
+    mbar_init(&bar.p_full, kMdSoftmax);
+    mbar_init(&bar.o_free, kMdSoftmax);
+    mbar_init(&bar.qs_free, 1);
+    for (int i = 0; i < kMdVBoxes; ++i) mbar_init(&bar.o_box[i], 1);
     mbar_init(&bar.done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
-  if (warp == 4 && lane == 0) { prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); }
+  if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (warp == 8 && lane == 0) { prefetch_tmap(&a.tq); prefetch_tmap(&a.tk); }
   // stage (and validate) the lengths, then number the items
   for (int bb = tid; bb < a.B; bb += kMdThreads) {
     const int l = a.lens[bb];
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
   const int total = pre[a.B] + pre2[a.B];
   const int n_items = cta < total ? (total - cta + ncta - 1) / ncta : 0;  // items j = cta + k * ncta
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int g = 0;  // ring stage counter
@@ -182,11 +186,22 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
           const int st = g % kMdNS;
           if (!(ok = mbar_wait(&bar.empty[st], ((g / kMdNS) & 1) ^ 1, ab))) break;
           unsigned char* sb = smem + st * kMdStage;
-          if (s < kMdKBoxes) {  // query box and key box s
+          if (s < kMdKBoxes) {  // query box and key box of S step s
             mbar_expect_tx(&bar.full[st], kMdStage);
-            tma_load_3d(sb, &a.tq, &bar.full[st], s * 64, 0, it.b);
-            tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], s * 64, it.chunk * kMdT, it.b);
-          } else {  // value box, in the key slot
+            tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], md_sbox(s) * 64, it.chunk * kMdT, it.b);
+            if (k == 0 || s >= kMdNS) {
+              tma_load_3d(sb, &a.tq, &bar.full[st], md_sbox(s) * 64, 0, it.b);
+            } else if (s == kMdNS - 1) {
+              // the previous item's epilogue staged its output in the query
+              // slots: the item's first query boxes wait until those stores
+              // have read them (its first key boxes are already on the way)
+              if (!(ok = mbar_wait(&bar.qs_free, (k - 1) & 1, ab))) break;
+              for (int s2 = 0; s2 < kMdNS; ++s2) {
+                const int st2 = (g - (kMdNS - 1) + s2) % kMdNS;
+                tma_load_3d(smem + st2 * kMdStage, &a.tq, &bar.full[st2], md_sbox(s2) * 64, 0, it.b);
+              }
+            }
+          } else {  // value box 0-4, in the key slot
             const int vb = s - kMdKBoxes;
             mbar_expect_tx(&bar.full[st], kMdKBox);
             tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], vb * 64, it.chunk * kMdT, it.b);
@@ -200,60 +215,85 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16(kMdRows, kMdT, 0, 0);  // Q (K-major) x K (K-major)
-      constexpr uint32_t IDESC_O = idesc_bf16(kMdRows, 64, 0, 1);    // P (K-major) x V (MN-major)
-      const uint32_t s0 = smem_u32(smem);
-      const uint64_t pdesc = sdesc_sw128(s0 + kMdOffP, 16, 1024);
-      int g = 0, nfix = 0;
-      bool ok = true;
-      for (int k = 0; k < n_items && ok; ++k) {
-        const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
-        const bool partial = it.len - it.chunk * kMdT < kMdT;
-        if (k > 0 && !(ok = mbar_wait(&bar.o_free, (k - 1) & 1, ab))) break;  // the last O read out
-        for (int c = 0; c < kMdKBoxes; ++c, ++g) {
-          const int st = g % kMdNS;
-          if (!(ok = mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab))) break;
+    // lane 0 issues; the whole warp waits for each stage in turn (never more
+    // than one phase behind its barrier: a stage is refilled only after this
+    // warp's MMAs on it) and, in a partial chunk, zeroes the value rows from
+    // the length up to the end of its last 16-position step, the only rows
+    // past the length that O reads (its steps past that are not issued):
+    // they come from a cache that may hold anything there
+    constexpr uint32_t IDESC_S = idesc_bf16(kMdRows, kMdT, 0, 0);  // Q (K-major) x K (K-major)
+    constexpr uint32_t IDESC_O = idesc_bf16(kMdRows, 64, 0, 1);    // P (K-major) x V (MN-major)
+    const uint32_t s0 = smem_u32(smem);
+    const uint64_t pdesc = sdesc_sw128(s0 + kMdOffP, 16, 1024);
+    int g = 0;
+    bool ok = true;
+    for (int k = 0; k < n_items && ok; ++k) {
+      const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
+      const int nvalid = min(kMdT, it.len - it.chunk * kMdT);
+      const int nk = (nvalid + 15) >> 4;  // 16-position steps of O that hold a valid position
+      if (k > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_free, (k - 1) & 1, ab)))) break;  // the last O read out
+      const int g0 = g;  // ring position of the item's first S stage
+      for (int c = 0; c < kMdKBoxes; ++c, ++g) {
+        const int st = g % kMdNS;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab)))) break;
+        if (lane == 0) {
           tc_fence_after();
           const uint64_t qd = sdesc_sw128(s0 + st * kMdStage, 16, 1024);
           const uint64_t kd = sdesc_sw128(s0 + st * kMdStage + kMdQBox, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ss(tmem, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bar.empty[st]);
+          if (c < kMdKBoxes - kMdVKept) mma_commit(&bar.empty[st]);  // the last stages stay for O
         }
-        if (!ok) break;
-        mma_commit(&bar.s_full);
-        if (!(ok = mbar_wait(&bar.p_full, k & 1, ab))) break;  // P written, S read: its columns take O
-        tc_fence_after();
-        for (int i = 0; i < kMdVBoxes; ++i, ++g) {
-          const int st = g % kMdNS;
-          if (!(ok = mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab))) break;
-          if (partial && !(ok = mbar_wait(&bar.vfix[i], nfix & 1, ab))) break;  // rows past the length zeroed
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&bar.s_full);
+      // P written, S read: its columns take O
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_full, k & 1, ab)))) break;
+      for (int i = 0; i < kMdVBoxes; ++i) {
+        const int vbox = md_vbox(i);
+        int st;
+        if (i < kMdVKept) {  // value box vbox is the key box of S step kMdKBoxes - kMdVKept + i, still in its stage
+          st = (g0 + kMdKBoxes - kMdVKept + i) % kMdNS;
+        } else {
+          st = g % kMdNS;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab)))) break;
+          ++g;
+        }
+        if (nvalid < 16 * nk) {
+          unsigned char* vb = smem + st * kMdStage + kMdQBox;
+          for (int x = lane; x < (16 * nk - nvalid) * 8; x += 32)  // 16-byte chunks, 8 per row
+            *reinterpret_cast<uint4*>(vb + (nvalid + (x >> 3)) * 128 + (x & 7) * 16) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
           tc_fence_after();
           const uint64_t vd = sdesc_sw128(s0 + st * kMdStage + kMdQBox, kMdKBox, 1024);
-#pragma unroll
-          for (int kk = 0; kk < kMdT / 16; ++kk)
-            mma_ss(tmem + (i < 4 ? 256 + 64 * i : 64 * (i - 4)), pdesc + ((((kk >> 2) * (kMdRows * 128)) + (kk & 3) * 32) >> 4),
-                   vd + ((kk * 16 * 128) >> 4), IDESC_O, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < nk; ++kk)
+            mma_ss(tmem + (vbox < 4 ? 256 + 64 * vbox : 64 * (vbox - 4)),
+                   pdesc + ((((kk >> 2) * (kMdRows * 128)) + (kk & 3) * 32) >> 4), vd + ((kk * 16 * 128) >> 4), IDESC_O,
+                   kk > 0 ? 1u : 0u);
           mma_commit(&bar.empty[st]);
+          mma_commit(&bar.o_box[vbox]);
         }
-        if (!ok) break;
-        if (partial) ++nfix;
-        mma_commit(&bar.o_full);
+        __syncwarp();
       }
-      mma_drain(&bar.done, a.err);
     }
-  } else if (warp < 4) {
+    if (lane == 0) mma_drain(&bar.done, a.err);
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax and epilogue
-    // thread r = head row = TMEM lane; a failed wait runs on (every wait is
-    // bounded and the barrier counts still complete)
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    // thread (r, hf): head row r = TMEM lane and half hf of the chunk's
+    // positions in the softmax; then warps 0-3 write the partial output box
+    // by box as O completes.  A failed wait runs on (every wait is bounded
+    // and the barrier counts still complete)
+    const int r = (warp & 3) * 32 + lane, hf = warp >> 2;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    float* red = reinterpret_cast<float*>(smem + kMdOffRed);  // [0, 256): row max by half, [256, 512): row sum
     const float sl2 = a.scale_log2;
-    int nfix = 0;
     for (int k = 0; k < n_items; ++k) {
       const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
       const int nvalid = min(kMdT, it.len - it.chunk * kMdT);  // positions of the chunk inside the cache
@@ -261,7 +301,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
       tc_fence_after();
       float m = -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < kMdT / 32; ++c) {
+      for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
         uint32_t sv[32];
         tmem_ld32(tmem + lane_base + 32 * c, sv);
         tmem_ld_wait();
@@ -269,10 +309,13 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
         for (int j = 0; j < 32; ++j)
           if (32 * c + j < nvalid) m = fmaxf(m, __uint_as_float(sv[j]));
       }
-      const float m2 = m * sl2;  // finite: every item holds at least one position
+      red[hf * kMdRows + r] = m;
+      named_bar(3, kMdSoftmax);
+      m = fmaxf(red[r], red[kMdRows + r]);  // finite: every item holds position 0 of its chunk
+      const float m2 = m * sl2;
       float l = 0.f;
 #pragma unroll 1
-      for (int c = 0; c < kMdT / 32; ++c) {
+      for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
         uint32_t sv[32];
         tmem_ld32(tmem + lane_base + 32 * c, sv);
         tmem_ld_wait();
@@ -293,107 +336,104 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
+      red[2 * kMdRows + hf * kMdRows + r] = l;
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&bar.p_full);
-      if (nvalid < kMdT) {
-        // zero the value rows past the length (stage of value box i of item k)
-        for (int i = 0; i < kMdVBoxes; ++i) {
-          const int g = k * kMdStagesPerItem + kMdKBoxes + i;
-          const int st = g % kMdNS;
-          mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab);
-          unsigned char* vb = smem + st * kMdStage + kMdQBox;
-          for (int row = r; row < kMdT; row += 128)
-            if (row >= nvalid)
-#pragma unroll
-              for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vb + row * 128 + q * 16) = make_uint4(0, 0, 0, 0);
-          fence_proxy_async_smem();
-          mbar_arrive(&bar.vfix[i]);
-        }
-        ++nfix;
-      }
-      // epilogue: this item's partial (o, row max, row sum); value columns
-      // 0-255 are in TMEM [256, 512), 256-511 in [0, 256).  o goes out as
-      // sixteen fp32 boxes of 32 columns x 128 head rows, staged four at a
-      // time in the P buffer (dead once O is complete; 128-byte swizzle) and
-      // written by TMA stores, so the 256 KiB leave in whole lines
-      mbar_wait(&bar.o_full, k & 1, ab);
-      tc_fence_after();
+      if (hf == 0) {
+        // epilogue, overlapping O: value box v (columns 64v..64v+63) is in
+        // TMEM [256 + 64v, ...) for v < 4 and [64(v-4), ...) after; each box
+        // goes out as two groups of 32 columns x 128 head rows, staged in
+        // turn in the three query slots (idle once S is done; 128-byte
+        // swizzle) and read back so that each warp store writes four whole
+        // 128-byte lines of four heads' rows.  Plain stores, not TMA: the
+        // TMA unit stays free for the value boxes that O still waits for
+        const size_t obase = ((size_t)it.b * a.H) * a.nch + it.chunk;  // partial row of (b, head 0, chunk)
 #pragma unroll 1
-      for (int c = 0; c < kMdDv / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + (c < 8 ? 256 + 32 * c : 32 * (c - 8)), ov);
-        tmem_ld_wait();
-        unsigned char* buf = smem + kMdOffP + (c & 3) * (kMdRows * 128);
-        if (c >= 4) {  // the store that last used this buffer has read it
-          if (r == 0) md_bulk_wait_read<3>();
-          named_bar(1, 128);
-        }
-        unsigned char* rp = buf + r * 128;
+        for (int c = 0; c < 2 * kMdVBoxes; ++c) {
+          const int vc = 2 * md_vbox(c >> 1) + (c & 1);  // 32-column group of the value, in the order O forms them
+          if ((c & 1) == 0) {
+            mbar_wait(&bar.o_box[vc >> 1], k & 1, ab);
+            tc_fence_after();
+          }
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + (vc < 8 ? 256 + 32 * vc : 32 * (vc - 8)), ov);
+          tmem_ld_wait();
+          unsigned char* buf = smem + (c % kMdNS) * kMdStage;
+          unsigned char* rp = buf + r * 128;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(rp + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(ov[4 * ch], ov[4 * ch + 1], ov[4 * ch + 2], ov[4 * ch + 3]);
-        fence_proxy_async_smem();
-        named_bar(1, 128);
-        if (r == 0) {
-          md_tma_store_4d(buf, &a.tpo, 32 * c, 0, it.chunk, it.b);
-          bulk_commit_group();
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(rp + ((ch ^ (r & 7)) << 4)) =
+                make_uint4(ov[4 * ch], ov[4 * ch + 1], ov[4 * ch + 2], ov[4 * ch + 3]);
+          named_bar(1, kMdRows);  // (the last reader of this slot passed the barrier of the group after it)
+          const int q = r & 7;    // 16-byte piece of a head's 128-byte row
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int head = (r >> 3) + 16 * j;
+            if (head < a.H)
+              *reinterpret_cast<uint4*>(a.part_o + (obase + (size_t)head * a.nch) * kMdDv + 32 * vc + 4 * q) =
+                  *reinterpret_cast<const uint4*>(buf + head * 128 + ((q ^ (head & 7)) << 4));
+          }
         }
       }
-      const size_t prow = ((size_t)it.b * a.nch + it.chunk) * a.H + r;
-      if (r < a.H) {
-        a.part_ml[2 * prow] = m2;
-        a.part_ml[2 * prow + 1] = l;
+      named_bar(3, kMdSoftmax);  // both halves' row sums are in; every O box has been read
+      const size_t mrow = ((size_t)it.b * a.H + r) * a.nchp + it.chunk;
+      if (hf == 0 && r < a.H) {
+        a.part_ml[2 * mrow] = m2;
+        a.part_ml[2 * mrow + 1] = red[2 * kMdRows + r] + red[3 * kMdRows + r];
       }
       tc_fence_before();
       mbar_arrive(&bar.o_free);
-      if (r == 0) md_bulk_wait_read<0>();  // the next item may write P
-      named_bar(1, 128);
+      if (tid == 0) mbar_arrive(&bar.qs_free);  // the query slots have been read back: the next item may load them
     }
-    if (r == 0) bulk_wait_all();  // the partials have landed before the CTA retires
-    (void)nfix;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-// merge of the chunks of each (b, h): one CTA of 128 threads per (b, h),
-// four value columns per thread; four chunks' loads in flight at a time,
-// merged online.  Launched as a programmatic dependent, so lens and the
-// partials are read only after the attention grid has completed.
+// merge of the chunks of each (b, h) row: one CTA of 128 threads per row,
+// four value columns per thread; eight chunks' loads in flight at a time
+// (every chunk of a 2048-position cache in one round), merged online.  The
+// row's partials are contiguous ([b][h][chunk]).  Launched as a programmatic
+// dependent, so the partials are read only after the attention grid has
+// completed.  (Fetching each row's partials into shared memory with bulk
+// copies, twelve rows ahead on a persistent grid, measured three times
+// slower: the copies arrived at about 14 GB/s per SM.)
 __global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_constant__ MlaDecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.x / a.H, h = blockIdx.x - b * a.H;
+  const int row = blockIdx.x, b = row / a.H;
   int len = a.lens[b];
   len = len < 0 ? 0 : (len > a.Smax ? a.Smax : len);
   const int nch = (len + kMdT - 1) / kMdT;
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.H + h) * kMdDv + 4 * threadIdx.x;
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (size_t)row * kMdDv + 4 * threadIdx.x;
   if (nch == 0) {  // empty cache: zeros
     *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
     return;
   }
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + (size_t)row * a.nch * kMdDv) + threadIdx.x;
+  const float* pml = a.part_ml + (size_t)row * a.nchp * 2;
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < nch; c0 += 4) {
-    float m[4], l[4];
-    float4 x[4];
+  for (int c0 = 0; c0 < nch; c0 += 8) {
+    float m[8], l[8];
+    float4 x[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool in = c0 + j < nch;
-      const size_t prow = ((size_t)b * a.nch + c0 + j) * a.H + h;
-      m[j] = in ? __ldcg(a.part_ml + 2 * prow) : -INFINITY;
-      l[j] = in ? __ldcg(a.part_ml + 2 * prow + 1) : 0.f;
-      x[j] = in ? __ldcg(reinterpret_cast<const float4*>(a.part_o + prow * kMdDv) + threadIdx.x)
-                : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 8; ++j) {  // past the last chunk: load the last one again (no branch), weight 0
+      const int c = min(c0 + j, nch - 1);
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + c);
+      m[j] = c0 + j < nch ? ml.x : -INFINITY;
+      l[j] = ml.y;
+      x[j] = __ldcg(po + (size_t)c * (kMdDv / 4));
     }
-    const float mn = fmaxf(M, fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])));  // finite: chunk 0 is in
+    float mn = M;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mn = fmaxf(mn, m[j]);  // finite: chunk c0 is in
     const float f = fast_exp2(M - mn);
     L *= f;
     acc.x *= f;
@@ -401,7 +441,7 @@ __global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_cons
     acc.z *= f;
     acc.w *= f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
       const float w = fast_exp2(m[j] - mn);  // 0 past the last chunk
       L = fmaf(l[j], w, L);
       acc.x = fmaf(x[j].x, w, acc.x);
@@ -429,12 +469,7 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a0, int num_sms, cudaStream_t
   unsigned long long kd[3] = {Dk, (unsigned long long)a.Smax, (unsigned long long)a.B};
   unsigned long long ks[2] = {Dk * 2, (unsigned long long)a.Smax * Dk * 2};
   unsigned kb[3] = {64, (unsigned)kMdT, 1};
-  unsigned long long pd[4] = {(unsigned long long)kMdDv, (unsigned long long)a.H, (unsigned long long)a.nch,
-                              (unsigned long long)a.B};
-  unsigned long long ps[3] = {kMdDv * 4ull, (unsigned long long)a.H * kMdDv * 4, (unsigned long long)a.nch * a.H * kMdDv * 4};
-  unsigned pb[4] = {32, (unsigned)(a.H < kMdRows ? a.H : kMdRows), 1, 1};
-  if (encode_tmap(&a.tq, a.q, 3, qd, qs, qb, 2) || encode_tmap(&a.tk, a.ckv, 3, kd, ks, kb, 2) ||
-      encode_tmap(&a.tpo, a.part_o, 4, pd, ps, pb, 4))
+  if (encode_tmap(&a.tq, a.q, 3, qd, qs, qb, 2) || encode_tmap(&a.tk, a.ckv, 3, kd, ks, kb, 2))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMdSmem);
   if (e != cudaSuccess) return e;

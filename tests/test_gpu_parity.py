@@ -498,6 +498,7 @@ def test_mla_shared_rope_zero_copy():
     (2, 16, 512, 256, 257),        # 16 heads, around a chunk boundary
     (1, 128, 256, 256, 256),       # one whole chunk
     (5, 64, 1300, 0, 1300),        # may include an empty cache
+    (2, 128, 3000, 2100, 3000),    # more than eight chunks per row: the merge takes them in two groups
 ])
 def test_mla_decode_parity(cfg):
     B, H, Smax, lo, hi = cfg
@@ -523,11 +524,13 @@ def test_mla_decode_repeatable_over_many_calls():
 
 
 def test_mla_decode_ignores_rows_past_the_length():
-    """Cache rows at or past lens[b] hold NaN: they get zero weight and their
-    value rows are cleared before the output product, so nothing leaks."""
-    B, H, Smax = 3, 128, 600
+    """Cache rows at or past lens[b] hold NaN: they get zero weight, and the
+    value rows of the last 16-position step that the output product reads
+    are cleared first, so nothing leaks (a last chunk of 44, 1, 1 and 32
+    positions: partial steps and a whole one)."""
+    B, H, Smax = 4, 128, 600
     q, ckv, lens = synth.mla_decode_inputs(B, H, Smax, 1, 600, seed=52)
-    lens = torch.tensor([300, 1, 513], dtype=torch.int32)
+    lens = torch.tensor([300, 1, 513, 288], dtype=torch.int32)
     dirty = ckv.clone()
     for b in range(B):
         dirty[b, int(lens[b]):] = float("nan")
