@@ -12,27 +12,30 @@
 // Work item = (sequence b, chunk of 256 positions), with the heads as the
 // MMA rows:
 //   S = Q K^T   M = 128 heads, N = 256 positions, K = 576 (nine 64-column boxes)
-//   O = P V     M = 128 heads, N = 8 x 64 value columns, K = 256 positions
+//   O = P V     M = 128 heads, N = 4 x 128 value columns, K = 256 positions
 // TMEM: S in columns [0, 256); after the softmax has read it, O's value
 // columns 256-511 go there and columns 0-255 go to [256, 512).  Each item
 // writes its partial (o, row max, row sum), laid out so that the chunks of a
-// (b, h) row are contiguous; a second kernel merges them.  Persistent grid, one CTA per SM: the whole chunks of all
-// sequences are numbered first and the partial last chunks after them, and
-// items are dealt round-robin, so with about one item per SM the short
-// chunks are the ones that share an SM.
+// (b, h) row are contiguous; a second kernel merges them.  Persistent grid,
+// one CTA per SM: the whole chunks of all sequences are numbered first and
+// the partial last chunks after them, and items are dealt round-robin, so
+// with about one item per SM the short chunks are the ones that share an SM.
 //
 // Roles (320 threads): warps 0-7 softmax, two threads per head row (TMEM
 // lane), warps 0-3 on the chunk's first 128 positions and warps 4-7 on the
-// rest; warp 8 TMA producer, warp 9 MMA issuer.  One ring of three 48 KB
-// stages carries, per item, nine (Q box, K box) pairs for S and then the
-// eight value boxes (the first 512 columns of the same rows, now from L2).
+// rest; warp 8 TMA producer, warp 9 MMA issuer.  A ring of three 48 KB
+// stages carries, per item, the nine (Q box, K box) pairs of S; the same
+// space then takes the eight value boxes (the first 512 columns of the same
+// rows, now from L2) in pairs, two slots of two boxes 32 KB apart, so that
+// each O step is one N = 128 product (sixteen N = 64 ones per box measured
+// 2 us slower on the 24 x 128-head decode: small products pace O).
 // Positions of a last chunk at or past lens[b] get zero weight, O's
 // 16-position steps past the length are not issued, and the MMA warp zeroes
 // the value rows past the length in the last step it issues, so whatever
 // the cache holds there cannot reach the output.  The partial output is
-// 256 KiB per item, which takes an SM about as long to write as the O
-// products take to form, so warps 0-3 write it box by box as O completes,
-// staged in the three query slots (idle once S is done).
+// 256 KiB per item, about as long for an SM to write as the O products take
+// to form, so warps 0-3 write it pair by pair as O completes, with plain
+// stores (TMA stores would queue on the TMA unit ahead of the value loads).
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,21 +49,17 @@ constexpr int kMdRows = 128;               // heads per MMA (rows past H are zer
 constexpr int kMdT = 256;                  // positions per chunk
 constexpr int kMdKBoxes = kMdDk / 64;      // 9
 constexpr int kMdVBoxes = kMdDv / 64;      // 8
-constexpr int kMdNS = 3;                   // ring stages
-// S takes the key boxes rope first (8, 0, 1, ..., 7), so its last three
-// stages hold value boxes 5-7: O reads those in place and only value boxes
-// 0-4 are fetched again
-constexpr int kMdVKept = kMdNS;
-constexpr int kMdStagesPerItem = kMdKBoxes + kMdVBoxes - kMdVKept;
-__host__ __device__ constexpr int md_sbox(int c) { return (c + kMdKBoxes - 1) % kMdKBoxes; }  // key box of S step c
-__host__ __device__ constexpr int md_vbox(int i) {  // value box of O step i: the kept ones first
-  return i < kMdVKept ? kMdVBoxes - kMdVKept + i : i - kMdVKept;
-}
-static_assert(md_sbox(kMdKBoxes - kMdVKept) == kMdVBoxes - kMdVKept && md_sbox(kMdKBoxes - 1) == kMdVBoxes - 1,
-              "the last S stages hold the kept value boxes");
+constexpr int kMdNS = 3;                   // S ring stages
 constexpr int kMdQBox = kMdRows * 128;   // 16 KB
 constexpr int kMdKBox = kMdT * 128;      // 32 KB
 constexpr int kMdStage = kMdQBox + kMdKBox;
+// after S the ring's space takes the value boxes in pairs, two slots of two
+// boxes 32 KB apart (one N = 128 operand of O), then the epilogue's staging
+constexpr int kMdVPair = 2 * kMdKBox;               // 64 KB
+constexpr int kMdNPairs = kMdVBoxes / 2;            // 4
+constexpr int kMdOffE = 2 * kMdVPair;               // 16 KB of output staging
+static_assert(kMdOffE + kMdQBox <= kMdNS * kMdStage && kMdNS == 3 && kMdKBoxes % kMdNS == 0,
+              "slot A lies over S stages 0-1, slot B over 1-2, the staging inside stage 2");
 constexpr int kMdOffP = kMdNS * kMdStage;          // P: 4 boxes of 64 positions x 128 rows
 constexpr int kMdPBytes = 4 * kMdRows * 128;       // 64 KB
 constexpr int kMdOffBar = kMdOffP + kMdPBytes;
@@ -75,13 +74,13 @@ static_assert(kMdSmem <= 232448, "shared memory budget");
 static_assert(kMdStage % 1024 == 0 && kMdOffP % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 struct MdBars {
-  uint64_t full[kMdNS], empty[kMdNS];
-  uint64_t s_full, p_full, o_free, qs_free;
-  uint64_t o_box[kMdVBoxes];  // O's value box i complete
+  uint64_t full[kMdNS], empty[kMdNS];  // S ring
+  uint64_t vfull[2], vempty[2];        // value pair slots
+  uint64_t s_full, p_full, o_free, e_free;
+  uint64_t o_pair[kMdNPairs];          // O's value pair p complete
   uint64_t done;
 };
 static_assert(sizeof(MdBars) <= 256, "barrier area");
-static_assert(kMdKBoxes >= kMdNS && kMdQBox == kMdRows * 128, "query slots: first stages of an item; epilogue staging");
 
 struct MdItem {
   int b, chunk, len;
@@ -151,8 +150,9 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.p_full, kMdSoftmax);
     mbar_init(&bar.o_free, kMdSoftmax);
-    mbar_init(&bar.qs_free, 1);
-    for (int i = 0; i < kMdVBoxes; ++i) mbar_init(&bar.o_box[i], 1);
+    mbar_init(&bar.e_free, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.vfull[i], 1); mbar_init(&bar.vempty[i], 1); }
+    for (int i = 0; i < kMdNPairs; ++i) mbar_init(&bar.o_pair[i], 1);
     mbar_init(&bar.done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -177,67 +177,82 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
+    // item k: key box c (with its query box) in stage c % 3, that stage's
+    // fill 3k + c / 3; then value pair p (boxes 2p, 2p + 1) in slot p & 1,
+    // that slot's fill 2k + p / 2.  A region is filled again only once
+    // everything that read it has released it: the first S stages of an
+    // item wait for the previous item's value pairs (and the last one for
+    // its output staging), the first pairs for the S stages under them.
     if (lane == 0) {
-      int g = 0;  // ring stage counter
       bool ok = true;
+      int sfill[kMdNS] = {0, 0, 0}, vfill[2] = {0, 0};
       for (int k = 0; k < n_items && ok; ++k) {
         const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
-        for (int s = 0; s < kMdStagesPerItem; ++s, ++g) {
-          const int st = g % kMdNS;
-          if (!(ok = mbar_wait(&bar.empty[st], ((g / kMdNS) & 1) ^ 1, ab))) break;
-          unsigned char* sb = smem + st * kMdStage;
-          if (s < kMdKBoxes) {  // query box and key box of S step s
-            mbar_expect_tx(&bar.full[st], kMdStage);
-            tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], md_sbox(s) * 64, it.chunk * kMdT, it.b);
-            if (k == 0 || s >= kMdNS) {
-              tma_load_3d(sb, &a.tq, &bar.full[st], md_sbox(s) * 64, 0, it.b);
-            } else if (s == kMdNS - 1) {
-              // the previous item's epilogue staged its output in the query
-              // slots: the item's first query boxes wait until those stores
-              // have read them (its first key boxes are already on the way)
-              if (!(ok = mbar_wait(&bar.qs_free, (k - 1) & 1, ab))) break;
-              for (int s2 = 0; s2 < kMdNS; ++s2) {
-                const int st2 = (g - (kMdNS - 1) + s2) % kMdNS;
-                tma_load_3d(smem + st2 * kMdStage, &a.tq, &bar.full[st2], md_sbox(s2) * 64, 0, it.b);
-              }
-            }
-          } else {  // value box 0-4, in the key slot
-            const int vb = s - kMdKBoxes;
-            mbar_expect_tx(&bar.full[st], kMdKBox);
-            tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], vb * 64, it.chunk * kMdT, it.b);
+        for (int c = 0; c < kMdKBoxes; ++c) {
+          const int st = c % kMdNS, f = (kMdKBoxes / kMdNS) * k + c / kMdNS;
+          ok = mbar_wait(&bar.empty[st], (f & 1) ^ 1, ab);
+          if (ok && k > 0 && c < kMdNS) {
+            if (st <= 1) ok = mbar_wait(&bar.vempty[0], 1, ab);  // slot A's second fill of item k - 1 released
+            if (ok && st >= 1) ok = mbar_wait(&bar.vempty[1], 1, ab);
+            if (ok && st == 2) ok = mbar_wait(&bar.e_free, (k - 1) & 1, ab);
           }
+          if (!ok) break;
+          unsigned char* sb = smem + st * kMdStage;
+          mbar_expect_tx(&bar.full[st], kMdStage);
+          tma_load_3d(sb, &a.tq, &bar.full[st], c * 64, 0, it.b);
+          tma_load_3d(sb + kMdQBox, &a.tk, &bar.full[st], c * 64, it.chunk * kMdT, it.b);
+          ++sfill[st];
+        }
+        for (int p = 0; p < kMdNPairs && ok; ++p) {
+          const int sl = p & 1;
+          if (p < 2) {  // the S stages under the slot (0-1 for A, 1-2 for B) read out: their fill 3k + 2
+            const uint32_t par = ((kMdKBoxes / kMdNS) * k + kMdKBoxes / kMdNS - 1) & 1;
+            ok = mbar_wait(&bar.empty[sl], par, ab) && mbar_wait(&bar.empty[sl + 1], par, ab);
+          } else {  // the slot's first pair of this item read out
+            ok = mbar_wait(&bar.vempty[sl], 0, ab);
+          }
+          if (!ok) break;
+          unsigned char* vb = smem + sl * kMdVPair;
+          mbar_expect_tx(&bar.vfull[sl], kMdVPair);
+          tma_load_3d(vb, &a.tk, &bar.vfull[sl], (2 * p) * 64, it.chunk * kMdT, it.b);
+          tma_load_3d(vb + kMdKBox, &a.tk, &bar.vfull[sl], (2 * p + 1) * 64, it.chunk * kMdT, it.b);
+          ++vfill[sl];
         }
       }
       if (!ok) {  // let the copies already issued land (each wait bounded on its own)
-        for (int h = g - 1; h >= 0 && h >= g - kMdNS; --h) {
-          volatile int own = 0;
-          mbar_wait(&bar.full[h % kMdNS], (h / kMdNS) & 1, Abort{&own, a.err});
-        }
+        for (int st = 0; st < kMdNS; ++st)
+          if (sfill[st] > 0) {
+            volatile int own = 0;
+            mbar_wait(&bar.full[st], (sfill[st] - 1) & 1, Abort{&own, a.err});
+          }
+        for (int sl = 0; sl < 2; ++sl)
+          if (vfill[sl] > 0) {
+            volatile int own = 0;
+            mbar_wait(&bar.vfull[sl], (vfill[sl] - 1) & 1, Abort{&own, a.err});
+          }
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // lane 0 issues; the whole warp waits for each stage in turn (never more
-    // than one phase behind its barrier: a stage is refilled only after this
-    // warp's MMAs on it) and, in a partial chunk, zeroes the value rows from
-    // the length up to the end of its last 16-position step, the only rows
-    // past the length that O reads (its steps past that are not issued):
-    // they come from a cache that may hold anything there
+    // lane 0 issues; the whole warp waits for each stage and slot in turn
+    // (never more than one phase behind its barrier: a region is refilled
+    // only after this warp's MMAs on it) and, in a partial chunk, zeroes the
+    // value rows from the length up to the end of its last 16-position step,
+    // the only rows past the length that O reads (its steps past that are
+    // not issued): they come from a cache that may hold anything there
     constexpr uint32_t IDESC_S = idesc_bf16(kMdRows, kMdT, 0, 0);  // Q (K-major) x K (K-major)
-    constexpr uint32_t IDESC_O = idesc_bf16(kMdRows, 64, 0, 1);    // P (K-major) x V (MN-major)
+    constexpr uint32_t IDESC_O = idesc_bf16(kMdRows, 128, 0, 1);   // P (K-major) x value pair (MN-major)
     const uint32_t s0 = smem_u32(smem);
     const uint64_t pdesc = sdesc_sw128(s0 + kMdOffP, 16, 1024);
-    int g = 0;
     bool ok = true;
     for (int k = 0; k < n_items && ok; ++k) {
       const MdItem it = md_item(cta + k * ncta, pre, pre2, lens_s, a.B);
       const int nvalid = min(kMdT, it.len - it.chunk * kMdT);
       const int nk = (nvalid + 15) >> 4;  // 16-position steps of O that hold a valid position
       if (k > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_free, (k - 1) & 1, ab)))) break;  // the last O read out
-      const int g0 = g;  // ring position of the item's first S stage
-      for (int c = 0; c < kMdKBoxes; ++c, ++g) {
-        const int st = g % kMdNS;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab)))) break;
+      for (int c = 0; c < kMdKBoxes; ++c) {
+        const int st = c % kMdNS, f = (kMdKBoxes / kMdNS) * k + c / kMdNS;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.full[st], f & 1, ab)))) break;
         if (lane == 0) {
           tc_fence_after();
           const uint64_t qd = sdesc_sw128(s0 + st * kMdStage, 16, 1024);
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ss(tmem, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), IDESC_S, (c > 0 || kk > 0) ? 1u : 0u);
-          if (c < kMdKBoxes - kMdVKept) mma_commit(&bar.empty[st]);  // the last stages stay for O
+          mma_commit(&bar.empty[st]);
         }
         __syncwarp();
       }
@@ -253,32 +268,28 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
       if (lane == 0) mma_commit(&bar.s_full);
       // P written, S read: its columns take O
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_full, k & 1, ab)))) break;
-      for (int i = 0; i < kMdVBoxes; ++i) {
-        const int vbox = md_vbox(i);
-        int st;
-        if (i < kMdVKept) {  // value box vbox is the key box of S step kMdKBoxes - kMdVKept + i, still in its stage
-          st = (g0 + kMdKBoxes - kMdVKept + i) % kMdNS;
-        } else {
-          st = g % kMdNS;
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.full[st], (g / kMdNS) & 1, ab)))) break;
-          ++g;
-        }
+      for (int p = 0; p < kMdNPairs; ++p) {
+        const int sl = p & 1;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.vfull[sl], (2 * k + (p >> 1)) & 1, ab)))) break;
+        unsigned char* vb = smem + sl * kMdVPair;
         if (nvalid < 16 * nk) {
-          unsigned char* vb = smem + st * kMdStage + kMdQBox;
-          for (int x = lane; x < (16 * nk - nvalid) * 8; x += 32)  // 16-byte chunks, 8 per row
-            *reinterpret_cast<uint4*>(vb + (nvalid + (x >> 3)) * 128 + (x & 7) * 16) = make_uint4(0, 0, 0, 0);
+          for (int x = lane; x < (16 * nk - nvalid) * 16; x += 32) {  // 16-byte chunks, 8 per row in each box
+            const int row = nvalid + (x >> 4), q = x & 15;
+            *reinterpret_cast<uint4*>(vb + (q >> 3) * kMdKBox + row * 128 + (q & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
           fence_proxy_async_smem();
           __syncwarp();
         }
         if (lane == 0) {
           tc_fence_after();
-          const uint64_t vd = sdesc_sw128(s0 + st * kMdStage + kMdQBox, kMdKBox, 1024);
+          // the pair's two 64-column boxes are the operand's MN blocks, 32 KB apart
+          const uint64_t vd = sdesc_sw128(s0 + sl * kMdVPair, kMdKBox, 1024);
           for (int kk = 0; kk < nk; ++kk)
-            mma_ss(tmem + (vbox < 4 ? 256 + 64 * vbox : 64 * (vbox - 4)),
+            mma_ss(tmem + (p < 2 ? 256 + 128 * p : 128 * (p - 2)),
                    pdesc + ((((kk >> 2) * (kMdRows * 128)) + (kk & 3) * 32) >> 4), vd + ((kk * 16 * 128) >> 4), IDESC_O,
                    kk > 0 ? 1u : 0u);
-          mma_commit(&bar.empty[st]);
-          mma_commit(&bar.o_box[vbox]);
+          mma_commit(&bar.vempty[sl]);
+          mma_commit(&bar.o_pair[p]);
         }
         __syncwarp();
       }
@@ -341,37 +352,38 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
       fence_proxy_async_smem();
       mbar_arrive(&bar.p_full);
       if (hf == 0) {
-        // epilogue, overlapping O: value box v (columns 64v..64v+63) is in
-        // TMEM [256 + 64v, ...) for v < 4 and [64(v-4), ...) after; each box
-        // goes out as two groups of 32 columns x 128 head rows, staged in
-        // turn in the three query slots (idle once S is done; 128-byte
-        // swizzle) and read back so that each warp store writes four whole
-        // 128-byte lines of four heads' rows.  Plain stores, not TMA: the
-        // TMA unit stays free for the value boxes that O still waits for
+        // epilogue, overlapping O: value pair p (columns 128p..128p+127) is
+        // in TMEM [256 + 128p, ...) for p < 2 and [128(p-2), ...) after; it
+        // goes out as four groups of 32 columns x 128 head rows, each staged
+        // in shared memory (128-byte swizzle) and read back so that each warp
+        // store writes four whole 128-byte lines of four heads' rows.  Plain
+        // stores, not TMA: the TMA unit stays free for the value pairs that
+        // O still waits for.  (Splitting this over two warp groups that pass
+        // 16-column groups through two buffers measured 3% slower.)
         const size_t obase = ((size_t)it.b * a.H) * a.nch + it.chunk;  // partial row of (b, head 0, chunk)
+        unsigned char* buf = smem + kMdOffE;
+        const int q = r & 7;  // 16-byte piece of a head's 128-byte row, in the read-back
 #pragma unroll 1
-        for (int c = 0; c < 2 * kMdVBoxes; ++c) {
-          const int vc = 2 * md_vbox(c >> 1) + (c & 1);  // 32-column group of the value, in the order O forms them
-          if ((c & 1) == 0) {
-            mbar_wait(&bar.o_box[vc >> 1], k & 1, ab);
+        for (int c = 0; c < kMdDv / 32; ++c) {
+          if ((c & 3) == 0) {
+            mbar_wait(&bar.o_pair[c >> 2], k & 1, ab);
             tc_fence_after();
           }
           uint32_t ov[32];
-          tmem_ld32(tmem + lane_base + (vc < 8 ? 256 + 32 * vc : 32 * (vc - 8)), ov);
+          tmem_ld32(tmem + lane_base + (c < 8 ? 256 + 32 * c : 32 * (c - 8)), ov);
           tmem_ld_wait();
-          unsigned char* buf = smem + (c % kMdNS) * kMdStage;
+          if (c > 0) named_bar(1, kMdRows);  // the previous group has been read back
           unsigned char* rp = buf + r * 128;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch)
             *reinterpret_cast<uint4*>(rp + ((ch ^ (r & 7)) << 4)) =
                 make_uint4(ov[4 * ch], ov[4 * ch + 1], ov[4 * ch + 2], ov[4 * ch + 3]);
-          named_bar(1, kMdRows);  // (the last reader of this slot passed the barrier of the group after it)
-          const int q = r & 7;    // 16-byte piece of a head's 128-byte row
+          named_bar(1, kMdRows);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int head = (r >> 3) + 16 * j;
             if (head < a.H)
-              *reinterpret_cast<uint4*>(a.part_o + (obase + (size_t)head * a.nch) * kMdDv + 32 * vc + 4 * q) =
+              *reinterpret_cast<uint4*>(a.part_o + (obase + (size_t)head * a.nch) * kMdDv + 32 * c + 4 * q) =
                   *reinterpret_cast<const uint4*>(buf + head * 128 + ((q ^ (head & 7)) << 4));
           }
         }
@@ -384,7 +396,7 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
       }
       tc_fence_before();
       mbar_arrive(&bar.o_free);
-      if (tid == 0) mbar_arrive(&bar.qs_free);  // the query slots have been read back: the next item may load them
+      if (tid == 0) mbar_arrive(&bar.e_free);  // the staging has been read back: the next item may load over it
     }
   }
 
