@@ -832,7 +832,19 @@ def measure_mla_decode(lens_host, peaks, cpattn, dev, seed, iters=30):
             "l2": "flushed before each launch (512 MB write + 512 MB read)"}
 
 
-def measure_shards(w, attn, cpattn, iters=3):
+def shard_medians(fns, rounds, inner):
+    """Median device ms per call of each fn, over rounds that each time every
+    fn once (inner calls back to back): interleaved, so that a clock that
+    drifts under the power cap during the measurement weighs on every shard
+    alike rather than on the last ones timed."""
+    ts = [[] for _ in fns]
+    for _ in range(rounds):
+        for i, f in enumerate(fns):
+            ts[i].append(time_steps(f, inner))
+    return [sorted(t)[len(t) // 2] for t in ts]
+
+
+def measure_shards(w, attn, cpattn, rounds=3, inner=1):
     """Per-shard forward and backward times, each shard's launch alone on the
     whole GPU, with load balancing on (slot-order tensors) and off (natural
     order), plus the tile-pair counts per head.  The backward of one shard
@@ -852,16 +864,15 @@ def measure_shards(w, attn, cpattn, iters=3):
         else:
             qq, kk, vv, dd = q, k, v, dout
         cpattn.attn_fwd(qq, kk, vv, cp, lb, out, lse)
-        fwd, bwd = [], []
-        for s in range(cp):
-            f = lambda: cpattn.attn_fwd_shard(qq, kk, vv, cp, s, lb, out, lse)  # noqa: E731
+        fns = [lambda s=s: cpattn.attn_fwd_shard(qq, kk, vv, cp, s, lb, out, lse) for s in range(cp)]
+        for f in fns:
             f()
-            fwd.append(time_steps(f, iters))
+        fwd = shard_medians(fns, rounds, inner)
         cpattn.attn_fwd(qq, kk, vv, cp, lb, out, lse)  # full out/lse for the backward
-        for s in range(cp):
-            f = lambda: cpattn.attn_bwd_shard(qq, kk, vv, out, lse, dd, cp, s, lb, dq, dkp, dvp)  # noqa: E731
+        fns = [lambda s=s: cpattn.attn_bwd_shard(qq, kk, vv, out, lse, dd, cp, s, lb, dq, dkp, dvp) for s in range(cp)]
+        for f in fns:
             f()
-            bwd.append(time_steps(f, iters))
+        bwd = shard_medians(fns, rounds, inner)
         e = {"tile_pairs_per_head": cpattn.tile_counts(w["S"], cp, lb), "fwd_ms": fwd,
              "fwd_max_over_min": max(fwd) / min(fwd)}
         if bwd:
@@ -904,7 +915,7 @@ def measure_workload(name, peaks, cpattn, dev, seed, steps=None, warmup=3):
            "config": {k: w[k] for k in ("B", "S", "Hq", "Hkv", "Dqk", "Dv", "cp", "lb")},
            "kernels": kernel_table(prof, w, peaks, timed_s)}
     if name in ("llama2_7b_s8192_cp4", "deepseek_v3_mla_s32768_cp4"):
-        res["shards"] = measure_shards(w, attn, cpattn, iters=10 if name.startswith("llama2") else 3)
+        res["shards"] = measure_shards(w, attn, cpattn, rounds=5, inner=10 if name.startswith("llama2") else 1)
     if w["lb"] and (S // (2 * w["cp"])) % 128 == 0:
         # the same step with load_balance = 2: natural-order tensors, no permutes
         cp = w["cp"]
