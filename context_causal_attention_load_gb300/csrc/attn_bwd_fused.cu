@@ -73,7 +73,8 @@ struct FCfg {
   static constexpr int VEC_BYTES = 2 * kRows * 4;
   static constexpr int OFF_BAR = OFF_VEC + 2 * VEC_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + 256;  // TMEM address, abort flag, StepInfo[2] at +32
-  static constexpr int SMEM = OFF_MISC + 64;
+  static constexpr int OFF_MROW = OFF_MISC + 64;  // memory row of each key row of the unit (-1 past S)
+  static constexpr int SMEM = OFF_MROW + kRows * 4;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TILE % 1024 == 0 && OFF_DS % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   // TMEM columns
@@ -704,34 +705,84 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       // dV and scale*dK of this key tile
       mbar_wait(&bar.acc_full, uc & 1, ab);
       tc_fence_after();
-      const size_t orow = ((size_t)u.b * pm.S + (kvalid ? mem_row<NAT>(pm, kslot) : 0)) * a.sh.Hkv + u.h;
-      const float sc = a.scale;
+      if constexpr (SHARD) {  // one shard's backward also writes unrounded fp32 partials
+        const size_t orow = ((size_t)u.b * pm.S + (kvalid ? mem_row<NAT>(pm, kslot) : 0)) * a.sh.Hkv + u.h;
+        const float sc = a.scale;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const float f = which ? sc : 1.f;
-        __nv_bfloat16* dst0 = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv);
-        float* part0 = which ? a.dk_part : a.dv_part;
+        for (int which = 0; which < 2; ++which) {
+          const float f = which ? sc : 1.f;
+          __nv_bfloat16* dst0 = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv);
+          float* part0 = which ? a.dk_part : a.dv_part;
 #pragma unroll 1
-        for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_base + (which ? C::T_DK : C::T_DV) + c0, o);
+          for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + (which ? C::T_DK : C::T_DV) + c0, o);
+            tmem_ld_wait();
+            if (kvalid && (!SHARD || dst0)) {
+              uint4* dst = reinterpret_cast<uint4*>(dst0 + orow * D + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                dst[v4] = make_uint4(pack_bf16(f * __uint_as_float(o[8 * v4 + 0]), f * __uint_as_float(o[8 * v4 + 1])),
+                                     pack_bf16(f * __uint_as_float(o[8 * v4 + 2]), f * __uint_as_float(o[8 * v4 + 3])),
+                                     pack_bf16(f * __uint_as_float(o[8 * v4 + 4]), f * __uint_as_float(o[8 * v4 + 5])),
+                                     pack_bf16(f * __uint_as_float(o[8 * v4 + 6]), f * __uint_as_float(o[8 * v4 + 7])));
+            }
+            if (SHARD && kvalid) {  // per-shard partial, unrounded
+              float4* dst = reinterpret_cast<float4*>(part0 + orow * D + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                dst[v4] = make_float4(f * __uint_as_float(o[4 * v4 + 0]), f * __uint_as_float(o[4 * v4 + 1]),
+                                      f * __uint_as_float(o[4 * v4 + 2]), f * __uint_as_float(o[4 * v4 + 3]));
+            }
+          }
+        }
+      } else {
+        // through the dS space (free once the last step's dQ tile has been
+        // reduced), so that each warp store writes whole lines: a thread
+        // stores its key row's half in bf16 (16-byte pieces, XOR-swizzled by
+        // row), then the 256 threads read the tile back row by row.  Stored
+        // straight from the TMEM rows instead, every warp store touched 32
+        // lines 16 bytes at a time and the epilogue took about 8,000 clocks
+        // (now about 6,000, a third of it the wait for the dS space).
+        // Writing dK/dV from the dQ read-out warps instead, so that these
+        // warps went straight on to the next unit, shortened the unit
+        // boundary but made every step about 4% slower.
+        mbar_wait(&bar.ds_free, (gs - 1) & 1, ab);
+        int* mrow_s = reinterpret_cast<int*>(smem + C::OFF_MROW);
+        if (g == 0) mrow_s[row] = kvalid ? mem_row<NAT>(pm, kslot) : -1;
+        constexpr int KC = D / 8;  // 16-byte pieces of a row
+        unsigned char* const stg = smem + C::OFF_DS;
+        const size_t rbase = (size_t)u.b * pm.S;
+        const int tid_ew = (warp << 5) + lane;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const float f = which ? a.scale : 1.f;
+          uint32_t o[2][32];
+          tmem_ld32(tmem + lane_base + (which ? C::T_DK : C::T_DV) + g * (D / 2), o[0]);
+          if (D / 2 > 32) tmem_ld32(tmem + lane_base + (which ? C::T_DK : C::T_DV) + g * (D / 2) + 32, o[1]);
           tmem_ld_wait();
-          if (kvalid && (!SHARD || dst0)) {
-            uint4* dst = reinterpret_cast<uint4*>(dst0 + orow * D + c0);
+          unsigned char* sr = stg + row * (D * 2);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pack_bf16(f * __uint_as_float(o[8 * v4 + 0]), f * __uint_as_float(o[8 * v4 + 1])),
-                                   pack_bf16(f * __uint_as_float(o[8 * v4 + 2]), f * __uint_as_float(o[8 * v4 + 3])),
-                                   pack_bf16(f * __uint_as_float(o[8 * v4 + 4]), f * __uint_as_float(o[8 * v4 + 5])),
-                                   pack_bf16(f * __uint_as_float(o[8 * v4 + 6]), f * __uint_as_float(o[8 * v4 + 7])));
+          for (int j = 0; j < KC / 2; ++j) {  // piece k = columns 8k..8k+7
+            const int k = g * (KC / 2) + j;
+            const uint32_t* x = &o[j >> 2][8 * (j & 3)];
+            *reinterpret_cast<uint4*>(sr + ((k ^ (row & 7)) << 4)) =
+                make_uint4(pack_bf16(f * __uint_as_float(x[0]), f * __uint_as_float(x[1])),
+                           pack_bf16(f * __uint_as_float(x[2]), f * __uint_as_float(x[3])),
+                           pack_bf16(f * __uint_as_float(x[4]), f * __uint_as_float(x[5])),
+                           pack_bf16(f * __uint_as_float(x[6]), f * __uint_as_float(x[7])));
           }
-          if (SHARD && kvalid) {  // per-shard partial, unrounded
-            float4* dst = reinterpret_cast<float4*>(part0 + orow * D + c0);
+          named_bar(1, 256);
+          __nv_bfloat16* dst0 = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv);
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[v4] = make_float4(f * __uint_as_float(o[4 * v4 + 0]), f * __uint_as_float(o[4 * v4 + 1]),
-                                    f * __uint_as_float(o[4 * v4 + 2]), f * __uint_as_float(o[4 * v4 + 3]));
+          for (int i = 0; i < KC / 2; ++i) {
+            const int pc = tid_ew + 256 * i, rr = pc / KC, k = pc % KC;
+            const int mr = mrow_s[rr];
+            if (mr >= 0)
+              *reinterpret_cast<uint4*>(dst0 + ((rbase + mr) * a.sh.Hkv + u.h) * D + 8 * k) =
+                  *reinterpret_cast<const uint4*>(stg + rr * (D * 2) + ((k ^ (rr & 7)) << 4));
           }
+          named_bar(1, 256);  // the tile is read back: the space takes dK, then the next unit's dS
         }
       }
       tc_fence_before();
