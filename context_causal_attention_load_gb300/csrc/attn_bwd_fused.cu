@@ -705,7 +705,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
       // dV and scale*dK of this key tile
       mbar_wait(&bar.acc_full, uc & 1, ab);
       tc_fence_after();
-      if constexpr (SHARD) {  // one shard's backward also writes unrounded fp32 partials
+      if constexpr (SHARD) {  // one shard's backward also writes unrounded fp32 partials (staged
+        // through the dS space half by half like the bf16 path below, they took 3% longer)
         const size_t orow = ((size_t)u.b * pm.S + (kvalid ? mem_row<NAT>(pm, kslot) : 0)) * a.sh.Hkv + u.h;
         const float sc = a.scale;
 #pragma unroll

@@ -213,6 +213,28 @@ def test_bwd_shard_partials(cfg):
     assert_close_grad(dv_sum.numpy(), _f64(dv_full), "sum of dv parts %s" % (cfg,))
 
 
+@pytest.mark.parametrize("cfg", [
+    (1, 512, 4, 2, 128, 128, 4, True),
+    (2, 256, 2, 2, 64, 64, 2, True),
+])
+def test_bwd_shard_bf16_copy_is_the_rounded_partial(cfg):
+    """Asked for them, one shard's backward also writes its dk/dv contributions
+    rounded to bf16: bit for bit the fp32 partials rounded to nearest even
+    (zero for the keys the shard does not touch)."""
+    B, S, Hq, Hkv, Dqk, Dv, cp, lb = cfg
+    r = _run_fwd(*cfg, seed=14)
+    doutd = cp_.lb_permute(r["dout"].cuda(), cp)
+    for s in range(cp):
+        dk = torch.empty_like(r["kd"])
+        dv = torch.empty_like(r["vd"])
+        _, dkp, dvp = cp_.attn_bwd_shard(r["qd"], r["kd"], r["vd"], r["out"], r["lse"], doutd, cp, s, lb,
+                                         dk=dk, dv=dv)
+        torch.cuda.synchronize()
+        cp_.check_device()
+        assert torch.equal(dk, dkp.to(torch.bfloat16)), "dk bf16 copy, shard %d %s" % (s, cfg)
+        assert torch.equal(dv, dvp.to(torch.bfloat16)), "dv bf16 copy, shard %d %s" % (s, cfg)
+
+
 def test_bwd_shard_rejects_natural_order():
     """The per-shard backward takes tensors in slot order only."""
     B, S, H, cp = 1, 256, 1, 2
