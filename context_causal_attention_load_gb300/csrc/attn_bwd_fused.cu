@@ -631,10 +631,21 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
     const uint64_t sl2x2 = f2pack(a.scale_log2, a.scale_log2);
     int gs = 0;
 
+    // the next unit's descriptor is fetched while this unit's dK/dV go out
+    // (pf: the unit index r it belongs to, -2 past the CTA's last unit)
+    int pf = -1;
+    BwdUnit un{};
     for (int r = 0, uc = 0;; ++r) {
-      const int ui = unit_index(a.cta_off, r, cta);
-      if (ui < 0) break;
-      const BwdUnit u = a.units[ui];
+      BwdUnit u;
+      if (pf == r) {
+        u = un;
+      } else {
+        if (pf == -2) break;
+        const int ui = unit_index(a.cta_off, r, cta);
+        if (ui < 0) break;
+        u = a.units[ui];
+      }
+      pf = -1;
       const int kslot = u.t * kRows + row;
       const bool kvalid = kslot < pm.S;
       const int kpos = kvalid ? pm.pos(kslot) : 0x7fffffff;
@@ -702,6 +713,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) attn_bwd_fused_kernel(const __gr
         mbar_arrive(&bar.dss_full);
         ++gs;
       } while (!last);
+      if constexpr (!SHARD) {  // (in the per-shard kernel it cost registers and 2% of its time)
+        const int ui2 = unit_index(a.cta_off, r + 1, cta);
+        if (ui2 >= 0) {
+          un = a.units[ui2];
+          pf = r + 1;
+        } else {
+          pf = -2;
+        }
+      }
       // dV and scale*dK of this key tile
       mbar_wait(&bar.acc_full, uc & 1, ab);
       tc_fence_after();
