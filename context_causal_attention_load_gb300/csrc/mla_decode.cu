@@ -410,14 +410,23 @@ __global__ void __launch_bounds__(kMdThreads, 1) mla_decode_kernel(const __grid_
 }
 
 // merge of the chunks of each (b, h) row: one CTA of 128 threads per row,
-// four value columns per thread; eight chunks' loads in flight at a time
-// (every chunk of a 2048-position cache in one round), merged online.  The
-// row's partials are contiguous ([b][h][chunk]).  Launched as a programmatic
-// dependent, so the partials are read only after the attention grid has
-// completed.  (Fetching each row's partials into shared memory with bulk
-// copies, twelve rows ahead on a persistent grid, measured three times
-// slower: the copies arrived at about 14 GB/s per SM.)
+// four value columns per thread, merged online.  The row's partials are
+// contiguous ([b][h][chunk]); each thread copies its 16 bytes of eight
+// chunks at a time into shared memory with cp.async (so no register holds a
+// load in flight, and 16 KB of shared memory per CTA, not the register file,
+// bounds how many rows are in flight on an SM) and reads them back.
+// Launched as a programmatic dependent, so the partials are read only after
+// the attention grid has completed.  (Loads into registers held 1520 rows in
+// flight and took two waves over the 3072 rows of the 24 x 128-head decode;
+// fetching each row's partials with bulk copies, twelve rows ahead on a
+// persistent grid, measured three times slower: about 14 GB/s per SM.)
+constexpr int kMgChunks = 8;
+constexpr int kMgSmem = kMgChunks * kMdDv * 4;  // 16 KB
+__device__ __forceinline__ void mg_cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
 __global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_constant__ MlaDecodeArgs a) {
+  extern __shared__ float4 mg_x[];  // [chunk][thread]
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.x, b = row / a.H;
   int len = a.lens[b];
@@ -429,23 +438,21 @@ __global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_cons
     return;
   }
   const float4* po = reinterpret_cast<const float4*>(a.part_o + (size_t)row * a.nch * kMdDv) + threadIdx.x;
-  const float* pml = a.part_ml + (size_t)row * a.nchp * 2;
+  const float2* pml = reinterpret_cast<const float2*>(a.part_ml + (size_t)row * a.nchp * 2);
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < nch; c0 += 8) {
-    float m[8], l[8];
-    float4 x[8];
+  for (int c0 = 0; c0 < nch; c0 += kMgChunks) {
+    const int nc = min(kMgChunks, nch - c0);
+    for (int j = 0; j < nc; ++j) mg_cp_async16(&mg_x[j * 128 + threadIdx.x], po + (size_t)(c0 + j) * (kMdDv / 4));
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    float2 ml[kMgChunks];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {  // past the last chunk: load the last one again (no branch), weight 0
-      const int c = min(c0 + j, nch - 1);
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + c);
-      m[j] = c0 + j < nch ? ml.x : -INFINITY;
-      l[j] = ml.y;
-      x[j] = __ldcg(po + (size_t)c * (kMdDv / 4));
-    }
+    for (int j = 0; j < kMgChunks; ++j) ml[j] = __ldcg(pml + min(c0 + j, nch - 1));  // past the last chunk: weight 0 below
+    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's own copies (it reads only those)
     float mn = M;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) mn = fmaxf(mn, m[j]);  // finite: chunk c0 is in
+    for (int j = 0; j < kMgChunks; ++j)
+      if (j < nc) mn = fmaxf(mn, ml[j].x);  // finite: chunk c0 is in
     const float f = fast_exp2(M - mn);
     L *= f;
     acc.x *= f;
@@ -453,14 +460,16 @@ __global__ void __launch_bounds__(128) mla_decode_merge_kernel(const __grid_cons
     acc.z *= f;
     acc.w *= f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float w = fast_exp2(m[j] - mn);  // 0 past the last chunk
-      L = fmaf(l[j], w, L);
-      acc.x = fmaf(x[j].x, w, acc.x);
-      acc.y = fmaf(x[j].y, w, acc.y);
-      acc.z = fmaf(x[j].z, w, acc.z);
-      acc.w = fmaf(x[j].w, w, acc.w);
-    }
+    for (int j = 0; j < kMgChunks; ++j)
+      if (j < nc) {
+        const float w = fast_exp2(ml[j].x - mn);
+        const float4 x = mg_x[j * 128 + threadIdx.x];
+        L = fmaf(ml[j].y, w, L);
+        acc.x = fmaf(x.x, w, acc.x);
+        acc.y = fmaf(x.y, w, acc.y);
+        acc.z = fmaf(x.z, w, acc.z);
+        acc.w = fmaf(x.w, w, acc.w);
+      }
     M = mn;
   }
   const float il = 1.f / L;
@@ -490,7 +499,7 @@ cudaError_t launch_mla_decode(const MlaDecodeArgs& a0, int num_sms, cudaStream_t
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B * a.H);
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kMgSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
