@@ -521,6 +521,7 @@ def test_mla_shared_rope_zero_copy():
     (1, 128, 256, 256, 256),       # one whole chunk
     (5, 64, 1300, 0, 1300),        # may include an empty cache
     (2, 128, 3000, 2100, 3000),    # more than eight chunks per row: the merge takes them in two groups
+    (64, 128, 2048, 1024, 2048),   # about 400 items: two or three per CTA, so items follow one another on an SM
 ])
 def test_mla_decode_parity(cfg):
     B, H, Smax, lo, hi = cfg
@@ -530,6 +531,18 @@ def test_mla_decode_parity(cfg):
     cp_.check_device()
     ref = O.mla_decode(_f64(q), _f64(ckv), lens.numpy())
     assert_close_out(_f64(out), ref, "mla decode %s" % (cfg,))
+
+
+def test_mla_decode_repeatable_with_several_items_per_cta():
+    """With more items than SMs a CTA's next item loads over the space its last
+    one used: 20 calls on a 64-sequence batch give identical bits."""
+    q, ckv, lens = synth.mla_decode_inputs(64, 128, 2048, 1, 2048, seed=57)
+    q, ckv, lens = q.cuda(), ckv.cuda(), lens.cuda()
+    ref = cp_.mla_decode(q, ckv, lens).clone()
+    bad = sum(not torch.equal(cp_.mla_decode(q, ckv, lens), ref) for _ in range(20))
+    torch.cuda.synchronize()
+    cp_.check_device()
+    assert bad == 0, "%d of 20 calls differ" % bad
 
 
 def test_mla_decode_repeatable_over_many_calls():
