@@ -582,7 +582,9 @@ def measure_e2e(args, make_step, inputs, f_step, ms_step, world, dev):
     host_out = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in o] for o in outs]
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = sum(x.numel() * x.element_size() for x in host_out[0])
-    n = max(3, min(args.steps, int(6000.0 / max(ms_step, 1e-3))))
+    # (up to about 15 s of steps: the first step's input copy and the last one's result copy, which no
+    # compute covers, are shared by that many steps, as in a long training or serving loop)
+    n = max(3, min(args.steps, int(15000.0 / max(ms_step, 1e-3))))
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
